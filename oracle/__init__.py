@@ -1,0 +1,178 @@
+"""numpy front end of the fp64 CPU oracle of the MoE expert layer.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` leg of ``bench.py`` may import this package.  It shares no code with the
+CUDA implementation and never imports it.
+
+Arrays: bf16 tensors travel as their raw 16-bit patterns (``numpy.uint16``); fp32 router
+logits are widened to fp64 exactly before they reach the C code.  Every function below
+calls one entry point of ``moe_oracle.cpp``; the docstrings of that file name the
+passages of the pages each step follows.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_p = ctypes.c_void_p
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        dims = [_i64, _int, _int, _int, _int]
+        lib.oracle_num_threads.restype = _int
+        lib.oracle_round_bf16.restype = ctypes.c_double
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_route.argtypes = [_p, _i64, _int, _int, _p, _p]
+        lib.oracle_dispatch.argtypes = [_p, _i64, _int, _int, _p, _p, _p, _p]
+        for n in ("oracle_forward_tokens_bf16", "oracle_forward_tokens_f64"):
+            getattr(lib, n).argtypes = [_p] * 5 + dims + [_int, _p, _i64, _p]
+        lib.oracle_forward_permuted_bf16.argtypes = [_p] * 5 + dims + [_int, _p, _p, _p]
+        for n in ("oracle_backward_tokens_bf16", "oracle_backward_tokens_f64"):
+            getattr(lib, n).argtypes = [_p] * 6 + dims + [_int, _p, _i64, _p, _p, _p]
+        for n in ("oracle_backward_dw_bf16", "oracle_backward_dw_f64"):
+            getattr(lib, n).argtypes = [_p] * 6 + dims + [_int, _p, _int, _p, _p, _p]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _check(rc):
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (rc=%d)" % rc)
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def round_bf16(v: float) -> float:
+    """Nearest bf16 value of ``v`` (ties to even), as a float."""
+    return _load().oracle_round_bf16(float(v))
+
+
+def _logits64(logits):
+    return _c(logits, np.float64)
+
+
+def route(logits, k):
+    """Top-k experts per token (descending logit, ties to the lower index) and the
+    softmax gate over the selected logits.  Returns (idx int32 [T,k], gate float64 [T,k])."""
+    l64 = _logits64(logits)
+    T, E = l64.shape
+    idx = np.empty((T, k), np.int32)
+    gate = np.empty((T, k), np.float64)
+    _check(_load().oracle_route(_ptr(l64), T, E, k, _ptr(idx), _ptr(gate)))
+    return idx, gate
+
+
+def dispatch(idx, E):
+    """counts [E], exclusive offsets [E+1], perm [T*k] (row -> pair t*k+j) and
+    pos [T*k] (pair -> row); rows ordered by (expert, token)."""
+    idx = _c(idx, np.int32)
+    T, k = idx.shape
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    perm = np.empty(T * k, np.int32)
+    pos = np.empty(T * k, np.int32)
+    _check(_load().oracle_dispatch(_ptr(idx), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm),
+                                   _ptr(pos)))
+    return counts, offsets, perm, pos
+
+
+def _unpack(inp):
+    x, logits, W1, W3, W2 = inp["x"], inp["logits"], inp["W1"], inp["W3"], inp["W2"]
+    T, d = x.shape
+    E, _, dff = W1.shape
+    return x, _logits64(logits), W1, W3, W2, T, d, E, dff
+
+
+def _wtype(x):
+    return "bf16" if x.dtype == np.uint16 else "f64"
+
+
+def _prep(a, wt):
+    return _c(a, np.uint16 if wt == "bf16" else np.float64)
+
+
+def forward_tokens(inp, k, tokens=None, round_h=True):
+    """Brute-force forward for the listed tokens (all if None): route each token, run its
+    k experts on its own row, sum the gate-weighted outputs in fp64.  Returns [n, d]."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    wt = _wtype(x)
+    x, W1, W3, W2 = (_prep(a, wt) for a in (x, W1, W3, W2))
+    tok = None if tokens is None else _c(tokens, np.int64)
+    n = T if tok is None else len(tok)
+    y = np.empty((n, d), np.float64)
+    fn = getattr(_load(), "oracle_forward_tokens_" + wt)
+    _check(fn(_ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), T, d, E, k, dff, int(round_h),
+              _ptr(tok), n, _ptr(y)))
+    return y
+
+
+def forward_permuted(inp, k, round_h=True):
+    """Permuted forward (route, dispatch, row copy, per-row expert FFN, combine), bf16
+    inputs.  Returns (y [T,d] f64, x_perm [T*k,d] uint16, o_perm [T*k,d] f64)."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    x, W1, W3, W2 = (_c(a, np.uint16) for a in (x, W1, W3, W2))
+    y = np.empty((T, d), np.float64)
+    xp = np.empty((T * k, d), np.uint16)
+    op = np.empty((T * k, d), np.float64)
+    _check(_load().oracle_forward_permuted_bf16(_ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2),
+                                                T, d, E, k, dff, int(round_h), _ptr(y), _ptr(xp),
+                                                _ptr(op)))
+    return y, xp, op
+
+
+def backward_tokens(inp, dy, k, tokens=None, round_h=True):
+    """Per-token backward: dx [n,d], dgate [n,k], dlogits [n,E] (all f64)."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    wt = _wtype(x)
+    x, W1, W3, W2, dy = (_prep(a, wt) for a in (x, W1, W3, W2, dy))
+    tok = None if tokens is None else _c(tokens, np.int64)
+    n = T if tok is None else len(tok)
+    dx = np.empty((n, d), np.float64)
+    dgate = np.empty((n, k), np.float64)
+    dlog = np.empty((n, E), np.float64)
+    fn = getattr(_load(), "oracle_backward_tokens_" + wt)
+    _check(fn(_ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), T, d, E, k, dff,
+              int(round_h), _ptr(tok), n, _ptr(dx), _ptr(dgate), _ptr(dlog)))
+    return dx, dgate, dlog
+
+
+def backward_dw(inp, dy, k, experts, round_h=True):
+    """Weight gradients of the listed experts: dW1, dW3 [n,d,dff] and dW2 [n,dff,d], f64."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    wt = _wtype(x)
+    x, W1, W3, W2, dy = (_prep(a, wt) for a in (x, W1, W3, W2, dy))
+    ex = _c(experts, np.int32)
+    n = len(ex)
+    dW1 = np.empty((n, d, dff), np.float64)
+    dW3 = np.empty((n, d, dff), np.float64)
+    dW2 = np.empty((n, dff, d), np.float64)
+    fn = getattr(_load(), "oracle_backward_dw_" + wt)
+    _check(fn(_ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), T, d, E, k, dff,
+              int(round_h), _ptr(ex), n, _ptr(dW1), _ptr(dW3), _ptr(dW2)))
+    return dW1, dW3, dW2
+
+
+def layer_flops(pairs: int, d: int, dff: int) -> int:
+    """Algorithmic FLOP of the expert stage: 6*d*dff per token-expert pair (gate, up and
+    down projections: three d x dff multiply-adds), as the report's section 1.4 counts it."""
+    return 6 * d * dff * pairs

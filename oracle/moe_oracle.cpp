@@ -1,0 +1,455 @@
+// MoE expert-layer oracle: plain, slow, fp64 CPU implementation.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing on the product path may load or call this
+// library; only the test suite, the smoke check and the benchmark's CPU-baseline
+// leg do.  It shares no code, header or constant with the CUDA implementation.
+//
+// What it computes (sources, by page title and section):
+//  * "DeepSeek-V4 并行策略：重叠计算与通信" (blog.lpkt.cn), section "EP 对 IB 网络的优化":
+//    an MoE layer is Dispatch -> Expert Compute -> Combine.
+//  * DeepSeek-V4 report reading (10100.com), section on fine-grained overlap of the EP
+//    all-to-all: the expert stage is Linear + activation + Linear.
+//  * DeepSeek-V4 report, Thai translation (itsolotime.com), section 1.4 "observations and
+//    suggestions": each token-expert pair costs 6hd FLOP covering the SwiGLU gate
+//    projection, the up projection and the down projection; the combine payload is BF16.
+//  * The same page, section 3, and the 10100.com reading, section on batch-invariant and
+//    deterministic kernels: results must not depend on batch size or run.
+//
+// Readings taken where the pages are silent (each repeated next to the code below):
+//  * router: top-k over fp32 logits, ties go to the lower expert index; the gate is the
+//    softmax over the k selected logits.
+//  * stable permute: permuted rows are ordered by (expert, token).
+//  * SwiGLU: h = silu(x W1) * (x W3), silu(a) = a / (1 + exp(-a)); h is rounded to bf16
+//    (round to nearest, ties to even) before the down projection when round_h != 0.
+//  * combine: y_t = sum_j g_j * o_j, here in fp64.
+//  * backward: the derivative of the bf16 rounding of h is taken as 1.
+//
+// All arithmetic is fp64.  bf16 inputs are passed as their raw 16-bit patterns and
+// widened exactly.  Loops run in the plain order of the definitions; OpenMP only
+// splits independent tokens, rows or output rows between threads.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+#include <omp.h>
+
+namespace {
+
+inline double widen(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+inline double widen(double v) { return v; }
+
+// Nearest bf16 value to v, ties to even (bf16: 8 significant bits, float's exponent range).
+double round_bf16(double v) {
+  if (v == 0.0 || std::isnan(v) || std::isinf(v)) return v;
+  const double a = std::fabs(v);
+  double r;
+  if (a < std::ldexp(1.0, -126)) {
+    // subnormal range of bf16: a multiple of 2^-133
+    r = std::nearbyint(std::ldexp(a, 133));
+    r = std::ldexp(r, -133);
+  } else {
+    int ex;
+    double m = std::frexp(a, &ex);          // a = m * 2^ex, m in [0.5, 1)
+    r = std::nearbyint(std::ldexp(m, 8));   // 8 significant bits, ties to even
+    r = std::ldexp(r, ex - 8);
+    if (r >= std::ldexp(1.0, 128)) r = INFINITY;
+  }
+  return v < 0 ? -r : r;
+}
+
+double sigmoid(double a) { return 1.0 / (1.0 + std::exp(-a)); }
+
+// Router for one token.  Experts are ordered by (logit descending, index ascending) and
+// the first k are kept; the gate is the softmax over those k logits.
+void route_token(const double* l, int E, int k, int32_t* idx, double* gate) {
+  std::vector<char> taken(E, 0);
+  for (int j = 0; j < k; ++j) {
+    int best = -1;
+    for (int e = 0; e < E; ++e) {
+      if (taken[e]) continue;
+      // strict '>' keeps the lower index when two logits compare equal (+0 == -0 too)
+      if (best < 0 || l[e] > l[best]) best = e;
+    }
+    taken[best] = 1;
+    idx[j] = best;
+  }
+  const double m = l[idx[0]];
+  double s = 0.0;
+  for (int j = 0; j < k; ++j) s += std::exp(l[idx[j]] - m);
+  for (int j = 0; j < k; ++j) gate[j] = std::exp(l[idx[j]] - m) / s;
+}
+
+// One expert applied to one row x[0..d): a = x W1, b = x W3, h = silu(a) * b, o = h W2.
+// W1e, W3e are [d][dff] and W2e is [dff][d], row-major.
+template <class V>
+void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int dff, int round_h,
+             double* a, double* b, double* h, double* o) {
+  for (int f = 0; f < dff; ++f) { a[f] = 0.0; b[f] = 0.0; }
+  for (int c = 0; c < d; ++c) {
+    const double xc = widen(x[c]);
+    const V* w1 = W1e + static_cast<int64_t>(c) * dff;
+    const V* w3 = W3e + static_cast<int64_t>(c) * dff;
+    for (int f = 0; f < dff; ++f) {
+      a[f] += xc * widen(w1[f]);
+      b[f] += xc * widen(w3[f]);
+    }
+  }
+  for (int f = 0; f < dff; ++f) {
+    const double hv = a[f] / (1.0 + std::exp(-a[f])) * b[f];
+    h[f] = round_h ? round_bf16(hv) : hv;
+  }
+  for (int c = 0; c < d; ++c) o[c] = 0.0;
+  for (int f = 0; f < dff; ++f) {
+    const V* w2 = W2e + static_cast<int64_t>(f) * d;
+    for (int c = 0; c < d; ++c) o[c] += h[f] * widen(w2[c]);
+  }
+}
+
+// Backward of one token-expert pair given its forward values (a, b, h, o), its gate g and
+// the upstream gradient dy of the layer output:
+//   dgate = <o, dy>, dO = g dy, dh = dO W2^T,
+//   da = dh * b * silu'(a) with silu'(a) = s (1 + a (1 - s)), s = sigmoid(a),
+//   db = dh * silu(a),  dxp = da W1^T + db W3^T.
+template <class V>
+void ffn_row_bwd(const V* W1e, const V* W3e, const V* W2e, int d, int dff, double g,
+                 const double* dy, const double* a, const double* b, const double* o,
+                 double* dgate, double* dO, double* dh, double* da, double* db, double* dxp) {
+  double s = 0.0;
+  for (int c = 0; c < d; ++c) s += o[c] * dy[c];
+  *dgate = s;
+  for (int c = 0; c < d; ++c) dO[c] = g * dy[c];
+  for (int f = 0; f < dff; ++f) {
+    const V* w2 = W2e + static_cast<int64_t>(f) * d;
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += dO[c] * widen(w2[c]);
+    dh[f] = acc;
+  }
+  for (int f = 0; f < dff; ++f) {
+    const double sg = sigmoid(a[f]);
+    da[f] = dh[f] * b[f] * sg * (1.0 + a[f] * (1.0 - sg));
+    db[f] = dh[f] * a[f] * sg;
+  }
+  for (int c = 0; c < d; ++c) {
+    const V* w1 = W1e + static_cast<int64_t>(c) * dff;
+    const V* w3 = W3e + static_cast<int64_t>(c) * dff;
+    double acc = 0.0;
+    for (int f = 0; f < dff; ++f) acc += da[f] * widen(w1[f]) + db[f] * widen(w3[f]);
+    dxp[c] = acc;
+  }
+}
+
+struct Dims {
+  int64_t T;
+  int d, E, k, dff;
+};
+
+template <class V>
+const V* w13(const V* W, const Dims& D, int e) { return W + static_cast<int64_t>(e) * D.d * D.dff; }
+template <class V>
+const V* w2of(const V* W, const Dims& D, int e) { return W + static_cast<int64_t>(e) * D.dff * D.d; }
+
+bool dims_ok(int64_t T, int d, int E, int k, int dff) {
+  return T >= 0 && d > 0 && E > 0 && k >= 1 && k <= E && dff > 0;
+}
+
+// Brute-force forward for a list of tokens: route each token, run its k experts on its own
+// row, sum gate-weighted outputs.
+template <class V>
+int forward_tokens(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
+                   const Dims& D, int round_h, const int64_t* tokens, int64_t n, double* y) {
+  int bad = 0;
+#pragma omp parallel
+  {
+    std::vector<int32_t> idx(D.k);
+    std::vector<double> gate(D.k), a(D.dff), b(D.dff), h(D.dff), o(D.d);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t t = tokens ? tokens[i] : i;
+      if (t < 0 || t >= D.T) {
+#pragma omp atomic write
+        bad = 1;
+        continue;
+      }
+      route_token(logits + t * D.E, D.E, D.k, idx.data(), gate.data());
+      double* yt = y + i * D.d;
+      for (int c = 0; c < D.d; ++c) yt[c] = 0.0;
+      for (int j = 0; j < D.k; ++j) {
+        const int e = idx[j];
+        ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, round_h,
+                a.data(), b.data(), h.data(), o.data());
+        for (int c = 0; c < D.d; ++c) yt[c] += gate[j] * o[c];
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+void route_all(const double* logits, const Dims& D, int32_t* idx, double* gate) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < D.T; ++t)
+    route_token(logits + t * D.E, D.E, D.k, idx + t * D.k, gate + t * D.k);
+}
+
+// counts, exclusive offsets and the stable permutation (rows ordered by expert, then token).
+void dispatch_all(const int32_t* idx, const Dims& D, int32_t* counts, int32_t* offsets,
+                  int32_t* perm, int32_t* pos) {
+  for (int e = 0; e < D.E; ++e) counts[e] = 0;
+  for (int64_t p = 0; p < D.T * D.k; ++p) counts[idx[p]] += 1;
+  offsets[0] = 0;
+  for (int e = 0; e < D.E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  std::vector<int64_t> fill(offsets, offsets + D.E);
+  for (int64_t t = 0; t < D.T; ++t)
+    for (int j = 0; j < D.k; ++j) {
+      const int64_t p = t * D.k + j;
+      const int64_t r = fill[idx[p]]++;
+      perm[r] = static_cast<int32_t>(p);
+      pos[p] = static_cast<int32_t>(r);
+    }
+}
+
+// Permuted forward: route, dispatch, copy rows into expert order, run each row through its
+// expert, combine back to token order.
+template <class V>
+int forward_permuted(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
+                     const Dims& D, int round_h, double* y, V* x_perm_out, double* o_perm_out) {
+  const int64_t P = D.T * D.k;
+  std::vector<int32_t> idx(P), counts(D.E), offsets(D.E + 1), perm(P), pos(P);
+  std::vector<double> gate(P);
+  route_all(logits, D, idx.data(), gate.data());
+  dispatch_all(idx.data(), D, counts.data(), offsets.data(), perm.data(), pos.data());
+  std::vector<V> xp(static_cast<size_t>(P) * D.d);
+  for (int64_t r = 0; r < P; ++r) {
+    const int64_t t = perm[r] / D.k;
+    for (int c = 0; c < D.d; ++c) xp[r * D.d + c] = x[t * D.d + c];
+  }
+  std::vector<int32_t> row_expert(P);
+  for (int e = 0; e < D.E; ++e)
+    for (int64_t r = offsets[e]; r < offsets[e + 1]; ++r) row_expert[r] = e;
+  std::vector<double> op(static_cast<size_t>(P) * D.d);
+#pragma omp parallel
+  {
+    std::vector<double> a(D.dff), b(D.dff), h(D.dff);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < P; ++r) {
+      const int e = row_expert[r];
+      ffn_row(xp.data() + r * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff,
+              round_h, a.data(), b.data(), h.data(), op.data() + r * D.d);
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < D.T; ++t) {
+    double* yt = y + t * D.d;
+    for (int c = 0; c < D.d; ++c) yt[c] = 0.0;
+    for (int j = 0; j < D.k; ++j) {
+      const double* orow = op.data() + static_cast<int64_t>(pos[t * D.k + j]) * D.d;
+      const double g = gate[t * D.k + j];
+      for (int c = 0; c < D.d; ++c) yt[c] += g * orow[c];
+    }
+  }
+  if (x_perm_out) std::memcpy(x_perm_out, xp.data(), xp.size() * sizeof(V));
+  if (o_perm_out) std::memcpy(o_perm_out, op.data(), op.size() * sizeof(double));
+  return 0;
+}
+
+// Per-token backward (brute force): dx_t = sum_j dxp_j, dgate_t, and dlogits_t through the
+// softmax over the selected logits: dl_{e_j} = g_j (dgate_j - sum_i g_i dgate_i), 0 elsewhere.
+template <class V, class G>
+int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
+                    const G* dy, const Dims& D, int round_h, const int64_t* tokens, int64_t n,
+                    double* dx, double* dgate, double* dlogits) {
+  int bad = 0;
+#pragma omp parallel
+  {
+    std::vector<int32_t> idx(D.k);
+    std::vector<double> gate(D.k), a(D.dff), b(D.dff), h(D.dff), o(D.d), dyv(D.d), dO(D.d),
+        dh(D.dff), da(D.dff), db(D.dff), dxp(D.d);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t t = tokens ? tokens[i] : i;
+      if (t < 0 || t >= D.T) {
+#pragma omp atomic write
+        bad = 1;
+        continue;
+      }
+      route_token(logits + t * D.E, D.E, D.k, idx.data(), gate.data());
+      for (int c = 0; c < D.d; ++c) dyv[c] = widen(dy[t * D.d + c]);
+      double* dxt = dx ? dx + i * D.d : nullptr;
+      if (dxt) for (int c = 0; c < D.d; ++c) dxt[c] = 0.0;
+      std::vector<double> dg(D.k);
+      for (int j = 0; j < D.k; ++j) {
+        const int e = idx[j];
+        ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, round_h,
+                a.data(), b.data(), h.data(), o.data());
+        ffn_row_bwd(w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, gate[j],
+                    dyv.data(), a.data(), b.data(), o.data(), &dg[j], dO.data(), dh.data(),
+                    da.data(), db.data(), dxp.data());
+        if (dxt) for (int c = 0; c < D.d; ++c) dxt[c] += dxp[c];
+      }
+      if (dgate) for (int j = 0; j < D.k; ++j) dgate[i * D.k + j] = dg[j];
+      if (dlogits) {
+        double* dl = dlogits + i * D.E;
+        for (int e = 0; e < D.E; ++e) dl[e] = 0.0;
+        double sgd = 0.0;
+        for (int j = 0; j < D.k; ++j) sgd += gate[j] * dg[j];
+        for (int j = 0; j < D.k; ++j) dl[idx[j]] = gate[j] * (dg[j] - sgd);
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+// Weight gradients of selected experts, summed over every pair routed to them:
+//   dW1[e] = sum x^T da, dW3[e] = sum x^T db, dW2[e] = sum h^T dO.
+template <class V, class G>
+int backward_dw(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
+                const G* dy, const Dims& D, int round_h, const int32_t* experts, int n_exp,
+                double* dW1, double* dW3, double* dW2) {
+  const int64_t P = D.T * D.k;
+  std::vector<int32_t> idx(P);
+  std::vector<double> gate(P);
+  route_all(logits, D, idx.data(), gate.data());
+  for (int q = 0; q < n_exp; ++q) {
+    const int e = experts[q];
+    if (e < 0 || e >= D.E) return -1;
+    std::vector<int64_t> pairs;  // pairs routed to e, in token order
+    for (int64_t p = 0; p < P; ++p)
+      if (idx[p] == e) pairs.push_back(p);
+    const int64_t R = static_cast<int64_t>(pairs.size());
+    std::vector<double> A(R * D.dff), B(R * D.dff), H(R * D.dff), DO(R * D.d), DA(R * D.dff),
+        DB(R * D.dff);
+#pragma omp parallel
+    {
+      std::vector<double> o(D.d), dyv(D.d), dh(D.dff), dxp(D.d);
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t r = 0; r < R; ++r) {
+        const int64_t p = pairs[r], t = p / D.k;
+        ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, round_h,
+                &A[r * D.dff], &B[r * D.dff], &H[r * D.dff], o.data());
+        for (int c = 0; c < D.d; ++c) dyv[c] = widen(dy[t * D.d + c]);
+        double dg;
+        ffn_row_bwd(w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, gate[p], dyv.data(),
+                    &A[r * D.dff], &B[r * D.dff], o.data(), &dg, &DO[r * D.d], dh.data(),
+                    &DA[r * D.dff], &DB[r * D.dff], dxp.data());
+      }
+    }
+    double* g1 = dW1 + static_cast<int64_t>(q) * D.d * D.dff;
+    double* g3 = dW3 + static_cast<int64_t>(q) * D.d * D.dff;
+    double* g2 = dW2 + static_cast<int64_t>(q) * D.dff * D.d;
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < D.d; ++c) {
+      double* r1 = g1 + static_cast<int64_t>(c) * D.dff;
+      double* r3 = g3 + static_cast<int64_t>(c) * D.dff;
+      for (int f = 0; f < D.dff; ++f) { r1[f] = 0.0; r3[f] = 0.0; }
+      for (int64_t r = 0; r < R; ++r) {
+        const double xc = widen(x[(pairs[r] / D.k) * D.d + c]);
+        for (int f = 0; f < D.dff; ++f) {
+          r1[f] += xc * DA[r * D.dff + f];
+          r3[f] += xc * DB[r * D.dff + f];
+        }
+      }
+    }
+#pragma omp parallel for schedule(static)
+    for (int f = 0; f < D.dff; ++f) {
+      double* r2 = g2 + static_cast<int64_t>(f) * D.d;
+      for (int c = 0; c < D.d; ++c) r2[c] = 0.0;
+      for (int64_t r = 0; r < R; ++r) {
+        const double hf = H[r * D.dff + f];
+        for (int c = 0; c < D.d; ++c) r2[c] += hf * DO[r * D.d + c];
+      }
+    }
+  }
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_num_threads(void) { return omp_get_max_threads(); }
+
+double oracle_round_bf16(double v) { return round_bf16(v); }
+
+int oracle_route(const double* logits, int64_t T, int E, int k, int32_t* idx, double* gate) {
+  if (!dims_ok(T, 1, E, k, 1)) return -1;
+  Dims D{T, 1, E, k, 1};
+  route_all(logits, D, idx, gate);
+  return 0;
+}
+
+int oracle_dispatch(const int32_t* idx, int64_t T, int E, int k, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, int32_t* pos) {
+  if (!dims_ok(T, 1, E, k, 1)) return -1;
+  for (int64_t p = 0; p < T * k; ++p)
+    if (idx[p] < 0 || idx[p] >= E) return -1;
+  Dims D{T, 1, E, k, 1};
+  dispatch_all(idx, D, counts, offsets, perm, pos);
+  return 0;
+}
+
+#define ORACLE_DIMS int64_t T, int d, int E, int k, int dff
+
+int oracle_forward_tokens_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
+                               const uint16_t* W3, const uint16_t* W2, ORACLE_DIMS, int round_h,
+                               const int64_t* tokens, int64_t n, double* y) {
+  if (!dims_ok(T, d, E, k, dff)) return -1;
+  return forward_tokens(x, logits, W1, W3, W2, Dims{T, d, E, k, dff}, round_h, tokens, n, y);
+}
+
+int oracle_forward_tokens_f64(const double* x, const double* logits, const double* W1,
+                              const double* W3, const double* W2, ORACLE_DIMS, int round_h,
+                              const int64_t* tokens, int64_t n, double* y) {
+  if (!dims_ok(T, d, E, k, dff)) return -1;
+  return forward_tokens(x, logits, W1, W3, W2, Dims{T, d, E, k, dff}, round_h, tokens, n, y);
+}
+
+int oracle_forward_permuted_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
+                                 const uint16_t* W3, const uint16_t* W2, ORACLE_DIMS, int round_h,
+                                 double* y, uint16_t* x_perm, double* o_perm) {
+  if (!dims_ok(T, d, E, k, dff)) return -1;
+  return forward_permuted(x, logits, W1, W3, W2, Dims{T, d, E, k, dff}, round_h, y, x_perm,
+                          o_perm);
+}
+
+int oracle_backward_tokens_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
+                                const uint16_t* W3, const uint16_t* W2, const uint16_t* dy,
+                                ORACLE_DIMS, int round_h, const int64_t* tokens, int64_t n,
+                                double* dx, double* dgate, double* dlogits) {
+  if (!dims_ok(T, d, E, k, dff)) return -1;
+  return backward_tokens(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, tokens, n,
+                         dx, dgate, dlogits);
+}
+
+int oracle_backward_tokens_f64(const double* x, const double* logits, const double* W1,
+                               const double* W3, const double* W2, const double* dy, ORACLE_DIMS,
+                               int round_h, const int64_t* tokens, int64_t n, double* dx,
+                               double* dgate, double* dlogits) {
+  if (!dims_ok(T, d, E, k, dff)) return -1;
+  return backward_tokens(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, tokens, n,
+                         dx, dgate, dlogits);
+}
+
+int oracle_backward_dw_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
+                            const uint16_t* W3, const uint16_t* W2, const uint16_t* dy,
+                            ORACLE_DIMS, int round_h, const int32_t* experts, int n_exp,
+                            double* dW1, double* dW3, double* dW2) {
+  if (!dims_ok(T, d, E, k, dff)) return -1;
+  return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, experts, n_exp,
+                     dW1, dW3, dW2);
+}
+
+int oracle_backward_dw_f64(const double* x, const double* logits, const double* W1,
+                           const double* W3, const double* W2, const double* dy, ORACLE_DIMS,
+                           int round_h, const int32_t* experts, int n_exp, double* dW1,
+                           double* dW3, double* dW2) {
+  if (!dims_ok(T, d, E, k, dff)) return -1;
+  return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, experts, n_exp,
+                     dW1, dW3, dW2);
+}
+
+}  // extern "C"
