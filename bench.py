@@ -1,0 +1,362 @@
+"""Benchmark of the MoE expert layer (one GB300 per process).
+
+A step is one moe_forward over one batch of the large skewed workload (T=16384 tokens,
+d=7168, E=256 experts, top-8, d_ff=2048, router logits with a Zipf(1.2) bias): routing,
+dispatch, grouped GEMM1 + SwiGLU, grouped GEMM2 and the fp32 combine, all in libmoe.so.
+Inputs are synthetic (moe_synth) and resident in HBM; the 22.5 GB of expert weights are far
+larger than the 129 MB L2, so no L2 flush is needed between steps.
+
+Prints one JSON line (rank 0).  With --gpus N > 1 (under torchrun) every rank runs an
+independent replica on its own GPU (the layer does not shard); value = all tokens / the
+slowest rank's time.  --impl reference times the fp64 CPU oracle instead, on a bounded
+sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import moe_synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s; grouped-GEMM bf16 TFLOP/s and dispatch GB/s as % of peak"
+UNIT = "tokens/s"
+WORKLOAD = "large_skewed"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"],
+                    bf16_sustained=p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def _workload_config(w):
+    return {"workload": "%s: T=%d d=%d E=%d top-%d d_ff=%d, logits N(0,1) - %.1f ln(e+1)"
+                        % (w.name, w.T, w.d, w.E, w.k, w.dff, w.zipf_s),
+            "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.dff,
+            "l2": "inputs larger than L2 (22.5 GB of expert weights read every step)",
+            "parallelism": "replicas (one independent layer per GPU)"}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm.append(float(parts[1]))
+                        mx.append(float(parts[2]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, parts[5:9]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _algorithmic(w, P):
+    d, dff, T, E, k = w.d, w.dff, w.T, w.E, w.k
+    return dict(
+        gemm_flops=6 * d * dff * P,             # 6 d dff per token-expert pair
+        gemm1_flops=4 * d * dff * P,            # gate + up projections
+        gemm2_flops=2 * d * dff * P,            # down projection
+        # logits read; topk, gate, pos, perm written; x read; x_perm written
+        dispatch_bytes=T * E * 4 + T * k * 16 + T * d * 2 + P * d * 2,
+        # fp32 expert-output rows read; gate + pos read; out written (bf16)
+        combine_bytes=P * d * 4 + T * k * 8 + T * d * 2,
+    )
+
+
+def _traffic_of(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the kernel source
+    has not changed since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        import hashlib
+        h = hashlib.sha256()
+        for name in rec["sources"]:
+            with open(os.path.join(ROOT, name), "rb") as g:
+                h.update(g.read())
+        if h.hexdigest() != rec["source_sha256"]:
+            return None
+        return rec["kernels"].get(kernel, {}).get("traffic_per_launch_full_workload")
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def run_cpu_baseline(w, inp_np, budget_s=15.0):
+    import oracle
+    cores = oracle.num_threads()
+    tok_all = np.random.default_rng(0).permutation(w.T)
+    n = 8
+    t0 = time.perf_counter()
+    oracle.forward_tokens(inp_np, w.k, tokens=tok_all[:n])
+    dt = time.perf_counter() - t0
+    n2 = int(max(n, min(w.T, n * budget_s / max(dt, 1e-3))))
+    t0 = time.perf_counter()
+    oracle.forward_tokens(inp_np, w.k, tokens=tok_all[:n2])
+    dt2 = time.perf_counter() - t0
+    return {"value": n2 / dt2, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d random tokens of the %s workload, fp64, %.1f s" % (n2, w.name, dt2)}
+
+
+def bench_reference(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    g = moe_synth.generate(w, device=dev)
+    inp = moe_synth.to_numpy(g)
+    del g
+    import oracle
+    cores = oracle.num_threads()
+    rng = np.random.default_rng(0)
+    per_step = 16
+    for _ in range(args.warmup):
+        oracle.forward_tokens(inp, w.k, tokens=rng.choice(w.T, per_step, replace=False))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward_tokens(inp, w.k, tokens=rng.choice(w.T, per_step, replace=False))
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "%d random tokens per step of the %s workload"
+                                       % (per_step, w.name)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_native(args, w):
+    import combine_fp32_router_gb300 as moe
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    g = moe_synth.generate(w, device=dev)
+    T, d, E, k, dff = w.T, w.d, w.E, w.k, w.dff
+    ws = torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, False), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nev = moe.MOE_FWD_NUM_EVENTS
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+
+    def step(ev=None):
+        moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+                        stage_events=ev, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = moe.moe_get_error(ws)
+    if st != 0:
+        raise RuntimeError("device error during warm-up: " + moe.moe_status_string(st))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        barrier()
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    st = moe.moe_get_error(ws)
+    if st != 0:
+        raise RuntimeError("device error: " + moe.moe_status_string(st))
+
+    stage_ms = [0.0] * (nev - 1)
+    for e in evs:
+        for j in range(nev - 1):
+            stage_ms[j] += e[j].elapsed_time(e[j + 1])
+    stage_ms = [s / args.steps for s in stage_ms]
+    P = T * k
+    alg = _algorithmic(w, P)
+    peaks = _peaks()
+    ms_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+
+    # end to end through the public API with pinned host buffers: H2D of x and logits,
+    # the layer, D2H of the output, every step
+    hx = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
+    hl = torch.empty(T, E, dtype=torch.float32, pin_memory=True)
+    ho = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(g["x"])
+    hl.copy_(g["logits"])
+    dx = torch.empty_like(g["x"])
+    dl = torch.empty_like(g["logits"])
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dl.copy_(hl, non_blocking=True)
+        moe.moe_forward(dx, dl, g["W1"], g["W3"], g["W2"], k, out, ws, stream=stream)
+        ho.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    stop.record(stream)
+    barrier()
+    ms_e2e = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e = {"value": world * T * args.steps / (ms_e2e / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4,
+           "d2h_bytes_per_step": ho.numel() * 2}
+
+    names = ["dispatch", "gemm1_swiglu", "gemm2", "combine"]
+    stages = dict(zip(names, stage_ms))
+    g1_tflops = alg["gemm1_flops"] / (stages["gemm1_swiglu"] * 1e-3) / 1e12
+    g_tflops = alg["gemm_flops"] / ((stages["gemm1_swiglu"] + stages["gemm2"]) * 1e-3) / 1e12
+    disp_gbs = alg["dispatch_bytes"] / (stages["dispatch"] * 1e-3) / 1e9
+    comb_gbs = alg["combine_bytes"] / (stages["combine"] * 1e-3) / 1e9
+    peak = peaks["bf16_sustained"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _workload_config(w),
+        "e2e": e2e,
+        "roofline": {"kernel": "grouped GEMM1 + SwiGLU (tcgen05)", "bound": "tensor",
+                     "achieved": g1_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": g1_tflops / peak,
+                     "peak_source": "%s bf16 sustained (MEASURED_PEAKS.json)" % peaks["source"],
+                     "traffic": _traffic_of("gemm1")},
+        "stages_ms": stages,
+        "gemm_tflops": g_tflops,
+        "gemm_frac_of_bf16_burst": g_tflops / peaks["bf16"],
+        "dispatch_gbs": disp_gbs, "dispatch_frac_of_hbm": disp_gbs / peaks["hbm"],
+        "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
+        "clocks": clocks.summary(),
+        "gpu_launches": 8 * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del ws, out
+        torch.cuda.empty_cache()
+        line["cpu_baseline"] = run_cpu_baseline(w, moe_synth.to_numpy(g))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--shape", default=None,
+                    help="T,d,E,k,d_ff of a custom workload (profiling captures of one kernel)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.shape:
+        T, d, E, k, dff = (int(v) for v in args.shape.split(","))
+        w = moe_synth.custom(T, d, E, k, dff, seed=1003, zipf_s=1.2, name="custom")
+    else:
+        w = moe_synth.by_name(args.workload)
+    if args.impl == "reference":
+        return bench_reference(args, w)
+    return bench_native(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

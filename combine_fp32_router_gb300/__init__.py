@@ -1,0 +1,163 @@
+"""Python binding of libmoe.so: one MoE expert layer on one GB300 GPU.
+
+The functions below carry the names of the C entry points in ``include/moe.h`` and only
+marshal arguments: they read sizes and device pointers off torch tensors, pass the current
+CUDA stream, and turn a non-zero status into ``MoeError``.  Every step of the layer runs in
+the library's CUDA kernels; there is no fallback.  torch provides device memory, streams
+and events only.
+
+Import fails loudly when ``libmoe.so`` has not been built (``build.build()``).
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_DEVICE_BOUNDS = 6
+MOE_FWD_SAVE_FOR_BACKWARD = 1
+MOE_FWD_NUM_EVENTS = 5
+MOE_BWD_NUM_EVENTS = 7
+
+# Exported symbols of include/moe.h, in declaration order.
+EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispatch",
+           "moe_forward", "moe_backward", "moe_get_error", "moe_set_wait_timeout_ns",
+           "moe_debug_set_flags", "moe_status_string")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, moe_status_string(status), status))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libmoe.so is missing: build it with "
+                          "combine_fp32_router_gb300.build.build() (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    p, i, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.moe_route_workspace_bytes.argtypes = [i64, i, i]
+    lib.moe_route_workspace_bytes.restype = sz
+    lib.moe_workspace_bytes.argtypes = [i64, i, i, i, i, i]
+    lib.moe_workspace_bytes.restype = sz
+    lib.moe_route_dispatch.argtypes = [p, p, i64, i, i, i] + [p] * 7 + [p, sz, p]
+    lib.moe_route_dispatch.restype = i
+    lib.moe_forward.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i, p, p]
+    lib.moe_forward.restype = i
+    lib.moe_backward.argtypes = [p] * 6 + [i64, i, i, i, i] + [p] * 6 + [p, sz, p, p]
+    lib.moe_backward.restype = i
+    lib.moe_get_error.argtypes = [p, p]
+    lib.moe_get_error.restype = i
+    lib.moe_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.moe_set_wait_timeout_ns.restype = None
+    lib.moe_debug_set_flags.argtypes = [i]
+    lib.moe_debug_set_flags.restype = None
+    lib.moe_status_string.argtypes = [i]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _events(events):
+    if events is None:
+        return None
+    handles = []
+    for ev in events:
+        if not ev.cuda_event:       # torch creates the CUDA event lazily on first record
+            ev.record()
+        handles.append(ev.cuda_event)
+    return (ctypes.c_void_p * len(handles))(*handles)
+
+
+def _check(st, where):
+    if st != MOE_OK:
+        raise MoeError(st, where)
+
+
+def moe_status_string(status):
+    return _lib.moe_status_string(int(status)).decode()
+
+
+def moe_route_workspace_bytes(T, E, k):
+    return int(_lib.moe_route_workspace_bytes(T, E, k))
+
+
+def moe_workspace_bytes(T, d, E, k, d_ff, with_backward=False):
+    return int(_lib.moe_workspace_bytes(T, d, E, k, d_ff, int(bool(with_backward))))
+
+
+def moe_route_dispatch(x, logits, k, topk_idx, gate, counts, offsets, perm, pos, x_perm, ws,
+                       stream=None):
+    """Routing + counts + offsets + stable permute into caller-owned outputs."""
+    T, d = x.shape
+    E = logits.shape[1]
+    _check(_lib.moe_route_dispatch(_ptr(x), _ptr(logits), T, d, E, k, _ptr(topk_idx),
+                                   _ptr(gate), _ptr(counts), _ptr(offsets), _ptr(perm),
+                                   _ptr(pos), _ptr(x_perm), _ptr(ws), _nbytes(ws),
+                                   _stream(stream)), "moe_route_dispatch")
+
+
+def moe_forward(x, logits, W1, W3, W2, k, out, ws, flags=0, stage_events=None, stream=None):
+    """Whole-layer forward into ``out`` [T, d] bf16."""
+    T, d = x.shape
+    E, _, d_ff = W1.shape
+    _check(_lib.moe_forward(_ptr(x), _ptr(logits), _ptr(W1), _ptr(W3), _ptr(W2), T, d, E, k,
+                            d_ff, _ptr(out), _ptr(ws), _nbytes(ws), int(flags),
+                            _events(stage_events), _stream(stream)), "moe_forward")
+
+
+def moe_backward(dy, x, logits, W1, W3, W2, k, dx, dW1, dW3, dW2, dgate, dlogits, ws,
+                 stage_events=None, stream=None):
+    """Whole-layer backward (after moe_forward with MOE_FWD_SAVE_FOR_BACKWARD on ``ws``)."""
+    T, d = x.shape
+    E, _, d_ff = W1.shape
+    _check(_lib.moe_backward(_ptr(dy), _ptr(x), _ptr(logits), _ptr(W1), _ptr(W3), _ptr(W2), T,
+                             d, E, k, d_ff, _ptr(dx), _ptr(dW1), _ptr(dW3), _ptr(dW2),
+                             _ptr(dgate), _ptr(dlogits), _ptr(ws), _nbytes(ws),
+                             _events(stage_events), _stream(stream)), "moe_backward")
+
+
+def moe_get_error(ws, stream=None):
+    """Synchronise the stream and return the device error status recorded in ``ws``."""
+    return int(_lib.moe_get_error(_ptr(ws), _stream(stream)))
+
+
+def moe_set_wait_timeout_ns(ns):
+    _lib.moe_set_wait_timeout_ns(int(ns))
+
+
+def moe_debug_set_flags(flags):
+    _lib.moe_debug_set_flags(int(flags))
+
+
+def library():
+    """The loaded ctypes library (for callers that want the raw C ABI)."""
+    return _lib

@@ -1,0 +1,101 @@
+// Forward grouped GEMMs: GEMM1 + SwiGLU (H) and GEMM2 (Y), plus the tensor-map helpers.
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace moe {
+
+void* tensor_map_encoder() {
+  static void* fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = f;
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map with 128-byte swizzle: `rows` rows of `inner` elements, row pitch
+// `row_bytes`; box of box_inner x box_rows elements (box_inner * 2 == 128 bytes).
+CUtensorMap make_map_2d(const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_rows, cudaError_t* st) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof m);
+  auto enc = reinterpret_cast<Encode>(tensor_map_encoder());
+  if (!enc) {
+    *st = cudaErrorNotSupported;
+    return m;
+  }
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) *st = cudaErrorInvalidValue;
+  return m;
+}
+
+GemmParams base_params(const GemmCtx& c) {
+  const WsLayout& L = *c.L;
+  GemmParams p{};
+  p.E = L.E;
+  p.d = L.d;
+  p.dff = L.dff;
+  p.n_mt = reinterpret_cast<const int32_t*>(c.ws + L.n_mt);
+  p.mt_expert = reinterpret_cast<const int32_t*>(c.ws + L.mt_expert);
+  p.mt_row0 = reinterpret_cast<const int32_t*>(c.ws + L.mt_row0);
+  p.counts = reinterpret_cast<const int32_t*>(c.ws + L.counts);
+  p.poff = reinterpret_cast<const int32_t*>(c.ws + L.poff);
+  p.err = c.err;
+  p.wait_ns = c.wait_ns;
+  p.debug_flags = c.debug_flags;
+  p.rows_cap = L.P_pad;
+  return p;
+}
+
+cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
+  const WsLayout& L = *c.L;
+  cudaError_t st = cudaSuccess;
+  const CUtensorMap a = make_map_2d(c.ws + L.xperm, L.d, L.P_pad, 2ull * L.d, 64, 128, &st);
+  const CUtensorMap b0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 64, &st);
+  const CUtensorMap b1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 64, &st);
+  if (st != cudaSuccess) return st;
+  GemmParams p = base_params(c);
+  p.nb = L.dff / 128;  // 128 h columns per tile (W1 half + W3 half = 256 accumulator columns)
+  p.nkb = L.d / kBK;
+  p.out0 = c.ws + L.H;
+  p.save_ab = c.save_ab;
+  p.save_a = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Asave) : nullptr;
+  p.save_b = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Bsave) : nullptr;
+  return run_grouped_gemm<kFwd1, 256>(a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
+}
+
+cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
+  const WsLayout& L = *c.L;
+  cudaError_t st = cudaSuccess;
+  const CUtensorMap a = make_map_2d(c.ws + L.H, L.dff, L.P_pad, 2ull * L.dff, 64, 128, &st);
+  const CUtensorMap b0 = make_map_2d(c.W2, L.d, static_cast<uint64_t>(L.E) * L.dff, 2ull * L.d, 64, 64, &st);
+  if (st != cudaSuccess) return st;
+  GemmParams p = base_params(c);
+  p.nkb = L.dff / kBK;
+  p.out0 = c.ws + L.Y;
+  if (L.d % 256 == 0) {
+    p.nb = L.d / 256;
+    return run_grouped_gemm<kFwd2, 256>(a, b0, b0, p, L.max_mt * p.nb, c.num_sms, s);
+  }
+  p.nb = L.d / 128;
+  return run_grouped_gemm<kFwd2, 128>(a, b0, b0, p, L.max_mt * p.nb, c.num_sms, s);
+}
+
+}  // namespace moe

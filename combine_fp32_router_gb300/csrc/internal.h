@@ -1,0 +1,80 @@
+// Host-side declarations shared between the translation units of libmoe.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kRouteTokensPerBlock = 128;  // tokens per routing CTA (4 warps x 32 tokens)
+constexpr int kTileRows = 128;             // rows of one expert GEMM tile; padded row unit
+constexpr int kMaxK = 16;
+constexpr int kMaxE = 1024;
+
+struct DevErr;
+
+// Workspace carve-up (byte offsets from ws, each 256-byte aligned).
+struct WsLayout {
+  int64_t T = 0, P = 0, P_pad = 0, max_mt = 0, nblk = 0;
+  int d = 0, E = 0, k = 0, dff = 0;
+  size_t err = 0, hist = 0, bbase = 0, counts = 0, offsets = 0, poff = 0, n_mt = 0,
+         mt_expert = 0, mt_row0 = 0, topk = 0, gate = 0, pos = 0, perm = 0, xperm = 0, H = 0,
+         Y = 0, Asave = 0, Bsave = 0, dO = 0, dAB = 0, dXp = 0;
+  size_t route_total = 0, fwd_total = 0, bwd_total = 0;
+};
+
+WsLayout make_layout(int64_t T, int d, int E, int k, int dff);
+
+// ---- routing / dispatch / combine launches (route.cu) -----------------------------------
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* topk,
+                              float* gate, int32_t* pos_local, int32_t* hist, DevErr* err,
+                              cudaStream_t s);
+cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* bbase,
+                             int32_t* counts, cudaStream_t s);
+// offsets (unpadded, may be null), poff (rows padded to `align`), and when align == 128
+// the 128-row tile tables (n_mt, mt_expert, mt_row0).
+cudaError_t launch_offsets(const int32_t* counts, int E, int align, int32_t* offsets,
+                           int32_t* poff, int32_t* n_mt, int32_t* mt_expert, int32_t* mt_row0,
+                           int64_t max_mt, DevErr* err, cudaStream_t s);
+cudaError_t launch_scatter(const uint16_t* x, int64_t T, int d, int E, int k,
+                           const int32_t* topk, const int32_t* bbase, const int32_t* poff,
+                           int32_t* pos, int32_t* perm, uint16_t* x_perm, int64_t rows_cap,
+                           DevErr* err, cudaStream_t s);
+// Padding rows of every expert segment: perm = -1 and (if rows != null) zero bytes.
+cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, int32_t* perm,
+                            void* rows, int64_t row_bytes, cudaStream_t s);
+cudaError_t launch_combine(const float* y_rows, const float* gate, const int32_t* pos,
+                           int64_t T, int k, int d, uint16_t* out, cudaStream_t s);
+cudaError_t launch_bwd_gate(const uint16_t* dy, const float* y_rows, const float* gate,
+                            const int32_t* pos, const int32_t* topk, int64_t T, int k, int d,
+                            int E, uint16_t* dO_rows, float* dgate, float* dlogits,
+                            cudaStream_t s);
+cudaError_t launch_combine_f32(const float* rows, const int32_t* pos, int64_t T, int k, int d,
+                               uint16_t* out, cudaStream_t s);
+
+// ---- grouped GEMMs (gemm_fwd.cu, gemm_bwd.cu) ------------------------------------------
+struct GemmCtx {
+  const WsLayout* L;
+  char* ws;
+  const uint16_t *x, *W1, *W3, *W2;
+  float *dW1, *dW3, *dW2;
+  int save_ab;
+  DevErr* err;
+  uint64_t wait_ns;
+  int debug_flags;
+  int num_sms;
+};
+cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s);   // H = SwiGLU(Xp W1, Xp W3)
+cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s);   // Y = H W2
+cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s);     // dA,dB from dO W2^T
+cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s);     // dXp = dA W1^T + dB W3^T
+cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s);    // dW2 = H^T dO
+cudaError_t launch_gemm_dw13(const GemmCtx& c, cudaStream_t s);   // dW1|dW3 = Xp^T [dA|dB]
+
+// tensor-map encoder from the driver, resolved once
+void* tensor_map_encoder();
+
+}  // namespace moe

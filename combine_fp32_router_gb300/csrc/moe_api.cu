@@ -1,0 +1,325 @@
+// C ABI of libmoe.so (declared in include/moe.h): argument validation on the host, the
+// workspace carve-up, and the launch sequence of each entry point on the caller's stream.
+// The host path does no allocation and no synchronisation (except moe_get_error); the
+// checks are plain integer tests, in the spirit of the report translation's section 2.1
+// (itsolotime.com): argument checking belongs in compiled host code, not in Python.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+std::atomic<int> g_debug_flags{0};
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by every entry point.  `need_gemm` adds the tile-shape constraints of the
+// expert GEMMs (d and d_ff multiples of 128).
+moe_status_t check_dims(int64_t T, int d, int E, int k, int dff, bool need_gemm) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || (need_gemm && dff <= 0))
+    return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || k > kMaxK || d > 65536 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (need_gemm && (d % 128 != 0 || dff % 128 != 0 || dff > 65536)) return MOE_ERR_UNSUPPORTED;
+  if (T > (int64_t{1} << 31) / k) return MOE_ERR_UNSUPPORTED;
+  if (T * k + static_cast<int64_t>(kTileRows) * E >= (int64_t{1} << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int num_sms_of_current_device() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                                    \
+  do {                                                   \
+    const cudaError_t e_ = (expr);                       \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA;          \
+  } while (0)
+
+void record(cudaEvent_t* ev, int i, cudaStream_t s) {
+  if (ev && ev[i]) cudaEventRecord(ev[i], s);
+}
+
+}  // namespace
+
+WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
+  WsLayout L;
+  L.T = T;
+  L.d = d;
+  L.E = E;
+  L.k = k;
+  L.dff = dff;
+  L.P = T * k;
+  L.nblk = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  // every non-empty expert segment is padded to a multiple of 128 rows
+  const int64_t busy = L.P < E ? L.P : E;
+  L.P_pad = round_up(static_cast<size_t>(L.P + (kTileRows - 1) * busy), kTileRows);
+  L.max_mt = L.P_pad / kTileRows;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += round_up(bytes ? bytes : 1, 256);
+    return o;
+  };
+  const size_t P = static_cast<size_t>(L.P), Pp = static_cast<size_t>(L.P_pad);
+  L.err = take(sizeof(DevErr));
+  L.hist = take(static_cast<size_t>(L.nblk) * E * 4);
+  L.bbase = take(static_cast<size_t>(L.nblk) * E * 4);
+  L.route_total = off;
+  L.counts = take(static_cast<size_t>(E) * 4);
+  L.offsets = take(static_cast<size_t>(E + 1) * 4);
+  L.poff = take(static_cast<size_t>(E + 1) * 4);
+  L.n_mt = take(16);
+  L.mt_expert = take(static_cast<size_t>(L.max_mt) * 4);
+  L.mt_row0 = take(static_cast<size_t>(L.max_mt) * 4);
+  L.topk = take(P * 4);
+  L.gate = take(P * 4);
+  L.pos = take(P * 4);
+  L.perm = take(Pp * 4);
+  L.xperm = take(Pp * d * 2);
+  L.H = take(Pp * dff * 2);
+  L.Y = take(Pp * d * 4);
+  L.fwd_total = off;
+  L.Asave = take(Pp * dff * 4);
+  L.Bsave = take(Pp * dff * 4);
+  L.dO = take(Pp * d * 2);
+  L.dAB = take(Pp * 2 * dff * 2);
+  L.dXp = take(Pp * d * 4);
+  L.bwd_total = off;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_route_workspace_bytes(int64_t T, int E, int k) {
+  if (check_dims(T, 8, E, k, 0, false) != MOE_OK) return 0;
+  return make_layout(T, 8, E, k, 128).route_total;
+}
+
+size_t moe_workspace_bytes(int64_t T, int d, int E, int k, int d_ff, int with_backward) {
+  if (check_dims(T, d, E, k, d_ff, true) != MOE_OK) return 0;
+  const WsLayout L = make_layout(T, d, E, k, d_ff);
+  return with_backward ? L.bwd_total : L.fwd_total;
+}
+
+moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_t T, int d,
+                                int E, int k, int32_t* topk_idx, float* gate, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, int32_t* pos,
+                                moe_bf16_t* x_perm, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
+  moe_status_t st = check_dims(T, d, E, k, 0, false);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets || !ws) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !logits || !topk_idx || !gate || !perm || !pos || !x_perm))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, logits, topk_idx, gate, counts, offsets, perm, pos, x_perm};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_layout(T, d, E, k, 128);
+  if (ws_bytes < L.route_total) return MOE_ERR_WORKSPACE;
+
+  char* w = static_cast<char*>(ws);
+  DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
+  if (T == 0) {
+    MOE_TRY(cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, stream));
+    MOE_TRY(cudaMemsetAsync(offsets, 0, static_cast<size_t>(E + 1) * 4, stream));
+    return MOE_OK;
+  }
+  int32_t* hist = reinterpret_cast<int32_t*>(w + L.hist);
+  int32_t* bbase = reinterpret_cast<int32_t*>(w + L.bbase);
+  MOE_TRY(launch_route_topk(logits, T, E, k, topk_idx, gate, pos, hist, err, stream));
+  MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
+  // unpadded rows: the padded offsets are the offsets themselves
+  MOE_TRY(launch_offsets(counts, E, 1, nullptr, offsets, nullptr, nullptr, nullptr, 0, err,
+                         stream));
+  MOE_TRY(launch_scatter(x, T, d, E, k, topk_idx, bbase, offsets, pos, perm, x_perm, L.P, err,
+                         stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf16_t* W1,
+                         const moe_bf16_t* W3, const moe_bf16_t* W2, int64_t T, int d, int E,
+                         int k, int d_ff, moe_bf16_t* out, void* ws, size_t ws_bytes, int flags,
+                         cudaEvent_t* stage_events, cudaStream_t stream) {
+  moe_status_t st = check_dims(T, d, E, k, d_ff, true);
+  if (st != MOE_OK) return st;
+  if (!W1 || !W3 || !W2 || !ws) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
+  if (flags & ~MOE_FWD_SAVE_FOR_BACKWARD) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, logits, W1, W3, W2, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  const bool save = (flags & MOE_FWD_SAVE_FOR_BACKWARD) != 0;
+  const WsLayout L = make_layout(T, d, E, k, d_ff);
+  if (ws_bytes < (save ? L.bwd_total : L.fwd_total)) return MOE_ERR_WORKSPACE;
+
+  char* w = static_cast<char*>(ws);
+  DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
+  record(stage_events, 0, stream);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
+  if (T == 0) {
+    for (int i = 1; i < MOE_FWD_NUM_EVENTS; ++i) record(stage_events, i, stream);
+    return MOE_OK;
+  }
+  int32_t* hist = reinterpret_cast<int32_t*>(w + L.hist);
+  int32_t* bbase = reinterpret_cast<int32_t*>(w + L.bbase);
+  int32_t* counts = reinterpret_cast<int32_t*>(w + L.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  int32_t* poff = reinterpret_cast<int32_t*>(w + L.poff);
+  int32_t* topk = reinterpret_cast<int32_t*>(w + L.topk);
+  float* gate = reinterpret_cast<float*>(w + L.gate);
+  int32_t* pos = reinterpret_cast<int32_t*>(w + L.pos);
+  int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
+  uint16_t* xperm = reinterpret_cast<uint16_t*>(w + L.xperm);
+
+  // dispatch: route, count, prefix sums (rows padded to 128 per expert), stable permute
+  MOE_TRY(launch_route_topk(logits, T, E, k, topk, gate, pos, hist, err, stream));
+  MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
+  MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff,
+                         reinterpret_cast<int32_t*>(w + L.n_mt),
+                         reinterpret_cast<int32_t*>(w + L.mt_expert),
+                         reinterpret_cast<int32_t*>(w + L.mt_row0), L.max_mt, err, stream));
+  MOE_TRY(launch_scatter(x, T, d, E, k, topk, bbase, poff, pos, perm, xperm, L.P_pad, err,
+                         stream));
+  // padding rows: perm = -1; zero x rows when the backward will read them as a K operand
+  MOE_TRY(launch_pad_rows(counts, poff, E, perm, save ? xperm : nullptr, 2ll * d, stream));
+  record(stage_events, 1, stream);
+
+  GemmCtx c{};
+  c.L = &L;
+  c.ws = w;
+  c.x = x;
+  c.W1 = W1;
+  c.W3 = W3;
+  c.W2 = W2;
+  c.save_ab = save ? 1 : 0;
+  c.err = err;
+  c.wait_ns = g_wait_ns.load();
+  c.debug_flags = g_debug_flags.load();
+  c.num_sms = num_sms_of_current_device();
+  MOE_TRY(launch_gemm_fwd1(c, stream));
+  record(stage_events, 2, stream);
+  MOE_TRY(launch_gemm_fwd2(c, stream));
+  record(stage_events, 3, stream);
+  MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,
+                         stream));
+  record(stage_events, 4, stream);
+  return MOE_OK;
+}
+
+moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float* logits,
+                          const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                          int64_t T, int d, int E, int k, int d_ff, moe_bf16_t* dx, float* dW1,
+                          float* dW3, float* dW2, float* dgate, float* dlogits, void* ws,
+                          size_t ws_bytes, cudaEvent_t* stage_events, cudaStream_t stream) {
+  moe_status_t st = check_dims(T, d, E, k, d_ff, true);
+  if (st != MOE_OK) return st;
+  if (!W1 || !W3 || !W2 || !dW1 || !dW3 || !dW2 || !ws) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!dy || !x || !logits || !dx || !dgate)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {dy, x, logits, W1, W3, W2, dx, dW1, dW3, dW2, dgate, dlogits};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_layout(T, d, E, k, d_ff);
+  if (ws_bytes < L.bwd_total) return MOE_ERR_WORKSPACE;
+
+  char* w = static_cast<char*>(ws);
+  DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
+  record(stage_events, 0, stream);
+  if (T == 0) {
+    const size_t wb = static_cast<size_t>(E) * d * d_ff * 4;
+    MOE_TRY(cudaMemsetAsync(dW1, 0, wb, stream));
+    MOE_TRY(cudaMemsetAsync(dW3, 0, wb, stream));
+    MOE_TRY(cudaMemsetAsync(dW2, 0, wb, stream));
+    for (int i = 1; i < MOE_BWD_NUM_EVENTS; ++i) record(stage_events, i, stream);
+    return MOE_OK;
+  }
+  const int32_t* counts = reinterpret_cast<const int32_t*>(w + L.counts);
+  const int32_t* poff = reinterpret_cast<const int32_t*>(w + L.poff);
+  const int32_t* topk = reinterpret_cast<const int32_t*>(w + L.topk);
+  const float* gate = reinterpret_cast<const float*>(w + L.gate);
+  const int32_t* pos = reinterpret_cast<const int32_t*>(w + L.pos);
+  uint16_t* dO = reinterpret_cast<uint16_t*>(w + L.dO);
+
+  MOE_TRY(launch_bwd_gate(dy, reinterpret_cast<const float*>(w + L.Y), gate, pos, topk, T, k,
+                          d, E, dO, dgate, dlogits, stream));
+  MOE_TRY(launch_pad_rows(counts, poff, E, nullptr, dO, 2ll * d, stream));
+  record(stage_events, 1, stream);
+
+  GemmCtx c{};
+  c.L = &L;
+  c.ws = w;
+  c.x = x;
+  c.W1 = W1;
+  c.W3 = W3;
+  c.W2 = W2;
+  c.dW1 = dW1;
+  c.dW3 = dW3;
+  c.dW2 = dW2;
+  c.err = err;
+  c.wait_ns = g_wait_ns.load();
+  c.debug_flags = g_debug_flags.load();
+  c.num_sms = num_sms_of_current_device();
+  MOE_TRY(launch_gemm_dh(c, stream));
+  record(stage_events, 2, stream);
+  MOE_TRY(launch_gemm_dx(c, stream));
+  record(stage_events, 3, stream);
+  MOE_TRY(launch_combine_f32(reinterpret_cast<const float*>(w + L.dXp), pos, T, k, d, dx,
+                             stream));
+  record(stage_events, 4, stream);
+  MOE_TRY(launch_gemm_dw2(c, stream));
+  record(stage_events, 5, stream);
+  MOE_TRY(launch_gemm_dw13(c, stream));
+  record(stage_events, 6, stream);
+  return MOE_OK;
+}
+
+moe_status_t moe_get_error(const void* ws, cudaStream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  DevErr e{};
+  if (cudaMemcpy(&e, ws, sizeof e, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status_t>(e.status);
+}
+
+void moe_set_wait_timeout_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : 1); }
+
+void moe_debug_set_flags(int flags) { g_debug_flags.store(flags); }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_BOUNDS: return "device-side index out of range";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

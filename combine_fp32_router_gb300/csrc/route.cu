@@ -1,0 +1,560 @@
+// Memory-bound kernels of the MoE layer: routing (top-k + softmax gate), per-expert
+// counting and exclusive prefix sums, the stable row permute (dispatch), padding rows, the
+// gate-weighted combine, and the per-token part of the backward.
+//
+// Dispatch -> Expert Compute -> Combine is the layer of "DeepSeek-V4 parallel strategy"
+// (blog.lpkt.cn, EP section).  On one GPU the combine reads the expert outputs as fp32 rows
+// and accumulates in fp32; the report translation's BF16 gather (itsolotime.com, section
+// 1.4) is a cross-GPU payload format and is not needed here.  Determinism follows the report's section 3
+// and the 10100.com reading: no floating-point atomics anywhere; counts come from
+// per-CTA shared-memory bit masks and histograms, positions from a fixed-order prefix sum,
+// and every floating-point reduction runs in a fixed order that depends only on d and k.
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------------------------ routing
+// Sortable key of (logit, expert): larger logit first, then lower index.  -0 is folded into
+// +0 so that the two compare equal (the lower index then wins), and the key of any real
+// entry is > 0 so that the padding entries (key 0) never win.
+__device__ __forceinline__ uint64_t route_key(float v, int e) {
+  if (v == 0.0f) v = 0.0f;
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - e);
+}
+__device__ __forceinline__ float key_value(uint64_t key) {
+  uint32_t u = static_cast<uint32_t>(key >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ int key_expert(uint64_t key) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+// One CTA = 128 consecutive tokens, 4 warps x 32 tokens.  Per token the warp holds the E
+// logits (EPL per lane) and runs k rounds of a warp arg-max.  Per warp chunk, a bit mask
+// per expert (bit i = token i of the chunk chose it) gives each pair its rank among the
+// chunk's earlier tokens; the masks' popcounts then give per-warp bases and the CTA's
+// histogram row.  pos_local receives the pair's rank among the CTA's tokens routed to the
+// same expert.
+template <int EPL>
+__global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict__ logits,
+                                                         int64_t T, int E, int k,
+                                                         int32_t* __restrict__ topk,
+                                                         float* __restrict__ gate,
+                                                         int32_t* __restrict__ pos_local,
+                                                         int32_t* __restrict__ hist) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* mask = sm;                                  // [4][E]
+  int32_t* wbase = reinterpret_cast<int32_t*>(sm + 4 * E);   // [4][E]
+  int32_t* tok_e = wbase + 4 * E;                       // [4][32][kMaxK]
+  int32_t* tok_r = tok_e + 4 * 32 * kMaxK;              // [4][32][kMaxK]
+
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 4 * E; i += blockDim.x) mask[i] = 0u;
+  __syncthreads();
+
+  const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * kRouteTokensPerBlock + w * 32;
+  int32_t* my_e = tok_e + w * 32 * kMaxK;
+  int32_t* my_r = tok_r + w * 32 * kMaxK;
+
+  for (int i = 0; i < 32; ++i) {
+    const int64_t t = tok0 + i;
+    if (t >= T) break;
+    const float* lt = logits + t * E;
+    uint64_t key[EPL];
+#pragma unroll
+    for (int c = 0; c < EPL; ++c) {
+      const int e = lane + 32 * c;
+      key[c] = (e < E) ? route_key(__ldg(lt + e), e) : 0ull;
+    }
+    int sel_e = 0;
+    float sel_v = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      uint64_t best = 0ull;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) best = key[c] > best ? key[c] : best;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+        best = o > best ? o : best;
+      }
+      const int ew = key_expert(best);
+#pragma unroll
+      for (int c = 0; c < EPL; ++c)
+        if (lane + 32 * c == ew) key[c] = 0ull;
+      if (lane == j) {
+        sel_e = ew;
+        sel_v = key_value(best);
+      }
+    }
+    // softmax over the k selected logits, fp32, summed in slot order
+    const float v0 = __shfl_sync(0xFFFFFFFFu, sel_v, 0);
+    const float ex = (lane < k) ? expf(sel_v - v0) : 0.0f;
+    float s = 0.0f;
+    for (int j = 0; j < k; ++j) s += __shfl_sync(0xFFFFFFFFu, ex, j);
+    if (lane < k) {
+      topk[t * k + lane] = sel_e;
+      gate[t * k + lane] = ex / s;
+      my_e[i * kMaxK + lane] = sel_e;
+    }
+  }
+  __syncwarp();
+  // ranks inside the warp's 32-token chunk
+  const int64_t t = tok0 + lane;
+  const bool valid = t < T;
+  if (valid)
+    for (int j = 0; j < k; ++j) atomicOr(&mask[w * E + my_e[lane * kMaxK + j]], 1u << lane);
+  __syncwarp();
+  if (valid)
+    for (int j = 0; j < k; ++j)
+      my_r[lane * kMaxK + j] =
+          __popc(mask[w * E + my_e[lane * kMaxK + j]] & ((1u << lane) - 1u));
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int ww = 0; ww < 4; ++ww) {
+      wbase[ww * E + e] = run;
+      run += __popc(mask[ww * E + e]);
+    }
+    hist[static_cast<int64_t>(blockIdx.x) * E + e] = run;
+  }
+  __syncthreads();
+  if (valid)
+    for (int j = 0; j < k; ++j) {
+      const int e = my_e[lane * kMaxK + j];
+      pos_local[t * k + j] = wbase[w * E + e] + my_r[lane * kMaxK + j];
+    }
+}
+
+// Column prefix over the routing CTAs: bbase[b][e] = sum_{b' < b} hist[b'][e], counts[e].
+// One CTA per 32 experts; warp w owns a contiguous range of routing CTAs.
+__global__ void __launch_bounds__(256) scan_cols_kernel(const int32_t* __restrict__ hist,
+                                                        int64_t nblk, int E,
+                                                        int32_t* __restrict__ bbase,
+                                                        int32_t* __restrict__ counts) {
+  __shared__ int part[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  const int64_t ch = (nblk + 7) / 8;
+  const int64_t b0 = w * ch, b1 = b0 + ch < nblk ? b0 + ch : nblk;
+  int sum = 0;
+  if (e < E)
+    for (int64_t b = b0; b < b1; ++b) sum += hist[b * E + e];
+  part[w][lane] = sum;
+  __syncthreads();
+  if (w == 0) {
+    int run = 0;
+    for (int ww = 0; ww < 8; ++ww) {
+      const int v = part[ww][lane];
+      part[ww][lane] = run;
+      run += v;
+    }
+    if (e < E) counts[e] = run;
+  }
+  __syncthreads();
+  int run = part[w][lane];
+  if (e < E)
+    for (int64_t b = b0; b < b1; ++b) {
+      const int v = hist[b * E + e];
+      bbase[b * E + e] = run;
+      run += v;
+    }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  __syncthreads();
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int x = warp_tot[lane];
+    int xi = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, xi, off);
+      if (lane >= off) xi += o;
+    }
+    warp_tot[lane] = xi - x;
+    if (lane == 31) *total = xi;
+  }
+  __syncthreads();
+  return warp_tot[w] + incl - v;
+}
+
+__global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E,
+                                                       int align, int32_t* __restrict__ offsets,
+                                                       int32_t* __restrict__ poff,
+                                                       int32_t* __restrict__ n_mt,
+                                                       int32_t* __restrict__ mt_expert,
+                                                       int32_t* __restrict__ mt_row0,
+                                                       int64_t max_mt, DevErr* err) {
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int e = threadIdx.x;
+  const int c = e < E ? counts[e] : 0;
+  const int pc = (c + align - 1) / align * align;
+  const int off = block_exclusive_scan(c, warp_tot, &total);
+  const int tot_c = total;
+  if (offsets) {
+    if (e < E) offsets[e] = off;
+    if (e == 0) offsets[E] = tot_c;
+  }
+  const int poffv = block_exclusive_scan(pc, warp_tot, &total);
+  const int tot_p = total;
+  if (e < E) poff[e] = poffv;
+  if (e == 0) poff[E] = tot_p;
+  if (n_mt) {
+    const int nm = pc / kTileRows;
+    const int ms = block_exclusive_scan(nm, warp_tot, &total);
+    if (e == 0) n_mt[0] = total;
+    if (e < E) {
+      if (ms + nm > max_mt) {
+        set_error(err, MOE_ERR_DEVICE_BOUNDS, 100);
+      } else {
+        for (int m = 0; m < nm; ++m) {
+          mt_expert[ms + m] = e;
+          mt_row0[ms + m] = poffv + m * kTileRows;
+        }
+      }
+    }
+  }
+}
+
+// Stable permute.  One warp per token: lanes j < k turn the CTA-local rank into the final
+// row (padded expert offset + rank of earlier routing CTAs + local rank), write pos/perm,
+// then the warp copies the token's row once from x and stores it k times (16-byte moves).
+__global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ x, int64_t T,
+                                                      int d, int E, int k,
+                                                      const int32_t* __restrict__ topk,
+                                                      const int32_t* __restrict__ bbase,
+                                                      const int32_t* __restrict__ poff,
+                                                      int32_t* __restrict__ pos,
+                                                      int32_t* __restrict__ perm,
+                                                      uint4* __restrict__ x_perm,
+                                                      int64_t rows_cap, DevErr* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int n16 = d >> 3;
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += nwarps) {
+    int row = 0;
+    if (lane < k) {
+      const int64_t p = t * k + lane;
+      const int e = topk[p];
+      const int64_t b = t / kRouteTokensPerBlock;
+      row = poff[e] + bbase[b * E + e] + pos[p];
+      if (row < 0 || row >= rows_cap || e < 0 || e >= E) {
+        set_error(reinterpret_cast<DevErr*>(err), MOE_ERR_DEVICE_BOUNDS, 200);
+        row = -1;
+      } else {
+        pos[p] = row;
+        perm[row] = static_cast<int32_t>(p);
+      }
+    }
+    int rows[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
+    const uint4* src = x + t * n16;
+    int c = lane;
+    for (; c + 32 < n16; c += 64) {
+      const uint4 v0 = ld_nc_v4(src + c), v1 = ld_nc_v4(src + c + 32);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k && rows[j] >= 0) {
+          uint4* dst = x_perm + static_cast<int64_t>(rows[j]) * n16;
+          st_v4(dst + c, v0);
+          st_v4(dst + c + 32, v1);
+        }
+    }
+    for (; c < n16; c += 32) {
+      const uint4 v0 = ld_nc_v4(src + c);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k && rows[j] >= 0) st_v4(x_perm + static_cast<int64_t>(rows[j]) * n16 + c, v0);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) pad_rows_kernel(const int32_t* __restrict__ counts,
+                                                       const int32_t* __restrict__ poff,
+                                                       int32_t* __restrict__ perm,
+                                                       uint4* __restrict__ rows,
+                                                       int64_t row16) {
+  const int e = blockIdx.x;
+  const int64_t r0 = static_cast<int64_t>(poff[e]) + counts[e];
+  const int64_t r1 = poff[e + 1];
+  if (perm)
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) perm[r] = -1;
+  if (rows) {
+    const int64_t n = (r1 - r0) * row16;
+    uint4* base = rows + r0 * row16;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) st_v4(base + i, z);
+  }
+}
+
+// Combine: out[t] = bf16( sum_j gate[t,j] * y[pos[t,j]] ) over the fp32 expert-output rows,
+// fp32 fused multiply-adds in slot order j = 0..k-1, one rounding at the end.  One warp per
+// token; each lane owns 8 consecutive columns per step (two 16-byte loads per slot).
+__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y,
+                                                      const float* __restrict__ gate,
+                                                      const int32_t* __restrict__ pos,
+                                                      int64_t T, int k, int d,
+                                                      uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int n8 = d >> 3;
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += nwarps) {
+    int row = 0;
+    float g = 0.0f;
+    if (lane < k) {
+      row = pos[t * k + lane];
+      g = gate[t * k + lane];
+    }
+    int rows[kMaxK];
+    float gs[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
+      gs[j] = __shfl_sync(0xFFFFFFFFu, g, j);
+    }
+    for (int c = lane; c < n8; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) {
+          const float4* src = y + (static_cast<int64_t>(rows[j]) * n8 + c) * 2;
+          const float4 a = __ldg(src), b = __ldg(src + 1);
+          acc[0] = __fmaf_rn(gs[j], a.x, acc[0]);
+          acc[1] = __fmaf_rn(gs[j], a.y, acc[1]);
+          acc[2] = __fmaf_rn(gs[j], a.z, acc[2]);
+          acc[3] = __fmaf_rn(gs[j], a.w, acc[3]);
+          acc[4] = __fmaf_rn(gs[j], b.x, acc[4]);
+          acc[5] = __fmaf_rn(gs[j], b.y, acc[5]);
+          acc[6] = __fmaf_rn(gs[j], b.z, acc[6]);
+          acc[7] = __fmaf_rn(gs[j], b.w, acc[7]);
+        }
+      st_v4(out + t * n8 + c, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+    }
+  }
+}
+
+// dx[t] = bf16( sum_j rows[pos[t,j]] ) with fp32 rows, adds in slot order.
+__global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restrict__ rowsp,
+                                                          const int32_t* __restrict__ pos,
+                                                          int64_t T, int k, int d,
+                                                          uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int n8 = d >> 3;
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += nwarps) {
+    const int row = lane < k ? pos[t * k + lane] : 0;
+    int rows[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
+    for (int c = lane; c < n8; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) {
+          const float4* src = rowsp + (static_cast<int64_t>(rows[j]) * n8 + c) * 2;
+          const float4 a = __ldg(src), b = __ldg(src + 1);
+          acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+          acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+      st_v4(out + t * n8 + c, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+    }
+  }
+}
+
+// Per-token backward of the combine and the gate:
+//   dgate[t,j] = <y[pos[t,j]], dy[t]> (fp32: per-lane partials over a fixed column set, then a
+//   fixed butterfly), dO[pos[t,j]] = bf16(gate[t,j] * dy[t]),
+//   dlogits[t, e_j] = g_j (dgate_j - sum_i g_i dgate_i), 0 for unselected experts.
+__global__ void __launch_bounds__(256) bwd_gate_kernel(
+    const uint4* __restrict__ dy, const float4* __restrict__ y, const float* __restrict__ gate,
+    const int32_t* __restrict__ pos, const int32_t* __restrict__ topk, int64_t T, int k, int d,
+    int E, uint4* __restrict__ dO, float* __restrict__ dgate, float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int n16 = d >> 3;
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += nwarps) {
+    int row = 0, ex = 0;
+    float g = 0.0f;
+    if (lane < k) {
+      row = pos[t * k + lane];
+      g = gate[t * k + lane];
+      ex = topk[t * k + lane];
+    }
+    int rows[kMaxK];
+    float gs[kMaxK], part[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
+      gs[j] = __shfl_sync(0xFFFFFFFFu, g, j);
+      part[j] = 0.0f;
+    }
+    for (int c = lane; c < n16; c += 32) {
+      const uint4 dv = ld_nc_v4(dy + t * n16 + c);
+      const uint32_t du[4] = {dv.x, dv.y, dv.z, dv.w};
+      float dyf[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dyf[2 * q] = bf16lo(du[q]);
+        dyf[2 * q + 1] = bf16hi(du[q]);
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) {
+          const float4* ys = y + (static_cast<int64_t>(rows[j]) * n16 + c) * 2;
+          const float4 ya = __ldg(ys), yb = __ldg(ys + 1);
+          const float yf[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) part[j] = __fmaf_rn(yf[q], dyf[q], part[j]);
+          uint4 o;
+          o.x = pack_bf16x2(gs[j] * dyf[0], gs[j] * dyf[1]);
+          o.y = pack_bf16x2(gs[j] * dyf[2], gs[j] * dyf[3]);
+          o.z = pack_bf16x2(gs[j] * dyf[4], gs[j] * dyf[5]);
+          o.w = pack_bf16x2(gs[j] * dyf[6], gs[j] * dyf[7]);
+          st_v4(dO + static_cast<int64_t>(rows[j]) * n16 + c, o);
+        }
+    }
+    float mydg = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j < k) {
+        float s = part[j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+        if (lane == j) mydg = s;
+      }
+    if (lane < k) dgate[t * k + lane] = mydg;
+    if (dlogits) {
+      float sgd = 0.0f;
+      for (int j = 0; j < k; ++j) sgd += __shfl_sync(0xFFFFFFFFu, g * mydg, j);
+      float* dl = dlogits + t * E;
+      for (int e = lane; e < E; e += 32) dl[e] = 0.0f;
+      __syncwarp();
+      if (lane < k) dl[ex] = g * (mydg - sgd);
+    }
+  }
+}
+
+int grid_for_warps(int64_t warps, int warps_per_block) {
+  int64_t b = (warps + warps_per_block - 1) / warps_per_block;
+  const int64_t cap = 152 * 16;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return static_cast<int>(b);
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* topk,
+                              float* gate, int32_t* pos_local, int32_t* hist, DevErr* err,
+                              cudaStream_t s) {
+  (void)err;
+  const int64_t nblk = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  if (nblk == 0) return cudaSuccess;
+  const size_t smem = (8 * static_cast<size_t>(E) + 2 * 4 * 32 * kMaxK) * 4;
+  const int epl = (E + 31) / 32;
+  void (*kern)(const float*, int64_t, int, int, int32_t*, float*, int32_t*, int32_t*);
+  if (epl <= 1) kern = route_topk_kernel<1>;
+  else if (epl <= 2) kern = route_topk_kernel<2>;
+  else if (epl <= 4) kern = route_topk_kernel<4>;
+  else if (epl <= 8) kern = route_topk_kernel<8>;
+  else if (epl <= 16) kern = route_topk_kernel<16>;
+  else kern = route_topk_kernel<32>;
+  cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+  if (st != cudaSuccess) return st;
+  kern<<<static_cast<unsigned>(nblk), 128, smem, s>>>(logits, T, E, k, topk, gate, pos_local,
+                                                      hist);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* bbase,
+                             int32_t* counts, cudaStream_t s) {
+  scan_cols_kernel<<<(E + 31) / 32, 256, 0, s>>>(hist, nblk, E, bbase, counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_offsets(const int32_t* counts, int E, int align, int32_t* offsets,
+                           int32_t* poff, int32_t* n_mt, int32_t* mt_expert, int32_t* mt_row0,
+                           int64_t max_mt, DevErr* err, cudaStream_t s) {
+  offsets_kernel<<<1, 1024, 0, s>>>(counts, E, align, offsets, poff, n_mt, mt_expert, mt_row0,
+                                    max_mt, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const uint16_t* x, int64_t T, int d, int E, int k,
+                           const int32_t* topk, const int32_t* bbase, const int32_t* poff,
+                           int32_t* pos, int32_t* perm, uint16_t* x_perm, int64_t rows_cap,
+                           DevErr* err, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  scatter_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(x), T, d, E, k, topk, bbase, poff, pos, perm,
+      reinterpret_cast<uint4*>(x_perm), rows_cap, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, int32_t* perm,
+                            void* rows, int64_t row_bytes, cudaStream_t s) {
+  pad_rows_kernel<<<E, 256, 0, s>>>(counts, poff, perm, reinterpret_cast<uint4*>(rows),
+                                    row_bytes / 16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* y_rows, const float* gate, const int32_t* pos,
+                           int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(reinterpret_cast<const float4*>(y_rows),
+                                                      gate, pos, T, k, d,
+                                                      reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_gate(const uint16_t* dy, const float* y_rows, const float* gate,
+                            const int32_t* pos, const int32_t* topk, int64_t T, int k, int d,
+                            int E, uint16_t* dO_rows, float* dgate, float* dlogits,
+                            cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  bwd_gate_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(dy), reinterpret_cast<const float4*>(y_rows), gate, pos, topk,
+      T, k, d, E, reinterpret_cast<uint4*>(dO_rows), dgate, dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_f32(const float* rows, const int32_t* pos, int64_t T, int k, int d,
+                               uint16_t* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  combine_f32_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(rows), pos, T, k, d, reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,162 @@
+/*
+ * moe.h - C ABI of libmoe.so: one Mixture-of-Experts expert layer on one GB300 GPU.
+ *
+ * The layer (sources by page title and section):
+ *   - "DeepSeek-V4 parallel strategy" (blog.lpkt.cn), section on EP and the IB network:
+ *     an MoE layer runs Dispatch -> Expert Compute -> Combine.
+ *   - DeepSeek-V4 report reading (10100.com), section on fine-grained compute/communication
+ *     overlap of the EP all-to-all: the expert stage is Linear + activation + Linear, and
+ *     experts are processed in waves.
+ *   - DeepSeek-V4 report, Thai translation (itsolotime.com), section 1.4: the activation is
+ *     SwiGLU (gate, up and down projections, 6hd FLOP per token-expert pair) and the
+ *     combine payload is BF16.  Section 3 and the 10100.com reading: every kernel is
+ *     batch-invariant and deterministic (no global unordered atomic adds; per-unit buffers
+ *     reduced in a fixed order).
+ * Readings where the pages are silent:
+ *   - routing is top-k over fp32 logits with ties going to the lower expert index (+0 and
+ *     -0 compare equal); the gate is the softmax over the k selected logits, computed in
+ *     fp32; slot j = 0..k-1 follows descending logit;
+ *   - the permutation orders rows by (expert, token);
+ *   - h = bf16(silu(x W1) * (x W3)) with silu(a) = a / (1 + exp(-a)); A = x W1 and B = x W3
+ *     stay fp32; the expert outputs y_j = h W2 stay fp32 (on one GPU the combine reads them
+ *     from HBM, so the pages' BF16 gather, a cross-GPU payload format, is not used) and are
+ *     combined as out_t = bf16(sum_j gate[t,j] * y_j), an fp32 accumulation in slot order.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major, 16-byte
+ *     aligned.  bf16 tensors are passed as moe_bf16_t (the raw 16-bit pattern).
+ *   - Shapes: x [T,d], logits [T,E] fp32, W1 and W3 [E,d,d_ff], W2 [E,d_ff,d], out [T,d].
+ *   - The library never allocates, frees or synchronises (except moe_get_error).  Every
+ *     launch is asynchronous on `stream`.  The workspace `ws` (device memory, 256-byte
+ *     aligned, size from moe_workspace_bytes) is caller-owned; calls that share one ws
+ *     must be ordered on the GPU (same stream, or synchronised).
+ *   - Argument errors are detected on the host before anything is launched and returned as
+ *     a status; nothing is written then.  Problems detected on the device (a bounded wait
+ *     that ran out, an index out of range) are recorded in an error word inside `ws` and
+ *     read with moe_get_error.
+ *   - Supported sizes: T >= 0 (T = 0 writes only the outputs that do not depend on T),
+ *     1 <= k <= min(E, 16), 1 <= E <= 1024, d and d_ff multiples of 128, d <= 65536,
+ *     d_ff <= 65536, T*k + 128*E < 2^31.  Violations return MOE_ERR_UNSUPPORTED.
+ *   - Results are bitwise reproducible run to run, and each token's outputs are bitwise
+ *     independent of the other tokens in the batch and of T.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16_t; /* raw bfloat16 bit pattern */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misalignment, k > E, ... */
+  MOE_ERR_UNSUPPORTED = 2,   /* a size outside the supported bounds above             */
+  MOE_ERR_WORKSPACE = 3,     /* ws_bytes smaller than the required workspace           */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed            */
+  MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out (moe_get_error)     */
+  MOE_ERR_DEVICE_BOUNDS = 6  /* a device-side index check failed (moe_get_error)       */
+} moe_status_t;
+
+/* Flags of moe_forward. */
+#define MOE_FWD_SAVE_FOR_BACKWARD 1 /* keep A = x W1 and B = x W3 (fp32) in ws for moe_backward */
+
+/* Stage events: moe_forward records MOE_FWD_NUM_EVENTS events and moe_backward
+ * MOE_BWD_NUM_EVENTS events on `stream` at its stage boundaries when `stage_events` is not
+ * NULL (each a cudaEvent_t created by the caller).
+ *   forward : [0] start, [1] after routing + dispatch, [2] after GEMM1 + SwiGLU,
+ *             [3] after GEMM2, [4] after combine.
+ *   backward: [0] start, [1] after gate grads + dO, [2] after dH + SwiGLU backward,
+ *             [3] after the dX GEMM, [4] after the dX combine, [5] after dW2, [6] after dW1/dW3. */
+#define MOE_FWD_NUM_EVENTS 5
+#define MOE_BWD_NUM_EVENTS 7
+
+/* Bytes of workspace needed by moe_route_dispatch for (T, E, k). */
+size_t moe_route_workspace_bytes(int64_t T, int E, int k);
+
+/* Bytes of workspace needed by moe_forward (and, with with_backward != 0, by
+ * moe_forward(..., MOE_FWD_SAVE_FOR_BACKWARD) followed by moe_backward).  Returns 0 for
+ * arguments outside the supported bounds. */
+size_t moe_workspace_bytes(int64_t T, int d, int E, int k, int d_ff, int with_backward);
+
+/*
+ * Dispatch (routing, counting, prefix sum, stable permute).
+ *   topk_idx [T,k] int32 : experts of token t in descending-logit order (ties: lower index)
+ *   gate     [T,k] fp32  : softmax over the k selected logits
+ *   counts   [E]   int32 : number of (token, slot) pairs routed to each expert
+ *   offsets  [E+1] int32 : exclusive prefix sum of counts, offsets[E] = T*k
+ *   perm     [T*k] int32 : perm[r] = t*k + j for the pair placed in permuted row r
+ *   pos      [T*k] int32 : pos[t*k + j] = r (the inverse of perm)
+ *   x_perm   [T*k,d] bf16: x_perm[r] = x[perm[r] / k], rows grouped by expert, ascending
+ *                          token order inside each expert
+ * Integer outputs and x_perm are exact (bitwise); gate is fp32.  Needs
+ * moe_route_workspace_bytes(T, E, k) bytes of ws.
+ */
+moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_t T, int d,
+                                int E, int k, int32_t* topk_idx, float* gate, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, int32_t* pos,
+                                moe_bf16_t* x_perm, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/*
+ * Forward of the whole layer: out [T,d] bf16.
+ *   out_t = bf16( sum_j gate[t,j] * (h_tj W2[e_j]) ),  h_tj = bf16(silu(x_t W1[e_j]) * (x_t W3[e_j]))
+ * with every matrix product accumulated in fp32 and the slot sum in fp32, in slot order.
+ * ws must hold moe_workspace_bytes(T, d, E, k, d_ff, flags & MOE_FWD_SAVE_FOR_BACKWARD)
+ * bytes; with MOE_FWD_SAVE_FOR_BACKWARD it keeps what moe_backward needs.  stage_events:
+ * NULL or MOE_FWD_NUM_EVENTS events (see above).
+ */
+moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf16_t* W1,
+                         const moe_bf16_t* W3, const moe_bf16_t* W2, int64_t T, int d, int E,
+                         int k, int d_ff, moe_bf16_t* out, void* ws, size_t ws_bytes, int flags,
+                         cudaEvent_t* stage_events, cudaStream_t stream);
+
+/*
+ * Backward of the layer for upstream gradient dy [T,d] bf16.  Precondition: ws holds the
+ * state of a moe_forward call with MOE_FWD_SAVE_FOR_BACKWARD on the same x, logits, W1, W3,
+ * W2 and sizes, with nothing else using ws in between.
+ * Outputs (all overwritten, none accumulated into):
+ *   dx      [T,d]        bf16 : sum over slots j (in slot order, fp32) of dA W1^T + dB W3^T
+ *   dW1,dW3 [E,d,d_ff]   fp32 : sum over the rows of each expert of x^T dA (resp. x^T dB)
+ *   dW2     [E,d_ff,d]   fp32 : sum over the rows of each expert of h^T dO
+ *   dgate   [T,k]        fp32 : <y_j, dy_t> with y_j the fp32 expert output
+ *   dlogits [T,E]        fp32 : gradient through the top-k softmax (0 for unselected
+ *                               experts); may be NULL
+ * with dO = gate * dy, dH = dO W2^T, dA = dH * B * silu'(A), dB = dH * silu(A); dO, dA and dB
+ * are rounded to bf16 as GEMM operands; every GEMM accumulates in fp32 in a fixed order.
+ * stage_events: NULL or MOE_BWD_NUM_EVENTS events.
+ */
+moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float* logits,
+                          const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                          int64_t T, int d, int E, int k, int d_ff, moe_bf16_t* dx, float* dW1,
+                          float* dW3, float* dW2, float* dgate, float* dlogits, void* ws,
+                          size_t ws_bytes, cudaEvent_t* stage_events, cudaStream_t stream);
+
+/* Synchronises `stream`, reads the device error word of `ws` and returns it (MOE_OK when
+ * no device-side problem was recorded since the last moe_route_dispatch / moe_forward on
+ * this ws, which clear it).  Returns MOE_ERR_CUDA if the stream reports an error. */
+moe_status_t moe_get_error(const void* ws, cudaStream_t stream);
+
+/* Upper bound, in nanoseconds, of every device-side wait of kernels launched after this
+ * call (process-wide; default 2e9).  A wait that runs out records MOE_ERR_TIMEOUT and its
+ * kernel returns without finishing the work. */
+void moe_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook, process-wide, 0 by default.  Bit 0: the first CTA of the next grouped-GEMM
+ * launches skips its first operand load so that the matching wait runs out (used to test
+ * the timeout path on a tiny problem with a short timeout). */
+void moe_debug_set_flags(int flags);
+
+/* Short English description of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

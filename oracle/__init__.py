@@ -38,9 +38,9 @@ def _load():
             getattr(lib, n).argtypes = [_p] * 5 + dims + [_int, _p, _i64, _p]
         lib.oracle_forward_permuted_bf16.argtypes = [_p] * 5 + dims + [_int, _p, _p, _p]
         for n in ("oracle_backward_tokens_bf16", "oracle_backward_tokens_f64"):
-            getattr(lib, n).argtypes = [_p] * 6 + dims + [_int, _p, _i64, _p, _p, _p]
+            getattr(lib, n).argtypes = [_p] * 6 + dims + [_int, _int, _p, _i64, _p, _p, _p]
         for n in ("oracle_backward_dw_bf16", "oracle_backward_dw_f64"):
-            getattr(lib, n).argtypes = [_p] * 6 + dims + [_int, _p, _int, _p, _p, _p]
+            getattr(lib, n).argtypes = [_p] * 6 + dims + [_int, _int, _p, _int, _p, _p, _p]
         _lib = lib
     return _lib
 
@@ -140,8 +140,9 @@ def forward_permuted(inp, k, round_h=True):
     return y, xp, op
 
 
-def backward_tokens(inp, dy, k, tokens=None, round_h=True):
-    """Per-token backward: dx [n,d], dgate [n,k], dlogits [n,E] (all f64)."""
+def backward_tokens(inp, dy, k, tokens=None, round_h=True, round_grad=True):
+    """Per-token backward: dx [n,d], dgate [n,k], dlogits [n,E] (all f64).  With round_grad,
+    the product operands dO = g dy, da and db are rounded to bf16 (as h is in the forward)."""
     x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
     wt = _wtype(x)
     x, W1, W3, W2, dy = (_prep(a, wt) for a in (x, W1, W3, W2, dy))
@@ -152,12 +153,13 @@ def backward_tokens(inp, dy, k, tokens=None, round_h=True):
     dlog = np.empty((n, E), np.float64)
     fn = getattr(_load(), "oracle_backward_tokens_" + wt)
     _check(fn(_ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), T, d, E, k, dff,
-              int(round_h), _ptr(tok), n, _ptr(dx), _ptr(dgate), _ptr(dlog)))
+              int(round_h), int(round_grad), _ptr(tok), n, _ptr(dx), _ptr(dgate), _ptr(dlog)))
     return dx, dgate, dlog
 
 
-def backward_dw(inp, dy, k, experts, round_h=True):
-    """Weight gradients of the listed experts: dW1, dW3 [n,d,dff] and dW2 [n,dff,d], f64."""
+def backward_dw(inp, dy, k, experts, round_h=True, round_grad=True):
+    """Weight gradients of the listed experts: dW1, dW3 [n,d,dff] and dW2 [n,dff,d], f64
+    (round_grad as in backward_tokens)."""
     x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
     wt = _wtype(x)
     x, W1, W3, W2, dy = (_prep(a, wt) for a in (x, W1, W3, W2, dy))
@@ -168,7 +170,7 @@ def backward_dw(inp, dy, k, experts, round_h=True):
     dW2 = np.empty((n, dff, d), np.float64)
     fn = getattr(_load(), "oracle_backward_dw_" + wt)
     _check(fn(_ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), T, d, E, k, dff,
-              int(round_h), _ptr(ex), n, _ptr(dW1), _ptr(dW3), _ptr(dW2)))
+              int(round_h), int(round_grad), _ptr(ex), n, _ptr(dW1), _ptr(dW3), _ptr(dW2)))
     return dW1, dW3, dW2
 
 

@@ -22,7 +22,9 @@
 //  * SwiGLU: h = silu(x W1) * (x W3), silu(a) = a / (1 + exp(-a)); h is rounded to bf16
 //    (round to nearest, ties to even) before the down projection when round_h != 0.
 //  * combine: y_t = sum_j g_j * o_j, here in fp64.
-//  * backward: the derivative of the bf16 rounding of h is taken as 1.
+//  * backward: the derivative of the bf16 rounding of h is taken as 1; with round_grad the
+//    matrix-product operands dO = g dy, da and db are rounded to bf16 (round to nearest
+//    even) like h, each product accumulating exactly (fp64).
 //
 // All arithmetic is fp64.  bf16 inputs are passed as their raw 16-bit patterns and
 // widened exactly.  Loops run in the plain order of the definitions; OpenMP only
@@ -116,14 +118,18 @@ void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int df
 //   dgate = <o, dy>, dO = g dy, dh = dO W2^T,
 //   da = dh * b * silu'(a) with silu'(a) = s (1 + a (1 - s)), s = sigmoid(a),
 //   db = dh * silu(a),  dxp = da W1^T + db W3^T.
+// With round_grad != 0, dO, da and db are rounded to bf16 where they become operands of a
+// matrix product (dh, dxp and the weight gradients), the reading that every product of the
+// layer takes bf16 operands and accumulates exactly (here in fp64).
 template <class V>
 void ffn_row_bwd(const V* W1e, const V* W3e, const V* W2e, int d, int dff, double g,
                  const double* dy, const double* a, const double* b, const double* o,
-                 double* dgate, double* dO, double* dh, double* da, double* db, double* dxp) {
+                 int round_grad, double* dgate, double* dO, double* dh, double* da, double* db,
+                 double* dxp) {
   double s = 0.0;
   for (int c = 0; c < d; ++c) s += o[c] * dy[c];
   *dgate = s;
-  for (int c = 0; c < d; ++c) dO[c] = g * dy[c];
+  for (int c = 0; c < d; ++c) dO[c] = round_grad ? round_bf16(g * dy[c]) : g * dy[c];
   for (int f = 0; f < dff; ++f) {
     const V* w2 = W2e + static_cast<int64_t>(f) * d;
     double acc = 0.0;
@@ -134,6 +140,10 @@ void ffn_row_bwd(const V* W1e, const V* W3e, const V* W2e, int d, int dff, doubl
     const double sg = sigmoid(a[f]);
     da[f] = dh[f] * b[f] * sg * (1.0 + a[f] * (1.0 - sg));
     db[f] = dh[f] * a[f] * sg;
+    if (round_grad) {
+      da[f] = round_bf16(da[f]);
+      db[f] = round_bf16(db[f]);
+    }
   }
   for (int c = 0; c < d; ++c) {
     const V* w1 = W1e + static_cast<int64_t>(c) * dff;
@@ -261,8 +271,9 @@ int forward_permuted(const V* x, const double* logits, const V* W1, const V* W3,
 // softmax over the selected logits: dl_{e_j} = g_j (dgate_j - sum_i g_i dgate_i), 0 elsewhere.
 template <class V, class G>
 int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
-                    const G* dy, const Dims& D, int round_h, const int64_t* tokens, int64_t n,
-                    double* dx, double* dgate, double* dlogits) {
+                    const G* dy, const Dims& D, int round_h, int round_grad,
+                    const int64_t* tokens, int64_t n, double* dx, double* dgate,
+                    double* dlogits) {
   int bad = 0;
 #pragma omp parallel
   {
@@ -287,8 +298,8 @@ int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, 
         ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, round_h,
                 a.data(), b.data(), h.data(), o.data());
         ffn_row_bwd(w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, gate[j],
-                    dyv.data(), a.data(), b.data(), o.data(), &dg[j], dO.data(), dh.data(),
-                    da.data(), db.data(), dxp.data());
+                    dyv.data(), a.data(), b.data(), o.data(), round_grad, &dg[j], dO.data(),
+                    dh.data(), da.data(), db.data(), dxp.data());
         if (dxt) for (int c = 0; c < D.d; ++c) dxt[c] += dxp[c];
       }
       if (dgate) for (int j = 0; j < D.k; ++j) dgate[i * D.k + j] = dg[j];
@@ -308,8 +319,8 @@ int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, 
 //   dW1[e] = sum x^T da, dW3[e] = sum x^T db, dW2[e] = sum h^T dO.
 template <class V, class G>
 int backward_dw(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
-                const G* dy, const Dims& D, int round_h, const int32_t* experts, int n_exp,
-                double* dW1, double* dW3, double* dW2) {
+                const G* dy, const Dims& D, int round_h, int round_grad, const int32_t* experts,
+                int n_exp, double* dW1, double* dW3, double* dW2) {
   const int64_t P = D.T * D.k;
   std::vector<int32_t> idx(P);
   std::vector<double> gate(P);
@@ -334,8 +345,8 @@ int backward_dw(const V* x, const double* logits, const V* W1, const V* W3, cons
         for (int c = 0; c < D.d; ++c) dyv[c] = widen(dy[t * D.d + c]);
         double dg;
         ffn_row_bwd(w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, gate[p], dyv.data(),
-                    &A[r * D.dff], &B[r * D.dff], o.data(), &dg, &DO[r * D.d], dh.data(),
-                    &DA[r * D.dff], &DB[r * D.dff], dxp.data());
+                    &A[r * D.dff], &B[r * D.dff], o.data(), round_grad, &dg, &DO[r * D.d],
+                    dh.data(), &DA[r * D.dff], &DB[r * D.dff], dxp.data());
       }
     }
     double* g1 = dW1 + static_cast<int64_t>(q) * D.d * D.dff;
@@ -418,38 +429,39 @@ int oracle_forward_permuted_bf16(const uint16_t* x, const double* logits, const 
 
 int oracle_backward_tokens_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
                                 const uint16_t* W3, const uint16_t* W2, const uint16_t* dy,
-                                ORACLE_DIMS, int round_h, const int64_t* tokens, int64_t n,
-                                double* dx, double* dgate, double* dlogits) {
+                                ORACLE_DIMS, int round_h, int round_grad,
+                                const int64_t* tokens, int64_t n, double* dx, double* dgate,
+                                double* dlogits) {
   if (!dims_ok(T, d, E, k, dff)) return -1;
-  return backward_tokens(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, tokens, n,
-                         dx, dgate, dlogits);
+  return backward_tokens(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, round_grad,
+                         tokens, n, dx, dgate, dlogits);
 }
 
 int oracle_backward_tokens_f64(const double* x, const double* logits, const double* W1,
                                const double* W3, const double* W2, const double* dy, ORACLE_DIMS,
-                               int round_h, const int64_t* tokens, int64_t n, double* dx,
-                               double* dgate, double* dlogits) {
+                               int round_h, int round_grad, const int64_t* tokens, int64_t n,
+                               double* dx, double* dgate, double* dlogits) {
   if (!dims_ok(T, d, E, k, dff)) return -1;
-  return backward_tokens(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, tokens, n,
-                         dx, dgate, dlogits);
+  return backward_tokens(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, round_grad,
+                         tokens, n, dx, dgate, dlogits);
 }
 
 int oracle_backward_dw_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
                             const uint16_t* W3, const uint16_t* W2, const uint16_t* dy,
-                            ORACLE_DIMS, int round_h, const int32_t* experts, int n_exp,
-                            double* dW1, double* dW3, double* dW2) {
+                            ORACLE_DIMS, int round_h, int round_grad, const int32_t* experts,
+                            int n_exp, double* dW1, double* dW3, double* dW2) {
   if (!dims_ok(T, d, E, k, dff)) return -1;
-  return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, experts, n_exp,
-                     dW1, dW3, dW2);
+  return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, round_grad,
+                     experts, n_exp, dW1, dW3, dW2);
 }
 
 int oracle_backward_dw_f64(const double* x, const double* logits, const double* W1,
                            const double* W3, const double* W2, const double* dy, ORACLE_DIMS,
-                           int round_h, const int32_t* experts, int n_exp, double* dW1,
-                           double* dW3, double* dW2) {
+                           int round_h, int round_grad, const int32_t* experts, int n_exp,
+                           double* dW1, double* dW3, double* dW2) {
   if (!dims_ok(T, d, E, k, dff)) return -1;
-  return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, experts, n_exp,
-                     dW1, dW3, dW2);
+  return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, round_grad,
+                     experts, n_exp, dW1, dW3, dW2);
 }
 
 }  // extern "C"

@@ -1,0 +1,95 @@
+"""Helpers shared by the GPU tests: run the CUDA path through the C ABI, run the oracle on
+the same inputs, compare with the stated tolerance."""
+import numpy as np
+import torch
+
+import moe_synth
+
+# Output tolerance of the layer (forward and gradients), elementwise against the fp64
+# oracle on the same bf16 inputs with h rounded to bf16 on both sides.
+RTOL = 2e-2
+ATOL = 2e-3
+
+
+def assert_close(got, ref, what, rtol=RTOL, atol=ATOL):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    err = np.abs(got - ref)
+    bad = err > rtol * np.abs(ref) + atol
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - rtol * np.abs(ref)), err.shape)
+        raise AssertionError("%s: %d / %d outside |d| <= %g|ref| + %g; worst at %s: got %r ref %r"
+                             % (what, int(bad.sum()), bad.size, rtol, atol, i, got[i], ref[i]))
+
+
+def to_dev(inp, dev="cuda"):
+    return {k: v.to(dev) for k, v in inp.items()}
+
+
+def route_dispatch(moe, g, k):
+    x, logits = g["x"], g["logits"]
+    T, d = x.shape
+    E = logits.shape[1]
+    dev = x.device
+    P = T * k
+    out = dict(
+        topk_idx=torch.empty(T, k, dtype=torch.int32, device=dev),
+        gate=torch.empty(T, k, dtype=torch.float32, device=dev),
+        counts=torch.empty(E, dtype=torch.int32, device=dev),
+        offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+        perm=torch.empty(P, dtype=torch.int32, device=dev),
+        pos=torch.empty(P, dtype=torch.int32, device=dev),
+        x_perm=torch.empty(P, d, dtype=torch.bfloat16, device=dev),
+    )
+    ws = torch.empty(max(moe.moe_route_workspace_bytes(T, E, k), 256), dtype=torch.uint8,
+                     device=dev)
+    moe.moe_route_dispatch(x, logits, k, out["topk_idx"], out["gate"], out["counts"],
+                           out["offsets"], out["perm"], out["pos"], out["x_perm"], ws)
+    assert moe.moe_get_error(ws) == 0
+    return out
+
+
+def forward(moe, g, k, save=False, ws=None):
+    x = g["x"]
+    T, d = x.shape
+    E, _, dff = g["W1"].shape
+    if ws is None:
+        ws = torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, save), dtype=torch.uint8,
+                         device=x.device)
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
+    moe.moe_forward(x, g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+                    flags=moe.MOE_FWD_SAVE_FOR_BACKWARD if save else 0)
+    return out, ws
+
+
+def backward(moe, g, k, ws):
+    x = g["x"]
+    T, d = x.shape
+    E, _, dff = g["W1"].shape
+    dev = x.device
+    res = dict(
+        dx=torch.empty(T, d, dtype=torch.bfloat16, device=dev),
+        dW1=torch.empty(E, d, dff, dtype=torch.float32, device=dev),
+        dW3=torch.empty(E, d, dff, dtype=torch.float32, device=dev),
+        dW2=torch.empty(E, dff, d, dtype=torch.float32, device=dev),
+        dgate=torch.empty(T, k, dtype=torch.float32, device=dev),
+        dlogits=torch.empty(T, E, dtype=torch.float32, device=dev),
+    )
+    moe.moe_backward(g["dy"], x, g["logits"], g["W1"], g["W3"], g["W2"], k, res["dx"],
+                     res["dW1"], res["dW3"], res["dW2"], res["dgate"], res["dlogits"], ws)
+    return res
+
+
+def np_of(t):
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.float().numpy().astype(np.float64)
+    return t.numpy()
+
+
+def sample_tokens(T, n, seed=0):
+    rng = np.random.default_rng(seed)
+    pick = {0, T - 1}
+    pick.update(rng.choice(T, size=min(n, T), replace=False).tolist())
+    return np.array(sorted(pick), np.int64)

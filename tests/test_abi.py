@@ -1,0 +1,73 @@
+"""The C ABI without a GPU: libmoe.so loads, exports every function include/moe.h declares,
+sizes its workspace, and rejects bad arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__._load_builder().build()
+    import combine_fp32_router_gb300 as moe
+    return moe
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(names) == set(lib.EXPORTS)
+    raw = lib.library()
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_workspace_sizes(lib):
+    small = lib.moe_workspace_bytes(64, 128, 8, 2, 256, False)
+    big = lib.moe_workspace_bytes(64, 128, 8, 2, 256, True)
+    assert 0 < small < big
+    assert small % 256 == 0
+    # the large skewed workload: padded rows P + 127 E, three row buffers of d bf16
+    fwd = lib.moe_workspace_bytes(16384, 7168, 256, 8, 2048, False)
+    P_pad = 16384 * 8 + 127 * 256
+    assert fwd >= P_pad * 7168 * 2 * 2 + P_pad * 2048 * 2
+    assert lib.moe_workspace_bytes(64, 100, 8, 2, 256, False) == 0      # d % 128 != 0
+    assert lib.moe_workspace_bytes(64, 128, 8, 9, 256, False) == 0      # k > E
+    assert lib.moe_workspace_bytes(64, 128, 2048, 2, 256, False) == 0   # E > 1024
+    assert lib.moe_route_workspace_bytes(1000, 64, 6) > 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    raw = lib.library()
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    p = [fake] * 5
+    st = raw.moe_forward(*p, 64, 128, 8, 9, 256, fake, fake, 1 << 30, 0, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG                      # k > E
+    st = raw.moe_forward(*p, 64, 100, 8, 2, 256, fake, fake, 1 << 30, 0, None, None)
+    assert st == lib.MOE_ERR_UNSUPPORTED                      # d % 128 != 0
+    st = raw.moe_forward(*p, -1, 128, 8, 2, 256, fake, fake, 1 << 30, 0, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG                      # T < 0
+    st = raw.moe_forward(*p, 64, 128, 8, 2, 256, fake, fake, 1 << 30, 4, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG                      # unknown flag
+    st = raw.moe_forward(*p, 64, 128, 8, 2, 256, fake, fake, 16, 0, None, None)
+    assert st == lib.MOE_ERR_WORKSPACE                        # workspace too small
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    st = raw.moe_forward(mis, *p[1:], 64, 128, 8, 2, 256, fake, fake, 1 << 30, 0, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG                      # x not 16-byte aligned
+    st = raw.moe_forward(None, *p[1:], 64, 128, 8, 2, 256, fake, fake, 1 << 30, 0, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG                      # null x
+    st = raw.moe_route_dispatch(fake, fake, 10, 64, 32, 17, *([fake] * 7), fake, 1 << 30, None)
+    assert st == lib.MOE_ERR_UNSUPPORTED                      # k > 16
+    st = raw.moe_backward(*([fake] * 6), 64, 128, 8, 2, 256, *([fake] * 6), fake, 16, None, None)
+    assert st == lib.MOE_ERR_WORKSPACE
+    assert lib.moe_status_string(lib.MOE_ERR_TIMEOUT) == "device-side wait timed out"

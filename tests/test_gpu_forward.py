@@ -1,0 +1,128 @@
+"""Forward of the whole layer on the GPU (moe_forward through the C ABI) against the oracle,
+batch invariance and run-to-run determinism (bitwise)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+import oracle
+from moe_harness import assert_close, forward, np_of, sample_tokens, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import combine_fp32_router_gb300 as m
+    return m
+
+
+def _full_check(moe, w):
+    inp = moe_synth.generate(w)
+    g = to_dev(inp)
+    out, ws = forward(moe, g, w.k)
+    assert moe.moe_get_error(ws) == 0
+    ref = oracle.forward_tokens(moe_synth.to_numpy(inp), w.k)
+    assert_close(np_of(out), ref, "out")
+    return g, out
+
+
+def test_forward_tiny_workload(moe):
+    _full_check(moe, moe_synth.by_name("tiny"))
+
+
+@pytest.mark.parametrize("T,d,E,k,dff", [
+    (300, 256, 16, 4, 384),    # ragged tiles, d % 256 == 0, dff % 256 != 0
+    (77, 384, 5, 3, 128),      # d % 256 != 0 (128-wide N tiles), one 128-wide h block
+    (1, 128, 4, 4, 256),       # a single token, k = E
+    (513, 128, 1, 1, 128),     # one expert: a dense SwiGLU MLP with 5 row tiles
+    (200, 128, 64, 2, 256),    # many empty experts
+])
+def test_forward_small_shapes(moe, T, d, E, k, dff):
+    _full_check(moe, moe_synth.custom(T, d, E, k, dff, seed=T * 7 + d))
+
+
+def test_forward_mid_workload_sampled(moe):
+    w = moe_synth.by_name("mid")
+    inp = moe_synth.generate(w)
+    g = to_dev(inp)
+    out, ws = forward(moe, g, w.k)
+    assert moe.moe_get_error(ws) == 0
+    tok = sample_tokens(w.T, 96, seed=1)
+    ref = oracle.forward_tokens(moe_synth.to_numpy(inp), w.k, tokens=tok)
+    assert_close(np_of(out)[tok], ref, "out (mid, sampled tokens)")
+
+
+def test_forward_skewed_one_expert_hot(moe):
+    # 90% of the pairs on expert 0: one expert spans many 128-row tiles, most are empty
+    w = moe_synth.custom(T=2000, d=256, E=32, k=2, dff=256, seed=5)
+    inp = moe_synth.generate(w)
+    inp["logits"][:1800, 0] += 50.0
+    g = to_dev(inp)
+    out, ws = forward(moe, g, w.k)
+    assert moe.moe_get_error(ws) == 0
+    ref = oracle.forward_tokens(moe_synth.to_numpy(inp), w.k)
+    assert_close(np_of(out), ref, "out (hot expert)")
+
+
+def test_forward_deterministic_and_ws_reuse(moe):
+    w = moe_synth.custom(T=1000, d=256, E=16, k=4, dff=256, seed=9)
+    g = to_dev(moe_synth.generate(w))
+    out0, ws = forward(moe, g, w.k)
+    for _ in range(5):
+        out1, _ = forward(moe, g, w.k, ws=ws)
+        assert torch.equal(out0.view(torch.int16), out1.view(torch.int16))
+
+
+def test_forward_batch_invariance_small(moe):
+    # each token's output is bitwise the same whatever the batch it sits in
+    w = moe_synth.custom(T=400, d=256, E=16, k=4, dff=256, seed=11)
+    g = to_dev(moe_synth.generate(w))
+    full, _ = forward(moe, g, w.k)
+    for T in (1, 3, 64, 129, 255):
+        part, _ = forward(moe, moe_synth.rows(g, T), w.k)
+        assert torch.equal(part.view(torch.int16), full[:T].view(torch.int16)), T
+    # a token placed in a different batch (reversed order) gives the same bits
+    rev = {kk: (v.flip(0).contiguous() if kk in ("x", "logits") else v) for kk, v in g.items()}
+    out_rev, _ = forward(moe, rev, w.k)
+    assert torch.equal(out_rev.flip(0).view(torch.int16), full.view(torch.int16))
+
+
+def _device_workload(name):
+    w = moe_synth.by_name(name)
+    return w, moe_synth.generate(w, device="cuda")
+
+
+def test_forward_sweep_batch_invariance(moe):
+    # T in {1, 2, 4, ..., 128} over the same 128 token rows, d=7168, E=256, top-8, dff=2048
+    w, g = _device_workload("sweep")
+    outs = {}
+    ws = torch.empty(moe.moe_workspace_bytes(128, w.d, w.E, w.k, w.dff, False),
+                     dtype=torch.uint8, device="cuda")
+    for T in w.sweep:
+        out, _ = forward(moe, moe_synth.rows(g, T), w.k, ws=ws)
+        assert moe.moe_get_error(ws) == 0
+        outs[T] = out.clone()
+    full = outs[128].view(torch.int16)
+    for T in w.sweep:
+        assert torch.equal(outs[T].view(torch.int16), full[:T]), T
+    tok = np.array([0, 1, 5, 77, 127])
+    npi = moe_synth.to_numpy(g)
+    ref = oracle.forward_tokens(npi, w.k, tokens=tok)
+    assert_close(np_of(outs[128])[tok], ref, "out (sweep, sampled tokens)")
+
+
+def test_forward_large_skewed_sampled(moe):
+    w, g = _device_workload("large_skewed")
+    out, ws = forward(moe, g, w.k)
+    assert moe.moe_get_error(ws) == 0
+    npi = moe_synth.to_numpy(g)
+    idx, _ = oracle.route(npi["logits"], w.k)
+    # sampled tokens plus tokens of the most and least loaded non-empty experts
+    counts = np.bincount(idx.reshape(-1), minlength=w.E)
+    hot = int(np.argmax(counts))
+    cold = int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
+    extra = [int(np.nonzero((idx == e).any(1))[0][-1]) for e in (hot, cold)]
+    tok = np.unique(np.concatenate([sample_tokens(w.T, 24, seed=3), extra]))
+    ref = oracle.forward_tokens(npi, w.k, tokens=tok)
+    assert_close(np_of(out)[tok], ref, "out (large skewed, sampled tokens)")

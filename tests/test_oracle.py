@@ -234,8 +234,8 @@ def test_backward_matches_central_finite_differences():
     inp = _rand_inputs(rng, T, d, E, k, dff, as_bf16=False)
     inp["logits"] = inp["logits"].astype(np.float64)   # perturbable
     dy = rng.standard_normal((T, d))
-    dx, dgate, dlog = oracle.backward_tokens(inp, dy, k, round_h=False)
-    dW1, dW3, dW2 = oracle.backward_dw(inp, dy, k, np.arange(E), round_h=False)
+    dx, dgate, dlog = oracle.backward_tokens(inp, dy, k, round_h=False, round_grad=False)
+    dW1, dW3, dW2 = oracle.backward_dw(inp, dy, k, np.arange(E), round_h=False, round_grad=False)
     tol = dict(rtol=1e-6, atol=1e-8)
     np.testing.assert_allclose(dx, _fd(inp, dy, k, "x", 1e-6), **tol)
     np.testing.assert_allclose(dW1, _fd(inp, dy, k, "W1", 1e-6), **tol)
@@ -272,13 +272,57 @@ def test_backward_closed_form_with_sympy():
     pts = [(1.0, 0.0), (0.0, -2.0)]
     inp = dict(x=np.array(pts), logits=np.zeros((2, 1)), W1=np.array(g["W1"], np.float64),
                W3=np.array(g["W3"], np.float64), W2=np.array(g["W2"], np.float64))
-    dx, dgate, dlog = oracle.backward_tokens(inp, np.array([dy, dy]), 1, round_h=False)
+    dx, dgate, dlog = oracle.backward_tokens(inp, np.array([dy, dy]), 1, round_h=False,
+                                             round_grad=False)
     for t, (p0, p1) in enumerate(pts):
         sub = {x0: p0, x1: p1}
         ref = [float(sp.diff(L, v).subs(sub).evalf(30)) for v in (x0, x1)]
         np.testing.assert_allclose(dx[t], ref, rtol=1e-13, atol=1e-15)
         np.testing.assert_allclose(dgate[t, 0], float(L.subs(sub).evalf(30)), rtol=1e-13)
     np.testing.assert_array_equal(dlog, 0.0)   # k = 1: the gate is constant 1
+
+
+def test_backward_round_grad_rounds_exactly_the_product_operands():
+    # With round_grad the oracle rounds dO = g*dy, da and db to bf16 before they enter a
+    # product.  Rebuild dW2 = sum h^T dO, dW1 = sum x^T da, dW3 = sum x^T db and
+    # dx = sum (da W1^T + db W3^T) for one expert with numpy products and torch's bf16 cast.
+    from scipy.special import softmax
+    rng = np.random.default_rng(31)
+    T, d, E, k, dff = 12, 16, 3, 2, 24
+    inp = _rand_inputs(rng, T, d, E, k, dff)
+    dy = _bf16_bits(rng.standard_normal((T, d)))
+    X, DY = _bits_to_f64(inp["x"]), _bits_to_f64(dy)
+    W1, W3, W2 = (_bits_to_f64(inp[n]) for n in ("W1", "W3", "W2"))
+    logits = inp["logits"].astype(np.float64)
+    order = np.argsort(-logits, axis=1, kind="stable")[:, :k]
+    gates = softmax(np.take_along_axis(logits, order, 1), axis=1)
+    e = 1
+    ref2 = np.zeros((dff, d)); ref1 = np.zeros((d, dff)); ref3 = np.zeros((d, dff))
+    dx_ref = np.zeros((T, d))
+    for t in range(T):
+        for j in range(k):
+            ee = order[t, j]
+            a, b = X[t] @ W1[ee], X[t] @ W3[ee]
+            h = _torch_bf16(_silu(a) * b)
+            dO = _torch_bf16(gates[t, j] * DY[t])
+            dh = W2[ee] @ dO
+            sg = 1 / (1 + np.exp(-a))
+            da = _torch_bf16(dh * b * sg * (1 + a * (1 - sg)))
+            db = _torch_bf16(dh * a * sg)
+            dx_ref[t] += W1[ee] @ da + W3[ee] @ db
+            if ee == e:
+                ref2 += np.outer(h, dO)
+                ref1 += np.outer(X[t], da)
+                ref3 += np.outer(X[t], db)
+    dW1, dW3, dW2 = oracle.backward_dw(inp, dy, k, [e])
+    np.testing.assert_allclose(dW2[0], ref2, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dW1[0], ref1, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dW3[0], ref3, rtol=1e-10, atol=1e-12)
+    dx, _, _ = oracle.backward_tokens(inp, dy, k)
+    np.testing.assert_allclose(dx, dx_ref, rtol=1e-10, atol=1e-12)
+    # and the rounding is really applied: the unrounded gradients differ
+    dW1u, _, _ = oracle.backward_dw(inp, dy, k, [e], round_grad=False)
+    assert np.abs(dW1u - dW1).max() > 0
 
 
 def test_layer_flops_is_six_h_d_per_pair():
