@@ -1,12 +1,17 @@
 """Backward of the layer on the GPU (moe_backward through the C ABI) against the oracle, and
-run-to-run bitwise determinism of forward + backward."""
+run-to-run bitwise determinism of forward + backward.
+
+Gradients use assert_close_grad: the stated bound |g - g_ref| <= 2e-2 |g_ref| + 2e-3 on all
+but a 1e-3 fraction of the elements, the rest within 1% of the tensor's rms: the residue of
+one-ulp bf16 rounding flips of the product operands (see moe_harness.assert_close_grad)."""
 import numpy as np
 import pytest
 import torch
 
 import moe_synth
 import oracle
-from moe_harness import assert_close, backward, forward, np_of, sample_tokens, to_dev
+from moe_harness import (assert_close, assert_close_grad, backward, forward, np_of,
+                         sample_tokens, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -30,14 +35,14 @@ def _check_all(moe, w, experts=None):
     res = _run(moe, g, w.k)
     npi = moe_synth.to_numpy(inp)
     dx, dgate, dlog = oracle.backward_tokens(npi, npi["dy"], w.k)
-    assert_close(np_of(res["dx"]), dx, "dx")
-    assert_close(np_of(res["dgate"]), dgate, "dgate")
-    assert_close(np_of(res["dlogits"]), dlog, "dlogits")
+    assert_close_grad(np_of(res["dx"]), dx, "dx")
+    assert_close_grad(np_of(res["dgate"]), dgate, "dgate")
+    assert_close_grad(np_of(res["dlogits"]), dlog, "dlogits")
     ex = np.arange(w.E) if experts is None else np.asarray(experts)
     r1, r3, r2 = oracle.backward_dw(npi, npi["dy"], w.k, ex)
-    assert_close(np_of(res["dW1"])[ex], r1, "dW1")
-    assert_close(np_of(res["dW3"])[ex], r3, "dW3")
-    assert_close(np_of(res["dW2"])[ex], r2, "dW2")
+    assert_close_grad(np_of(res["dW1"])[ex], r1, "dW1")
+    assert_close_grad(np_of(res["dW3"])[ex], r3, "dW3")
+    assert_close_grad(np_of(res["dW2"])[ex], r2, "dW2")
 
 
 def test_backward_tiny_workload(moe):
@@ -88,11 +93,11 @@ def test_fwd_bwd_workload_sampled_and_deterministic(moe):
     y = oracle.forward_tokens(npi, w.k, tokens=tok)
     assert_close(np_of(ref["out"])[tok], y, "out (fwd_bwd, sampled tokens)")
     dx, dgate, dlog = oracle.backward_tokens(npi, npi["dy"], w.k, tokens=tok)
-    assert_close(np_of(ref["dx"])[tok], dx, "dx (sampled tokens)")
-    assert_close(np_of(ref["dgate"])[tok], dgate, "dgate (sampled tokens)")
-    assert_close(np_of(ref["dlogits"])[tok], dlog, "dlogits (sampled tokens)")
+    assert_close_grad(np_of(ref["dx"])[tok], dx, "dx (sampled tokens)")
+    assert_close_grad(np_of(ref["dgate"])[tok], dgate, "dgate (sampled tokens)")
+    assert_close_grad(np_of(ref["dlogits"])[tok], dlog, "dlogits (sampled tokens)")
     ex = np.array([0, 77])
     r1, r3, r2 = oracle.backward_dw(npi, npi["dy"], w.k, ex)
-    assert_close(np_of(ref["dW1"][ex.tolist()]), r1, "dW1 (experts 0, 77)")
-    assert_close(np_of(ref["dW3"][ex.tolist()]), r3, "dW3 (experts 0, 77)")
-    assert_close(np_of(ref["dW2"][ex.tolist()]), r2, "dW2 (experts 0, 77)")
+    assert_close_grad(np_of(ref["dW1"][ex.tolist()]), r1, "dW1 (experts 0, 77)")
+    assert_close_grad(np_of(ref["dW3"][ex.tolist()]), r3, "dW3 (experts 0, 77)")
+    assert_close_grad(np_of(ref["dW2"][ex.tolist()]), r2, "dW2 (experts 0, 77)")
