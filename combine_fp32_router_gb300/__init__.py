@@ -29,8 +29,8 @@ MOE_BWD_NUM_EVENTS = 7
 
 # Exported symbols of include/moe.h, in declaration order.
 EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispatch",
-           "moe_forward", "moe_backward", "moe_get_error", "moe_set_wait_timeout_ns",
-           "moe_debug_set_flags", "moe_status_string")
+           "moe_forward", "moe_backward", "moe_route_dispatch_noalloc", "moe_get_error",
+           "moe_set_wait_timeout_ns", "moe_debug_set_flags", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -55,6 +55,8 @@ def _load():
     lib.moe_forward.restype = i
     lib.moe_backward.argtypes = [p] * 6 + [i64, i, i, i, i] + [p] * 6 + [p, sz, p, p]
     lib.moe_backward.restype = i
+    lib.moe_route_dispatch_noalloc.argtypes = [p, p, i64, i, i, i] + [p] * 7 + [p]
+    lib.moe_route_dispatch_noalloc.restype = i
     lib.moe_get_error.argtypes = [p, p]
     lib.moe_get_error.restype = i
     lib.moe_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -143,6 +145,19 @@ def moe_backward(dy, x, logits, W1, W3, W2, k, dx, dW1, dW3, dW2, dgate, dlogits
                              d, E, k, d_ff, _ptr(dx), _ptr(dW1), _ptr(dW3), _ptr(dW2),
                              _ptr(dgate), _ptr(dlogits), _ptr(ws), _nbytes(ws),
                              _events(stage_events), _stream(stream)), "moe_backward")
+
+
+def moe_route_dispatch_noalloc(x, logits, k, topk_idx, gate, counts, offsets, perm, pos,
+                               x_perm, stream=None):
+    """moe_route_dispatch for callers that cannot allocate device memory: no workspace
+    argument; the scratch is a fixed array inside the library (see include/moe.h for the size
+    limit and the rule that calls must not overlap on the GPU)."""
+    T, d = x.shape
+    E = logits.shape[1]
+    _check(_lib.moe_route_dispatch_noalloc(_ptr(x), _ptr(logits), T, d, E, k, _ptr(topk_idx),
+                                           _ptr(gate), _ptr(counts), _ptr(offsets), _ptr(perm),
+                                           _ptr(pos), _ptr(x_perm), _stream(stream)),
+           "moe_route_dispatch_noalloc")
 
 
 def moe_get_error(ws, stream=None):

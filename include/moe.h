@@ -137,6 +137,26 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
                           float* dW3, float* dW2, float* dgate, float* dlogits, void* ws,
                           size_t ws_bytes, cudaEvent_t* stage_events, cudaStream_t stream);
 
+/*
+ * moe_route_dispatch without a workspace, for callers that cannot allocate device memory
+ * (code inside a host framework that owns every device allocation, serving loops where an
+ * allocation is not allowed, runtimes with a device memory budget fixed at start-up).  The
+ * pages have no counterpart: it is a packaging of moe_route_dispatch, same arguments minus
+ * ws/ws_bytes, same outputs and the same bit-exact results.
+ * Its scratch is a 2 MiB array inside the library image, held in the device memory of every
+ * GPU that loads the library until the process exits.  Limit: ceil(T/128) * E <= 262080
+ * (for example T = 131072 tokens with E = 256, or T = 32640 with E = 1024); larger sizes
+ * return MOE_ERR_UNSUPPORTED before anything is launched.  The first call on a device looks
+ * up the array's device address (the device must be current); make that first call before
+ * any stream capture.  Every call shares the array: calls that overlap on the GPU (unordered
+ * streams, or several host threads) race and give undefined results.  Device-side checks of
+ * this variant are recorded in the library's scratch and are not readable by the caller.
+ */
+moe_status_t moe_route_dispatch_noalloc(const moe_bf16_t* x, const float* logits, int64_t T,
+                                        int d, int E, int k, int32_t* topk_idx, float* gate,
+                                        int32_t* counts, int32_t* offsets, int32_t* perm,
+                                        int32_t* pos, moe_bf16_t* x_perm, cudaStream_t stream);
+
 /* Synchronises `stream`, reads the device error word of `ws` and returns it (MOE_OK when
  * no device-side problem was recorded since the last moe_route_dispatch / moe_forward on
  * this ws, which clear it).  Returns MOE_ERR_CUDA if the stream reports an error. */
