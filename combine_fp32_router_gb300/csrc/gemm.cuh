@@ -66,6 +66,10 @@ struct GemmParams {
   int debug_flags;
   int64_t max_tiles;  // tiles the workspace tables can describe
   int64_t rows_cap;   // permuted rows allocated in the workspace
+  const int32_t* n_pt;       // 256-row pair tiles (two 128-row tiles of one expert)
+  const int32_t* pt_expert;
+  const int32_t* pt_row0;
+  int M;                     // M extent of the K-over-rows kinds (d or d_ff)
 };
 
 constexpr int kBM = 128;
@@ -73,13 +77,18 @@ constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kEpiThreads = 128;
 
-template <int BN>
+template <int BN, bool PAIR = false>
 struct GemmCfg {
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
-  static constexpr uint32_t kBBytes = BN * kBK * 2;
+  // a CTA pair holds half of the B tile in each CTA
+  static constexpr int kBLocal = PAIR ? BN / 2 : BN;
+  static constexpr int kStages = (kABytes + kBLocal * kBK * 2 <= 32768) ? 6 : 4;
+  static constexpr uint32_t kBBytes = kBLocal * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
-  static constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 1024 + 256;
+  static constexpr int kBars = 2 * kStages + 5;  // full, empty, tfull x2, tempty x2, drain
+  static constexpr size_t kEpiBytes = 4 * 32 * 33 * 4;  // one transpose buffer per epilogue warp
+  static constexpr size_t kSmemBytes =
+      static_cast<size_t>(kStages) * kStageBytes + 1024 + 8 * kBars + 64 + kEpiBytes;
 };
 
 struct TileInfo {
@@ -89,30 +98,48 @@ struct TileInfo {
   int m0;     // first M index (K-over-rows)
   int n0;     // first N index
   int nk;     // number of 64-wide K blocks
+  int mvalid; // valid M rows of this CTA's 128 (K-over-rows kinds)
+  int nseg;   // rows of this CTA inside the expert's padded row segment (rows-grouped kinds);
+              // with PAIR the second half of an expert's last tile can lie past the segment,
+              // on the next expert's rows, and must not be written
   bool bad;   // tile tables out of range: every role skips the tile
 };
 
-template <int KIND, int BN>
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile) {
+// Tile -> (expert, rows, N block, K blocks) for this CTA.  With PAIR a tile is 256 rows of
+// one expert (rows-grouped kinds: two consecutive 128-row tiles; K-over-rows kinds: 256 rows
+// of M) and CTA rank r of the pair owns rows [128 r, 128 r + 128) of it.
+template <int KIND, int BN, bool PAIR>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, int rank) {
   TileInfo ti;
   if constexpr (KindTraits<KIND>::kRowsM) {
     const int mt = tile / p.nb;
     ti.n0 = (tile % p.nb) * BN;
-    ti.e = p.mt_expert[mt];
-    ti.row0 = p.mt_row0[mt];
-    ti.nvalid = p.poff[ti.e] + p.counts[ti.e] - ti.row0;
+    if constexpr (PAIR) {
+      ti.e = p.pt_expert[mt];
+      const int r0 = p.pt_row0[mt];
+      ti.bad = ti.e < 0 || ti.e >= p.E || r0 < 0 || r0 + kBM > p.rows_cap;
+      ti.row0 = r0 + kBM * rank;
+    } else {
+      ti.e = p.mt_expert[mt];
+      ti.row0 = p.mt_row0[mt];
+      ti.bad = ti.e < 0 || ti.e >= p.E || ti.row0 < 0 || ti.row0 + kBM > p.rows_cap;
+    }
+    ti.nvalid = ti.bad ? 0 : p.poff[ti.e] + p.counts[ti.e] - ti.row0;
+    ti.nseg = ti.bad ? 0 : p.poff[ti.e + 1] - ti.row0;
     ti.m0 = 0;
     ti.nk = p.nkb;
-    ti.bad = ti.e < 0 || ti.e >= p.E || ti.row0 < 0 || ti.row0 + kBM > p.rows_cap;
+    ti.mvalid = kBM;
   } else {
     const int per_e = p.mb * p.nb;
     ti.e = tile / per_e;
     const int rem = tile % per_e;
-    ti.m0 = (rem / p.nb) * kBM;
+    ti.m0 = (rem / p.nb) * (PAIR ? 2 * kBM : kBM) + (PAIR ? kBM * rank : 0);
     ti.n0 = (rem % p.nb) * BN;
     ti.row0 = p.poff[ti.e];
     ti.nk = (p.poff[ti.e + 1] - p.poff[ti.e]) / kBK;
     ti.nvalid = kBM;
+    ti.nseg = kBM;
+    ti.mvalid = p.M - ti.m0 < kBM ? (p.M - ti.m0 > 0 ? p.M - ti.m0 : 0) : kBM;
     ti.bad = ti.row0 < 0 || ti.nk < 0 || ti.row0 + ti.nk * kBK > p.rows_cap;
   }
   return ti;
@@ -148,137 +175,200 @@ __device__ __forceinline__ void ld_f32x16(const float* p, float (&v)[16]) {
   }
 }
 
-// Epilogue of one tile for one thread (= one accumulator row).
+// Each epilogue warp owns 32 accumulator rows (one per lane) and writes them 32 columns at a
+// time.  A lane holds 32 consecutive values of its own row; the warp transposes the 32 x 32
+// chunk through a padded shared buffer (32 x 33 floats, conflict-free both ways) so that every
+// global store instruction writes whole 128-byte lines of 4 (fp32) or 8 (bf16) rows.
+constexpr int kEpiBufFloats = 32 * 33;
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  float a[16], b[16];
+  tmem_ld16x2(taddr, taddr + 16, a, b);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = a[i];
+    v[16 + i] = b[i];
+  }
+}
+
+// rows [0, nstore) of the chunk are written; base points at (row 0, first column of chunk)
+template <bool BF16>
+__device__ __forceinline__ void store_chunk(float* buf, const float (&v)[32], char* base,
+                                            int64_t row_bytes, int nstore, int lane) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) buf[lane * 33 + c] = v[c];
+  __syncwarp();
+  if constexpr (BF16) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = 8 * i + (lane >> 2), c0 = (lane & 3) * 8;
+      const float* src = buf + row * 33 + c0;
+      if (row < nstore)
+        st_v4(base + row * row_bytes + c0 * 2,
+              make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
+                         pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7])));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int row = 4 * i + (lane >> 3), c0 = (lane & 7) * 4;
+      const float* src = buf + row * 33 + c0;
+      if (row < nstore)
+        st_v4(base + row * row_bytes + c0 * 4,
+              make_uint4(__float_as_uint(src[0]), __float_as_uint(src[1]),
+                         __float_as_uint(src[2]), __float_as_uint(src[3])));
+    }
+  }
+  __syncwarp();
+}
+
+// Epilogue of one tile for one epilogue warp (rows q*32 .. q*32+31 of the accumulator).
+// `tacc` is the warp's TMEM address (lane base q*32, accumulator column 0); `r` = q*32 + lane.
 template <int KIND, int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& ti,
-                                              uint32_t tacc, int r) {
+                                              uint32_t tacc, int q, int lane, float* buf) {
+  const int r = q * 32 + lane;
   const bool valid = r < ti.nvalid;
+  const int w0 = q * 32;  // first row of this warp
+  auto clamp_rows = [&](int n) { return n - w0 < 0 ? 0 : (n - w0 > 32 ? 32 : n - w0); };
   if constexpr (KIND == kFwd1) {
     constexpr int HALF = BN / 2;
-    const int64_t row = ti.row0 + r;
     const int c0 = ti.n0 / 2;  // h column of this tile's first accumulator column
-    uint16_t* H = static_cast<uint16_t*>(p.out0) + row * p.dff + c0;
+    const int64_t row0 = ti.row0 + w0;
+    char* H = reinterpret_cast<char*>(static_cast<uint16_t*>(p.out0) + row0 * p.dff + c0);
+    const int nstore = clamp_rows(ti.nseg);      // pad rows are written as zeros
+    const int nsave = clamp_rows(ti.nvalid);
 #pragma unroll 1
-    for (int ch = 0; ch < HALF / 16; ++ch) {
-      float a[16], b[16];
-      tmem_ld16x2(tacc + ch * 16, tacc + HALF + ch * 16, a, b);
-      if (valid) {
-        float h[16];
+    for (int ch = 0; ch < HALF / 32; ++ch) {
+      float a[32], b[32], h[32];
+      tmem_ld32(tacc + ch * 32, a);
+      tmem_ld32(tacc + HALF + ch * 32, b);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) h[i] = silu_f(a[i]) * b[i];
-        st_bf16x16(H + ch * 16, h);
-        if (p.save_ab) {
-          st_f32x16(p.save_a + row * p.dff + c0 + ch * 16, a);
-          st_f32x16(p.save_b + row * p.dff + c0 + ch * 16, b);
-        }
-      } else {
-        st_zero32(H + ch * 16);
+      for (int i = 0; i < 32; ++i) h[i] = valid ? silu_f(a[i]) * b[i] : 0.0f;
+      store_chunk<true>(buf, h, H + ch * 64, 2ll * p.dff, nstore, lane);
+      if (p.save_ab) {
+        char* SA = reinterpret_cast<char*>(p.save_a + row0 * p.dff + c0 + ch * 32);
+        char* SB = reinterpret_cast<char*>(p.save_b + row0 * p.dff + c0 + ch * 32);
+        store_chunk<false>(buf, a, SA, 4ll * p.dff, nsave, lane);
+        store_chunk<false>(buf, b, SB, 4ll * p.dff, nsave, lane);
       }
     }
-  } else if constexpr (KIND == kFwd2) {
-    const int64_t row = ti.row0 + r;
-    float* Y = static_cast<float*>(p.out0) + row * p.d + ti.n0;
+  } else if constexpr (KIND == kFwd2 || KIND == kDx) {
+    const int64_t row0 = ti.row0 + w0;
+    char* out = reinterpret_cast<char*>(static_cast<float*>(p.out0) + row0 * p.d + ti.n0);
+    const int nstore = clamp_rows(ti.nvalid);
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 16; ++ch) {
-      float v[16];
-      tmem_ld16(tacc + ch * 16, v);
-      if (valid) st_f32x16(Y + ch * 16, v);
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      float v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      store_chunk<false>(buf, v, out + ch * 128, 4ll * p.d, nstore, lane);
     }
   } else if constexpr (KIND == kDh) {
     const int64_t row = ti.row0 + r;
-    uint16_t* dA = static_cast<uint16_t*>(p.out0) + row * (2 * p.dff) + ti.n0;
-    uint16_t* dB = dA + p.dff;
+    const int64_t row0 = ti.row0 + w0;
+    char* dA = reinterpret_cast<char*>(static_cast<uint16_t*>(p.out0) + row0 * (2 * p.dff) + ti.n0);
+    char* dB = dA + 2ll * p.dff;
     const float* sa = p.save_a + row * p.dff + ti.n0;
     const float* sb = p.save_b + row * p.dff + ti.n0;
+    const int nstore = clamp_rows(ti.nseg);      // pad rows are written as zeros
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 16; ++ch) {
-      float dh[16];
-      tmem_ld16(tacc + ch * 16, dh);
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      float dh[32], da[32], db[32];
+      tmem_ld32(tacc + ch * 32, dh);
       if (valid) {
-        float a[16], b[16], da[16], db[16];
-        ld_f32x16(sa + ch * 16, a);
-        ld_f32x16(sb + ch * 16, b);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float sg = 1.0f / (1.0f + expf(-a[i]));
-          da[i] = dh[i] * b[i] * (sg * (1.0f + a[i] * (1.0f - sg)));
-          db[i] = dh[i] * (a[i] * sg);
+        for (int h = 0; h < 2; ++h) {
+          float a[16], b[16];
+          ld_f32x16(sa + ch * 32 + 16 * h, a);
+          ld_f32x16(sb + ch * 32 + 16 * h, b);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float sg = 1.0f / (1.0f + expf(-a[i]));
+            da[16 * h + i] = dh[16 * h + i] * b[i] * (sg * (1.0f + a[i] * (1.0f - sg)));
+            db[16 * h + i] = dh[16 * h + i] * (a[i] * sg);
+          }
         }
-        st_bf16x16(dA + ch * 16, da);
-        st_bf16x16(dB + ch * 16, db);
       } else {
-        st_zero32(dA + ch * 16);
-        st_zero32(dB + ch * 16);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          da[i] = 0.0f;
+          db[i] = 0.0f;
+        }
       }
-    }
-  } else if constexpr (KIND == kDx) {
-    const int64_t row = ti.row0 + r;
-    float* out = static_cast<float*>(p.out0) + row * p.d + ti.n0;
-#pragma unroll 1
-    for (int ch = 0; ch < BN / 16; ++ch) {
-      float v[16];
-      tmem_ld16(tacc + ch * 16, v);
-      if (valid) st_f32x16(out + ch * 16, v);
+      store_chunk<true>(buf, da, dA + ch * 64, 4ll * p.dff, nstore, lane);
+      store_chunk<true>(buf, db, dB + ch * 64, 4ll * p.dff, nstore, lane);
     }
   } else {
-    // K-over-rows kinds: output row m0 + r of expert e's weight gradient.
-    float* out;
-    int ld;
+    // K-over-rows kinds: output rows m0 + w0 .. of expert e's weight gradient.
+    char* out;
+    int64_t row_bytes;
     if constexpr (KIND == kDw2) {
-      ld = p.d;
-      out = static_cast<float*>(p.out0) +
-            (static_cast<int64_t>(ti.e) * p.dff + ti.m0 + r) * p.d + ti.n0;
+      row_bytes = 4ll * p.d;
+      out = reinterpret_cast<char*>(static_cast<float*>(p.out0) +
+                                    (static_cast<int64_t>(ti.e) * p.dff + ti.m0 + w0) * p.d + ti.n0);
     } else {
-      ld = p.dff;
+      row_bytes = 4ll * p.dff;
       const bool first = ti.n0 < p.dff;
-      float* base = static_cast<float*>(first ? p.out0 : p.out1);
-      out = base + (static_cast<int64_t>(ti.e) * p.d + ti.m0 + r) * p.dff +
-            (first ? ti.n0 : ti.n0 - p.dff);
+      float* basep = static_cast<float*>(first ? p.out0 : p.out1);
+      out = reinterpret_cast<char*>(basep + (static_cast<int64_t>(ti.e) * p.d + ti.m0 + w0) * p.dff +
+                                    (first ? ti.n0 : ti.n0 - p.dff));
     }
-    (void)ld;
+    const int nstore = clamp_rows(ti.mvalid);
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 16; ++ch) {
-      float v[16];
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      float v[32];
       if (ti.nk > 0) {
-        tmem_ld16(tacc + ch * 16, v);
+        tmem_ld32(tacc + ch * 32, v);
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
       }
-      st_f32x16(out + ch * 16, v);
+      store_chunk<false>(buf, v, out + ch * 128, row_bytes, nstore, lane);
     }
   }
 }
 
-template <int KIND, int BN>
+// PAIR: a cluster of two CTAs on two SMs computes one 256 x BN tile with
+// tcgen05.mma.cta_group::2.  Each CTA loads its own 128 rows of A and half of B into its own
+// shared memory; rank 0 issues the MMAs (M = 256), whose result lands in both CTAs' TMEM
+// (128 rows each).  Both CTAs' loads complete on rank 0's full barrier (TMA .cta_group::2),
+// armed by rank 0 for both, so the MMA issuer waits on the barrier the data itself lands
+// on; rank 0's commits arrive on both CTAs' empty / tmem-full barriers (multicast); both
+// epilogues release the accumulator on rank 0's tmem-empty barrier.
+template <int KIND, int BN, bool PAIR>
 __global__ void __launch_bounds__(256, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapB0,
                         const __grid_constant__ CUtensorMap mapB1, const GemmParams p) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, PAIR>;
   using Tr = KindTraits<KIND>;
   constexpr int S = Cfg::kStages;
-  constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN, Tr::kAmn, Tr::kBmn);
+  constexpr int BL = Cfg::kBLocal;  // B columns held by this CTA
+  constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN, Tr::kAmn, Tr::kBmn);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t bar0 = base + S * Cfg::kStageBytes;
-  // barrier block: full[S], empty[S], tfull[2], tempty[2], drain  (8 bytes each)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
-  uint8_t* misc = gbase + S * Cfg::kStageBytes + 8 * (2 * S + 5);
+  uint8_t* misc = gbase + S * Cfg::kStageBytes + 8 * Cfg::kBars;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(misc + 8);
+  volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(misc + 12);
+  float* epi_buf = reinterpret_cast<float*>(misc + 64);  // 4 x (32 x 33) floats
   auto stage_a = [&](int s) { return base + s * Cfg::kStageBytes; };
   auto stage_b = [&](int s) { return base + s * Cfg::kStageBytes + kABytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int nunits = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -287,29 +377,37 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiThreads);
+      mbar_init(tempty_bar(a), PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     *consumed = 0u;
+    *peer_issued = 0u;
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_holder)), Cfg::kTmemCols);
+    if constexpr (PAIR) tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_holder)), Cfg::kTmemCols);
+    else tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_holder)), Cfg::kTmemCols);
     tc_fence_before();
   }
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // peer barriers initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
   int64_t ntiles64;
-  if constexpr (Tr::kRowsM) ntiles64 = static_cast<int64_t>(p.n_mt[0]) * p.nb;
+  if constexpr (Tr::kRowsM) ntiles64 = static_cast<int64_t>(PAIR ? p.n_pt[0] : p.n_mt[0]) * p.nb;
   else ntiles64 = static_cast<int64_t>(p.E) * p.mb * p.nb;
   if (ntiles64 > p.max_tiles || ntiles64 < 0) {
     if (threadIdx.x == 0) set_error(p.err, MOE_ERR_DEVICE_BOUNDS, 10);
     ntiles64 = 0;
   }
   const int ntiles = static_cast<int>(ntiles64);
+
+  auto wait_bar = [&](uint32_t bar, uint32_t par, volatile int* ab, int site) {
+    if constexpr (PAIR) return mbar_wait_cluster(bar, par, ab, p.err, site, p.wait_ns);
+    else return mbar_wait(bar, par, ab, p.err, site, p.wait_ns);
+  };
 
   uint32_t issued = 0;
   int skipped = -1;
@@ -321,74 +419,89 @@ __global__ void __launch_bounds__(256, 1)
     tma_prefetch_desc(&mapB1);
     uint32_t fill = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND, BN>(p, tile);
+    // with PAIR every load completes on rank 0's full barrier
+    auto load = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y) {
+      if constexpr (PAIR) tma_load_2d_pair(dst, m, mapa_shared(fb, 0), x, y);
+      else tma_load_2d(dst, m, fb, x, y);
+    };
+    for (int tile = unit; tile < ntiles && ok; tile += nunits) {
+      const TileInfo ti = decode_tile<KIND, BN, PAIR>(p, tile, rank);
       if (ti.bad) {
         set_error(p.err, MOE_ERR_DEVICE_BOUNDS, 11);
         continue;
       }
+      const int nb0 = ti.n0 + rank * BL;  // first B column held by this CTA
       for (int kb = 0; kb < ti.nk; ++kb) {
         const int s = fill % S;
         const uint32_t ph = (fill / S) & 1u;
-        if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err, 1, p.wait_ns)) {
+        if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, 1)) {
           ok = false;
           break;
         }
         const uint32_t fb = full_bar(s), sa = stage_a(s), sb = stage_b(s);
         if ((p.debug_flags & 1) && blockIdx.x == 0 && fill == 0) {
-          skipped = 0;  // test hook: this stage is never filled
+          skipped = 0;  // test hook: this stage is never armed nor filled by this CTA
         } else {
-          mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+          // rank 0 arms its barrier for both CTAs' bytes; rank 1 only loads
+          if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * Cfg::kStageBytes : Cfg::kStageBytes);
           const int k0 = kb * kBK;
           if constexpr (KIND == kFwd1) {
-            tma_load_2d(sa, &mapA, fb, k0, ti.row0);
+            load(sa, &mapA, fb, k0, ti.row0);
             const int wrow = ti.e * p.d + k0;
+            const int h0 = ti.n0 / 2;  // first h column of the tile
+            if constexpr (PAIR) {
+              // rank 0 holds the W1 half of B, rank 1 the W3 half
+              const CUtensorMap* wm = rank == 0 ? &mapB0 : &mapB1;
 #pragma unroll
-            for (int i = 0; i < BN / 128; ++i) {
-              tma_load_2d(sb + 8192u * i, &mapB0, fb, ti.n0 / 2 + 64 * i, wrow);
-              tma_load_2d(sb + 8192u * (BN / 128 + i), &mapB1, fb, ti.n0 / 2 + 64 * i, wrow);
+              for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, wm, fb, h0 + 64 * i, wrow);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN / 128; ++i) {
+                load(sb + 8192u * i, &mapB0, fb, h0 + 64 * i, wrow);
+                load(sb + 8192u * (BN / 128 + i), &mapB1, fb, h0 + 64 * i, wrow);
+              }
             }
           } else if constexpr (KIND == kFwd2) {
-            tma_load_2d(sa, &mapA, fb, k0, ti.row0);
+            load(sa, &mapA, fb, k0, ti.row0);
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_2d(sb + 8192u * i, &mapB0, fb, ti.n0 + 64 * i, ti.e * p.dff + k0);
+            for (int i = 0; i < BL / 64; ++i)
+              load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, ti.e * p.dff + k0);
           } else if constexpr (KIND == kDh) {
-            tma_load_2d(sa, &mapA, fb, k0, ti.row0);
-            tma_load_2d(sb, &mapB0, fb, k0, ti.e * p.dff + ti.n0);
+            load(sa, &mapA, fb, k0, ti.row0);
+            load(sb, &mapB0, fb, k0, ti.e * p.dff + nb0);
           } else if constexpr (KIND == kDx) {
-            tma_load_2d(sa, &mapA, fb, k0, ti.row0);
-            if (k0 < p.dff) tma_load_2d(sb, &mapB0, fb, k0, ti.e * p.d + ti.n0);
-            else tma_load_2d(sb, &mapB1, fb, k0 - p.dff, ti.e * p.d + ti.n0);
+            load(sa, &mapA, fb, k0, ti.row0);
+            if (k0 < p.dff) load(sb, &mapB0, fb, k0, ti.e * p.d + nb0);
+            else load(sb, &mapB1, fb, k0 - p.dff, ti.e * p.d + nb0);
           } else {
             const int r = ti.row0 + k0;
-            tma_load_2d(sa, &mapA, fb, ti.m0, r);
-            tma_load_2d(sa + 8192u, &mapA, fb, ti.m0 + 64, r);
+            load(sa, &mapA, fb, ti.m0, r);
+            load(sa + 8192u, &mapA, fb, ti.m0 + 64, r);
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + 8192u * i, &mapB0, fb, ti.n0 + 64 * i, r);
+            for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, r);
           }
         }
         ++fill;
       }
     }
     issued = fill;
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------------------ MMA issuer
     uint32_t fill = 0;
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND, BN>(p, tile);
+    for (int tile = unit; tile < ntiles && ok; tile += nunits) {
+      const TileInfo ti = decode_tile<KIND, BN, PAIR>(p, tile, 0);
       if (ti.bad) continue;
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1u;
-      if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.err, 2, p.wait_ns)) break;
+      if (!wait_bar(tempty_bar(acc), aph ^ 1u, abort_flag, 2)) break;
       tc_fence_after();
       const uint32_t dtm = tmem_base + acc * BN;
       for (int kb = 0; kb < ti.nk; ++kb) {
         const int s = fill % S;
         const uint32_t ph = (fill / S) & 1u;
-        if (!mbar_wait(full_bar(s), ph, abort_flag, p.err, 3, p.wait_ns)) {
+        if (!wait_bar(full_bar(s), ph, abort_flag, 3)) {
           ok = false;
           break;
         }
@@ -400,56 +513,87 @@ __global__ void __launch_bounds__(256, 1)
                                        : smem_desc_sw128(sa + kk * 32u, 16u, 1024u);
           const uint64_t bd = Tr::kBmn ? smem_desc_sw128(sb + kk * 2048u, 8192u, 1024u)
                                        : smem_desc_sw128(sb + kk * 32u, 16u, 1024u);
-          umma_f16(dtm, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          if constexpr (PAIR) umma_f16_pair(dtm, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          else umma_f16(dtm, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
         }
-        umma_commit(empty_bar(s));
+        if constexpr (PAIR) umma_commit_pair(empty_bar(s), 3);
+        else umma_commit(empty_bar(s));
         ++fill;
         *consumed = fill;
       }
       if (!ok) break;
-      umma_commit(tfull_bar(acc));
+      if constexpr (PAIR) umma_commit_pair(tfull_bar(acc), 3);
+      else umma_commit(tfull_bar(acc));
       ++it;
     }
     // all MMAs issued by this thread complete before TMEM is released
-    umma_commit(drain_bar);
+    if constexpr (PAIR) umma_commit_pair(drain_bar, 1);
+    else umma_commit(drain_bar);
     mbar_wait(drain_bar, 0u, nullptr, p.err, 4, p.wait_ns);
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp - 4;
     const int r = q * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND, BN>(p, tile);
+    const uint32_t release_to = PAIR ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+    for (int tile = unit; tile < ntiles; tile += nunits) {
+      const TileInfo ti = decode_tile<KIND, BN, PAIR>(p, tile, rank);
       if (ti.bad) continue;
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1u;
       // warp-uniform decision: the tcgen05.ld below is .sync.aligned
-      const bool ok = mbar_wait(tfull_bar(acc), aph, abort_flag, p.err, 5, p.wait_ns);
+      const bool ok = wait_bar(tfull_bar(acc), aph, abort_flag, 5);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<KIND, BN>(p, ti, tacc, r);
+      epilogue_tile<KIND, BN>(p, ti, tacc, q, lane, epi_buf + q * kEpiBufFloats);
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(release_to + 8u * acc);
+        else mbar_arrive(release_to + 8u * acc);
+      }
       ++it;
     }
   }
 
   __syncthreads();
-  if (warp == 0 && lane == 0) {
-    // wait for every operand load still in flight (only after an abort)
-    for (uint32_t f = *consumed; f < issued; ++f) {
-      if (static_cast<int>(f) == skipped) continue;
+  // After an abort, wait for every operand load still in flight before TMEM is released and
+  // the CTAs exit.  With PAIR all loads complete on rank 0's barriers: rank 1 reports how many
+  // fills it issued, rank 0 re-balances the expected bytes of fills only one CTA issued and
+  // waits for them, then both CTAs leave together.
+  if constexpr (PAIR) {
+    if (rank == 1 && warp == 0 && lane == 0)
+      st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_issued)), 0), issued);
+    cluster_sync_all();
+  }
+  if (rank == 0 && warp == 0 && lane == 0) {
+    const uint32_t iss_p = PAIR ? *peer_issued : 0u;
+    const uint32_t last = issued > iss_p ? issued : iss_p;
+    for (uint32_t f = *consumed; f < last; ++f) {
       const int s = f % S;
-      uint64_t t0 = global_ns();
+      const bool armed = f < issued && static_cast<int>(f) != skipped;
+      if constexpr (PAIR) {
+        const bool peer_loaded = f < iss_p;
+        if (!armed) mbar_arrive_expect_tx(full_bar(s), peer_loaded ? Cfg::kStageBytes : 0u);
+        else if (!peer_loaded) mbar_complete_tx(full_bar(s), Cfg::kStageBytes);
+      } else {
+        if (!armed) continue;
+      }
+      const uint64_t t0 = global_ns();
       while (!mbar_try_wait(full_bar(s), (f / S) & 1u)) {
         if (global_ns() - t0 > p.wait_ns) break;
       }
     }
   }
+  if constexpr (PAIR) {
+    __syncthreads();
+    cluster_sync_all();  // no load, remote arrival or MMA into the peer after this point
+  }
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    else tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
 }
 
@@ -457,29 +601,41 @@ __global__ void __launch_bounds__(256, 1)
 CUtensorMap make_map_2d(const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                         uint32_t box_inner, uint32_t box_rows, cudaError_t* st);
 
-template <int KIND, int BN>
+template <int KIND, int BN, bool PAIR>
 cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                              const GemmParams& p, int64_t max_tiles, int num_sms,
                              cudaStream_t s) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, PAIR>;
+  auto kern = grouped_gemm_kernel<KIND, BN, PAIR>;
   // the opt-in shared-memory size is a per-device function attribute: set it once per device
   static unsigned long long attr_set_mask = 0ull;
   int dev = 0;
   cudaError_t st = cudaGetDevice(&dev);
   if (st != cudaSuccess) return st;
   if (dev < 64 && !(attr_set_mask & (1ull << dev))) {
-    st = cudaFuncSetAttribute(grouped_gemm_kernel<KIND, BN>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+    st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(Cfg::kSmemBytes));
     if (st != cudaSuccess) return st;
     attr_set_mask |= 1ull << dev;
   }
   GemmParams pp = p;
   pp.max_tiles = max_tiles;
-  int64_t grid = max_tiles < num_sms ? max_tiles : num_sms;
-  if (grid < 1) grid = 1;
-  grouped_gemm_kernel<KIND, BN><<<static_cast<unsigned>(grid), 256, Cfg::kSmemBytes, s>>>(a, b0, b1, pp);
-  return cudaGetLastError();
+  const int64_t units_max = PAIR ? num_sms / 2 : num_sms;
+  int64_t units = max_tiles < units_max ? max_tiles : units_max;
+  if (units < 1) units = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * units : units), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, pp);
 }
 
 }  // namespace moe

@@ -5,13 +5,28 @@ namespace moe {
 
 GemmParams base_params(const GemmCtx& c);
 
+namespace {
+template <int KIND>
+cudaError_t run_bn(int BN, bool pair, const CUtensorMap& a, const CUtensorMap& b0,
+                   const CUtensorMap& b1, const GemmParams& p, int64_t tiles, int sms,
+                   cudaStream_t s) {
+  if (BN == 256) {
+    if (pair) return run_grouped_gemm<KIND, 256, true>(a, b0, b1, p, tiles, sms, s);
+    return run_grouped_gemm<KIND, 256, false>(a, b0, b1, p, tiles, sms, s);
+  }
+  if (pair) return run_grouped_gemm<KIND, 128, true>(a, b0, b1, p, tiles, sms, s);
+  return run_grouped_gemm<KIND, 128, false>(a, b0, b1, p, tiles, sms, s);
+}
+}  // namespace
+
 cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s) {
   const WsLayout& L = *c.L;
   const int BN = (L.dff % 256 == 0) ? 256 : 128;
+  const uint32_t brows = c.pair ? BN / 2 : BN;
   cudaError_t st = cudaSuccess;
   // A = dO rows (K = d, K-major); B = W2[e] viewed as [dff rows][d] (K-major)
   const CUtensorMap a = make_map_2d(c.ws + L.dO, L.d, L.P_pad, 2ull * L.d, 64, 128, &st);
-  const CUtensorMap b0 = make_map_2d(c.W2, L.d, static_cast<uint64_t>(L.E) * L.dff, 2ull * L.d, 64, BN, &st);
+  const CUtensorMap b0 = make_map_2d(c.W2, L.d, static_cast<uint64_t>(L.E) * L.dff, 2ull * L.d, 64, brows, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = base_params(c);
   p.nb = L.dff / BN;
@@ -19,25 +34,24 @@ cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s) {
   p.out0 = c.ws + L.dAB;
   p.save_a = reinterpret_cast<float*>(c.ws + L.Asave);
   p.save_b = reinterpret_cast<float*>(c.ws + L.Bsave);
-  if (BN == 256) return run_grouped_gemm<kDh, 256>(a, b0, b0, p, L.max_mt * p.nb, c.num_sms, s);
-  return run_grouped_gemm<kDh, 128>(a, b0, b0, p, L.max_mt * p.nb, c.num_sms, s);
+  return run_bn<kDh>(BN, c.pair, a, b0, b0, p, L.max_mt * p.nb, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s) {
   const WsLayout& L = *c.L;
   const int BN = (L.d % 256 == 0) ? 256 : 128;
+  const uint32_t brows = c.pair ? BN / 2 : BN;
   cudaError_t st = cudaSuccess;
   // A = [dA|dB] rows (K = 2 dff); B = W1[e] / W3[e] viewed as [d rows][dff] (K-major)
   const CUtensorMap a = make_map_2d(c.ws + L.dAB, 2ull * L.dff, L.P_pad, 4ull * L.dff, 64, 128, &st);
-  const CUtensorMap b0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, BN, &st);
-  const CUtensorMap b1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, BN, &st);
+  const CUtensorMap b0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, brows, &st);
+  const CUtensorMap b1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, brows, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = base_params(c);
   p.nb = L.d / BN;
   p.nkb = 2 * L.dff / kBK;
   p.out0 = c.ws + L.dXp;
-  if (BN == 256) return run_grouped_gemm<kDx, 256>(a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
-  return run_grouped_gemm<kDx, 128>(a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
+  return run_bn<kDx>(BN, c.pair, a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s) {
@@ -49,12 +63,13 @@ cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s) {
   const CUtensorMap b0 = make_map_2d(c.ws + L.dO, L.d, L.P_pad, 2ull * L.d, 64, 64, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = base_params(c);
-  p.mb = L.dff / kBM;
+  p.M = L.dff;
+  const int mrows = c.pair ? 2 * kBM : kBM;
+  p.mb = (L.dff + mrows - 1) / mrows;
   p.nb = L.d / BN;
   p.out0 = c.dW2;
   const int64_t tiles = static_cast<int64_t>(L.E) * p.mb * p.nb;
-  if (BN == 256) return run_grouped_gemm<kDw2, 256>(a, b0, b0, p, tiles, c.num_sms, s);
-  return run_grouped_gemm<kDw2, 128>(a, b0, b0, p, tiles, c.num_sms, s);
+  return run_bn<kDw2>(BN, c.pair, a, b0, b0, p, tiles, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_dw13(const GemmCtx& c, cudaStream_t s) {
@@ -66,13 +81,14 @@ cudaError_t launch_gemm_dw13(const GemmCtx& c, cudaStream_t s) {
   const CUtensorMap b0 = make_map_2d(c.ws + L.dAB, 2ull * L.dff, L.P_pad, 4ull * L.dff, 64, 64, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = base_params(c);
-  p.mb = L.d / kBM;
+  p.M = L.d;
+  const int mrows = c.pair ? 2 * kBM : kBM;
+  p.mb = (L.d + mrows - 1) / mrows;
   p.nb = 2 * L.dff / BN;
   p.out0 = c.dW1;
   p.out1 = c.dW3;
   const int64_t tiles = static_cast<int64_t>(L.E) * p.mb * p.nb;
-  if (BN == 256) return run_grouped_gemm<kDw13, 256>(a, b0, b0, p, tiles, c.num_sms, s);
-  return run_grouped_gemm<kDw13, 128>(a, b0, b0, p, tiles, c.num_sms, s);
+  return run_bn<kDw13>(BN, c.pair, a, b0, b0, p, tiles, c.num_sms, s);
 }
 
 }  // namespace moe

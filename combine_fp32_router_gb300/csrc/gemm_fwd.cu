@@ -55,6 +55,9 @@ GemmParams base_params(const GemmCtx& c) {
   p.n_mt = reinterpret_cast<const int32_t*>(c.ws + L.n_mt);
   p.mt_expert = reinterpret_cast<const int32_t*>(c.ws + L.mt_expert);
   p.mt_row0 = reinterpret_cast<const int32_t*>(c.ws + L.mt_row0);
+  p.n_pt = reinterpret_cast<const int32_t*>(c.ws + L.n_pt);
+  p.pt_expert = reinterpret_cast<const int32_t*>(c.ws + L.pt_expert);
+  p.pt_row0 = reinterpret_cast<const int32_t*>(c.ws + L.pt_row0);
   p.counts = reinterpret_cast<const int32_t*>(c.ws + L.counts);
   p.poff = reinterpret_cast<const int32_t*>(c.ws + L.poff);
   p.err = c.err;
@@ -78,7 +81,8 @@ cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
   p.save_ab = c.save_ab;
   p.save_a = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Asave) : nullptr;
   p.save_b = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Bsave) : nullptr;
-  return run_grouped_gemm<kFwd1, 256>(a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
+  if (c.pair) return run_grouped_gemm<kFwd1, 256, true>(a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
+  return run_grouped_gemm<kFwd1, 256, false>(a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
@@ -90,12 +94,15 @@ cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
   GemmParams p = base_params(c);
   p.nkb = L.dff / kBK;
   p.out0 = c.ws + L.Y;
-  if (L.d % 256 == 0) {
-    p.nb = L.d / 256;
-    return run_grouped_gemm<kFwd2, 256>(a, b0, b0, p, L.max_mt * p.nb, c.num_sms, s);
+  const int BN = (L.d % 256 == 0) ? 256 : 128;
+  p.nb = L.d / BN;
+  const int64_t tiles = L.max_mt * p.nb;
+  if (BN == 256) {
+    if (c.pair) return run_grouped_gemm<kFwd2, 256, true>(a, b0, b0, p, tiles, c.num_sms, s);
+    return run_grouped_gemm<kFwd2, 256, false>(a, b0, b0, p, tiles, c.num_sms, s);
   }
-  p.nb = L.d / 128;
-  return run_grouped_gemm<kFwd2, 128>(a, b0, b0, p, L.max_mt * p.nb, c.num_sms, s);
+  if (c.pair) return run_grouped_gemm<kFwd2, 128, true>(a, b0, b0, p, tiles, c.num_sms, s);
+  return run_grouped_gemm<kFwd2, 128, false>(a, b0, b0, p, tiles, c.num_sms, s);
 }
 
 }  // namespace moe

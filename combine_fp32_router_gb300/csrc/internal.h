@@ -21,8 +21,9 @@ struct WsLayout {
   int64_t T = 0, P = 0, P_pad = 0, max_mt = 0, nblk = 0;
   int d = 0, E = 0, k = 0, dff = 0;
   size_t err = 0, hist = 0, bbase = 0, counts = 0, offsets = 0, poff = 0, n_mt = 0,
-         mt_expert = 0, mt_row0 = 0, topk = 0, gate = 0, pos = 0, perm = 0, xperm = 0, H = 0,
-         Y = 0, Asave = 0, Bsave = 0, dO = 0, dAB = 0, dXp = 0;
+         mt_expert = 0, mt_row0 = 0, n_pt = 0, pt_expert = 0, pt_row0 = 0, topk = 0, gate = 0,
+         pos = 0, perm = 0, xperm = 0, H = 0, Y = 0, Asave = 0, Bsave = 0, dO = 0, dAB = 0,
+         dXp = 0;
   size_t route_total = 0, fwd_total = 0, bwd_total = 0;
 };
 
@@ -35,10 +36,15 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
 cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* bbase,
                              int32_t* counts, cudaStream_t s);
 // offsets (unpadded, may be null), poff (rows padded to `align`), and when align == 128
-// the 128-row tile tables (n_mt, mt_expert, mt_row0).
+// the 128-row tile tables (n_mt, mt_expert, mt_row0) and the 256-row pair-tile tables
+// (n_pt, pt_expert, pt_row0; two consecutive 128-row tiles of one expert).
+struct TileTables {
+  int32_t *n_mt, *mt_expert, *mt_row0, *n_pt, *pt_expert, *pt_row0;
+  int64_t max_mt;
+};
 cudaError_t launch_offsets(const int32_t* counts, int E, int align, int32_t* offsets,
-                           int32_t* poff, int32_t* n_mt, int32_t* mt_expert, int32_t* mt_row0,
-                           int64_t max_mt, DevErr* err, cudaStream_t s);
+                           int32_t* poff, const TileTables* tables, DevErr* err,
+                           cudaStream_t s);
 cudaError_t launch_scatter(const uint16_t* x, int64_t T, int d, int E, int k,
                            const int32_t* topk, const int32_t* bbase, const int32_t* poff,
                            int32_t* pos, int32_t* perm, uint16_t* x_perm, int64_t rows_cap,
@@ -66,6 +72,7 @@ struct GemmCtx {
   uint64_t wait_ns;
   int debug_flags;
   int num_sms;
+  bool pair;  // 256-row tiles on CTA pairs (tcgen05 cta_group::2)
 };
 cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s);   // H = SwiGLU(Xp W1, Xp W3)
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s);   // Y = H W2

@@ -4,6 +4,7 @@
 // checks are plain integer tests, in the spirit of the report translation's section 2.1
 // (itsolotime.com): argument checking belongs in compiled host code, not in Python.
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -14,6 +15,17 @@ namespace {
 
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
 std::atomic<int> g_debug_flags{0};
+
+// Grouped GEMMs on CTA pairs (256-row tiles, tcgen05 cta_group::2) unless the environment
+// variable MOE_GEMM_PAIR is "0" (single-CTA 128-row tiles).  Both give bitwise identical
+// results; the switch exists to compare the two.
+bool use_pairs() {
+  static const bool v = [] {
+    const char* e = std::getenv("MOE_GEMM_PAIR");
+    return !(e && e[0] == '0');
+  }();
+  return v;
+}
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -88,6 +100,9 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   L.n_mt = take(16);
   L.mt_expert = take(static_cast<size_t>(L.max_mt) * 4);
   L.mt_row0 = take(static_cast<size_t>(L.max_mt) * 4);
+  L.n_pt = take(16);
+  L.pt_expert = take(static_cast<size_t>(L.max_mt) * 4);
+  L.pt_row0 = take(static_cast<size_t>(L.max_mt) * 4);
   L.topk = take(P * 4);
   L.gate = take(P * 4);
   L.pos = take(P * 4);
@@ -152,8 +167,7 @@ moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_
   MOE_TRY(launch_route_topk(logits, T, E, k, topk_idx, gate, pos, hist, err, stream));
   MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
   // unpadded rows: the padded offsets are the offsets themselves
-  MOE_TRY(launch_offsets(counts, E, 1, nullptr, offsets, nullptr, nullptr, nullptr, 0, err,
-                         stream));
+  MOE_TRY(launch_offsets(counts, E, 1, nullptr, offsets, nullptr, err, stream));
   MOE_TRY(launch_scatter(x, T, d, E, k, topk_idx, bbase, offsets, pos, perm, x_perm, L.P, err,
                          stream));
   return MOE_OK;
@@ -198,10 +212,15 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   // dispatch: route, count, prefix sums (rows padded to 128 per expert), stable permute
   MOE_TRY(launch_route_topk(logits, T, E, k, topk, gate, pos, hist, err, stream));
   MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
-  MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff,
-                         reinterpret_cast<int32_t*>(w + L.n_mt),
-                         reinterpret_cast<int32_t*>(w + L.mt_expert),
-                         reinterpret_cast<int32_t*>(w + L.mt_row0), L.max_mt, err, stream));
+  TileTables tt;
+  tt.n_mt = reinterpret_cast<int32_t*>(w + L.n_mt);
+  tt.mt_expert = reinterpret_cast<int32_t*>(w + L.mt_expert);
+  tt.mt_row0 = reinterpret_cast<int32_t*>(w + L.mt_row0);
+  tt.n_pt = reinterpret_cast<int32_t*>(w + L.n_pt);
+  tt.pt_expert = reinterpret_cast<int32_t*>(w + L.pt_expert);
+  tt.pt_row0 = reinterpret_cast<int32_t*>(w + L.pt_row0);
+  tt.max_mt = L.max_mt;
+  MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
   MOE_TRY(launch_scatter(x, T, d, E, k, topk, bbase, poff, pos, perm, xperm, L.P_pad, err,
                          stream));
   // padding rows: perm = -1; zero x rows when the backward will read them as a K operand
@@ -220,6 +239,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.wait_ns = g_wait_ns.load();
   c.debug_flags = g_debug_flags.load();
   c.num_sms = num_sms_of_current_device();
+  c.pair = use_pairs();
   MOE_TRY(launch_gemm_fwd1(c, stream));
   record(stage_events, 2, stream);
   MOE_TRY(launch_gemm_fwd2(c, stream));
@@ -283,6 +303,7 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   c.wait_ns = g_wait_ns.load();
   c.debug_flags = g_debug_flags.load();
   c.num_sms = num_sms_of_current_device();
+  c.pair = use_pairs();
   MOE_TRY(launch_gemm_dh(c, stream));
   record(stage_events, 2, stream);
   MOE_TRY(launch_gemm_dx(c, stream));

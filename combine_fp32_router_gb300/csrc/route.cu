@@ -198,11 +198,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
 
 __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E,
                                                        int align, int32_t* __restrict__ offsets,
-                                                       int32_t* __restrict__ poff,
-                                                       int32_t* __restrict__ n_mt,
-                                                       int32_t* __restrict__ mt_expert,
-                                                       int32_t* __restrict__ mt_row0,
-                                                       int64_t max_mt, DevErr* err) {
+                                                       int32_t* __restrict__ poff, TileTables tt,
+                                                       int with_tables, DevErr* err) {
   __shared__ int warp_tot[32];
   __shared__ int total;
   const int e = threadIdx.x;
@@ -218,17 +215,32 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   const int tot_p = total;
   if (e < E) poff[e] = poffv;
   if (e == 0) poff[E] = tot_p;
-  if (n_mt) {
+  if (with_tables) {
+    // 128-row tiles
     const int nm = pc / kTileRows;
     const int ms = block_exclusive_scan(nm, warp_tot, &total);
-    if (e == 0) n_mt[0] = total;
+    if (e == 0) tt.n_mt[0] = total;
     if (e < E) {
-      if (ms + nm > max_mt) {
+      if (ms + nm > tt.max_mt) {
         set_error(err, MOE_ERR_DEVICE_BOUNDS, 100);
       } else {
         for (int m = 0; m < nm; ++m) {
-          mt_expert[ms + m] = e;
-          mt_row0[ms + m] = poffv + m * kTileRows;
+          tt.mt_expert[ms + m] = e;
+          tt.mt_row0[ms + m] = poffv + m * kTileRows;
+        }
+      }
+    }
+    // 256-row pair tiles: two consecutive 128-row tiles of the same expert
+    const int np = (nm + 1) / 2;
+    const int ps = block_exclusive_scan(np, warp_tot, &total);
+    if (e == 0) tt.n_pt[0] = total;
+    if (e < E) {
+      if (ps + np > tt.max_mt) {
+        set_error(err, MOE_ERR_DEVICE_BOUNDS, 101);
+      } else {
+        for (int m = 0; m < np; ++m) {
+          tt.pt_expert[ps + m] = e;
+          tt.pt_row0[ps + m] = poffv + m * 2 * kTileRows;
         }
       }
     }
@@ -504,10 +516,11 @@ cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* 
 }
 
 cudaError_t launch_offsets(const int32_t* counts, int E, int align, int32_t* offsets,
-                           int32_t* poff, int32_t* n_mt, int32_t* mt_expert, int32_t* mt_row0,
-                           int64_t max_mt, DevErr* err, cudaStream_t s) {
-  offsets_kernel<<<1, 1024, 0, s>>>(counts, E, align, offsets, poff, n_mt, mt_expert, mt_row0,
-                                    max_mt, err);
+                           int32_t* poff, const TileTables* tables, DevErr* err,
+                           cudaStream_t s) {
+  TileTables tt{};
+  if (tables) tt = *tables;
+  offsets_kernel<<<1, 1024, 0, s>>>(counts, E, align, offsets, poff, tt, tables ? 1 : 0, err);
   return cudaGetLastError();
 }
 

@@ -94,8 +94,7 @@ extern "C" moe_status_t moe_route_dispatch_noalloc(
   if (launch_route_topk(logits, T, E, k, topk_idx, gate, pos, hist, err, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_scan_cols(hist, nblk, E, bbase, counts, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_offsets(counts, E, 1, nullptr, offsets, nullptr, nullptr, nullptr, 0, err, stream) !=
-      cudaSuccess)
+  if (launch_offsets(counts, E, 1, nullptr, offsets, nullptr, err, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_scatter(x, T, d, E, k, topk_idx, bbase, offsets, pos, perm, x_perm, T * k, err,
                      stream) != cudaSuccess)
