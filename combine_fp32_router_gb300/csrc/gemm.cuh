@@ -70,12 +70,21 @@ struct GemmParams {
   const int32_t* pt_expert;
   const int32_t* pt_row0;
   int M;                     // M extent of the K-over-rows kinds (d or d_ff)
+  // GEMM2 with the combine fused in (see combine_segment)
+  int fuse_combine;
+  const int32_t* perm;       // permuted row -> pair t*k + j
+  const int32_t* pos;        // pair -> permuted row
+  const float* gate;         // [T, k]
+  int32_t* seg_count;        // [T, nb]: rows of (token, N block) written so far
+  uint16_t* comb_out;        // [T, d] bf16 layer output
+  int k;
 };
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kEpiThreads = 128;
+
 
 template <int BN, bool PAIR = false>
 struct GemmCfg {
@@ -175,6 +184,62 @@ __device__ __forceinline__ void ld_f32x16(const float* p, float (&v)[16]) {
   }
 }
 
+// ---------------------------------------------------------------------------- fused combine
+// GEMM2 can run the combine itself.  When an epilogue warp has stored its 32 rows of a tile,
+// each row's lane counts one more finished row of its (token, N block) segment (integer
+// atomics: exact whatever their order).  A lane that brings a segment to k rows has the
+// whole warp combine it right away: out[t, cols] = bf16(sum_j gate[t,j] * Y[pos[t,j], cols])
+// with fp32 fused multiply-adds in slot order, the same arithmetic as the stand-alone
+// combine, so the result is bitwise identical.  The combine of earlier experts' tokens thus
+// runs under the MMAs of later experts (the accumulator is double-buffered, so the epilogue
+// has a whole tile's main loop to finish).
+template <int BN>
+__device__ __forceinline__ void combine_segment(const GemmParams& p, int seg, int lane) {
+  constexpr int CPL = BN / 32;  // columns per lane (8 or 4)
+  const int t = seg / p.nb, nblk = seg % p.nb;
+  int row = 0;
+  float g = 0.0f;
+  if (lane < p.k) {
+    row = p.pos[static_cast<int64_t>(t) * p.k + lane];
+    g = p.gate[static_cast<int64_t>(t) * p.k + lane];
+  }
+  const int col = nblk * BN + lane * CPL;
+  const float* Y = static_cast<const float*>(p.out0);
+  float4 y[kMaxK][CPL / 4];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    const int rj = __shfl_sync(0xFFFFFFFFu, row, j);
+    if (j < p.k) {
+      const float4* src = reinterpret_cast<const float4*>(Y + static_cast<int64_t>(rj) * p.d + col);
+#pragma unroll
+      for (int c4 = 0; c4 < CPL / 4; ++c4) y[j][c4] = __ldcg(src + c4);
+    }
+  }
+  float acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    const float gj = __shfl_sync(0xFFFFFFFFu, g, j);
+    if (j < p.k) {
+#pragma unroll
+      for (int c4 = 0; c4 < CPL / 4; ++c4) {
+        acc[4 * c4 + 0] = __fmaf_rn(gj, y[j][c4].x, acc[4 * c4 + 0]);
+        acc[4 * c4 + 1] = __fmaf_rn(gj, y[j][c4].y, acc[4 * c4 + 1]);
+        acc[4 * c4 + 2] = __fmaf_rn(gj, y[j][c4].z, acc[4 * c4 + 2]);
+        acc[4 * c4 + 3] = __fmaf_rn(gj, y[j][c4].w, acc[4 * c4 + 3]);
+      }
+    }
+  }
+  uint16_t* o = p.comb_out + static_cast<int64_t>(t) * p.d + col;
+  if constexpr (CPL == 8) {
+    st_v4(o, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+  } else {
+    *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+  }
+}
+
 // Each epilogue warp owns 32 accumulator rows (one per lane) and writes them 32 columns at a
 // time.  A lane holds 32 consecutive values of its own row; the warp transposes the 32 x 32
 // chunk through a padded shared buffer (32 x 33 floats, conflict-free both ways) so that every
@@ -262,6 +327,25 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       float v[32];
       tmem_ld32(tacc + ch * 32, v);
       store_chunk<false>(buf, v, out + ch * 128, 4ll * p.d, nstore, lane);
+    }
+    if constexpr (KIND == kFwd2) {
+      if (p.fuse_combine) {
+        __threadfence();  // this lane's row stores are visible device-wide ...
+        __syncwarp();     // ... before any lane of the warp counts its row as finished
+        int seg = -1;
+        if (valid) {
+          const int pair = p.perm[ti.row0 + r];
+          seg = (pair / p.k) * p.nb + ti.n0 / BN;
+          if (atomicAdd(&p.seg_count[seg], 1) != p.k - 1) seg = -1;
+        }
+        unsigned ready = __ballot_sync(0xFFFFFFFFu, seg >= 0);
+        if (ready) __threadfence();  // the other rows of those segments are visible
+        while (ready) {
+          const int src = __ffs(ready) - 1;
+          ready &= ready - 1;
+          combine_segment<BN>(p, __shfl_sync(0xFFFFFFFFu, seg, src), lane);
+        }
+      }
     }
   } else if constexpr (KIND == kDh) {
     const int64_t row = ti.row0 + r;
@@ -636,6 +720,23 @@ cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const 
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, pp);
+}
+
+// A rows-grouped GEMM: with pairs, every expert's full 256-row pair tiles run on CTA pairs
+// and its odd last 128-row tile on single CTAs (second launch); both give bitwise the same
+// rows.  `lo` carries the leftover tile table in place of the 128-row tile table; b0/b1 are
+// the B maps of the pair launch (a K-major B box holds BN/2 rows there), sb0/sb1 those of
+// single-CTA launches (BN rows).
+template <int KIND, int BN>
+cudaError_t run_rows_kind(bool pair, const CUtensorMap& a, const CUtensorMap& b0,
+                          const CUtensorMap& b1, const CUtensorMap& sb0, const CUtensorMap& sb1,
+                          const GemmParams& p, const GemmParams& lo, int64_t max_mt, int E,
+                          int num_sms, cudaStream_t s) {
+  if (!pair) return run_grouped_gemm<KIND, BN, false>(a, sb0, sb1, p, max_mt * p.nb, num_sms, s);
+  cudaError_t st = run_grouped_gemm<KIND, BN, true>(a, b0, b1, p, max_mt * p.nb, num_sms, s);
+  if (st != cudaSuccess) return st;
+  return run_grouped_gemm<KIND, BN, false>(a, sb0, sb1, lo, static_cast<int64_t>(E) * lo.nb,
+                                           num_sms, s);
 }
 
 }  // namespace moe

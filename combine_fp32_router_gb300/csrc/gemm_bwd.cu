@@ -4,6 +4,7 @@
 namespace moe {
 
 GemmParams base_params(const GemmCtx& c);
+GemmParams leftover_params(const GemmParams& p, const GemmCtx& c);
 
 namespace {
 template <int KIND>
@@ -27,6 +28,7 @@ cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s) {
   // A = dO rows (K = d, K-major); B = W2[e] viewed as [dff rows][d] (K-major)
   const CUtensorMap a = make_map_2d(c.ws + L.dO, L.d, L.P_pad, 2ull * L.d, 64, 128, &st);
   const CUtensorMap b0 = make_map_2d(c.W2, L.d, static_cast<uint64_t>(L.E) * L.dff, 2ull * L.d, 64, brows, &st);
+  const CUtensorMap sb0 = make_map_2d(c.W2, L.d, static_cast<uint64_t>(L.E) * L.dff, 2ull * L.d, 64, BN, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = base_params(c);
   p.nb = L.dff / BN;
@@ -34,7 +36,9 @@ cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s) {
   p.out0 = c.ws + L.dAB;
   p.save_a = reinterpret_cast<float*>(c.ws + L.Asave);
   p.save_b = reinterpret_cast<float*>(c.ws + L.Bsave);
-  return run_bn<kDh>(BN, c.pair, a, b0, b0, p, L.max_mt * p.nb, c.num_sms, s);
+  const GemmParams lo = leftover_params(p, c);
+  if (BN == 256) return run_rows_kind<kDh, 256>(c.pair, a, b0, b0, sb0, sb0, p, lo, L.max_mt, L.E, c.num_sms, s);
+  return run_rows_kind<kDh, 128>(c.pair, a, b0, b0, sb0, sb0, p, lo, L.max_mt, L.E, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s) {
@@ -46,12 +50,16 @@ cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s) {
   const CUtensorMap a = make_map_2d(c.ws + L.dAB, 2ull * L.dff, L.P_pad, 4ull * L.dff, 64, 128, &st);
   const CUtensorMap b0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, brows, &st);
   const CUtensorMap b1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, brows, &st);
+  const CUtensorMap sb0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, BN, &st);
+  const CUtensorMap sb1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, BN, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = base_params(c);
   p.nb = L.d / BN;
   p.nkb = 2 * L.dff / kBK;
   p.out0 = c.ws + L.dXp;
-  return run_bn<kDx>(BN, c.pair, a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
+  const GemmParams lo = leftover_params(p, c);
+  if (BN == 256) return run_rows_kind<kDx, 256>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, L.E, c.num_sms, s);
+  return run_rows_kind<kDx, 128>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, L.E, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s) {

@@ -67,6 +67,15 @@ GemmParams base_params(const GemmCtx& c) {
   return p;
 }
 
+// The same parameters with the leftover-tile table in place of the 128-row tile table.
+GemmParams leftover_params(const GemmParams& p, const GemmCtx& c) {
+  GemmParams lo = p;
+  lo.n_mt = reinterpret_cast<const int32_t*>(c.ws + c.L->n_lo);
+  lo.mt_expert = reinterpret_cast<const int32_t*>(c.ws + c.L->lo_expert);
+  lo.mt_row0 = reinterpret_cast<const int32_t*>(c.ws + c.L->lo_row0);
+  return lo;
+}
+
 cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
   const WsLayout& L = *c.L;
   cudaError_t st = cudaSuccess;
@@ -81,8 +90,8 @@ cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
   p.save_ab = c.save_ab;
   p.save_a = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Asave) : nullptr;
   p.save_b = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Bsave) : nullptr;
-  if (c.pair) return run_grouped_gemm<kFwd1, 256, true>(a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
-  return run_grouped_gemm<kFwd1, 256, false>(a, b0, b1, p, L.max_mt * p.nb, c.num_sms, s);
+  return run_rows_kind<kFwd1, 256>(c.pair, a, b0, b1, b0, b1, p, leftover_params(p, c), L.max_mt,
+                                   L.E, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
@@ -96,13 +105,17 @@ cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
   p.out0 = c.ws + L.Y;
   const int BN = (L.d % 256 == 0) ? 256 : 128;
   p.nb = L.d / BN;
-  const int64_t tiles = L.max_mt * p.nb;
-  if (BN == 256) {
-    if (c.pair) return run_grouped_gemm<kFwd2, 256, true>(a, b0, b0, p, tiles, c.num_sms, s);
-    return run_grouped_gemm<kFwd2, 256, false>(a, b0, b0, p, tiles, c.num_sms, s);
-  }
-  if (c.pair) return run_grouped_gemm<kFwd2, 128, true>(a, b0, b0, p, tiles, c.num_sms, s);
-  return run_grouped_gemm<kFwd2, 128, false>(a, b0, b0, p, tiles, c.num_sms, s);
+  p.fuse_combine = c.fuse_combine ? 1 : 0;
+  p.perm = reinterpret_cast<const int32_t*>(c.ws + L.perm);
+  p.pos = reinterpret_cast<const int32_t*>(c.ws + L.pos);
+  p.gate = reinterpret_cast<const float*>(c.ws + L.gate);
+  p.seg_count = reinterpret_cast<int32_t*>(c.ws + L.seg);
+  p.comb_out = c.out;
+  p.k = L.k;
+  const GemmParams lo = leftover_params(p, c);
+  if (BN == 256)
+    return run_rows_kind<kFwd2, 256>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, L.E, c.num_sms, s);
+  return run_rows_kind<kFwd2, 128>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, L.E, c.num_sms, s);
 }
 
 }  // namespace moe

@@ -21,9 +21,10 @@ struct WsLayout {
   int64_t T = 0, P = 0, P_pad = 0, max_mt = 0, nblk = 0;
   int d = 0, E = 0, k = 0, dff = 0;
   size_t err = 0, hist = 0, bbase = 0, counts = 0, offsets = 0, poff = 0, n_mt = 0,
-         mt_expert = 0, mt_row0 = 0, n_pt = 0, pt_expert = 0, pt_row0 = 0, topk = 0, gate = 0,
+         mt_expert = 0, mt_row0 = 0, n_pt = 0, pt_expert = 0, pt_row0 = 0, n_lo = 0,
+         lo_expert = 0, lo_row0 = 0, topk = 0, gate = 0,
          pos = 0, perm = 0, xperm = 0, H = 0, Y = 0, Asave = 0, Bsave = 0, dO = 0, dAB = 0,
-         dXp = 0;
+         dXp = 0, seg = 0;
   size_t route_total = 0, fwd_total = 0, bwd_total = 0;
 };
 
@@ -36,10 +37,11 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
 cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* bbase,
                              int32_t* counts, cudaStream_t s);
 // offsets (unpadded, may be null), poff (rows padded to `align`), and when align == 128
-// the 128-row tile tables (n_mt, mt_expert, mt_row0) and the 256-row pair-tile tables
-// (n_pt, pt_expert, pt_row0; two consecutive 128-row tiles of one expert).
+// the tile tables: every 128-row tile (n_mt, mt_expert, mt_row0); the 256-row pair tiles
+// (n_pt, pt_expert, pt_row0: two consecutive 128-row tiles of one expert); and each
+// expert's odd last 128-row tile (n_lo, lo_expert, lo_row0), which pairs leave over.
 struct TileTables {
-  int32_t *n_mt, *mt_expert, *mt_row0, *n_pt, *pt_expert, *pt_row0;
+  int32_t *n_mt, *mt_expert, *mt_row0, *n_pt, *pt_expert, *pt_row0, *n_lo, *lo_expert, *lo_row0;
   int64_t max_mt;
 };
 cudaError_t launch_offsets(const int32_t* counts, int E, int align, int32_t* offsets,
@@ -73,6 +75,8 @@ struct GemmCtx {
   int debug_flags;
   int num_sms;
   bool pair;  // 256-row tiles on CTA pairs (tcgen05 cta_group::2)
+  bool fuse_combine;     // GEMM2 also combines finished tokens into `out`
+  uint16_t* out;         // layer output [T, d] (fused combine)
 };
 cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s);   // H = SwiGLU(Xp W1, Xp W3)
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s);   // Y = H W2

@@ -103,6 +103,9 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   L.n_pt = take(16);
   L.pt_expert = take(static_cast<size_t>(L.max_mt) * 4);
   L.pt_row0 = take(static_cast<size_t>(L.max_mt) * 4);
+  L.n_lo = take(16);
+  L.lo_expert = take(static_cast<size_t>(E) * 4);
+  L.lo_row0 = take(static_cast<size_t>(E) * 4);
   L.topk = take(P * 4);
   L.gate = take(P * 4);
   L.pos = take(P * 4);
@@ -110,6 +113,7 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   L.xperm = take(Pp * d * 2);
   L.H = take(Pp * dff * 2);
   L.Y = take(Pp * d * 4);
+  L.seg = take(P / (k > 0 ? k : 1) * static_cast<size_t>(d / 128) * 4);  // [T, d/128] counters
   L.fwd_total = off;
   L.Asave = take(Pp * dff * 4);
   L.Bsave = take(Pp * dff * 4);
@@ -181,7 +185,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   if (st != MOE_OK) return st;
   if (!W1 || !W3 || !W2 || !ws) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
-  if (flags & ~MOE_FWD_SAVE_FOR_BACKWARD) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_FWD_SAVE_FOR_BACKWARD | MOE_FWD_FUSED_COMBINE)) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, logits, W1, W3, W2, out};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
@@ -219,6 +223,9 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   tt.n_pt = reinterpret_cast<int32_t*>(w + L.n_pt);
   tt.pt_expert = reinterpret_cast<int32_t*>(w + L.pt_expert);
   tt.pt_row0 = reinterpret_cast<int32_t*>(w + L.pt_row0);
+  tt.n_lo = reinterpret_cast<int32_t*>(w + L.n_lo);
+  tt.lo_expert = reinterpret_cast<int32_t*>(w + L.lo_expert);
+  tt.lo_row0 = reinterpret_cast<int32_t*>(w + L.lo_row0);
   tt.max_mt = L.max_mt;
   MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
   MOE_TRY(launch_scatter(x, T, d, E, k, topk, bbase, poff, pos, perm, xperm, L.P_pad, err,
@@ -240,8 +247,19 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.debug_flags = g_debug_flags.load();
   c.num_sms = num_sms_of_current_device();
   c.pair = use_pairs();
+  c.fuse_combine = (flags & MOE_FWD_FUSED_COMBINE) != 0;
+  c.out = out;
   MOE_TRY(launch_gemm_fwd1(c, stream));
   record(stage_events, 2, stream);
+  if (c.fuse_combine) {
+    // GEMM2 combines each token as soon as its k expert rows are written
+    const int bn2 = (d % 256 == 0) ? 256 : 128;
+    MOE_TRY(cudaMemsetAsync(w + L.seg, 0, static_cast<size_t>(T) * (d / bn2) * 4, stream));
+    MOE_TRY(launch_gemm_fwd2(c, stream));
+    record(stage_events, 3, stream);
+    record(stage_events, 4, stream);
+    return MOE_OK;
+  }
   MOE_TRY(launch_gemm_fwd2(c, stream));
   record(stage_events, 3, stream);
   MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,

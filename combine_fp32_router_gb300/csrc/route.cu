@@ -196,6 +196,23 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
   return warp_tot[w] + incl - v;
 }
 
+// Position of element i of list A (length na) when A and B (length nb) are merged in
+// proportion: element i of A sits at relative time (i + 1/2) / na, element j of B at
+// (j + 1/2) / nb; ties go to the first list (`a_first`).  Positions form a permutation of
+// [0, na + nb) and keep each list's order.
+__device__ __forceinline__ int merge_position(int i, int na, int nb, bool a_first) {
+  if (nb == 0) return i;
+  const int64_t num = (2ll * i + 1) * nb - na;
+  int64_t before;  // elements of B placed before element i of A
+  if (a_first) {   // B elements strictly earlier: (2j+1) na < (2i+1) nb
+    before = num <= 0 ? 0 : (num + 2ll * na - 1) / (2ll * na);
+  } else {         // B elements earlier or tied: (2j+1) na <= (2i+1) nb
+    before = num < 0 ? 0 : num / (2ll * na) + 1;
+  }
+  if (before > nb) before = nb;
+  return i + static_cast<int>(before);
+}
+
 __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E,
                                                        int align, int32_t* __restrict__ offsets,
                                                        int32_t* __restrict__ poff, TileTables tt,
@@ -216,33 +233,51 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   if (e < E) poff[e] = poffv;
   if (e == 0) poff[E] = tot_p;
   if (with_tables) {
-    // 128-row tiles
+    // Tile order.  Experts with one 128-row tile are bound by reading their weights (a tile
+    // does 2 FLOP per weight byte per row, far below the GPU's FLOP/byte ratio), the others by
+    // the tensor cores.  Both lists keep expert order and are merged in proportion, so the
+    // weight streams of light experts overlap the math of heavy ones instead of all coming
+    // last.  The order changes no result: every tile is computed the same way wherever it runs.
     const int nm = pc / kTileRows;
-    const int ms = block_exclusive_scan(nm, warp_tot, &total);
-    if (e == 0) tt.n_mt[0] = total;
+    const bool heavy = nm >= 2;
+    const int hs = block_exclusive_scan(heavy ? nm : 0, warp_tot, &total);
+    const int H = total;
+    const int ls = block_exclusive_scan(heavy ? 0 : nm, warp_tot, &total);
+    const int L = total;
+    if (e == 0) tt.n_mt[0] = H + L;
     if (e < E) {
-      if (ms + nm > tt.max_mt) {
+      if (H + L > tt.max_mt) {
         set_error(err, MOE_ERR_DEVICE_BOUNDS, 100);
       } else {
         for (int m = 0; m < nm; ++m) {
-          tt.mt_expert[ms + m] = e;
-          tt.mt_row0[ms + m] = poffv + m * kTileRows;
+          const int at = heavy ? merge_position(hs + m, H, L, true) : merge_position(ls + m, L, H, false);
+          tt.mt_expert[at] = e;
+          tt.mt_row0[at] = poffv + m * kTileRows;
         }
       }
     }
-    // 256-row pair tiles: two consecutive 128-row tiles of the same expert
-    const int np = (nm + 1) / 2;
-    const int ps = block_exclusive_scan(np, warp_tot, &total);
-    if (e == 0) tt.n_pt[0] = total;
-    if (e < E) {
-      if (ps + np > tt.max_mt) {
-        set_error(err, MOE_ERR_DEVICE_BOUNDS, 101);
-      } else {
-        for (int m = 0; m < np; ++m) {
-          tt.pt_expert[ps + m] = e;
-          tt.pt_row0[ps + m] = poffv + m * 2 * kTileRows;
-        }
+    // 256-row pair tiles (two consecutive 128-row tiles of one expert), same blend; an odd
+    // last tile goes to the leftover table (computed by single-CTA tiles, same results)
+    const int np = nm / 2;
+    const bool pheavy = np >= 2;
+    const int phs = block_exclusive_scan(pheavy ? np : 0, warp_tot, &total);
+    const int PH = total;
+    const int pls = block_exclusive_scan(pheavy ? 0 : np, warp_tot, &total);
+    const int PL = total;
+    if (e == 0) tt.n_pt[0] = PH + PL;
+    if (e < E && PH + PL <= tt.max_mt) {
+      for (int m = 0; m < np; ++m) {
+        const int at = pheavy ? merge_position(phs + m, PH, PL, true) : merge_position(pls + m, PL, PH, false);
+        tt.pt_expert[at] = e;
+        tt.pt_row0[at] = poffv + m * 2 * kTileRows;
       }
+    }
+    const int odd = nm & 1;
+    const int los = block_exclusive_scan(odd, warp_tot, &total);
+    if (e == 0) tt.n_lo[0] = total;
+    if (e < E && odd) {
+      tt.lo_expert[los] = e;
+      tt.lo_row0[los] = poffv + (nm - 1) * kTileRows;
     }
   }
 }

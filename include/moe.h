@@ -65,12 +65,16 @@ typedef enum moe_status {
 
 /* Flags of moe_forward. */
 #define MOE_FWD_SAVE_FOR_BACKWARD 1 /* keep A = x W1 and B = x W3 (fp32) in ws for moe_backward */
+#define MOE_FWD_FUSED_COMBINE 2     /* GEMM2 combines each token as soon as its k expert rows are
+                                       written (the single-GPU form of the overlapped combine of
+                                       waves); bitwise the same output as the default separate
+                                       combine kernel, which is faster on GB300 */
 
 /* Stage events: moe_forward records MOE_FWD_NUM_EVENTS events and moe_backward
  * MOE_BWD_NUM_EVENTS events on `stream` at its stage boundaries when `stage_events` is not
  * NULL (each a cudaEvent_t created by the caller).
  *   forward : [0] start, [1] after routing + dispatch, [2] after GEMM1 + SwiGLU,
- *             [3] after GEMM2, [4] after combine.
+ *             [3] after GEMM2, [4] after combine ([3] == [4] with MOE_FWD_FUSED_COMBINE).
  *   backward: [0] start, [1] after gate grads + dO, [2] after dH + SwiGLU backward,
  *             [3] after the dX GEMM, [4] after the dX combine, [5] after dW2, [6] after dW1/dW3. */
 #define MOE_FWD_NUM_EVENTS 5

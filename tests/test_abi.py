@@ -57,7 +57,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert st == lib.MOE_ERR_UNSUPPORTED                      # d % 128 != 0
     st = raw.moe_forward(*p, -1, 128, 8, 2, 256, fake, fake, 1 << 30, 0, None, None)
     assert st == lib.MOE_ERR_INVALID_ARG                      # T < 0
-    st = raw.moe_forward(*p, 64, 128, 8, 2, 256, fake, fake, 1 << 30, 4, None, None)
+    st = raw.moe_forward(*p, 64, 128, 8, 2, 256, fake, fake, 1 << 30, 8, None, None)
     assert st == lib.MOE_ERR_INVALID_ARG                      # unknown flag
     st = raw.moe_forward(*p, 64, 128, 8, 2, 256, fake, fake, 16, 0, None, None)
     assert st == lib.MOE_ERR_WORKSPACE                        # workspace too small

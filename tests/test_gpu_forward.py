@@ -88,6 +88,28 @@ def test_forward_batch_invariance_small(moe):
     assert torch.equal(out_rev.flip(0).view(torch.int16), full.view(torch.int16))
 
 
+@pytest.mark.parametrize("T,d,E,k,dff", [
+    (64, 128, 8, 2, 256),       # tiny
+    (300, 256, 16, 4, 384),     # ragged tiles
+    (77, 384, 5, 3, 128),       # 128-wide GEMM2 tiles
+    (2000, 256, 32, 2, 256),    # one expert takes most tokens
+    (4096, 2048, 64, 6, 1024),  # mid workload
+])
+def test_fused_combine_equals_separate_stages(moe, T, d, E, k, dff):
+    # GEMM2 with the combine fused in gives bitwise the same output as GEMM2 + combine kernel
+    w = moe_synth.custom(T, d, E, k, dff, seed=T + 13)
+    inp = moe_synth.generate(w)
+    if T == 2000:
+        inp["logits"][:, 0] += 50.0
+    g = to_dev(inp)
+    sep, ws = forward(moe, g, k)
+    fused = torch.empty_like(sep)
+    moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, fused, ws,
+                    flags=moe.MOE_FWD_FUSED_COMBINE)
+    assert moe.moe_get_error(ws) == 0
+    assert torch.equal(fused.view(torch.int16), sep.view(torch.int16))
+
+
 def _device_workload(name):
     w = moe_synth.by_name(name)
     return w, moe_synth.generate(w, device="cuda")
