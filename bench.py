@@ -8,8 +8,10 @@ larger than the 129 MB L2, so no L2 flush is needed between steps.
 
 Prints one JSON line (rank 0).  With --gpus N > 1 (under torchrun) every rank runs an
 independent replica on its own GPU (the layer does not shard); value = all tokens / the
-slowest rank's time.  --impl reference times the fp64 CPU oracle instead, on a bounded
-sample of the same workload.
+slowest rank's time.  The line also carries the forward + backward time of the fwd_bwd
+workload (T=8192, d=4096, E=128, top-8, d_ff=1536) unless --no-backward, and the time of the
+overlapped-wave forward variant.  --impl reference times the fp64 CPU oracle instead, on a
+bounded sample of the same workload.
 """
 import argparse
 import json
@@ -154,6 +156,75 @@ def _traffic_of(kernel):
         return None
 
 
+def _pair():
+    return os.environ.get("MOE_GEMM_PAIR", "1") != "0"
+
+
+def fwd_launches():
+    # routing, column scan, offsets/tile tables, scatter, padding rows, GEMM1, GEMM2, combine;
+    # with CTA pairs each GEMM is a pair launch plus a single-CTA launch for leftover tiles
+    return 10 if _pair() else 8
+
+
+def bwd_launches():
+    # gate grads, dO padding, dH (+ leftover), dX (+ leftover), dX combine, dW2, dW1/dW3
+    return 9 if _pair() else 7
+
+
+def bench_fwd_bwd(moe, dev, steps, warmup):
+    """Forward (saving for backward) + backward of the fwd_bwd workload (T=8192, d=4096,
+    E=128, top-8, d_ff=1536), device-resident, with the backward's stage times."""
+    w = moe_synth.by_name("fwd_bwd")
+    g = moe_synth.generate(w, device=dev, with_dy=True)
+    T, d, E, k, dff = w.T, w.d, w.E, w.k, w.dff
+    ws = torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, True), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    res = dict(dx=torch.empty(T, d, dtype=torch.bfloat16, device=dev),
+               dW1=torch.empty(E, d, dff, dtype=torch.float32, device=dev),
+               dW3=torch.empty(E, d, dff, dtype=torch.float32, device=dev),
+               dW2=torch.empty(E, dff, d, dtype=torch.float32, device=dev),
+               dgate=torch.empty(T, k, dtype=torch.float32, device=dev),
+               dlogits=torch.empty(T, E, dtype=torch.float32, device=dev))
+    stream = torch.cuda.current_stream(dev)
+    nb = moe.MOE_BWD_NUM_EVENTS
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nb)] for _ in range(steps)]
+
+    def step(ev=None):
+        moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+                        flags=moe.MOE_FWD_SAVE_FOR_BACKWARD, stream=stream)
+        moe.moe_backward(g["dy"], g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k,
+                         res["dx"], res["dW1"], res["dW3"], res["dW2"], res["dgate"],
+                         res["dlogits"], ws, stage_events=ev, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    st = moe.moe_get_error(ws)
+    if st != 0:
+        raise RuntimeError("device error in forward + backward: " + moe.moe_status_string(st))
+    ms = start.elapsed_time(stop) / steps
+    names = ["gate_grads", "dh_swiglu_bwd", "dx_gemm", "dx_combine", "dw2", "dw13"]
+    stages = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / steps
+              for j, n in enumerate(names)}
+    bwd_ms = sum(stages.values())
+    P = T * k
+    # backward GEMM flops per token-expert pair: dH = dO W2^T (2 d dff), dX from dA and dB
+    # (4 d dff), dW1 and dW3 (4 d dff), dW2 (2 d dff): 12 d dff in total
+    bwd_flops = 12 * d * dff * P
+    return {"workload": "fwd_bwd: T=%d d=%d E=%d top-%d d_ff=%d" % (T, d, E, k, dff),
+            "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
+            "backward_ms": bwd_ms, "backward_stages_ms": stages,
+            "backward_tflops": bwd_flops / (bwd_ms * 1e-3) / 1e12,
+            "launches_per_step": fwd_launches() + bwd_launches()}
+
+
 def run_cpu_baseline(w, inp_np, budget_s=15.0):
     import oracle
     cores = oracle.num_threads()
@@ -294,6 +365,25 @@ def bench_native(args, w):
         t = torch.tensor([ms_e2e], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_e2e = float(t.item())
+    # the overlapped-wave variant (GEMM1 gathers rows from x, GEMM2 fuses the combine),
+    # timed for comparison; bitwise the same output
+    wave_flags = moe.MOE_FWD_GATHER_ROWS | moe.MOE_FWD_FUSED_COMBINE
+    for _ in range(2):
+        moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+                        flags=wave_flags, stream=stream)
+    barrier()
+    n_wave = max(1, min(args.steps, 10))
+    start.record(stream)
+    for _ in range(n_wave):
+        moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+                        flags=wave_flags, stream=stream)
+    stop.record(stream)
+    barrier()
+    waved_ms = start.elapsed_time(stop) / n_wave
+    st = moe.moe_get_error(ws)
+    if st != 0:
+        raise RuntimeError("device error (waved forward): " + moe.moe_status_string(st))
+
     e2e = {"value": world * T * args.steps / (ms_e2e / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4,
            "d2h_bytes_per_step": ho.numel() * 2}
@@ -321,11 +411,16 @@ def bench_native(args, w):
         "gemm_frac_of_bf16_burst": g_tflops / peaks["bf16"],
         "dispatch_gbs": disp_gbs, "dispatch_frac_of_hbm": disp_gbs / peaks["hbm"],
         "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
+        "waved_forward_ms_per_step": waved_ms,
         "clocks": clocks.summary(),
-        "gpu_launches": 8 * args.steps,
+        "gpu_launches": fwd_launches() * args.steps,
     }
+    if not args.no_backward:
+        del ws
+        torch.cuda.empty_cache()
+        line["fwd_bwd"] = bench_fwd_bwd(moe, dev, max(1, min(args.steps, 10)), args.warmup)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        del ws, out
+        del out
         torch.cuda.empty_cache()
         line["cpu_baseline"] = run_cpu_baseline(w, moe_synth.to_numpy(g))
     if world > 1:
@@ -345,6 +440,8 @@ def main():
     ap.add_argument("--shape", default=None,
                     help="T,d,E,k,d_ff of a custom workload (profiling captures of one kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the forward + backward timing of the fwd_bwd workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -25,6 +25,7 @@ MOE_ERR_TIMEOUT = 5
 MOE_ERR_DEVICE_BOUNDS = 6
 MOE_FWD_SAVE_FOR_BACKWARD = 1
 MOE_FWD_FUSED_COMBINE = 2
+MOE_FWD_GATHER_ROWS = 4
 MOE_FWD_NUM_EVENTS = 5
 MOE_BWD_NUM_EVENTS = 7
 

@@ -304,6 +304,26 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* map, 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
 }
+// Four 128-byte rows (box of 64 bf16 x 1 row) of a 2-D tensor, rows r0..r3 at column x, into
+// consecutive 128-byte rows of shared memory starting at dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, uint32_t bar, int x, int r0,
+                                            int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+// Same, completing on a barrier that may live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const void* map, uint32_t bar_cluster,
+                                                 int x, int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(bar_cluster)
+      : "memory");
+}
 __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }

@@ -72,6 +72,8 @@ struct GemmParams {
   int M;                     // M extent of the K-over-rows kinds (d or d_ff)
   // GEMM2 with the combine fused in (see combine_segment)
   int fuse_combine;
+  // GEMM1 reading its A rows straight from x (rows gathered by token, TMA tile::gather4)
+  int gather_x;
   const int32_t* perm;       // permuted row -> pair t*k + j
   const int32_t* pos;        // pair -> permuted row
   const float* gate;         // [T, k]
@@ -96,8 +98,9 @@ struct GemmCfg {
   static constexpr uint32_t kTmemCols = 2 * BN;
   static constexpr int kBars = 2 * kStages + 5;  // full, empty, tfull x2, tempty x2, drain
   static constexpr size_t kEpiBytes = 4 * 32 * 33 * 4;  // one transpose buffer per epilogue warp
-  static constexpr size_t kSmemBytes =
-      static_cast<size_t>(kStages) * kStageBytes + 1024 + 8 * kBars + 64 + kEpiBytes;
+  static constexpr size_t kGatherBytes = kBM * 4;  // token index of each A row of a tile
+  static constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 1024 +
+                                       8 * kBars + 64 + kEpiBytes + kGatherBytes;
 };
 
 struct TileInfo {
@@ -446,6 +449,7 @@ __global__ void __launch_bounds__(256, 1)
   volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(misc + 8);
   volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(misc + 12);
   float* epi_buf = reinterpret_cast<float*>(misc + 64);  // 4 x (32 x 33) floats
+  int32_t* gather_ids = reinterpret_cast<int32_t*>(misc + 64 + Cfg::kEpiBytes);
   auto stage_a = [&](int s) { return base + s * Cfg::kStageBytes; };
   auto stage_b = [&](int s) { return base + s * Cfg::kStageBytes + kABytes; };
 
@@ -496,11 +500,16 @@ __global__ void __launch_bounds__(256, 1)
   uint32_t issued = 0;
   int skipped = -1;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    tma_prefetch_desc(&mapA);
-    tma_prefetch_desc(&mapB0);
-    tma_prefetch_desc(&mapB1);
+    // Lane 0 waits and issues every load.  With gather_x the whole warp first stages the
+    // token index of each of the tile's A rows (padding rows read token 0; they are never
+    // stored).
+    if (lane == 0) {
+      tma_prefetch_desc(&mapA);
+      tma_prefetch_desc(&mapB0);
+      tma_prefetch_desc(&mapB1);
+    }
     uint32_t fill = 0;
     bool ok = true;
     // with PAIR every load completes on rank 0's full barrier
@@ -508,12 +517,27 @@ __global__ void __launch_bounds__(256, 1)
       if constexpr (PAIR) tma_load_2d_pair(dst, m, mapa_shared(fb, 0), x, y);
       else tma_load_2d(dst, m, fb, x, y);
     };
-    for (int tile = unit; tile < ntiles && ok; tile += nunits) {
+    for (int tile = unit; tile < ntiles; tile += nunits) {
+      // the warp is converged here: lanes 1..31 wait below while lane 0 issues a tile
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
       const TileInfo ti = decode_tile<KIND, BN, PAIR>(p, tile, rank);
       if (ti.bad) {
-        set_error(p.err, MOE_ERR_DEVICE_BOUNDS, 11);
+        if (lane == 0) set_error(p.err, MOE_ERR_DEVICE_BOUNDS, 11);
         continue;
       }
+      if constexpr (KIND == kFwd1) {
+        if (p.gather_x) {
+#pragma unroll
+          for (int i = 0; i < kBM / 32; ++i) {
+            const int rr = i * 32 + lane;
+            const int pr = rr < ti.nvalid ? p.perm[ti.row0 + rr] : -1;
+            gather_ids[rr] = pr >= 0 ? pr / p.k : 0;
+          }
+          __syncwarp();
+        }
+      }
+      if (lane == 0) {
       const int nb0 = ti.n0 + rank * BL;  // first B column held by this CTA
       for (int kb = 0; kb < ti.nk; ++kb) {
         const int s = fill % S;
@@ -530,7 +554,18 @@ __global__ void __launch_bounds__(256, 1)
           if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * Cfg::kStageBytes : Cfg::kStageBytes);
           const int k0 = kb * kBK;
           if constexpr (KIND == kFwd1) {
-            load(sa, &mapA, fb, k0, ti.row0);
+            if (p.gather_x) {
+#pragma unroll 4
+              for (int i = 0; i < kBM / 4; ++i) {
+                const int* g4 = gather_ids + 4 * i;
+                if constexpr (PAIR)
+                  tma_gather4_pair(sa + 512u * i, &mapA, mapa_shared(fb, 0), k0, g4[0], g4[1], g4[2], g4[3]);
+                else
+                  tma_gather4(sa + 512u * i, &mapA, fb, k0, g4[0], g4[1], g4[2], g4[3]);
+              }
+            } else {
+              load(sa, &mapA, fb, k0, ti.row0);
+            }
             const int wrow = ti.e * p.d + k0;
             const int h0 = ti.n0 / 2;  // first h column of the tile
             if constexpr (PAIR) {
@@ -567,6 +602,8 @@ __global__ void __launch_bounds__(256, 1)
         }
         ++fill;
       }
+      }  // lane 0
+      __syncwarp();  // gather_ids may be rewritten only after lane 0 has issued the tile
     }
     issued = fill;
   } else if (warp == 1 && lane == 0 && rank == 0) {

@@ -9,7 +9,7 @@
 
 namespace moe {
 
-constexpr int kRouteTokensPerBlock = 128;  // tokens per routing CTA (4 warps x 32 tokens)
+constexpr int kRouteTokensPerBlock = 128;  // tokens per routing CTA (4 ranking chunks of 32)
 constexpr int kTileRows = 128;             // rows of one expert GEMM tile; padded row unit
 constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
@@ -76,6 +76,7 @@ struct GemmCtx {
   int num_sms;
   bool pair;  // 256-row tiles on CTA pairs (tcgen05 cta_group::2)
   bool fuse_combine;     // GEMM2 also combines finished tokens into `out`
+  bool gather_x;         // GEMM1 gathers its A rows from x (no x_perm)
   uint16_t* out;         // layer output [T, d] (fused combine)
 };
 cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s);   // H = SwiGLU(Xp W1, Xp W3)

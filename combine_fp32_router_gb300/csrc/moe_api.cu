@@ -1,6 +1,6 @@
 // C ABI of libmoe.so (declared in include/moe.h): argument validation on the host, the
 // workspace carve-up, and the launch sequence of each entry point on the caller's stream.
-// The host path does no allocation and no synchronisation (except moe_get_error); the
+// The host path allocates no memory and does not synchronise (except moe_get_error); the
 // checks are plain integer tests, in the spirit of the report translation's section 2.1
 // (itsolotime.com): argument checking belongs in compiled host code, not in Python.
 #include <atomic>
@@ -28,6 +28,7 @@ bool use_pairs() {
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -185,7 +186,8 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   if (st != MOE_OK) return st;
   if (!W1 || !W3 || !W2 || !ws) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
-  if (flags & ~(MOE_FWD_SAVE_FOR_BACKWARD | MOE_FWD_FUSED_COMBINE)) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_FWD_SAVE_FOR_BACKWARD | MOE_FWD_FUSED_COMBINE | MOE_FWD_GATHER_ROWS))
+    return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, logits, W1, W3, W2, out};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
@@ -228,8 +230,12 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   tt.lo_row0 = reinterpret_cast<int32_t*>(w + L.lo_row0);
   tt.max_mt = L.max_mt;
   MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
-  MOE_TRY(launch_scatter(x, T, d, E, k, topk, bbase, poff, pos, perm, xperm, L.P_pad, err,
-                         stream));
+  // With MOE_FWD_GATHER_ROWS (and no backward, which reads x_perm as a K operand) GEMM1
+  // gathers its rows from x itself: the dispatch copy of the next tiles overlaps the MMAs of
+  // the current ones.
+  const bool gather = !save && (flags & MOE_FWD_GATHER_ROWS) != 0;
+  MOE_TRY(launch_scatter(x, T, d, E, k, topk, bbase, poff, pos, perm, gather ? nullptr : xperm,
+                         L.P_pad, err, stream));
   // padding rows: perm = -1; zero x rows when the backward will read them as a K operand
   MOE_TRY(launch_pad_rows(counts, poff, E, perm, save ? xperm : nullptr, 2ll * d, stream));
   record(stage_events, 1, stream);
@@ -248,6 +254,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.num_sms = num_sms_of_current_device();
   c.pair = use_pairs();
   c.fuse_combine = (flags & MOE_FWD_FUSED_COMBINE) != 0;
+  c.gather_x = gather;
   c.out = out;
   MOE_TRY(launch_gemm_fwd1(c, stream));
   record(stage_events, 2, stream);

@@ -19,96 +19,108 @@ namespace moe {
 namespace {
 
 // ------------------------------------------------------------------------------ routing
-// Sortable key of (logit, expert): larger logit first, then lower index.  -0 is folded into
-// +0 so that the two compare equal (the lower index then wins), and the key of any real
-// entry is > 0 so that the padding entries (key 0) never win.
-__device__ __forceinline__ uint64_t route_key(float v, int e) {
+// Order key of a logit: an unsigned integer that sorts like the float (larger logit, larger
+// key), with -0 folded into +0 so that the two compare equal (the lower expert index then
+// wins the tie).
+__device__ __forceinline__ uint32_t order_key(float v) {
   if (v == 0.0f) v = 0.0f;
-  uint32_t u = __float_as_uint(v);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - e);
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ float key_value(uint64_t key) {
-  uint32_t u = static_cast<uint32_t>(key >> 32);
-  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
-  return __uint_as_float(u);
-}
-__device__ __forceinline__ int key_expert(uint64_t key) {
-  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+__device__ __forceinline__ float order_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// One CTA = 128 consecutive tokens, 4 warps x 32 tokens.  Per token the warp holds the E
-// logits (EPL per lane) and runs k rounds of a warp arg-max.  Per warp chunk, a bit mask
-// per expert (bit i = token i of the chunk chose it) gives each pair its rank among the
-// chunk's earlier tokens; the masks' popcounts then give per-warp bases and the CTA's
-// histogram row.  pos_local receives the pair's rank among the CTA's tokens routed to the
-// same expert.
+constexpr int kRouteWarps = 16;                                     // warps per routing CTA
+constexpr int kRouteTokPerWarp = kRouteTokensPerBlock / kRouteWarps;  // top-k tokens per warp
+static_assert(kRouteTokensPerBlock == 128 && kRouteTokPerWarp * kRouteWarps == 128, "");
+
+// One CTA = 128 consecutive tokens.
+// Top-k: 16 warps x 8 tokens.  A warp first loads the logits of NB of its tokens (EPL per
+// lane each) so that their loads are in flight together, then per token runs k rounds of a
+// warp arg-max: one warp max-reduction of the order keys, one min-reduction of the expert
+// indices holding that key (ties -> lower index), and the winner is marked taken.
+// Ranking: per 32-token chunk (warps 0..3), a bit mask per expert (bit i = token i of the
+// chunk chose it) gives each pair its rank among the chunk's earlier tokens; the masks'
+// popcounts then give per-chunk bases and the CTA's histogram row.  pos_local receives the
+// pair's rank among the CTA's tokens routed to the same expert.
 template <int EPL>
-__global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict__ logits,
-                                                         int64_t T, int E, int k,
-                                                         int32_t* __restrict__ topk,
-                                                         float* __restrict__ gate,
-                                                         int32_t* __restrict__ pos_local,
-                                                         int32_t* __restrict__ hist) {
+__global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
+    const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ topk,
+    float* __restrict__ gate, int32_t* __restrict__ pos_local, int32_t* __restrict__ hist) {
+  constexpr int NB = EPL <= 8 ? 8 : (EPL <= 16 ? 4 : 2);
+  static_assert(kRouteTokPerWarp % NB == 0, "");
   extern __shared__ uint32_t sm[];
-  uint32_t* mask = sm;                                  // [4][E]
+  uint32_t* mask = sm;                                        // [4][E]
   int32_t* wbase = reinterpret_cast<int32_t*>(sm + 4 * E);   // [4][E]
-  int32_t* tok_e = wbase + 4 * E;                       // [4][32][kMaxK]
-  int32_t* tok_r = tok_e + 4 * 32 * kMaxK;              // [4][32][kMaxK]
+  int32_t* tok_e = wbase + 4 * E;                             // [128][kMaxK]
+  int32_t* tok_r = tok_e + kRouteTokensPerBlock * kMaxK;     // [128][kMaxK]
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < 4 * E; i += blockDim.x) mask[i] = 0u;
-  __syncthreads();
 
-  const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * kRouteTokensPerBlock + w * 32;
-  int32_t* my_e = tok_e + w * 32 * kMaxK;
-  int32_t* my_r = tok_r + w * 32 * kMaxK;
-
-  for (int i = 0; i < 32; ++i) {
-    const int64_t t = tok0 + i;
-    if (t >= T) break;
-    const float* lt = logits + t * E;
-    uint64_t key[EPL];
+  const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * kRouteTokensPerBlock;
+  const int wt0 = w * kRouteTokPerWarp;
+  for (int b0 = 0; b0 < kRouteTokPerWarp; b0 += NB) {
+    float v[NB][EPL];
 #pragma unroll
-    for (int c = 0; c < EPL; ++c) {
-      const int e = lane + 32 * c;
-      key[c] = (e < E) ? route_key(__ldg(lt + e), e) : 0ull;
-    }
-    int sel_e = 0;
-    float sel_v = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      uint64_t best = 0ull;
+    for (int i = 0; i < NB; ++i) {
+      const int64_t t = blk0 + wt0 + b0 + i;
 #pragma unroll
-      for (int c = 0; c < EPL; ++c) best = key[c] > best ? key[c] : best;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        best = o > best ? o : best;
+      for (int c = 0; c < EPL; ++c) {
+        const int e = lane + 32 * c;
+        v[i][c] = (t < T && e < E) ? __ldg(logits + t * E + e) : 0.0f;
       }
-      const int ew = key_expert(best);
+    }
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      const int64_t t = blk0 + wt0 + b0 + i;
+      if (t >= T) break;
+      uint32_t key[EPL];
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) key[c] = order_key(v[i][c]);
+      uint32_t live = 0;  // bit c: expert lane + 32c exists and is not yet taken
 #pragma unroll
       for (int c = 0; c < EPL; ++c)
-        if (lane + 32 * c == ew) key[c] = 0ull;
-      if (lane == j) {
-        sel_e = ew;
-        sel_v = key_value(best);
+        if (lane + 32 * c < E) live |= 1u << c;
+      int sel_e = 0;
+      float sel_v = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        uint32_t best = 0u;  // a lane with no live expert offers 0, never above a live key
+#pragma unroll
+        for (int c = 0; c < EPL; ++c)
+          if (((live >> c) & 1u) && key[c] > best) best = key[c];
+        const uint32_t bk = __reduce_max_sync(0xFFFFFFFFu, best);
+        uint32_t mine = 0xFFFFFFFFu;
+#pragma unroll
+        for (int c = EPL - 1; c >= 0; --c)
+          if (((live >> c) & 1u) && key[c] == bk) mine = static_cast<uint32_t>(lane + 32 * c);
+        const uint32_t ew = __reduce_min_sync(0xFFFFFFFFu, mine);
+        if ((ew & 31u) == static_cast<uint32_t>(lane)) live &= ~(1u << (ew >> 5));
+        if (lane == j) {
+          sel_e = static_cast<int>(ew);
+          sel_v = order_value(bk);
+        }
+      }
+      // softmax over the k selected logits, fp32, summed in slot order
+      const float v0 = __shfl_sync(0xFFFFFFFFu, sel_v, 0);
+      const float ex = (lane < k) ? expf(sel_v - v0) : 0.0f;
+      float s = 0.0f;
+      for (int j = 0; j < k; ++j) s += __shfl_sync(0xFFFFFFFFu, ex, j);
+      if (lane < k) {
+        topk[t * k + lane] = sel_e;
+        gate[t * k + lane] = ex / s;
+        tok_e[(wt0 + b0 + i) * kMaxK + lane] = sel_e;
       }
     }
-    // softmax over the k selected logits, fp32, summed in slot order
-    const float v0 = __shfl_sync(0xFFFFFFFFu, sel_v, 0);
-    const float ex = (lane < k) ? expf(sel_v - v0) : 0.0f;
-    float s = 0.0f;
-    for (int j = 0; j < k; ++j) s += __shfl_sync(0xFFFFFFFFu, ex, j);
-    if (lane < k) {
-      topk[t * k + lane] = sel_e;
-      gate[t * k + lane] = ex / s;
-      my_e[i * kMaxK + lane] = sel_e;
-    }
   }
-  __syncwarp();
-  // ranks inside the warp's 32-token chunk
-  const int64_t t = tok0 + lane;
-  const bool valid = t < T;
+  __syncthreads();
+  // ranks inside each 32-token chunk
+  const int64_t t = blk0 + w * 32 + lane;
+  const bool ranker = w < kRouteTokensPerBlock / 32;
+  const bool valid = ranker && t < T;
+  int32_t* my_e = tok_e + w * 32 * kMaxK;
+  int32_t* my_r = tok_r + w * 32 * kMaxK;
   if (valid)
     for (int j = 0; j < k; ++j) atomicOr(&mask[w * E + my_e[lane * kMaxK + j]], 1u << lane);
   __syncwarp();
@@ -120,7 +132,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
 #pragma unroll
-    for (int ww = 0; ww < 4; ++ww) {
+    for (int ww = 0; ww < kRouteTokensPerBlock / 32; ++ww) {
       wbase[ww * E + e] = run;
       run += __popc(mask[ww * E + e]);
     }
@@ -196,21 +208,54 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
   return warp_tot[w] + incl - v;
 }
 
-// Position of element i of list A (length na) when A and B (length nb) are merged in
-// proportion: element i of A sits at relative time (i + 1/2) / na, element j of B at
-// (j + 1/2) / nb; ties go to the first list (`a_first`).  Positions form a permutation of
-// [0, na + nb) and keep each list's order.
-__device__ __forceinline__ int merge_position(int i, int na, int nb, bool a_first) {
-  if (nb == 0) return i;
+// Merge of two lists in proportion: element i of list A (length na) sits at relative time
+// (i + 1/2) / na, element j of B (length nb) at (j + 1/2) / nb; ties go to the first list.
+// merge_before(i) = number of B elements placed before element i of A; its position is
+// i + merge_before(i).  Positions form a permutation of [0, na + nb) and keep each list's
+// order.
+__device__ __forceinline__ int merge_before(int i, int na, int nb, bool a_first) {
+  if (nb == 0) return 0;
   const int64_t num = (2ll * i + 1) * nb - na;
-  int64_t before;  // elements of B placed before element i of A
+  int64_t before;
   if (a_first) {   // B elements strictly earlier: (2j+1) na < (2i+1) nb
     before = num <= 0 ? 0 : (num + 2ll * na - 1) / (2ll * na);
   } else {         // B elements earlier or tied: (2j+1) na <= (2i+1) nb
     before = num < 0 ? 0 : num / (2ll * na) + 1;
   }
-  if (before > nb) before = nb;
-  return i + static_cast<int>(before);
+  return before > nb ? nb : static_cast<int>(before);
+}
+
+// Number of entries of the non-decreasing array incl[0..n) that are <= i: the owner of
+// element i of a list whose per-expert inclusive prefix is incl.
+__device__ __forceinline__ int owner_of(const int* incl, int n, int i) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (incl[mid] <= i) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// One tile table: list A = experts with >= 2 tiles (bound by the tensor cores), list B = the
+// others (one tile each, bound by reading their weights).  Each list keeps expert order; the
+// two are merged in proportion so that the weight streams of light experts overlap the math
+// of heavy ones instead of all coming last.  One thread per table entry.  The order changes
+// no result: every tile is computed the same way wherever it runs.
+__device__ __forceinline__ void fill_tile_table(const int* a_incl, const int* b_incl,
+                                                const int* poff, int E, int na, int nb,
+                                                int rows_per_tile, int32_t* t_expert,
+                                                int32_t* t_row0) {
+  for (int idx = threadIdx.x; idx < na + nb; idx += blockDim.x) {
+    const bool in_a = idx < na;
+    const int i = in_a ? idx : idx - na;
+    const int* incl = in_a ? a_incl : b_incl;
+    const int e = owner_of(incl, E, i);
+    const int m = i - (e > 0 ? incl[e - 1] : 0);
+    const int at = i + (in_a ? merge_before(i, na, nb, true) : merge_before(i, nb, na, false));
+    t_expert[at] = e;
+    t_row0[at] = poff[e] + m * rows_per_tile;
+  }
 }
 
 __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E,
@@ -219,6 +264,7 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
                                                        int with_tables, DevErr* err) {
   __shared__ int warp_tot[32];
   __shared__ int total;
+  __shared__ int s_poff[1024], s_a[1024], s_b[1024], s_pa[1024], s_pb[1024];
   const int e = threadIdx.x;
   const int c = e < E ? counts[e] : 0;
   const int pc = (c + align - 1) / align * align;
@@ -232,59 +278,51 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   const int tot_p = total;
   if (e < E) poff[e] = poffv;
   if (e == 0) poff[E] = tot_p;
-  if (with_tables) {
-    // Tile order.  Experts with one 128-row tile are bound by reading their weights (a tile
-    // does 2 FLOP per weight byte per row, far below the GPU's FLOP/byte ratio), the others by
-    // the tensor cores.  Both lists keep expert order and are merged in proportion, so the
-    // weight streams of light experts overlap the math of heavy ones instead of all coming
-    // last.  The order changes no result: every tile is computed the same way wherever it runs.
-    const int nm = pc / kTileRows;
-    const bool heavy = nm >= 2;
-    const int hs = block_exclusive_scan(heavy ? nm : 0, warp_tot, &total);
-    const int H = total;
-    const int ls = block_exclusive_scan(heavy ? 0 : nm, warp_tot, &total);
-    const int L = total;
-    if (e == 0) tt.n_mt[0] = H + L;
-    if (e < E) {
-      if (H + L > tt.max_mt) {
-        set_error(err, MOE_ERR_DEVICE_BOUNDS, 100);
-      } else {
-        for (int m = 0; m < nm; ++m) {
-          const int at = heavy ? merge_position(hs + m, H, L, true) : merge_position(ls + m, L, H, false);
-          tt.mt_expert[at] = e;
-          tt.mt_row0[at] = poffv + m * kTileRows;
-        }
-      }
-    }
-    // 256-row pair tiles (two consecutive 128-row tiles of one expert), same blend; an odd
-    // last tile goes to the leftover table (computed by single-CTA tiles, same results)
-    const int np = nm / 2;
-    const bool pheavy = np >= 2;
-    const int phs = block_exclusive_scan(pheavy ? np : 0, warp_tot, &total);
-    const int PH = total;
-    const int pls = block_exclusive_scan(pheavy ? 0 : np, warp_tot, &total);
-    const int PL = total;
-    if (e == 0) tt.n_pt[0] = PH + PL;
-    if (e < E && PH + PL <= tt.max_mt) {
-      for (int m = 0; m < np; ++m) {
-        const int at = pheavy ? merge_position(phs + m, PH, PL, true) : merge_position(pls + m, PL, PH, false);
-        tt.pt_expert[at] = e;
-        tt.pt_row0[at] = poffv + m * 2 * kTileRows;
-      }
-    }
-    const int odd = nm & 1;
-    const int los = block_exclusive_scan(odd, warp_tot, &total);
-    if (e == 0) tt.n_lo[0] = total;
-    if (e < E && odd) {
+  if (!with_tables) return;
+  // 128-row tiles; 256-row pair tiles (two consecutive 128-row tiles of one expert) with an
+  // odd last tile in the leftover table (computed by single-CTA tiles, same results)
+  const int nm = pc / kTileRows;
+  const int np = nm / 2;
+  const int ha = block_exclusive_scan(nm >= 2 ? nm : 0, warp_tot, &total) + (nm >= 2 ? nm : 0);
+  const int H = total;
+  const int lb = block_exclusive_scan(nm >= 2 ? 0 : nm, warp_tot, &total) + (nm >= 2 ? 0 : nm);
+  const int L = total;
+  const int pa = block_exclusive_scan(np >= 2 ? np : 0, warp_tot, &total) + (np >= 2 ? np : 0);
+  const int PH = total;
+  const int pb = block_exclusive_scan(np >= 2 ? 0 : np, warp_tot, &total) + (np >= 2 ? 0 : np);
+  const int PL = total;
+  const int odd = nm & 1;
+  const int los = block_exclusive_scan(odd, warp_tot, &total);
+  const int NLO = total;
+  if (e < E) {
+    s_poff[e] = poffv;
+    s_a[e] = ha;
+    s_b[e] = lb;
+    s_pa[e] = pa;
+    s_pb[e] = pb;
+    if (odd) {
       tt.lo_expert[los] = e;
       tt.lo_row0[los] = poffv + (nm - 1) * kTileRows;
     }
   }
+  if (e == 0) {
+    tt.n_mt[0] = H + L;
+    tt.n_pt[0] = PH + PL;
+    tt.n_lo[0] = NLO;
+  }
+  __syncthreads();
+  if (H + L > tt.max_mt) {
+    if (e == 0) set_error(err, MOE_ERR_DEVICE_BOUNDS, 100);
+    return;
+  }
+  fill_tile_table(s_a, s_b, s_poff, E, H, L, kTileRows, tt.mt_expert, tt.mt_row0);
+  fill_tile_table(s_pa, s_pb, s_poff, E, PH, PL, 2 * kTileRows, tt.pt_expert, tt.pt_row0);
 }
 
 // Stable permute.  One warp per token: lanes j < k turn the CTA-local rank into the final
 // row (padded expert offset + rank of earlier routing CTAs + local rank), write pos/perm,
-// then the warp copies the token's row once from x and stores it k times (16-byte moves).
+// then (unless x_perm is null) the warp copies the token's row once from x and stores it k
+// times (16-byte moves).
 __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ x, int64_t T,
                                                       int d, int E, int k,
                                                       const int32_t* __restrict__ topk,
@@ -313,6 +351,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
         perm[row] = static_cast<int32_t>(p);
       }
     }
+    if (!x_perm) continue;  // indices only (the expert GEMM gathers rows from x itself)
     int rows[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
@@ -527,7 +566,7 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
   (void)err;
   const int64_t nblk = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   if (nblk == 0) return cudaSuccess;
-  const size_t smem = (8 * static_cast<size_t>(E) + 2 * 4 * 32 * kMaxK) * 4;
+  const size_t smem = (8 * static_cast<size_t>(E) + 2 * kRouteTokensPerBlock * kMaxK) * 4;
   const int epl = (E + 31) / 32;
   void (*kern)(const float*, int64_t, int, int, int32_t*, float*, int32_t*, int32_t*);
   if (epl <= 1) kern = route_topk_kernel<1>;
@@ -539,8 +578,8 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem));
   if (st != cudaSuccess) return st;
-  kern<<<static_cast<unsigned>(nblk), 128, smem, s>>>(logits, T, E, k, topk, gate, pos_local,
-                                                      hist);
+  kern<<<static_cast<unsigned>(nblk), kRouteWarps * 32, smem, s>>>(logits, T, E, k, topk, gate,
+                                                                    pos_local, hist);
   return cudaGetLastError();
 }
 

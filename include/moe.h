@@ -26,10 +26,10 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller, row-major, 16-byte
  *     aligned.  bf16 tensors are passed as moe_bf16_t (the raw 16-bit pattern).
  *   - Shapes: x [T,d], logits [T,E] fp32, W1 and W3 [E,d,d_ff], W2 [E,d_ff,d], out [T,d].
- *   - The library never allocates, frees or synchronises (except moe_get_error).  Every
- *     launch is asynchronous on `stream`.  The workspace `ws` (device memory, 256-byte
- *     aligned, size from moe_workspace_bytes) is caller-owned; calls that share one ws
- *     must be ordered on the GPU (same stream, or synchronised).
+ *   - The library never allocates or frees memory and never synchronises (except
+ *     moe_get_error).  Every launch is asynchronous on `stream`.  The workspace `ws`
+ *     (device memory, 256-byte aligned, size from moe_workspace_bytes) is caller-owned;
+ *     calls that share one ws must be ordered on the GPU (same stream, or synchronised).
  *   - Argument errors are detected on the host before anything is launched and returned as
  *     a status; nothing is written then.  Problems detected on the device (a bounded wait
  *     that ran out, an index out of range) are recorded in an error word inside `ws` and
@@ -69,6 +69,10 @@ typedef enum moe_status {
                                        written (the single-GPU form of the overlapped combine of
                                        waves); bitwise the same output as the default separate
                                        combine kernel, which is faster on GB300 */
+#define MOE_FWD_GATHER_ROWS 4       /* GEMM1 gathers its rows from x by token (TMA gather4) instead
+                                       of reading a permuted copy (the overlapped dispatch of
+                                       waves); bitwise the same output; slower on GB300; ignored
+                                       with MOE_FWD_SAVE_FOR_BACKWARD (the backward needs the copy) */
 
 /* Stage events: moe_forward records MOE_FWD_NUM_EVENTS events and moe_backward
  * MOE_BWD_NUM_EVENTS events on `stream` at its stage boundaries when `stage_events` is not

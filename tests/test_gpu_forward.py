@@ -110,6 +110,30 @@ def test_fused_combine_equals_separate_stages(moe, T, d, E, k, dff):
     assert torch.equal(fused.view(torch.int16), sep.view(torch.int16))
 
 
+@pytest.mark.parametrize("T,d,E,k,dff,flags", [
+    (64, 128, 8, 2, 256, 0),          # tiny
+    (300, 256, 16, 4, 384, 0),        # ragged tiles: padding rows gather token 0, never stored
+    (77, 384, 5, 3, 128, 0),          # 128-wide GEMM2 tiles
+    (2000, 256, 32, 2, 256, 0),       # one expert takes most tokens
+    (4096, 2048, 64, 6, 1024, 0),     # mid workload
+    (4096, 2048, 64, 6, 1024, 2),     # gather + fused combine: the overlapped waves together
+])
+def test_row_gather_equals_permuted_copy(moe, T, d, E, k, dff, flags):
+    # GEMM1 gathering its rows from x (TMA gather4) gives bitwise the same output as GEMM1
+    # reading the dispatch's permuted copy
+    w = moe_synth.custom(T, d, E, k, dff, seed=T + 17)
+    inp = moe_synth.generate(w)
+    if T == 2000:
+        inp["logits"][:, 0] += 50.0
+    g = to_dev(inp)
+    sep, ws = forward(moe, g, k)
+    got = torch.empty_like(sep)
+    moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, got, ws,
+                    flags=moe.MOE_FWD_GATHER_ROWS | flags)
+    assert moe.moe_get_error(ws) == 0
+    assert torch.equal(got.view(torch.int16), sep.view(torch.int16))
+
+
 def _device_workload(name):
     w = moe_synth.by_name(name)
     return w, moe_synth.generate(w, device="cuda")
