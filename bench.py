@@ -167,8 +167,9 @@ def fwd_launches():
 
 
 def bwd_launches():
-    # gate grads, dO padding, dH (+ leftover), dX (+ leftover), dX combine, dW2, dW1/dW3
-    return 9 if _pair() else 7
+    # gate grads (rows + per token), dO padding, dH (+ leftover), dX (+ leftover), dX combine,
+    # dW2, dW1/dW3
+    return 10 if _pair() else 8
 
 
 def bench_fwd_bwd(moe, dev, steps, warmup):

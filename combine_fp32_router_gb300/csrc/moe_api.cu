@@ -309,8 +309,9 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   const int32_t* pos = reinterpret_cast<const int32_t*>(w + L.pos);
   uint16_t* dO = reinterpret_cast<uint16_t*>(w + L.dO);
 
+  // the dX rows' buffer is free until the dX GEMM: it holds the gate grads' partial sums
   MOE_TRY(launch_bwd_gate(dy, reinterpret_cast<const float*>(w + L.Y), gate, pos, topk, T, k,
-                          d, E, dO, dgate, dlogits, stream));
+                          d, E, dO, dgate, dlogits, reinterpret_cast<float*>(w + L.dXp), stream));
   MOE_TRY(launch_pad_rows(counts, poff, E, nullptr, dO, 2ll * d, stream));
   record(stage_events, 1, stream);
 

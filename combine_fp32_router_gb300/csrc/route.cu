@@ -394,9 +394,15 @@ __global__ void __launch_bounds__(256) pad_rows_kernel(const int32_t* __restrict
   }
 }
 
+// Work unit of the combines: (token, block of kCombCols columns).  A warp takes units
+// u, u + nwarps, ... of a grid sized to the GPU's resident capacity, so that the last wave is
+// at most one unit per warp instead of a partial wave of whole blocks.
+constexpr int kCombChunks = 128;  // 8-column chunks per unit (1024 columns, 4 per lane)
+
 // Combine: out[t] = bf16( sum_j gate[t,j] * y[pos[t,j]] ) over the fp32 expert-output rows,
-// fp32 fused multiply-adds in slot order j = 0..k-1, one rounding at the end.  One warp per
-// token; each lane owns 8 consecutive columns per step (two 16-byte loads per slot).
+// fp32 fused multiply-adds in slot order j = 0..k-1, one rounding at the end.  Each lane owns
+// 8 consecutive columns per step (two 16-byte loads per slot).  KC >= k bounds the slots.
+template <int KC>
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y,
                                                       const float* __restrict__ gate,
                                                       const int32_t* __restrict__ pos,
@@ -405,27 +411,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n8 = d >> 3;
-  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
-       t += nwarps) {
+  const int upt = (n8 + kCombChunks - 1) / kCombChunks;
+  for (int64_t u = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       u < T * upt; u += nwarps) {
+    const int64_t t = u / upt;
+    const int c0 = static_cast<int>(u - t * upt) * kCombChunks;
     int row = 0;
     float g = 0.0f;
     if (lane < k) {
       row = pos[t * k + lane];
       g = gate[t * k + lane];
     }
-    int rows[kMaxK];
-    float gs[kMaxK];
+    int rows[KC];
+    float gs[KC];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KC; ++j) {
       rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
       gs[j] = __shfl_sync(0xFFFFFFFFu, g, j);
     }
-    for (int c = lane; c < n8; c += 32) {
+#pragma unroll 1
+    for (int c = c0 + lane; c < c0 + kCombChunks && c < n8; c += 32) {
       float acc[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
+      for (int j = 0; j < KC; ++j)
         if (j < k) {
           const float4* src = y + (static_cast<int64_t>(rows[j]) * n8 + c) * 2;
           const float4 a = __ldg(src), b = __ldg(src + 1);
@@ -444,7 +454,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
   }
 }
 
-// dx[t] = bf16( sum_j rows[pos[t,j]] ) with fp32 rows, adds in slot order.
+// dx[t] = bf16( sum_j rows[pos[t,j]] ) with fp32 rows, adds in slot order; same units.
+template <int KC>
 __global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restrict__ rowsp,
                                                           const int32_t* __restrict__ pos,
                                                           int64_t T, int k, int d,
@@ -452,18 +463,22 @@ __global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restri
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n8 = d >> 3;
-  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
-       t += nwarps) {
+  const int upt = (n8 + kCombChunks - 1) / kCombChunks;
+  for (int64_t u = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       u < T * upt; u += nwarps) {
+    const int64_t t = u / upt;
+    const int c0 = static_cast<int>(u - t * upt) * kCombChunks;
     const int row = lane < k ? pos[t * k + lane] : 0;
-    int rows[kMaxK];
+    int rows[KC];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
-    for (int c = lane; c < n8; c += 32) {
+    for (int j = 0; j < KC; ++j) rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
+#pragma unroll 1
+    for (int c = c0 + lane; c < c0 + kCombChunks && c < n8; c += 32) {
       float acc[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
+      for (int j = 0; j < KC; ++j)
         if (j < k) {
           const float4* src = rowsp + (static_cast<int64_t>(rows[j]) * n8 + c) * 2;
           const float4 a = __ldg(src), b = __ldg(src + 1);
@@ -476,36 +491,42 @@ __global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restri
   }
 }
 
-// Per-token backward of the combine and the gate:
-//   dgate[t,j] = <y[pos[t,j]], dy[t]> (fp32: per-lane partials over a fixed column set, then a
-//   fixed butterfly), dO[pos[t,j]] = bf16(gate[t,j] * dy[t]),
-//   dlogits[t, e_j] = g_j (dgate_j - sum_i g_i dgate_i), 0 for unselected experts.
-__global__ void __launch_bounds__(256) bwd_gate_kernel(
+// Backward of the combine and the gate, in two passes.
+// Pass 1, per (token, column block) unit: dO[pos[t,j]] = bf16(gate[t,j] * dy[t]) and the
+// block's partial dot products <y[pos[t,j]], dy[t]> (fp32: per-lane partials over the lane's
+// columns of the block, then a fixed butterfly), stored to part[t][block][j].
+// Pass 2, per token: dgate[t,j] = sum of the blocks' partials in block order,
+// dlogits[t, e_j] = g_j (dgate_j - sum_i g_i dgate_i), 0 for unselected experts.
+template <int KC>
+__global__ void __launch_bounds__(256) bwd_gate_rows_kernel(
     const uint4* __restrict__ dy, const float4* __restrict__ y, const float* __restrict__ gate,
-    const int32_t* __restrict__ pos, const int32_t* __restrict__ topk, int64_t T, int k, int d,
-    int E, uint4* __restrict__ dO, float* __restrict__ dgate, float* __restrict__ dlogits) {
+    const int32_t* __restrict__ pos, int64_t T, int k, int d, uint4* __restrict__ dO,
+    float* __restrict__ part) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  const int n16 = d >> 3;
-  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
-       t += nwarps) {
-    int row = 0, ex = 0;
+  const int n8 = d >> 3;
+  const int upt = (n8 + kCombChunks - 1) / kCombChunks;
+  for (int64_t u = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       u < T * upt; u += nwarps) {
+    const int64_t t = u / upt;
+    const int c0 = static_cast<int>(u - t * upt) * kCombChunks;
+    int row = 0;
     float g = 0.0f;
     if (lane < k) {
       row = pos[t * k + lane];
       g = gate[t * k + lane];
-      ex = topk[t * k + lane];
     }
-    int rows[kMaxK];
-    float gs[kMaxK], part[kMaxK];
+    int rows[KC];
+    float gs[KC], dot[KC];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KC; ++j) {
       rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
       gs[j] = __shfl_sync(0xFFFFFFFFu, g, j);
-      part[j] = 0.0f;
+      dot[j] = 0.0f;
     }
-    for (int c = lane; c < n16; c += 32) {
-      const uint4 dv = ld_nc_v4(dy + t * n16 + c);
+#pragma unroll 1
+    for (int c = c0 + lane; c < c0 + kCombChunks && c < n8; c += 32) {
+      const uint4 dv = ld_nc_v4(dy + t * n8 + c);
       const uint32_t du[4] = {dv.x, dv.y, dv.z, dv.w};
       float dyf[8];
 #pragma unroll
@@ -514,38 +535,57 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(
         dyf[2 * q + 1] = bf16hi(du[q]);
       }
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
+      for (int j = 0; j < KC; ++j)
         if (j < k) {
-          const float4* ys = y + (static_cast<int64_t>(rows[j]) * n16 + c) * 2;
+          const float4* ys = y + (static_cast<int64_t>(rows[j]) * n8 + c) * 2;
           const float4 ya = __ldg(ys), yb = __ldg(ys + 1);
           const float yf[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
 #pragma unroll
-          for (int q = 0; q < 8; ++q) part[j] = __fmaf_rn(yf[q], dyf[q], part[j]);
+          for (int q = 0; q < 8; ++q) dot[j] = __fmaf_rn(yf[q], dyf[q], dot[j]);
           uint4 o;
           o.x = pack_bf16x2(gs[j] * dyf[0], gs[j] * dyf[1]);
           o.y = pack_bf16x2(gs[j] * dyf[2], gs[j] * dyf[3]);
           o.z = pack_bf16x2(gs[j] * dyf[4], gs[j] * dyf[5]);
           o.w = pack_bf16x2(gs[j] * dyf[6], gs[j] * dyf[7]);
-          st_v4(dO + static_cast<int64_t>(rows[j]) * n16 + c, o);
+          st_v4(dO + static_cast<int64_t>(rows[j]) * n8 + c, o);
         }
     }
-    float mydg = 0.0f;
+    float mine = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
+    for (int j = 0; j < KC; ++j)
       if (j < k) {
-        float s = part[j];
+        float v = dot[j];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-        if (lane == j) mydg = s;
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        if (lane == j) mine = v;
       }
-    if (lane < k) dgate[t * k + lane] = mydg;
+    if (lane < k) part[u * k + lane] = mine;
+  }
+}
+
+__global__ void __launch_bounds__(256) bwd_gate_finish_kernel(
+    const float* __restrict__ part, const float* __restrict__ gate,
+    const int32_t* __restrict__ topk, int64_t T, int k, int upt, int E,
+    float* __restrict__ dgate, float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += nwarps) {
+    float dg = 0.0f, g = 0.0f;
+    int ex = 0;
+    if (lane < k) {
+      for (int b = 0; b < upt; ++b) dg += part[(t * upt + b) * k + lane];
+      g = gate[t * k + lane];
+      ex = topk[t * k + lane];
+      dgate[t * k + lane] = dg;
+    }
     if (dlogits) {
       float sgd = 0.0f;
-      for (int j = 0; j < k; ++j) sgd += __shfl_sync(0xFFFFFFFFu, g * mydg, j);
+      for (int j = 0; j < k; ++j) sgd += __shfl_sync(0xFFFFFFFFu, g * dg, j);
       float* dl = dlogits + t * E;
       for (int e = lane; e < E; e += 32) dl[e] = 0.0f;
       __syncwarp();
-      if (lane < k) dl[ex] = g * (mydg - sgd);
+      if (lane < k) dl[ex] = g * (dg - sgd);
     }
   }
 }
@@ -556,6 +596,67 @@ int grid_for_warps(int64_t warps, int warps_per_block) {
   if (b > cap) b = cap;
   if (b < 1) b = 1;
   return static_cast<int>(b);
+}
+
+// Blocks of `kern` (256 threads) resident on the whole current device at once, cached per
+// device and kernel; 0 if the query fails.
+template <typename K>
+int resident_blocks(K kern) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev]) return cache[dev];
+  int per_sm = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  cache[dev] = per_sm * sms;
+  return cache[dev];
+}
+
+// Grid for a warp-per-unit kernel: one warp per unit, at most the resident capacity.
+template <typename K>
+int unit_grid(K kern, int64_t units) {
+  int64_t b = (units + 7) / 8;
+  const int cap = resident_blocks(kern);
+  if (cap > 0 && b > cap) b = cap;
+  if (b > (1ll << 30)) b = 1ll << 30;
+  return static_cast<int>(b < 1 ? 1 : b);
+}
+
+// k -> kernel instantiation with KC = the next power of two >= k
+#define MOE_DISPATCH_KC(k, KERNEL, ...)                      \
+  ((k) <= 1 ? KERNEL<1>(__VA_ARGS__)                         \
+   : (k) <= 2 ? KERNEL<2>(__VA_ARGS__)                       \
+   : (k) <= 4 ? KERNEL<4>(__VA_ARGS__)                       \
+   : (k) <= 8 ? KERNEL<8>(__VA_ARGS__)                       \
+              : KERNEL<16>(__VA_ARGS__))
+
+template <int KC>
+cudaError_t launch_combine_kc(const float* y_rows, const float* gate, const int32_t* pos,
+                              int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
+  const int64_t units = T * ((d / 8 + kCombChunks - 1) / kCombChunks);
+  combine_kernel<KC><<<unit_grid(combine_kernel<KC>, units), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(y_rows), gate, pos, T, k, d, reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+template <int KC>
+cudaError_t launch_combine_f32_kc(const float* rows, const int32_t* pos, int64_t T, int k, int d,
+                                  uint16_t* out, cudaStream_t s) {
+  const int64_t units = T * ((d / 8 + kCombChunks - 1) / kCombChunks);
+  combine_f32_kernel<KC><<<unit_grid(combine_f32_kernel<KC>, units), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(rows), pos, T, k, d, reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+template <int KC>
+cudaError_t launch_bwd_gate_kc(const uint16_t* dy, const float* y_rows, const float* gate,
+                               const int32_t* pos, int64_t T, int k, int d, uint16_t* dO_rows,
+                               float* part, cudaStream_t s) {
+  const int64_t units = T * ((d / 8 + kCombChunks - 1) / kCombChunks);
+  bwd_gate_rows_kernel<KC><<<unit_grid(bwd_gate_rows_kernel<KC>, units), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(dy), reinterpret_cast<const float4*>(y_rows), gate, pos, T,
+      k, d, reinterpret_cast<uint4*>(dO_rows), part);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -619,29 +720,27 @@ cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, i
 cudaError_t launch_combine(const float* y_rows, const float* gate, const int32_t* pos,
                            int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(reinterpret_cast<const float4*>(y_rows),
-                                                      gate, pos, T, k, d,
-                                                      reinterpret_cast<uint4*>(out));
-  return cudaGetLastError();
+  return MOE_DISPATCH_KC(k, launch_combine_kc, y_rows, gate, pos, T, k, d, out, s);
 }
 
 cudaError_t launch_bwd_gate(const uint16_t* dy, const float* y_rows, const float* gate,
                             const int32_t* pos, const int32_t* topk, int64_t T, int k, int d,
-                            int E, uint16_t* dO_rows, float* dgate, float* dlogits,
+                            int E, uint16_t* dO_rows, float* dgate, float* dlogits, float* part,
                             cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  bwd_gate_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(dy), reinterpret_cast<const float4*>(y_rows), gate, pos, topk,
-      T, k, d, E, reinterpret_cast<uint4*>(dO_rows), dgate, dlogits);
+  const cudaError_t st =
+      MOE_DISPATCH_KC(k, launch_bwd_gate_kc, dy, y_rows, gate, pos, T, k, d, dO_rows, part, s);
+  if (st != cudaSuccess) return st;
+  const int upt = (d / 8 + kCombChunks - 1) / kCombChunks;
+  bwd_gate_finish_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(part, gate, topk, T, k, upt, E,
+                                                              dgate, dlogits);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_f32(const float* rows, const int32_t* pos, int64_t T, int k, int d,
                                uint16_t* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  combine_f32_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
-      reinterpret_cast<const float4*>(rows), pos, T, k, d, reinterpret_cast<uint4*>(out));
-  return cudaGetLastError();
+  return MOE_DISPATCH_KC(k, launch_combine_f32_kc, rows, pos, T, k, d, out, s);
 }
 
 }  // namespace moe
