@@ -47,6 +47,10 @@ struct KindTraits {
 };
 
 struct GemmParams {
+  // fp32 output tiles written by TMA stores (32 x 32 boxes, 128-byte swizzle) when tma_store:
+  // c0 = out0, c1 = out1
+  CUtensorMap mapC0, mapC1;
+  int tma_store;
   int E, d, dff;
   int nb;   // BN blocks along N
   int nkb;  // 64-wide K blocks (row-grouped kinds)
@@ -97,10 +101,14 @@ struct GemmCfg {
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
   static constexpr int kBars = 2 * kStages + 5;  // full, empty, tfull x2, tempty x2, drain
-  static constexpr size_t kEpiBytes = 4 * 32 * 33 * 4;  // one transpose buffer per epilogue warp
+  // one 1024-aligned 5 KB region per epilogue warp: a 32 x 33 fp32 transpose buffer, or the
+  // 32 x 32 fp32 staging box of a TMA store
+  static constexpr size_t kEpiWarpBytes = 5120;
+  static constexpr size_t kEpiBytes = 4 * kEpiWarpBytes;
   static constexpr size_t kGatherBytes = kBM * 4;  // token index of each A row of a tile
   static constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 1024 +
-                                       8 * kBars + 64 + kEpiBytes + kGatherBytes;
+                                       kEpiBytes + 8 * kBars + 64 + kGatherBytes;
+  static_assert(kStageBytes % 1024 == 0, "stages keep the epilogue regions 1024-aligned");
 };
 
 struct TileInfo {
@@ -247,7 +255,6 @@ __device__ __forceinline__ void combine_segment(const GemmParams& p, int seg, in
 // time.  A lane holds 32 consecutive values of its own row; the warp transposes the 32 x 32
 // chunk through a padded shared buffer (32 x 33 floats, conflict-free both ways) so that every
 // global store instruction writes whole 128-byte lines of 4 (fp32) or 8 (bf16) rows.
-constexpr int kEpiBufFloats = 32 * 33;
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   float a[16], b[16];
@@ -290,11 +297,37 @@ __device__ __forceinline__ void store_chunk(float* buf, const float (&v)[32], ch
   __syncwarp();
 }
 
+// 32 rows (one per lane) x 32 fp32 columns to global memory with one TMA store of box (x, y).
+// The warp writes the box into its staging region in the 128-byte-swizzled layout the tensor
+// map expects (16-byte chunk c of row r at chunk c ^ (r & 7)), then lane 0 issues the store.
+// Before the warp rewrites the region, lane 0 waits until the previous store has read it.
+__device__ __forceinline__ void store_chunk_tma(uint32_t stage, const float (&v)[32],
+                                                const CUtensorMap* map, int x, int y, int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+  const uint32_t row = stage + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t dst = row + static_cast<uint32_t>((c ^ (lane & 7)) * 16);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                 "r"(__float_as_uint(v[4 * c])), "r"(__float_as_uint(v[4 * c + 1])),
+                 "r"(__float_as_uint(v[4 * c + 2])), "r"(__float_as_uint(v[4 * c + 3]))
+                 : "memory");
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, stage, x, y);
+    bulk_commit();
+  }
+}
+
 // Epilogue of one tile for one epilogue warp (rows q*32 .. q*32+31 of the accumulator).
 // `tacc` is the warp's TMEM address (lane base q*32, accumulator column 0); `r` = q*32 + lane.
 template <int KIND, int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& ti,
-                                              uint32_t tacc, int q, int lane, float* buf) {
+                                              uint32_t tacc, int q, int lane, float* buf,
+                                              uint32_t stage) {
   const int r = q * 32 + lane;
   const bool valid = r < ti.nvalid;
   const int w0 = q * 32;  // first row of this warp
@@ -325,11 +358,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     const int64_t row0 = ti.row0 + w0;
     char* out = reinterpret_cast<char*>(static_cast<float*>(p.out0) + row0 * p.d + ti.n0);
     const int nstore = clamp_rows(ti.nvalid);
+    // TMA stores write all 32 rows of the warp: rows past the expert's count are padding rows
+    // of its own segment (zeros: their A rows are zero), which nothing reads
+    const bool tma = p.tma_store && !p.fuse_combine && clamp_rows(ti.nseg) == 32;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
       float v[32];
       tmem_ld32(tacc + ch * 32, v);
-      store_chunk<false>(buf, v, out + ch * 128, 4ll * p.d, nstore, lane);
+      if (tma) {
+        store_chunk_tma(stage, v, &p.mapC0, ti.n0 + ch * 32, static_cast<int>(row0), lane);
+      } else {
+        if (p.tma_store && lane == 0) bulk_wait_read_all();  // the region may still be read
+        __syncwarp();
+        store_chunk<false>(buf, v, out + ch * 128, 4ll * p.d, nstore, lane);
+      }
     }
     if constexpr (KIND == kFwd2) {
       if (p.fuse_combine) {
@@ -401,6 +443,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
                                     (first ? ti.n0 : ti.n0 - p.dff));
     }
     const int nstore = clamp_rows(ti.mvalid);
+    const CUtensorMap* cmap = &p.mapC0;
+    int cx = ti.n0, cy;
+    if constexpr (KIND == kDw2) {
+      cy = ti.e * p.dff + ti.m0 + w0;
+    } else {
+      cy = ti.e * p.d + ti.m0 + w0;
+      if (ti.n0 >= p.dff) {
+        cmap = &p.mapC1;
+        cx = ti.n0 - p.dff;
+      }
+    }
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
       float v[32];
@@ -410,7 +463,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
       }
-      store_chunk<false>(buf, v, out + ch * 128, row_bytes, nstore, lane);
+      if (p.tma_store && nstore == 32) {
+        store_chunk_tma(stage, v, cmap, cx + ch * 32, cy, lane);
+      } else {
+        if (p.tma_store && lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        store_chunk<false>(buf, v, out + ch * 128, row_bytes, nstore, lane);
+      }
     }
   }
 }
@@ -426,7 +485,8 @@ template <int KIND, int BN, bool PAIR>
 __global__ void __launch_bounds__(256, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapB0,
-                        const __grid_constant__ CUtensorMap mapB1, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap mapB1,
+                        const __grid_constant__ GemmParams p) {
   using Cfg = GemmCfg<BN, PAIR>;
   using Tr = KindTraits<KIND>;
   constexpr int S = Cfg::kStages;
@@ -437,19 +497,20 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bar0 = base + S * Cfg::kStageBytes;
+  const uint32_t epi0 = base + S * Cfg::kStageBytes;  // epilogue regions (1024-aligned)
+  const uint32_t bar0 = epi0 + static_cast<uint32_t>(Cfg::kEpiBytes);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
-  uint8_t* misc = gbase + S * Cfg::kStageBytes + 8 * Cfg::kBars;
+  uint8_t* misc = gbase + S * Cfg::kStageBytes + Cfg::kEpiBytes + 8 * Cfg::kBars;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(misc + 8);
   volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(misc + 12);
-  float* epi_buf = reinterpret_cast<float*>(misc + 64);  // 4 x (32 x 33) floats
-  int32_t* gather_ids = reinterpret_cast<int32_t*>(misc + 64 + Cfg::kEpiBytes);
+  float* epi_buf = reinterpret_cast<float*>(gbase + S * Cfg::kStageBytes);
+  int32_t* gather_ids = reinterpret_cast<int32_t*>(misc + 64);
   auto stage_a = [&](int s) { return base + s * Cfg::kStageBytes; };
   auto stage_b = [&](int s) { return base + s * Cfg::kStageBytes + kABytes; };
 
@@ -654,7 +715,6 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp - 4;
-    const int r = q * 32 + lane;
     int it = 0;
     const uint32_t release_to = PAIR ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     for (int tile = unit; tile < ntiles; tile += nunits) {
@@ -667,15 +727,21 @@ __global__ void __launch_bounds__(256, 1)
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<KIND, BN>(p, ti, tacc, q, lane, epi_buf + q * kEpiBufFloats);
+      epilogue_tile<KIND, BN>(p, ti, tacc, q, lane,
+                              epi_buf + q * (Cfg::kEpiWarpBytes / 4),
+                              epi0 + q * static_cast<uint32_t>(Cfg::kEpiWarpBytes));
       tc_fence_before();
       __syncwarp();
+      // The accumulator is free once every lane's tcgen05.ld has completed (they have: the
+      // values are in registers).  The arrival is relaxed so that it does not wait for the
+      // warp's global stores of this tile, which nothing on the MMA side reads.
       if (lane == 0) {
-        if constexpr (PAIR) mbar_arrive_cluster(release_to + 8u * acc);
-        else mbar_arrive(release_to + 8u * acc);
+        if constexpr (PAIR) mbar_arrive_cluster_relaxed(release_to + 8u * acc);
+        else mbar_arrive_relaxed(release_to + 8u * acc);
       }
       ++it;
     }
+    if (p.tma_store && lane == 0) bulk_wait_all();  // stores done before the CTA exits
   }
 
   __syncthreads();
@@ -721,6 +787,8 @@ __global__ void __launch_bounds__(256, 1)
 // ------------------------------------------------------------------ host side
 CUtensorMap make_map_2d(const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                         uint32_t box_inner, uint32_t box_rows, cudaError_t* st);
+CUtensorMap make_store_map_f32(void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                               cudaError_t* st);
 
 template <int KIND, int BN, bool PAIR>
 cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,

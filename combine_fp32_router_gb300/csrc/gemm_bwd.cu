@@ -57,6 +57,9 @@ cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s) {
   p.nb = L.d / BN;
   p.nkb = 2 * L.dff / kBK;
   p.out0 = c.ws + L.dXp;
+  p.mapC0 = make_store_map_f32(c.ws + L.dXp, L.d, L.P_pad, 4ull * L.d, &st);
+  if (st != cudaSuccess) return st;
+  p.tma_store = 1;
   const GemmParams lo = leftover_params(p, c);
   if (BN == 256) return run_rows_kind<kDx, 256>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, L.E, c.num_sms, s);
   return run_rows_kind<kDx, 128>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, L.E, c.num_sms, s);
@@ -76,6 +79,9 @@ cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s) {
   p.mb = (L.dff + mrows - 1) / mrows;
   p.nb = L.d / BN;
   p.out0 = c.dW2;
+  p.mapC0 = make_store_map_f32(c.dW2, L.d, static_cast<uint64_t>(L.E) * L.dff, 4ull * L.d, &st);
+  if (st != cudaSuccess) return st;
+  p.tma_store = 1;
   const int64_t tiles = static_cast<int64_t>(L.E) * p.mb * p.nb;
   return run_bn<kDw2>(BN, c.pair, a, b0, b0, p, tiles, c.num_sms, s);
 }
@@ -95,6 +101,10 @@ cudaError_t launch_gemm_dw13(const GemmCtx& c, cudaStream_t s) {
   p.nb = 2 * L.dff / BN;
   p.out0 = c.dW1;
   p.out1 = c.dW3;
+  p.mapC0 = make_store_map_f32(c.dW1, L.dff, static_cast<uint64_t>(L.E) * L.d, 4ull * L.dff, &st);
+  p.mapC1 = make_store_map_f32(c.dW3, L.dff, static_cast<uint64_t>(L.E) * L.d, 4ull * L.dff, &st);
+  if (st != cudaSuccess) return st;
+  p.tma_store = 1;
   const int64_t tiles = static_cast<int64_t>(L.E) * p.mb * p.nb;
   return run_bn<kDw13>(BN, c.pair, a, b0, b0, p, tiles, c.num_sms, s);
 }

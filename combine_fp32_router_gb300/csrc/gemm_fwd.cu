@@ -46,6 +46,31 @@ CUtensorMap make_map_2d(const void* base, uint64_t inner, uint64_t rows, uint64_
   return m;
 }
 
+// 2-D fp32 tensor map for TMA stores of 32 x 32 boxes with 128-byte swizzle.
+CUtensorMap make_store_map_f32(void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                               cudaError_t* st) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof m);
+  auto enc = reinterpret_cast<Encode>(tensor_map_encoder());
+  if (!enc) {
+    *st = cudaErrorNotSupported;
+    return m;
+  }
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) *st = cudaErrorInvalidValue;
+  return m;
+}
+
 GemmParams base_params(const GemmCtx& c) {
   const WsLayout& L = *c.L;
   GemmParams p{};
@@ -118,6 +143,11 @@ cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
   p.seg_count = reinterpret_cast<int32_t*>(c.ws + L.seg);
   p.comb_out = c.out;
   p.k = L.k;
+  if (!c.fuse_combine) {
+    p.mapC0 = make_store_map_f32(c.ws + L.Y, L.d, L.P_pad, 4ull * L.d, &st);
+    if (st != cudaSuccess) return st;
+    p.tma_store = 1;
+  }
   const GemmParams lo = leftover_params(p, c);
   if (BN == 256)
     return run_rows_kind<kFwd2, 256>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, L.E, c.num_sms, s);
