@@ -563,9 +563,9 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    // Lane 0 waits and issues every load.  With gather_x the whole warp first stages the
-    // token index of each of the tile's A rows (padding rows read token 0; they are never
-    // stored).
+    // Lane 0 waits for each stage and issues the tile loads.  With gather_x the warp first
+    // stages the token index of each of the tile's A rows (padding rows read token 0; they are
+    // never stored), then every lane gathers 4 of the 128 rows per stage.
     if (lane == 0) {
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB0);
@@ -579,7 +579,6 @@ __global__ void __launch_bounds__(256, 1)
       else tma_load_2d(dst, m, fb, x, y);
     };
     for (int tile = unit; tile < ntiles; tile += nunits) {
-      // the warp is converged here: lanes 1..31 wait below while lane 0 issues a tile
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       const TileInfo ti = decode_tile<KIND, BN, PAIR>(p, tile, rank);
@@ -598,12 +597,15 @@ __global__ void __launch_bounds__(256, 1)
           __syncwarp();
         }
       }
-      if (lane == 0) {
       const int nb0 = ti.n0 + rank * BL;  // first B column held by this CTA
+      // The warp walks the K blocks together: lane 0 waits for the stage, arms it and issues
+      // the tile loads; with gather_x every lane also issues one gather of 4 A rows.
       for (int kb = 0; kb < ti.nk; ++kb) {
         const int s = fill % S;
         const uint32_t ph = (fill / S) & 1u;
-        if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, 1)) {
+        bool got = true;
+        if (lane == 0) got = wait_bar(empty_bar(s), ph ^ 1u, abort_flag, 1);
+        if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
           ok = false;
           break;
         }
@@ -611,60 +613,60 @@ __global__ void __launch_bounds__(256, 1)
         if ((p.debug_flags & 1) && blockIdx.x == 0 && fill == 0) {
           skipped = 0;  // test hook: this stage is never armed nor filled by this CTA
         } else {
-          // rank 0 arms its barrier for both CTAs' bytes; rank 1 only loads
-          if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * Cfg::kStageBytes : Cfg::kStageBytes);
           const int k0 = kb * kBK;
           if constexpr (KIND == kFwd1) {
             if (p.gather_x) {
-#pragma unroll 4
-              for (int i = 0; i < kBM / 4; ++i) {
-                const int* g4 = gather_ids + 4 * i;
-                if constexpr (PAIR)
-                  tma_gather4_pair(sa + 512u * i, &mapA, mapa_shared(fb, 0), k0, g4[0], g4[1], g4[2], g4[3]);
-                else
-                  tma_gather4(sa + 512u * i, &mapA, fb, k0, g4[0], g4[1], g4[2], g4[3]);
-              }
-            } else {
-              load(sa, &mapA, fb, k0, ti.row0);
+              const int* g4 = gather_ids + 4 * lane;  // rows 4 lane .. 4 lane + 3
+              if constexpr (PAIR)
+                tma_gather4_pair(sa + 512u * lane, &mapA, mapa_shared(fb, 0), k0, g4[0], g4[1],
+                                 g4[2], g4[3]);
+              else
+                tma_gather4(sa + 512u * lane, &mapA, fb, k0, g4[0], g4[1], g4[2], g4[3]);
             }
-            const int wrow = ti.e * p.d + k0;
-            const int h0 = ti.n0 / 2;  // first h column of the tile
-            if constexpr (PAIR) {
-              // rank 0 holds the W1 half of B, rank 1 the W3 half
-              const CUtensorMap* wm = rank == 0 ? &mapB0 : &mapB1;
-#pragma unroll
-              for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, wm, fb, h0 + 64 * i, wrow);
-            } else {
-#pragma unroll
-              for (int i = 0; i < BN / 128; ++i) {
-                load(sb + 8192u * i, &mapB0, fb, h0 + 64 * i, wrow);
-                load(sb + 8192u * (BN / 128 + i), &mapB1, fb, h0 + 64 * i, wrow);
-              }
-            }
-          } else if constexpr (KIND == kFwd2) {
-            load(sa, &mapA, fb, k0, ti.row0);
-#pragma unroll
-            for (int i = 0; i < BL / 64; ++i)
-              load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, ti.e * p.dff + k0);
-          } else if constexpr (KIND == kDh) {
-            load(sa, &mapA, fb, k0, ti.row0);
-            load(sb, &mapB0, fb, k0, ti.e * p.dff + nb0);
-          } else if constexpr (KIND == kDx) {
-            load(sa, &mapA, fb, k0, ti.row0);
-            if (k0 < p.dff) load(sb, &mapB0, fb, k0, ti.e * p.d + nb0);
-            else load(sb, &mapB1, fb, k0 - p.dff, ti.e * p.d + nb0);
-          } else {
-            const int r = ti.row0 + k0;
-            load(sa, &mapA, fb, ti.m0, r);
-            load(sa + 8192u, &mapA, fb, ti.m0 + 64, r);
-#pragma unroll
-            for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, r);
           }
+          if (lane == 0) {
+            // rank 0 arms its barrier for both CTAs' bytes; rank 1 only loads
+            if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * Cfg::kStageBytes : Cfg::kStageBytes);
+            if constexpr (KIND == kFwd1) {
+              if (!p.gather_x) load(sa, &mapA, fb, k0, ti.row0);
+              const int wrow = ti.e * p.d + k0;
+              const int h0 = ti.n0 / 2;  // first h column of the tile
+              if constexpr (PAIR) {
+                // rank 0 holds the W1 half of B, rank 1 the W3 half
+                const CUtensorMap* wm = rank == 0 ? &mapB0 : &mapB1;
+#pragma unroll
+                for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, wm, fb, h0 + 64 * i, wrow);
+              } else {
+#pragma unroll
+                for (int i = 0; i < BN / 128; ++i) {
+                  load(sb + 8192u * i, &mapB0, fb, h0 + 64 * i, wrow);
+                  load(sb + 8192u * (BN / 128 + i), &mapB1, fb, h0 + 64 * i, wrow);
+                }
+              }
+            } else if constexpr (KIND == kFwd2) {
+              load(sa, &mapA, fb, k0, ti.row0);
+#pragma unroll
+              for (int i = 0; i < BL / 64; ++i)
+                load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, ti.e * p.dff + k0);
+            } else if constexpr (KIND == kDh) {
+              load(sa, &mapA, fb, k0, ti.row0);
+              load(sb, &mapB0, fb, k0, ti.e * p.dff + nb0);
+            } else if constexpr (KIND == kDx) {
+              load(sa, &mapA, fb, k0, ti.row0);
+              if (k0 < p.dff) load(sb, &mapB0, fb, k0, ti.e * p.d + nb0);
+              else load(sb, &mapB1, fb, k0 - p.dff, ti.e * p.d + nb0);
+            } else {
+              const int r = ti.row0 + k0;
+              load(sa, &mapA, fb, ti.m0, r);
+              load(sa + 8192u, &mapA, fb, ti.m0 + 64, r);
+#pragma unroll
+              for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, r);
+            }
+          }  // lane 0
         }
         ++fill;
       }
-      }  // lane 0
-      __syncwarp();  // gather_ids may be rewritten only after lane 0 has issued the tile
+      __syncwarp();  // gather_ids may be rewritten only after the tile's gathers are issued
     }
     issued = fill;
   } else if (warp == 1 && lane == 0 && rank == 0) {
