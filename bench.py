@@ -391,6 +391,22 @@ def bench_native(args, w):
 
     names = ["dispatch", "gemm1_swiglu", "gemm2", "combine"]
     stages = dict(zip(names, stage_ms))
+    # per-expert roofline of the grouped GEMMs under this workload's load: every active expert
+    # streams its 3 weight matrices once and does 6 d d_ff FLOP per routed row
+    counts = torch.bincount(torch.topk(g["logits"], k, dim=1).indices.flatten(),
+                            minlength=E).double().cpu().numpy()
+    active = counts > 0
+    w_bytes = 3 * 2 * d * dff  # per active expert
+    t_e = np.maximum(6 * d * dff * counts[active] / (peaks["bf16"] * 1e12), w_bytes / (peaks["hbm"] * 1e9))
+    gemm_ms = stages["gemm1_swiglu"] + stages["gemm2"]
+    roof = {"per_expert_sum_ms": float(t_e.sum() * 1e3),
+            "overlapped_ms": float(max(6 * d * dff * counts.sum() / (peaks["bf16"] * 1e12),
+                                       active.sum() * w_bytes / (peaks["hbm"] * 1e9)) * 1e3),
+            "active_experts": int(active.sum()),
+            "weights_gb": float(active.sum() * w_bytes / 1e9),
+            "weights_gbs": float(active.sum() * w_bytes / (gemm_ms * 1e-3) / 1e9)}
+    roof["gemm_frac_of_per_expert_sum"] = roof["per_expert_sum_ms"] / gemm_ms
+    roof["gemm_frac_of_overlapped"] = roof["overlapped_ms"] / gemm_ms
     g1_tflops = alg["gemm1_flops"] / (stages["gemm1_swiglu"] * 1e-3) / 1e12
     g_tflops = alg["gemm_flops"] / ((stages["gemm1_swiglu"] + stages["gemm2"]) * 1e-3) / 1e12
     disp_gbs = alg["dispatch_bytes"] / (stages["dispatch"] * 1e-3) / 1e9
@@ -410,6 +426,7 @@ def bench_native(args, w):
         "stages_ms": stages,
         "gemm_tflops": g_tflops,
         "gemm_frac_of_bf16_burst": g_tflops / peaks["bf16"],
+        "gemm_roofline_under_load": roof,
         "dispatch_gbs": disp_gbs, "dispatch_frac_of_hbm": disp_gbs / peaks["hbm"],
         "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
         "waved_forward_ms_per_step": waved_ms,
@@ -441,6 +458,8 @@ def main():
     ap.add_argument("--shape", default=None,
                     help="T,d,E,k,d_ff of a custom workload (profiling captures of one kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count T (e.g. the small-batch sweep)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the forward + backward timing of the fwd_bwd workload")
     args = ap.parse_args()
@@ -451,6 +470,9 @@ def main():
         w = moe_synth.custom(T, d, E, k, dff, seed=1003, zipf_s=1.2, name="custom")
     else:
         w = moe_synth.by_name(args.workload)
+    if args.tokens is not None:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.tokens)
     if args.impl == "reference":
         return bench_reference(args, w)
     return bench_native(args, w)

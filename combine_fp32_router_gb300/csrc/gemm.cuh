@@ -565,7 +565,8 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------------ TMA producer
     // Lane 0 waits for each stage and issues the tile loads.  With gather_x the warp first
     // stages the token index of each of the tile's A rows (padding rows read token 0; they are
-    // never stored), then every lane gathers 4 of the 128 rows per stage.
+    // never stored), then every lane gathers 4 of the 128 rows per stage.  `fill`, `ok` and
+    // `skipped` are lane 0's (the tile loop broadcasts `ok`).
     if (lane == 0) {
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB0);
@@ -598,73 +599,85 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       const int nb0 = ti.n0 + rank * BL;  // first B column held by this CTA
-      // The warp walks the K blocks together: lane 0 waits for the stage, arms it and issues
-      // the tile loads; with gather_x every lane also issues one gather of 4 A rows.
-      for (int kb = 0; kb < ti.nk; ++kb) {
-        const int s = fill % S;
-        const uint32_t ph = (fill / S) & 1u;
-        bool got = true;
-        if (lane == 0) got = wait_bar(empty_bar(s), ph ^ 1u, abort_flag, 1);
-        if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
-          ok = false;
-          break;
-        }
-        const uint32_t fb = full_bar(s), sa = stage_a(s), sb = stage_b(s);
-        if ((p.debug_flags & 1) && blockIdx.x == 0 && fill == 0) {
-          skipped = 0;  // test hook: this stage is never armed nor filled by this CTA
-        } else {
-          const int k0 = kb * kBK;
-          if constexpr (KIND == kFwd1) {
-            if (p.gather_x) {
-              const int* g4 = gather_ids + 4 * lane;  // rows 4 lane .. 4 lane + 3
-              if constexpr (PAIR)
-                tma_gather4_pair(sa + 512u * lane, &mapA, mapa_shared(fb, 0), k0, g4[0], g4[1],
-                                 g4[2], g4[3]);
-              else
-                tma_gather4(sa + 512u * lane, &mapA, fb, k0, g4[0], g4[1], g4[2], g4[3]);
+      // lane 0: arm stage (fb) and issue the tile loads of K block kb (A too unless gathered)
+      auto issue_stage = [&](int kb, uint32_t fb, uint32_t sa, uint32_t sb) {
+        // rank 0 arms its barrier for both CTAs' bytes; rank 1 only loads
+        if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * Cfg::kStageBytes : Cfg::kStageBytes);
+        const int k0 = kb * kBK;
+        if constexpr (KIND == kFwd1) {
+          if (!p.gather_x) load(sa, &mapA, fb, k0, ti.row0);
+          const int wrow = ti.e * p.d + k0;
+          const int h0 = ti.n0 / 2;  // first h column of the tile
+          if constexpr (PAIR) {
+            // rank 0 holds the W1 half of B, rank 1 the W3 half
+            const CUtensorMap* wm = rank == 0 ? &mapB0 : &mapB1;
+#pragma unroll
+            for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, wm, fb, h0 + 64 * i, wrow);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i) {
+              load(sb + 8192u * i, &mapB0, fb, h0 + 64 * i, wrow);
+              load(sb + 8192u * (BN / 128 + i), &mapB1, fb, h0 + 64 * i, wrow);
             }
           }
-          if (lane == 0) {
-            // rank 0 arms its barrier for both CTAs' bytes; rank 1 only loads
-            if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * Cfg::kStageBytes : Cfg::kStageBytes);
-            if constexpr (KIND == kFwd1) {
-              if (!p.gather_x) load(sa, &mapA, fb, k0, ti.row0);
-              const int wrow = ti.e * p.d + k0;
-              const int h0 = ti.n0 / 2;  // first h column of the tile
-              if constexpr (PAIR) {
-                // rank 0 holds the W1 half of B, rank 1 the W3 half
-                const CUtensorMap* wm = rank == 0 ? &mapB0 : &mapB1;
+        } else if constexpr (KIND == kFwd2) {
+          load(sa, &mapA, fb, k0, ti.row0);
 #pragma unroll
-                for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, wm, fb, h0 + 64 * i, wrow);
-              } else {
+          for (int i = 0; i < BL / 64; ++i)
+            load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, ti.e * p.dff + k0);
+        } else if constexpr (KIND == kDh) {
+          load(sa, &mapA, fb, k0, ti.row0);
+          load(sb, &mapB0, fb, k0, ti.e * p.dff + nb0);
+        } else if constexpr (KIND == kDx) {
+          load(sa, &mapA, fb, k0, ti.row0);
+          if (k0 < p.dff) load(sb, &mapB0, fb, k0, ti.e * p.d + nb0);
+          else load(sb, &mapB1, fb, k0 - p.dff, ti.e * p.d + nb0);
+        } else {
+          const int r = ti.row0 + k0;
+          load(sa, &mapA, fb, ti.m0, r);
+          load(sa + 8192u, &mapA, fb, ti.m0 + 64, r);
 #pragma unroll
-                for (int i = 0; i < BN / 128; ++i) {
-                  load(sb + 8192u * i, &mapB0, fb, h0 + 64 * i, wrow);
-                  load(sb + 8192u * (BN / 128 + i), &mapB1, fb, h0 + 64 * i, wrow);
-                }
-              }
-            } else if constexpr (KIND == kFwd2) {
-              load(sa, &mapA, fb, k0, ti.row0);
-#pragma unroll
-              for (int i = 0; i < BL / 64; ++i)
-                load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, ti.e * p.dff + k0);
-            } else if constexpr (KIND == kDh) {
-              load(sa, &mapA, fb, k0, ti.row0);
-              load(sb, &mapB0, fb, k0, ti.e * p.dff + nb0);
-            } else if constexpr (KIND == kDx) {
-              load(sa, &mapA, fb, k0, ti.row0);
-              if (k0 < p.dff) load(sb, &mapB0, fb, k0, ti.e * p.d + nb0);
-              else load(sb, &mapB1, fb, k0 - p.dff, ti.e * p.d + nb0);
-            } else {
-              const int r = ti.row0 + k0;
-              load(sa, &mapA, fb, ti.m0, r);
-              load(sa + 8192u, &mapA, fb, ti.m0 + 64, r);
-#pragma unroll
-              for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, r);
-            }
-          }  // lane 0
+          for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, r);
         }
-        ++fill;
+      };
+      const bool skip_hook = (p.debug_flags & 1) && blockIdx.x == 0;
+      if (KIND == kFwd1 && p.gather_x) {
+        // The warp walks the K blocks together: every lane gathers 4 of the 128 A rows.
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          const int s = fill % S;
+          const uint32_t ph = (fill / S) & 1u;
+          bool got = true;
+          if (lane == 0) got = wait_bar(empty_bar(s), ph ^ 1u, abort_flag, 1);
+          if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(s), sa = stage_a(s), sb = stage_b(s);
+          if (skip_hook && fill == 0) {
+            skipped = 0;  // test hook: this stage is never armed nor filled by this CTA
+          } else {
+            const int* g4 = gather_ids + 4 * lane;  // rows 4 lane .. 4 lane + 3
+            if constexpr (PAIR)
+              tma_gather4_pair(sa + 512u * lane, &mapA, mapa_shared(fb, 0), kb * kBK, g4[0],
+                               g4[1], g4[2], g4[3]);
+            else
+              tma_gather4(sa + 512u * lane, &mapA, fb, kb * kBK, g4[0], g4[1], g4[2], g4[3]);
+            if (lane == 0) issue_stage(kb, fb, sa, sb);
+          }
+          ++fill;
+        }
+      } else if (lane == 0) {
+        for (int kb = 0; kb < ti.nk; ++kb) {
+          const int s = fill % S;
+          const uint32_t ph = (fill / S) & 1u;
+          if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, 1)) {
+            ok = false;
+            break;
+          }
+          if (skip_hook && fill == 0) skipped = 0;  // test hook (see above)
+          else issue_stage(kb, full_bar(s), stage_a(s), stage_b(s));
+          ++fill;
+        }
       }
       __syncwarp();  // gather_ids may be rewritten only after the tile's gathers are issued
     }
