@@ -337,28 +337,34 @@ def bench_native(args, w):
     ms_step = ms / args.steps
     value = world * T * args.steps / (ms / 1e3)
 
-    # end to end through the public API with pinned host buffers: H2D of x and logits,
-    # the layer, D2H of the output, every step
-    hx = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
-    hl = torch.empty(T, E, dtype=torch.float32, pin_memory=True)
-    ho = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
-    hx.copy_(g["x"])
-    hl.copy_(g["logits"])
-    dx = torch.empty_like(g["x"])
-    dl = torch.empty_like(g["logits"])
+    # end to end through the public API with host buffers: moe_forward_host copies the step's
+    # x and logits from page-locked host memory into its workspace, runs the layer and copies
+    # the output back.  Two workspaces on two streams take alternate steps, so one step's
+    # copies overlap the other step's layer; every step still moves its own inputs and output.
+    ws_io = [torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, False, host_io=True),
+                         dtype=torch.uint8, device=dev) for _ in range(2)]
+    io_streams = [torch.cuda.Stream(dev) for _ in range(2)]
+    hx = [g["x"].cpu().pin_memory() for _ in range(2)]
+    hl = [g["logits"].cpu().pin_memory() for _ in range(2)]
+    ho = [torch.empty(T, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
 
-    def e2e_step():
-        dx.copy_(hx, non_blocking=True)
-        dl.copy_(hl, non_blocking=True)
-        moe.moe_forward(dx, dl, g["W1"], g["W3"], g["W2"], k, out, ws, stream=stream)
-        ho.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        j = i % 2
+        moe.moe_forward_host(hx[j], hl[j], g["W1"], g["W3"], g["W2"], k, ho[j], ws_io[j],
+                             stream=io_streams[j])
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    for i in range(max(2, args.warmup)):
+        e2e_step(i)
     barrier()
+    ends = [torch.cuda.Event() for _ in range(2)]
     start.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    for s_ in io_streams:
+        s_.wait_event(start)
+    for i in range(args.steps):
+        e2e_step(i)
+    for s_, e_ in zip(io_streams, ends):
+        e_.record(s_)
+        stream.wait_event(e_)
     stop.record(stream)
     barrier()
     ms_e2e = start.elapsed_time(stop)
@@ -366,6 +372,15 @@ def bench_native(args, w):
         t = torch.tensor([ms_e2e], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_e2e = float(t.item())
+    for wsi in ws_io:
+        st = moe.moe_get_error(wsi)
+        if st != 0:
+            raise RuntimeError("device error (host-buffer forward): " + moe.moe_status_string(st))
+    e2e_out = ho[(args.steps - 1) % 2]
+    if not torch.equal(e2e_out.view(torch.int16), out.cpu().view(torch.int16)):
+        raise RuntimeError("host-buffer forward differs from the device forward")
+    del ws_io
+
     # the overlapped-wave variant (GEMM1 gathers rows from x, GEMM2 fuses the combine),
     # timed for comparison; bitwise the same output
     wave_flags = moe.MOE_FWD_GATHER_ROWS | moe.MOE_FWD_FUSED_COMBINE
@@ -386,8 +401,9 @@ def bench_native(args, w):
         raise RuntimeError("device error (waved forward): " + moe.moe_status_string(st))
 
     e2e = {"value": world * T * args.steps / (ms_e2e / 1e3), "unit": UNIT,
-           "h2d_bytes_per_step": hx.numel() * 2 + hl.numel() * 4,
-           "d2h_bytes_per_step": ho.numel() * 2}
+           "h2d_bytes_per_step": T * d * 2 + T * E * 4, "d2h_bytes_per_step": T * d * 2,
+           "api": "moe_forward_host, page-locked host buffers, two streams taking alternate "
+                  "steps"}
 
     names = ["dispatch", "gemm1_swiglu", "gemm2", "combine"]
     stages = dict(zip(names, stage_ms))

@@ -26,13 +26,16 @@ MOE_ERR_DEVICE_BOUNDS = 6
 MOE_FWD_SAVE_FOR_BACKWARD = 1
 MOE_FWD_FUSED_COMBINE = 2
 MOE_FWD_GATHER_ROWS = 4
+MOE_WS_BACKWARD = 1
+MOE_WS_HOST_IO = 2
 MOE_FWD_NUM_EVENTS = 5
 MOE_BWD_NUM_EVENTS = 7
 
 # Exported symbols of include/moe.h, in declaration order.
 EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispatch",
-           "moe_forward", "moe_backward", "moe_route_dispatch_noalloc", "moe_get_error",
-           "moe_set_wait_timeout_ns", "moe_debug_set_flags", "moe_status_string")
+           "moe_forward", "moe_forward_host", "moe_backward", "moe_route_dispatch_noalloc",
+           "moe_get_error", "moe_set_wait_timeout_ns", "moe_debug_set_flags",
+           "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -54,6 +57,8 @@ def _load():
     lib.moe_route_dispatch.argtypes = [p, p, i64, i, i, i] + [p] * 7 + [p, sz, p]
     lib.moe_route_dispatch.restype = i
     lib.moe_forward.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i, p, p]
+    lib.moe_forward_host.restype = i
+    lib.moe_forward_host.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i, p, p]
     lib.moe_forward.restype = i
     lib.moe_backward.argtypes = [p] * 6 + [i64, i, i, i, i] + [p] * 6 + [p, sz, p, p]
     lib.moe_backward.restype = i
@@ -114,8 +119,9 @@ def moe_route_workspace_bytes(T, E, k):
     return int(_lib.moe_route_workspace_bytes(T, E, k))
 
 
-def moe_workspace_bytes(T, d, E, k, d_ff, with_backward=False):
-    return int(_lib.moe_workspace_bytes(T, d, E, k, d_ff, int(bool(with_backward))))
+def moe_workspace_bytes(T, d, E, k, d_ff, with_backward=False, host_io=False):
+    needs = (MOE_WS_BACKWARD if with_backward else 0) | (MOE_WS_HOST_IO if host_io else 0)
+    return int(_lib.moe_workspace_bytes(T, d, E, k, d_ff, needs))
 
 
 def moe_route_dispatch(x, logits, k, topk_idx, gate, counts, offsets, perm, pos, x_perm, ws,
@@ -136,6 +142,18 @@ def moe_forward(x, logits, W1, W3, W2, k, out, ws, flags=0, stage_events=None, s
     _check(_lib.moe_forward(_ptr(x), _ptr(logits), _ptr(W1), _ptr(W3), _ptr(W2), T, d, E, k,
                             d_ff, _ptr(out), _ptr(ws), _nbytes(ws), int(flags),
                             _events(stage_events), _stream(stream)), "moe_forward")
+
+
+def moe_forward_host(x_host, logits_host, W1, W3, W2, k, out_host, ws, flags=0,
+                     stage_events=None, stream=None):
+    """Whole-layer forward with x, logits and out in host memory (page-locked for
+    asynchronous copies); the weights and ``ws`` are device tensors."""
+    T, d = x_host.shape
+    E, _, d_ff = W1.shape
+    _check(_lib.moe_forward_host(_ptr(x_host), _ptr(logits_host), _ptr(W1), _ptr(W3), _ptr(W2),
+                                 T, d, E, k, d_ff, _ptr(out_host), _ptr(ws), _nbytes(ws),
+                                 int(flags), _events(stage_events), _stream(stream)),
+           "moe_forward_host")
 
 
 def moe_backward(dy, x, logits, W1, W3, W2, k, dx, dW1, dW3, dW2, dgate, dlogits, ws,

@@ -29,6 +29,12 @@ bool use_pairs() {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// moe_forward_host's staging at the end of the workspace: x, logits, out (256-byte aligned)
+size_t host_io_bytes(int64_t T, int d, int E) {
+  const size_t t = static_cast<size_t>(T);
+  return round_up(t * d * 2, 256) + round_up(t * E * 4, 256) + round_up(t * d * 2, 256);
+}
+
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -136,10 +142,12 @@ size_t moe_route_workspace_bytes(int64_t T, int E, int k) {
   return make_layout(T, 8, E, k, 128).route_total;
 }
 
-size_t moe_workspace_bytes(int64_t T, int d, int E, int k, int d_ff, int with_backward) {
+size_t moe_workspace_bytes(int64_t T, int d, int E, int k, int d_ff, int needs) {
   if (check_dims(T, d, E, k, d_ff, true) != MOE_OK) return 0;
+  if (needs & ~(MOE_WS_BACKWARD | MOE_WS_HOST_IO)) return 0;
   const WsLayout L = make_layout(T, d, E, k, d_ff);
-  return with_backward ? L.bwd_total : L.fwd_total;
+  return ((needs & MOE_WS_BACKWARD) ? L.bwd_total : L.fwd_total) +
+         ((needs & MOE_WS_HOST_IO) ? host_io_bytes(T, d, E) : 0);
 }
 
 moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_t T, int d,
@@ -272,6 +280,41 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,
                          stream));
   record(stage_events, 4, stream);
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host,
+                              const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                              int64_t T, int d, int E, int k, int d_ff, moe_bf16_t* out_host,
+                              void* ws, size_t ws_bytes, int flags, cudaEvent_t* stage_events,
+                              cudaStream_t stream) {
+  moe_status_t st = check_dims(T, d, E, k, d_ff, true);
+  if (st != MOE_OK) return st;
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x_host || !logits_host || !out_host)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_layout(T, d, E, k, d_ff);
+  const bool save = (flags & MOE_FWD_SAVE_FOR_BACKWARD) != 0;
+  const size_t io = host_io_bytes(T, d, E);
+  const size_t layer = save ? L.bwd_total : L.fwd_total;
+  if (ws_bytes < layer + io) return MOE_ERR_WORKSPACE;
+  // staging at the end of ws; the layer's own region stays [0, io0), as for moe_forward
+  const size_t io0 = (ws_bytes - io) & ~static_cast<size_t>(255);
+  char* w = static_cast<char*>(ws);
+  moe_bf16_t* x = reinterpret_cast<moe_bf16_t*>(w + io0);
+  float* logits = reinterpret_cast<float*>(w + io0 + round_up(static_cast<size_t>(T) * d * 2, 256));
+  moe_bf16_t* out = reinterpret_cast<moe_bf16_t*>(
+      w + io0 + round_up(static_cast<size_t>(T) * d * 2, 256) +
+      round_up(static_cast<size_t>(T) * E * 4, 256));
+  const size_t xb = static_cast<size_t>(T) * d * 2, lb = static_cast<size_t>(T) * E * 4;
+  if (T > 0) {
+    MOE_TRY(cudaMemcpyAsync(x, x_host, xb, cudaMemcpyHostToDevice, stream));
+    MOE_TRY(cudaMemcpyAsync(logits, logits_host, lb, cudaMemcpyHostToDevice, stream));
+  }
+  st = moe_forward(x, logits, W1, W3, W2, T, d, E, k, d_ff, out, ws, io0, flags, stage_events,
+                   stream);
+  if (st != MOE_OK) return st;
+  if (T > 0) MOE_TRY(cudaMemcpyAsync(out_host, out, xb, cudaMemcpyDeviceToHost, stream));
   return MOE_OK;
 }
 

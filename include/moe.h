@@ -87,10 +87,14 @@ typedef enum moe_status {
 /* Bytes of workspace needed by moe_route_dispatch for (T, E, k). */
 size_t moe_route_workspace_bytes(int64_t T, int E, int k);
 
-/* Bytes of workspace needed by moe_forward (and, with with_backward != 0, by
- * moe_forward(..., MOE_FWD_SAVE_FOR_BACKWARD) followed by moe_backward).  Returns 0 for
- * arguments outside the supported bounds. */
-size_t moe_workspace_bytes(int64_t T, int d, int E, int k, int d_ff, int with_backward);
+/* Workspace needs, the bits of moe_workspace_bytes's last argument. */
+#define MOE_WS_BACKWARD 1  /* moe_forward(..., MOE_FWD_SAVE_FOR_BACKWARD) + moe_backward */
+#define MOE_WS_HOST_IO 2   /* moe_forward_host: device copies of x, logits and out */
+
+/* Bytes of workspace needed by moe_forward, plus what the MOE_WS_* bits in `needs` add
+ * (needs = 1, the former with_backward flag, is MOE_WS_BACKWARD).  Returns 0 for arguments
+ * outside the supported bounds or an unknown bit. */
+size_t moe_workspace_bytes(int64_t T, int d, int E, int k, int d_ff, int needs);
 
 /*
  * Dispatch (routing, counting, prefix sum, stable permute).
@@ -115,14 +119,35 @@ moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_
  * Forward of the whole layer: out [T,d] bf16.
  *   out_t = bf16( sum_j gate[t,j] * (h_tj W2[e_j]) ),  h_tj = bf16(silu(x_t W1[e_j]) * (x_t W3[e_j]))
  * with every matrix product accumulated in fp32 and the slot sum in fp32, in slot order.
- * ws must hold moe_workspace_bytes(T, d, E, k, d_ff, flags & MOE_FWD_SAVE_FOR_BACKWARD)
- * bytes; with MOE_FWD_SAVE_FOR_BACKWARD it keeps what moe_backward needs.  stage_events:
+ * ws must hold moe_workspace_bytes(T, d, E, k, d_ff, MOE_WS_BACKWARD if
+ * MOE_FWD_SAVE_FOR_BACKWARD else 0) bytes; with MOE_FWD_SAVE_FOR_BACKWARD it keeps what
+ * moe_backward needs.  stage_events:
  * NULL or MOE_FWD_NUM_EVENTS events (see above).
  */
 moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf16_t* W1,
                          const moe_bf16_t* W3, const moe_bf16_t* W2, int64_t T, int d, int E,
                          int k, int d_ff, moe_bf16_t* out, void* ws, size_t ws_bytes, int flags,
                          cudaEvent_t* stage_events, cudaStream_t stream);
+
+/*
+ * moe_forward with the batch in HOST memory: x_host [T,d] bf16 and logits_host [T,E] fp32
+ * are copied into the end of the workspace, the layer runs on those copies, and out is copied
+ * back to out_host [T,d] bf16.  The copies are asynchronous on `stream` (cudaMemcpyAsync);
+ * with page-locked host buffers they overlap work on other streams, so a caller can run
+ * batches on two streams with two workspaces and hide the copies behind the other batch's
+ * layer.  The host buffers are read / written when the stream reaches the copies: keep x_host
+ * and logits_host unchanged, and do not read out_host, until the stream has passed the call.
+ * W1, W3, W2 and ws are device memory as for moe_forward.  ws must hold
+ * moe_workspace_bytes(T, d, E, k, d_ff, MOE_WS_HOST_IO) bytes (| MOE_WS_BACKWARD with
+ * MOE_FWD_SAVE_FOR_BACKWARD; moe_backward then takes the same ws and ws_bytes and device
+ * x, logits, dy).  flags and stage_events as moe_forward: the events bracket the layer, after
+ * the input copies and before the output copy.
+ */
+moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host,
+                              const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                              int64_t T, int d, int E, int k, int d_ff, moe_bf16_t* out_host,
+                              void* ws, size_t ws_bytes, int flags, cudaEvent_t* stage_events,
+                              cudaStream_t stream);
 
 /*
  * Backward of the layer for upstream gradient dy [T,d] bf16.  Precondition: ws holds the

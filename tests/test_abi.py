@@ -45,6 +45,11 @@ def test_workspace_sizes(lib):
     assert lib.moe_workspace_bytes(64, 128, 8, 9, 256, False) == 0      # k > E
     assert lib.moe_workspace_bytes(64, 128, 2048, 2, 256, False) == 0   # E > 1024
     assert lib.moe_route_workspace_bytes(1000, 64, 6) > 0
+    # host staging: x, logits, out copies at the end of the workspace
+    hio = lib.moe_workspace_bytes(64, 128, 8, 2, 256, False, host_io=True)
+    assert hio == small + 64 * 128 * 2 + 64 * 8 * 4 + 64 * 128 * 2  # each a multiple of 256
+    assert lib.moe_workspace_bytes(64, 128, 8, 2, 256, True, host_io=True) == big + hio - small
+    assert lib.library().moe_workspace_bytes(64, 128, 8, 2, 256, 4) == 0  # unknown need bit
 
 
 def test_host_validation_rejects_before_launch(lib):
@@ -71,3 +76,25 @@ def test_host_validation_rejects_before_launch(lib):
     st = raw.moe_backward(*([fake] * 6), 64, 128, 8, 2, 256, *([fake] * 6), fake, 16, None, None)
     assert st == lib.MOE_ERR_WORKSPACE
     assert lib.moe_status_string(lib.MOE_ERR_TIMEOUT) == "device-side wait timed out"
+
+
+def test_forward_host_validation(lib):
+    raw = lib.library()
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    w = [fake] * 3
+    need = lib.moe_workspace_bytes(64, 128, 8, 2, 256, False, host_io=True)
+    # null host buffers with T > 0
+    st = raw.moe_forward_host(None, fake, *w, 64, 128, 8, 2, 256, fake, fake, need, 0, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG
+    st = raw.moe_forward_host(fake, fake, *w, 64, 128, 8, 2, 256, None, fake, need, 0, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG
+    # a workspace sized without the host staging, or without the backward state when saving
+    small = lib.moe_workspace_bytes(64, 128, 8, 2, 256, False)
+    st = raw.moe_forward_host(fake, fake, *w, 64, 128, 8, 2, 256, fake, fake, small, 0, None, None)
+    assert st == lib.MOE_ERR_WORKSPACE
+    st = raw.moe_forward_host(fake, fake, *w, 64, 128, 8, 2, 256, fake, fake, need,
+                              lib.MOE_FWD_SAVE_FOR_BACKWARD, None, None)
+    assert st == lib.MOE_ERR_WORKSPACE
+    # shape checks as moe_forward
+    st = raw.moe_forward_host(fake, fake, *w, 64, 100, 8, 2, 256, fake, fake, need, 0, None, None)
+    assert st == lib.MOE_ERR_UNSUPPORTED

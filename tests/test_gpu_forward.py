@@ -6,7 +6,7 @@ import torch
 
 import moe_synth
 import oracle
-from moe_harness import assert_close, forward, np_of, sample_tokens, to_dev
+from moe_harness import assert_close, backward, forward, np_of, sample_tokens, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -132,6 +132,41 @@ def test_row_gather_equals_permuted_copy(moe, T, d, E, k, dff, flags):
                     flags=moe.MOE_FWD_GATHER_ROWS | flags)
     assert moe.moe_get_error(ws) == 0
     assert torch.equal(got.view(torch.int16), sep.view(torch.int16))
+
+
+@pytest.mark.parametrize("T,pinned,save", [
+    (300, True, False),
+    (300, False, False),   # pageable host buffers
+    (1, True, False),
+    (0, True, False),
+    (200, True, True),     # saving for backward: moe_backward then runs on the same ws
+])
+def test_forward_host_equals_device(moe, T, pinned, save):
+    d, E, k, dff = 256, 16, 4, 384
+    w = moe_synth.custom(max(T, 1), d, E, k, dff, seed=77)
+    inp = moe_synth.generate(w, with_dy=True)
+    inp = moe_synth.rows(inp, T)
+    g = to_dev(inp)
+    ref, ws_ref = forward(moe, g, k, save=save)
+    ws = torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, save, host_io=True),
+                     dtype=torch.uint8, device="cuda")
+    hx = inp["x"].clone().pin_memory() if pinned else inp["x"].clone()
+    hl = inp["logits"].clone().pin_memory() if pinned else inp["logits"].clone()
+    ho = torch.empty(T, d, dtype=torch.bfloat16)
+    ho = ho.pin_memory() if pinned else ho
+    ho.fill_(7.0)
+    moe.moe_forward_host(hx, hl, g["W1"], g["W3"], g["W2"], k, ho, ws,
+                         flags=moe.MOE_FWD_SAVE_FOR_BACKWARD if save else 0)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(ws) == 0
+    assert torch.equal(ho.view(torch.int16), ref.cpu().view(torch.int16))
+    if save:
+        r_dev = backward(moe, g, k, ws_ref)
+        r_host = backward(moe, g, k, ws)
+        for name, v in r_dev.items():
+            a = v.view(torch.int16) if v.dtype == torch.bfloat16 else v.view(torch.int32)
+            b = r_host[name].view(torch.int16) if v.dtype == torch.bfloat16 else r_host[name].view(torch.int32)
+            assert torch.equal(a, b), name
 
 
 def _device_workload(name):
