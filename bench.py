@@ -172,10 +172,13 @@ def bwd_launches():
     return 10 if _pair() else 8
 
 
-def bench_fwd_bwd(moe, dev, steps, warmup):
+def bench_fwd_bwd(moe, dev, steps, warmup, shape=None):
     """Forward (saving for backward) + backward of the fwd_bwd workload (T=8192, d=4096,
-    E=128, top-8, d_ff=1536), device-resident, with the backward's stage times."""
+    E=128, top-8, d_ff=1536; or `shape` = (T, d, E, k, d_ff)), device-resident, with the
+    backward's stage times."""
     w = moe_synth.by_name("fwd_bwd")
+    if shape:
+        w = moe_synth.custom(*shape, seed=w.seed, name="fwd_bwd_custom")
     g = moe_synth.generate(w, device=dev, with_dy=True)
     T, d, E, k, dff = w.T, w.d, w.E, w.k, w.dff
     ws = torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, True), dtype=torch.uint8,
@@ -452,7 +455,9 @@ def bench_native(args, w):
     if not args.no_backward:
         del ws
         torch.cuda.empty_cache()
-        line["fwd_bwd"] = bench_fwd_bwd(moe, dev, max(1, min(args.steps, 10)), args.warmup)
+        bshape = tuple(int(v) for v in args.bwd_shape.split(",")) if args.bwd_shape else None
+        line["fwd_bwd"] = bench_fwd_bwd(moe, dev, max(1, min(args.steps, 10)), args.warmup,
+                                        bshape)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del out
         torch.cuda.empty_cache()
@@ -476,6 +481,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count T (e.g. the small-batch sweep)")
+    ap.add_argument("--bwd-shape", default=None,
+                    help="T,d,E,k,d_ff of the forward + backward timing (profiling captures)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the forward + backward timing of the fwd_bwd workload")
     args = ap.parse_args()

@@ -393,39 +393,59 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       }
     }
   } else if constexpr (KIND == kDh) {
-    const int64_t row = ti.row0 + r;
+    // The warp puts its 32 x 32 chunk of dH through the padded shared buffer, then works row
+    // by row: 8 lanes per row read the row's saved A and B (16 bytes each, whole 128-byte
+    // lines), apply the SwiGLU backward and store dA and dB (8 bytes each).
     const int64_t row0 = ti.row0 + w0;
-    char* dA = reinterpret_cast<char*>(static_cast<uint16_t*>(p.out0) + row0 * (2 * p.dff) + ti.n0);
-    char* dB = dA + 2ll * p.dff;
-    const float* sa = p.save_a + row * p.dff + ti.n0;
-    const float* sb = p.save_b + row * p.dff + ti.n0;
+    uint16_t* dA0 = static_cast<uint16_t*>(p.out0) + row0 * (2 * p.dff) + ti.n0;
+    const float* sa0 = p.save_a + row0 * p.dff + ti.n0;
+    const float* sb0 = p.save_b + row0 * p.dff + ti.n0;
     const int nstore = clamp_rows(ti.nseg);      // pad rows are written as zeros
+    const int nval = clamp_rows(ti.nvalid);
+    const int rsub = lane >> 3, c4 = (lane & 7) * 4;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 32; ++ch) {
-      float dh[32], da[32], db[32];
-      tmem_ld32(tacc + ch * 32, dh);
-      if (valid) {
+      // all 16 loads of the chunk in flight first; the accumulator read and the shared
+      // transpose run under their latency
+      uint4 ua[8], ub[8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float a[16], b[16];
-          ld_f32x16(sa + ch * 32 + 16 * h, a);
-          ld_f32x16(sb + ch * 32 + 16 * h, b);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float sg = 1.0f / (1.0f + expf(-a[i]));
-            da[16 * h + i] = dh[16 * h + i] * b[i] * (sg * (1.0f + a[i] * (1.0f - sg)));
-            db[16 * h + i] = dh[16 * h + i] * (a[i] * sg);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          da[i] = 0.0f;
-          db[i] = 0.0f;
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + rsub;
+        if (rr < nval) {
+          ua[i] = ld_v4(sa0 + rr * p.dff + ch * 32 + c4);
+          ub[i] = ld_v4(sb0 + rr * p.dff + ch * 32 + c4);
         }
       }
-      store_chunk<true>(buf, da, dA + ch * 64, 4ll * p.dff, nstore, lane);
-      store_chunk<true>(buf, db, dB + ch * 64, 4ll * p.dff, nstore, lane);
+      float dh[32];
+      tmem_ld32(tacc + ch * 32, dh);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) buf[lane * 33 + c] = dh[c];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + rsub;
+        if (rr < nstore) {
+          float da[4] = {0.0f, 0.0f, 0.0f, 0.0f}, db[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if (rr < nval) {
+            const float av[4] = {__uint_as_float(ua[i].x), __uint_as_float(ua[i].y),
+                                 __uint_as_float(ua[i].z), __uint_as_float(ua[i].w)};
+            const float bv[4] = {__uint_as_float(ub[i].x), __uint_as_float(ub[i].y),
+                                 __uint_as_float(ub[i].z), __uint_as_float(ub[i].w)};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float g = buf[rr * 33 + c4 + q];
+              const float sg = 1.0f / (1.0f + expf(-av[q]));
+              da[q] = g * bv[q] * (sg * (1.0f + av[q] * (1.0f - sg)));
+              db[q] = g * (av[q] * sg);
+            }
+          }
+          uint16_t* o = dA0 + rr * (2 * p.dff) + ch * 32 + c4;
+          *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(da[0], da[1]), pack_bf16x2(da[2], da[3]));
+          *reinterpret_cast<uint2*>(o + p.dff) =
+              make_uint2(pack_bf16x2(db[0], db[1]), pack_bf16x2(db[2], db[3]));
+        }
+      }
+      __syncwarp();
     }
   } else {
     // K-over-rows kinds: output rows m0 + w0 .. of expert e's weight gradient.
