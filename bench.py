@@ -156,6 +156,16 @@ def _traffic_of(kernel):
         return None
 
 
+def max_over_ranks(value, device):
+    """The largest `value` over all ranks (the slowest rank's time); `value` itself with one
+    process."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _pair():
     return os.environ.get("MOE_GEMM_PAIR", "1") != "0"
 
@@ -320,11 +330,7 @@ def bench_native(args, w):
             step(evs[i])
         stop.record(stream)
         barrier()
-    ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(stop), dev)
     st = moe.moe_get_error(ws)
     if st != 0:
         raise RuntimeError("device error: " + moe.moe_status_string(st))
@@ -370,11 +376,7 @@ def bench_native(args, w):
         stream.wait_event(e_)
     stop.record(stream)
     barrier()
-    ms_e2e = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(start.elapsed_time(stop), dev)
     for wsi in ws_io:
         st = moe.moe_get_error(wsi)
         if st != 0:
