@@ -90,6 +90,10 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kEpiThreads = 128;
+// L2 eviction priority of the operand loads of the row-grouped forward GEMMs: 0 = default,
+// 1 = evict_last, 2 = evict_first.  A = permuted rows, B = expert weights.
+constexpr int kL2HintA = 0;
+constexpr int kL2HintB = 1;
 
 
 template <int BN, bool PAIR = false>
@@ -599,6 +603,17 @@ __global__ void __launch_bounds__(256, 1)
       if constexpr (PAIR) tma_load_2d_pair(dst, m, mapa_shared(fb, 0), x, y);
       else tma_load_2d(dst, m, fb, x, y);
     };
+    const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
+    // forward operand loads with the eviction priority of kL2HintA / kL2HintB
+    auto load_h = [&](int hint, uint32_t dst, const CUtensorMap* m, uint32_t fb, int x, int y) {
+      if (hint == 0) {
+        load(dst, m, fb, x, y);
+      } else {
+        const uint64_t pol = hint == 1 ? pol_last : pol_first;
+        if constexpr (PAIR) tma_load_2d_pair_hint(dst, m, mapa_shared(fb, 0), x, y, pol);
+        else tma_load_2d_hint(dst, m, fb, x, y, pol);
+      }
+    };
     for (int tile = unit; tile < ntiles; tile += nunits) {
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
@@ -625,26 +640,27 @@ __global__ void __launch_bounds__(256, 1)
         if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * Cfg::kStageBytes : Cfg::kStageBytes);
         const int k0 = kb * kBK;
         if constexpr (KIND == kFwd1) {
-          if (!p.gather_x) load(sa, &mapA, fb, k0, ti.row0);
+          if (!p.gather_x) load_h(kL2HintA, sa, &mapA, fb, k0, ti.row0);
           const int wrow = ti.e * p.d + k0;
           const int h0 = ti.n0 / 2;  // first h column of the tile
           if constexpr (PAIR) {
             // rank 0 holds the W1 half of B, rank 1 the W3 half
             const CUtensorMap* wm = rank == 0 ? &mapB0 : &mapB1;
 #pragma unroll
-            for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, wm, fb, h0 + 64 * i, wrow);
+            for (int i = 0; i < BL / 64; ++i)
+              load_h(kL2HintB, sb + 8192u * i, wm, fb, h0 + 64 * i, wrow);
           } else {
 #pragma unroll
             for (int i = 0; i < BN / 128; ++i) {
-              load(sb + 8192u * i, &mapB0, fb, h0 + 64 * i, wrow);
-              load(sb + 8192u * (BN / 128 + i), &mapB1, fb, h0 + 64 * i, wrow);
+              load_h(kL2HintB, sb + 8192u * i, &mapB0, fb, h0 + 64 * i, wrow);
+              load_h(kL2HintB, sb + 8192u * (BN / 128 + i), &mapB1, fb, h0 + 64 * i, wrow);
             }
           }
         } else if constexpr (KIND == kFwd2) {
-          load(sa, &mapA, fb, k0, ti.row0);
+          load_h(kL2HintA, sa, &mapA, fb, k0, ti.row0);
 #pragma unroll
           for (int i = 0; i < BL / 64; ++i)
-            load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, ti.e * p.dff + k0);
+            load_h(kL2HintB, sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, ti.e * p.dff + k0);
         } else if constexpr (KIND == kDh) {
           load(sa, &mapA, fb, k0, ti.row0);
           load(sb, &mapB0, fb, k0, ti.e * p.dff + nb0);
