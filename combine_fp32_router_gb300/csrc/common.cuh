@@ -343,26 +343,6 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster), "l"(pol)
       : "memory");
 }
-// Four 128-byte rows (box of 64 bf16 x 1 row) of a 2-D tensor, rows r0..r3 at column x, into
-// consecutive 128-byte rows of shared memory starting at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* map, uint32_t bar, int x, int r0,
-                                            int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-// Same, completing on a barrier that may live in the peer CTA of the pair.
-__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const void* map, uint32_t bar_cluster,
-                                                 int x, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(bar_cluster)
-      : "memory");
-}
 // TMA tile store from this CTA's shared memory (bulk async-group of the issuing thread).
 __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -381,9 +361,21 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
-// generic-proxy writes to shared memory become visible to the async proxy (TMA)
+// generic-proxy writes to shared memory become visible to the async proxy (TMA, tcgen05)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 16-byte asynchronous copy global -> shared (L2 only), and an arrival on a shared
+// mbarrier when all of this thread's earlier cp.async copies have landed; the arrival is not
+// counted in advance (.noinc): the barrier's expected count includes it.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");

@@ -76,8 +76,9 @@ struct GemmParams {
   int M;                     // M extent of the K-over-rows kinds (d or d_ff)
   // GEMM2 with the combine fused in (see combine_segment)
   int fuse_combine;
-  // GEMM1 reading its A rows straight from x (rows gathered by token, TMA tile::gather4)
+  // GEMM1 reading its A rows straight from x (rows gathered by token with cp.async)
   int gather_x;
+  const uint16_t* gather_src;  // x [T, d] bf16
   const int32_t* perm;       // permuted row -> pair t*k + j
   const int32_t* pos;        // pair -> permuted row
   const float* gate;         // [T, k]
@@ -104,14 +105,14 @@ struct GemmCfg {
   static constexpr uint32_t kBBytes = kBLocal * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
-  static constexpr int kBars = 2 * kStages + 5;  // full, empty, tfull x2, tempty x2, drain
+  // full, empty, tfull x2, tempty x2, drain, gathered-rows landed
+  static constexpr int kBars = 3 * kStages + 5;
   // one 1024-aligned 5 KB region per epilogue warp: a 32 x 33 fp32 transpose buffer, or the
   // 32 x 32 fp32 staging box of a TMA store
   static constexpr size_t kEpiWarpBytes = 5120;
   static constexpr size_t kEpiBytes = 4 * kEpiWarpBytes;
-  static constexpr size_t kGatherBytes = kBM * 4;  // token index of each A row of a tile
   static constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 1024 +
-                                       kEpiBytes + 8 * kBars + 64 + kGatherBytes;
+                                       kEpiBytes + 8 * kBars + 64;
   static_assert(kStageBytes % 1024 == 0, "stages keep the epilogue regions 1024-aligned");
 };
 
@@ -528,25 +529,32 @@ __global__ void __launch_bounds__(256, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  auto gather_bar = [&](int s) { return bar0 + 8u * (2 * S + 5 + s); };
   uint8_t* misc = gbase + S * Cfg::kStageBytes + Cfg::kEpiBytes + 8 * Cfg::kBars;
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(misc + 8);
   volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(misc + 12);
   float* epi_buf = reinterpret_cast<float*>(gbase + S * Cfg::kStageBytes);
-  int32_t* gather_ids = reinterpret_cast<int32_t*>(misc + 64);
   auto stage_a = [&](int s) { return base + s * Cfg::kStageBytes; };
   auto stage_b = [&](int s) { return base + s * Cfg::kStageBytes + kABytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool gather = KIND == kFwd1 && p.gather_x != 0;
   const int unit = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int nunits = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
+    // A full barrier completes on its arming arrival (with the TMA bytes).  With gathered A
+    // rows, each CTA's 32 producer lanes' cp.async arrivals complete its gather barrier, and
+    // the CTA's gather-fence thread then adds one arrival on the full barrier (rank 0's, with
+    // PAIR).
+    const int full_count = !gather ? 1 : (PAIR ? 3 : 2);
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), full_count);
       mbar_init(empty_bar(s), 1);
+      mbar_init(gather_bar(s), 64);  // the lanes of the two gathering warps
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -585,7 +593,7 @@ __global__ void __launch_bounds__(256, 1)
   uint32_t issued = 0;
   int skipped = -1;
 
-  if (warp == 0) {
+  if (warp == 0 || (gather && warp == 2)) {
     // ------------------------------------------------------------------ TMA producer
     // Lane 0 waits for each stage and issues the tile loads.  With gather_x the warp first
     // stages the token index of each of the tile's A rows (padding rows read token 0; they are
@@ -622,22 +630,25 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) set_error(p.err, MOE_ERR_DEVICE_BOUNDS, 11);
         continue;
       }
-      if constexpr (KIND == kFwd1) {
-        if (p.gather_x) {
+      // gathered A rows: warp 0 copies rows [0, 64) of the CTA's 128, warp 2 rows [64, 128);
+      // lane l takes chunk l & 7 of rows r0 + 4 i + (l >> 3).  Source rows in x (padding
+      // rows read token 0; they are never stored):
+      const uint16_t* src_row[kBM / 8];
+      if (gather) {
+        const int r0 = warp == 0 ? 0 : kBM / 2;
 #pragma unroll
-          for (int i = 0; i < kBM / 32; ++i) {
-            const int rr = i * 32 + lane;
-            const int pr = rr < ti.nvalid ? p.perm[ti.row0 + rr] : -1;
-            gather_ids[rr] = pr >= 0 ? pr / p.k : 0;
-          }
-          __syncwarp();
+        for (int i = 0; i < kBM / 8; ++i) {
+          const int rr = r0 + 4 * i + (lane >> 3);
+          const int pr = rr < ti.nvalid ? p.perm[ti.row0 + rr] : -1;
+          src_row[i] = p.gather_src + static_cast<int64_t>(pr >= 0 ? pr / p.k : 0) * p.d;
         }
       }
       const int nb0 = ti.n0 + rank * BL;  // first B column held by this CTA
       // lane 0: arm stage (fb) and issue the tile loads of K block kb (A too unless gathered)
       auto issue_stage = [&](int kb, uint32_t fb, uint32_t sa, uint32_t sb) {
         // rank 0 arms its barrier for both CTAs' bytes; rank 1 only loads
-        if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * Cfg::kStageBytes : Cfg::kStageBytes);
+        const uint32_t tx = gather ? Cfg::kBBytes : Cfg::kStageBytes;
+        if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * tx : tx);
         const int k0 = kb * kBK;
         if constexpr (KIND == kFwd1) {
           if (!p.gather_x) load_h(kL2HintA, sa, &mapA, fb, k0, ti.row0);
@@ -677,8 +688,12 @@ __global__ void __launch_bounds__(256, 1)
         }
       };
       const bool skip_hook = (p.debug_flags & 1) && blockIdx.x == 0;
-      if (KIND == kFwd1 && p.gather_x) {
-        // The warp walks the K blocks together: every lane gathers 4 of the 128 A rows.
+      if (gather) {
+        // Warps 0 and 2 walk the K blocks together, each copying 64 of the stage's 128 A rows
+        // with cp.async: each instruction moves 4 whole 128-byte row pieces (8 lanes per row, one
+        // 16-byte chunk each), placed in the 128-byte-swizzled layout the MMA reads (chunk c
+        // of row r at chunk c ^ (r & 7)); every lane arrives on the CTA's gather barrier when
+        // its copies have landed.
         for (int kb = 0; kb < ti.nk; ++kb) {
           const int s = fill % S;
           const uint32_t ph = (fill / S) & 1u;
@@ -692,13 +707,17 @@ __global__ void __launch_bounds__(256, 1)
           if (skip_hook && fill == 0) {
             skipped = 0;  // test hook: this stage is never armed nor filled by this CTA
           } else {
-            const int* g4 = gather_ids + 4 * lane;  // rows 4 lane .. 4 lane + 3
-            if constexpr (PAIR)
-              tma_gather4_pair(sa + 512u * lane, &mapA, mapa_shared(fb, 0), kb * kBK, g4[0],
-                               g4[1], g4[2], g4[3]);
-            else
-              tma_gather4(sa + 512u * lane, &mapA, fb, kb * kBK, g4[0], g4[1], g4[2], g4[3]);
-            if (lane == 0) issue_stage(kb, fb, sa, sb);
+            const int c = lane & 7;
+            const int r0 = warp == 0 ? 0 : kBM / 2;
+#pragma unroll
+            for (int i = 0; i < kBM / 8; ++i) {
+              const int rr = r0 + 4 * i + (lane >> 3);
+              cp_async_16(sa + static_cast<uint32_t>(rr) * 128u +
+                              static_cast<uint32_t>((c ^ (rr & 7)) * 16),
+                          src_row[i] + kb * kBK + 8 * c);
+            }
+            cp_async_arrive_noinc(gather_bar(s));
+            if (warp == 0 && lane == 0) issue_stage(kb, fb, sa, sb);
           }
           ++fill;
         }
@@ -715,8 +734,9 @@ __global__ void __launch_bounds__(256, 1)
           ++fill;
         }
       }
-      __syncwarp();  // gather_ids may be rewritten only after the tile's gathers are issued
+      __syncwarp();
     }
+    if (gather) cp_async_wait_all();  // no copy in flight into shared memory at exit
     issued = fill;
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------------------ MMA issuer
@@ -763,6 +783,30 @@ __global__ void __launch_bounds__(256, 1)
     if constexpr (PAIR) umma_commit_pair(drain_bar, 1);
     else umma_commit(drain_bar);
     mbar_wait(drain_bar, 0u, nullptr, p.err, 4, p.wait_ns);
+  } else if (gather && warp == 3 && lane == 0) {
+    // ------------------------------------------------------------------ gather fence
+    // cp.async writes shared memory through the generic proxy and the MMAs read it through
+    // the async proxy.  Once a stage's gathered rows have landed in this CTA (its gather
+    // barrier), this thread fences the proxies and passes one arrival on to the full
+    // barrier the MMA issuer waits on (rank 0's with PAIR), so the issuer itself never
+    // fences.
+    uint32_t fill = 0;
+    bool ok = true;
+    for (int tile = unit; tile < ntiles && ok; tile += nunits) {
+      const TileInfo ti = decode_tile<KIND, BN, PAIR>(p, tile, rank);
+      if (ti.bad) continue;
+      for (int kb = 0; kb < ti.nk; ++kb) {
+        const int s = fill % S;
+        if (!mbar_wait(gather_bar(s), (fill / S) & 1u, abort_flag, p.err, 8, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        fence_proxy_async_smem();
+        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(full_bar(s), 0));
+        else mbar_arrive(full_bar(s));
+        ++fill;
+      }
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp - 4;

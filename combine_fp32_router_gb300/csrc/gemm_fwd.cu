@@ -104,10 +104,9 @@ GemmParams leftover_params(const GemmParams& p, const GemmCtx& c) {
 cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
   const WsLayout& L = *c.L;
   cudaError_t st = cudaSuccess;
-  // A rows: gathered from x by token (one-row boxes for tile::gather4), or the permuted copy
-  const CUtensorMap a = c.gather_x
-                            ? make_map_2d(c.x, L.d, static_cast<uint64_t>(L.T), 2ull * L.d, 64, 1, &st)
-                            : make_map_2d(c.ws + L.xperm, L.d, L.P_pad, 2ull * L.d, 64, 128, &st);
+  // A rows: the permuted copy (with gather_x the kernel copies the rows from x itself and
+  // this map is not read)
+  const CUtensorMap a = make_map_2d(c.ws + L.xperm, L.d, L.P_pad, 2ull * L.d, 64, 128, &st);
   const CUtensorMap b0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 64, &st);
   const CUtensorMap b1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 64, &st);
   if (st != cudaSuccess) return st;
@@ -119,6 +118,7 @@ cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
   p.save_a = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Asave) : nullptr;
   p.save_b = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Bsave) : nullptr;
   p.gather_x = c.gather_x ? 1 : 0;
+  p.gather_src = c.x;
   p.perm = reinterpret_cast<const int32_t*>(c.ws + L.perm);
   p.k = L.k;
   return run_rows_kind<kFwd1, 256>(c.pair, a, b0, b1, b0, b1, p, leftover_params(p, c), L.max_mt,
