@@ -69,10 +69,11 @@ typedef enum moe_status {
                                        written (the single-GPU form of the overlapped combine of
                                        waves); bitwise the same output as the default separate
                                        combine kernel, which is faster on GB300 */
-#define MOE_FWD_GATHER_ROWS 4       /* GEMM1 gathers its rows from x by token (TMA gather4) instead
-                                       of reading a permuted copy (the overlapped dispatch of
-                                       waves); bitwise the same output; slower on GB300; ignored
-                                       with MOE_FWD_SAVE_FOR_BACKWARD (the backward needs the copy) */
+#define MOE_FWD_GATHER_ROWS 4       /* GEMM1 copies its rows from x by token (cp.async into the
+                                       operand stages) instead of reading a permuted copy (the
+                                       overlapped dispatch of waves); bitwise the same output;
+                                       slower on GB300; ignored with MOE_FWD_SAVE_FOR_BACKWARD
+                                       (the backward needs the copy) */
 
 /* Stage events: moe_forward records MOE_FWD_NUM_EVENTS events and moe_backward
  * MOE_BWD_NUM_EVENTS events on `stream` at its stage boundaries when `stage_events` is not

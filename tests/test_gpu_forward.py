@@ -119,7 +119,7 @@ def test_fused_combine_equals_separate_stages(moe, T, d, E, k, dff):
     (4096, 2048, 64, 6, 1024, 2),     # gather + fused combine: the overlapped waves together
 ])
 def test_row_gather_equals_permuted_copy(moe, T, d, E, k, dff, flags):
-    # GEMM1 gathering its rows from x (TMA gather4) gives bitwise the same output as GEMM1
+    # GEMM1 gathering its rows from x (cp.async) gives bitwise the same output as GEMM1
     # reading the dispatch's permuted copy
     w = moe_synth.custom(T, d, E, k, dff, seed=T + 17)
     inp = moe_synth.generate(w)
