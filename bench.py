@@ -170,10 +170,11 @@ def _pair():
     return os.environ.get("MOE_GEMM_PAIR", "1") != "0"
 
 
-def fwd_launches():
+def fwd_launches(T=None):
     # routing, column scan, offsets/tile tables, scatter, padding rows, GEMM1, GEMM2, combine;
-    # with CTA pairs each GEMM is a pair launch plus a single-CTA launch for leftover tiles
-    return 10 if _pair() else 8
+    # with CTA pairs (used when T > 128) each GEMM is a pair launch plus a single-CTA launch
+    # for leftover tiles
+    return 10 if _pair() and (T is None or T > 128) else 8
 
 
 def bwd_launches():
@@ -452,7 +453,7 @@ def bench_native(args, w):
         "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
         "waved_forward_ms_per_step": waved_ms,
         "clocks": clocks.summary(),
-        "gpu_launches": fwd_launches() * args.steps,
+        "gpu_launches": fwd_launches(T) * args.steps,
     }
     if not args.no_backward:
         del ws

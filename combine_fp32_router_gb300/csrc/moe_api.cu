@@ -260,7 +260,9 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.wait_ns = g_wait_ns.load();
   c.debug_flags = g_debug_flags.load();
   c.num_sms = num_sms_of_current_device();
-  c.pair = use_pairs();
+  // an expert has at most T rows, so with T <= 128 no expert fills a 256-row pair tile: one
+  // single-CTA launch per GEMM then covers every tile
+  c.pair = use_pairs() && T > kTileRows;
   c.fuse_combine = (flags & MOE_FWD_FUSED_COMBINE) != 0;
   c.gather_x = gather;
   c.out = out;
