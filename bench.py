@@ -387,6 +387,24 @@ def bench_native(args, w):
         raise RuntimeError("host-buffer forward differs from the device forward")
     del ws_io
 
+    # the same step replayed from a captured CUDA graph (the launch-overhead path)
+    graph = moe.moe_forward_graph_create(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out,
+                                         ws)
+    for _ in range(2):
+        graph.launch(stream)
+    barrier()
+    n_graph = max(1, min(args.steps, 20))
+    start.record(stream)
+    for _ in range(n_graph):
+        graph.launch(stream)
+    stop.record(stream)
+    barrier()
+    graph_ms = start.elapsed_time(stop) / n_graph
+    graph.close()
+    st = moe.moe_get_error(ws)
+    if st != 0:
+        raise RuntimeError("device error (graph replay): " + moe.moe_status_string(st))
+
     # the overlapped-wave variant (GEMM1 gathers rows from x, GEMM2 fuses the combine),
     # timed for comparison; bitwise the same output
     wave_flags = moe.MOE_FWD_GATHER_ROWS | moe.MOE_FWD_FUSED_COMBINE
@@ -452,6 +470,7 @@ def bench_native(args, w):
         "dispatch_gbs": disp_gbs, "dispatch_frac_of_hbm": disp_gbs / peaks["hbm"],
         "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
         "waved_forward_ms_per_step": waved_ms,
+        "graph_forward_ms_per_step": graph_ms,
         "clocks": clocks.summary(),
         "gpu_launches": fwd_launches(T) * args.steps,
     }

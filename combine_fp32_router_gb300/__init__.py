@@ -33,9 +33,10 @@ MOE_BWD_NUM_EVENTS = 7
 
 # Exported symbols of include/moe.h, in declaration order.
 EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispatch",
-           "moe_forward", "moe_forward_host", "moe_backward", "moe_route_dispatch_noalloc",
-           "moe_get_error", "moe_set_wait_timeout_ns", "moe_debug_set_flags",
-           "moe_status_string")
+           "moe_forward", "moe_forward_graph_create", "moe_forward_graph_launch",
+           "moe_forward_graph_destroy", "moe_forward_host", "moe_backward",
+           "moe_route_dispatch_noalloc", "moe_get_error", "moe_set_wait_timeout_ns",
+           "moe_debug_set_flags", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -57,6 +58,13 @@ def _load():
     lib.moe_route_dispatch.argtypes = [p, p, i64, i, i, i] + [p] * 7 + [p, sz, p]
     lib.moe_route_dispatch.restype = i
     lib.moe_forward.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i, p, p]
+    lib.moe_forward_graph_create.restype = i
+    lib.moe_forward_graph_create.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i,
+                                                       ctypes.POINTER(ctypes.c_void_p)]
+    lib.moe_forward_graph_launch.restype = i
+    lib.moe_forward_graph_launch.argtypes = [p, p]
+    lib.moe_forward_graph_destroy.restype = None
+    lib.moe_forward_graph_destroy.argtypes = [p]
     lib.moe_forward_host.restype = i
     lib.moe_forward_host.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i, p, p]
     lib.moe_forward.restype = i
@@ -142,6 +150,44 @@ def moe_forward(x, logits, W1, W3, W2, k, out, ws, flags=0, stage_events=None, s
     _check(_lib.moe_forward(_ptr(x), _ptr(logits), _ptr(W1), _ptr(W3), _ptr(W2), T, d, E, k,
                             d_ff, _ptr(out), _ptr(ws), _nbytes(ws), int(flags),
                             _events(stage_events), _stream(stream)), "moe_forward")
+
+
+class ForwardGraph:
+    """A moe_forward captured once (moe_forward_graph_create) and replayed with launch().  The
+    tensors given at creation are baked in: replays read x and logits as they are then and
+    write the same out.  close() (or garbage collection) releases the graph."""
+
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep  # the captured tensors must outlive the graph
+
+    def launch(self, stream=None):
+        if not self._h:
+            raise ValueError("graph already closed")
+        _check(_lib.moe_forward_graph_launch(self._h, _stream(stream)), "moe_forward_graph_launch")
+
+    def close(self):
+        if self._h:
+            _lib.moe_forward_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def moe_forward_graph_create(x, logits, W1, W3, W2, k, out, ws, flags=0):
+    """Capture moe_forward with these tensors into a replayable graph (ForwardGraph)."""
+    T, d = x.shape
+    E, _, d_ff = W1.shape
+    h = ctypes.c_void_p()
+    _check(_lib.moe_forward_graph_create(_ptr(x), _ptr(logits), _ptr(W1), _ptr(W3), _ptr(W2),
+                                         T, d, E, k, d_ff, _ptr(out), _ptr(ws), _nbytes(ws),
+                                         int(flags), ctypes.byref(h)),
+           "moe_forward_graph_create")
+    return ForwardGraph(h, (x, logits, W1, W3, W2, out, ws))
 
 
 def moe_forward_host(x_host, logits_host, W1, W3, W2, k, out_host, ws, flags=0,

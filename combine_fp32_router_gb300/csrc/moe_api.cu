@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <new>
 
 #include "common.cuh"
 #include "internal.h"
@@ -186,10 +187,13 @@ moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_
   return MOE_OK;
 }
 
-moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf16_t* W1,
-                         const moe_bf16_t* W3, const moe_bf16_t* W2, int64_t T, int d, int E,
-                         int k, int d_ff, moe_bf16_t* out, void* ws, size_t ws_bytes, int flags,
-                         cudaEvent_t* stage_events, cudaStream_t stream) {
+namespace moe {
+namespace {
+// Host-side argument checks of moe_forward (nothing is launched).
+moe_status_t check_forward(const moe_bf16_t* x, const float* logits, const moe_bf16_t* W1,
+                           const moe_bf16_t* W3, const moe_bf16_t* W2, int64_t T, int d, int E,
+                           int k, int d_ff, const moe_bf16_t* out, const void* ws,
+                           size_t ws_bytes, int flags) {
   moe_status_t st = check_dims(T, d, E, k, d_ff, true);
   if (st != MOE_OK) return st;
   if (!W1 || !W3 || !W2 || !ws) return MOE_ERR_INVALID_ARG;
@@ -203,6 +207,20 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   const bool save = (flags & MOE_FWD_SAVE_FOR_BACKWARD) != 0;
   const WsLayout L = make_layout(T, d, E, k, d_ff);
   if (ws_bytes < (save ? L.bwd_total : L.fwd_total)) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
+moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf16_t* W1,
+                         const moe_bf16_t* W3, const moe_bf16_t* W2, int64_t T, int d, int E,
+                         int k, int d_ff, moe_bf16_t* out, void* ws, size_t ws_bytes, int flags,
+                         cudaEvent_t* stage_events, cudaStream_t stream) {
+  moe_status_t st = check_forward(x, logits, W1, W3, W2, T, d, E, k, d_ff, out, ws, ws_bytes,
+                                  flags);
+  if (st != MOE_OK) return st;
+  const bool save = (flags & MOE_FWD_SAVE_FOR_BACKWARD) != 0;
+  const WsLayout L = make_layout(T, d, E, k, d_ff);
 
   char* w = static_cast<char*>(ws);
   DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
@@ -283,6 +301,65 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
                          stream));
   record(stage_events, 4, stream);
   return MOE_OK;
+}
+
+struct moe_forward_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+moe_status_t moe_forward_graph_create(const moe_bf16_t* x, const float* logits,
+                                      const moe_bf16_t* W1, const moe_bf16_t* W3,
+                                      const moe_bf16_t* W2, int64_t T, int d, int E, int k,
+                                      int d_ff, moe_bf16_t* out, void* ws, size_t ws_bytes,
+                                      int flags, moe_forward_graph_t* graph) {
+  if (!graph) return MOE_ERR_INVALID_ARG;
+  *graph = nullptr;
+  moe_status_t st = check_forward(x, logits, W1, W3, W2, T, d, E, k, d_ff, out, ws, ws_bytes,
+                                  flags);
+  if (st != MOE_OK) return st;
+  // record the launches of one moe_forward on a private stream (nothing runs), then
+  // instantiate them
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaGraph_t g = nullptr;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return MOE_ERR_CUDA;
+  }
+  st = moe_forward(x, logits, W1, W3, W2, T, d, E, k, d_ff, out, ws, ws_bytes, flags, nullptr,
+                   cs);
+  const cudaError_t ce = cudaStreamEndCapture(cs, &g);
+  cudaStreamDestroy(cs);
+  if (st != MOE_OK || ce != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    return st != MOE_OK ? st : MOE_ERR_CUDA;
+  }
+  cudaGraphExec_t ex = nullptr;
+  if (cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return MOE_ERR_CUDA;
+  }
+  auto* h = new (std::nothrow) moe_forward_graph{g, ex};
+  if (!h) {
+    cudaGraphExecDestroy(ex);
+    cudaGraphDestroy(g);
+    return MOE_ERR_CUDA;
+  }
+  *graph = h;
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_graph_launch(moe_forward_graph_t graph, cudaStream_t stream) {
+  if (!graph) return MOE_ERR_INVALID_ARG;
+  return cudaGraphLaunch(graph->exec, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+void moe_forward_graph_destroy(moe_forward_graph_t graph) {
+  if (!graph) return;
+  cudaGraphExecDestroy(graph->exec);
+  cudaGraphDestroy(graph->graph);
+  delete graph;
 }
 
 moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host,

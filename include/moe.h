@@ -26,8 +26,9 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller, row-major, 16-byte
  *     aligned.  bf16 tensors are passed as moe_bf16_t (the raw 16-bit pattern).
  *   - Shapes: x [T,d], logits [T,E] fp32, W1 and W3 [E,d,d_ff], W2 [E,d_ff,d], out [T,d].
- *   - The library never allocates or frees memory and never synchronises (except
- *     moe_get_error).  Every launch is asynchronous on `stream`.  The workspace `ws`
+ *   - The library never allocates or frees device memory and never synchronises (except
+ *     moe_get_error); only the graph entry points create (host and driver) objects.  Every
+ *     launch is asynchronous on `stream`.  The workspace `ws`
  *     (device memory, 256-byte aligned, size from moe_workspace_bytes) is caller-owned;
  *     calls that share one ws must be ordered on the GPU (same stream, or synchronised).
  *   - Argument errors are detected on the host before anything is launched and returned as
@@ -129,6 +130,25 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
                          const moe_bf16_t* W3, const moe_bf16_t* W2, int64_t T, int d, int E,
                          int k, int d_ff, moe_bf16_t* out, void* ws, size_t ws_bytes, int flags,
                          cudaEvent_t* stage_events, cudaStream_t stream);
+
+/*
+ * The launch-overhead path for small batches: one moe_forward captured into a CUDA graph and
+ * replayed.  moe_forward_graph_create checks the arguments as moe_forward does, records
+ * moe_forward(x, logits, W1, W3, W2, ..., out, ws, ws_bytes, flags) with exactly these
+ * pointers and sizes on a private stream (stream capture: nothing runs) and instantiates it.
+ * moe_forward_graph_launch replays it on `stream`: the layer on whatever x and logits hold
+ * when the replay runs, into the same out and ws (calls sharing ws must be ordered, as for
+ * moe_forward).  The handle owns the graph (host and driver objects, no device memory of the
+ * library's own); moe_forward_graph_destroy releases it.  On failure *graph is NULL.
+ */
+typedef struct moe_forward_graph* moe_forward_graph_t;
+moe_status_t moe_forward_graph_create(const moe_bf16_t* x, const float* logits,
+                                      const moe_bf16_t* W1, const moe_bf16_t* W3,
+                                      const moe_bf16_t* W2, int64_t T, int d, int E, int k,
+                                      int d_ff, moe_bf16_t* out, void* ws, size_t ws_bytes,
+                                      int flags, moe_forward_graph_t* graph);
+moe_status_t moe_forward_graph_launch(moe_forward_graph_t graph, cudaStream_t stream);
+void moe_forward_graph_destroy(moe_forward_graph_t graph);
 
 /*
  * moe_forward with the batch in HOST memory: x_host [T,d] bf16 and logits_host [T,E] fp32

@@ -98,3 +98,18 @@ def test_forward_host_validation(lib):
     # shape checks as moe_forward
     st = raw.moe_forward_host(fake, fake, *w, 64, 100, 8, 2, 256, fake, fake, need, 0, None, None)
     assert st == lib.MOE_ERR_UNSUPPORTED
+
+
+def test_forward_graph_validation(lib):
+    raw = lib.library()
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    h = ctypes.c_void_p(123)
+    need = lib.moe_workspace_bytes(64, 128, 8, 2, 256, False)
+    st = raw.moe_forward_graph_create(fake, fake, fake, fake, fake, 64, 128, 8, 9, 256, fake,
+                                      fake, need, 0, ctypes.byref(h))
+    assert st == lib.MOE_ERR_INVALID_ARG and not h.value          # k > E
+    st = raw.moe_forward_graph_create(fake, fake, fake, fake, fake, 64, 128, 8, 2, 256, fake,
+                                      fake, need - 256, 0, ctypes.byref(h))
+    assert st == lib.MOE_ERR_WORKSPACE and not h.value
+    assert raw.moe_forward_graph_launch(None, None) == lib.MOE_ERR_INVALID_ARG
+    raw.moe_forward_graph_destroy(None)                           # no-op

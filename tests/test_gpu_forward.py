@@ -169,6 +169,33 @@ def test_forward_host_equals_device(moe, T, pinned, save):
             assert torch.equal(a, b), name
 
 
+@pytest.mark.parametrize("T,flags", [(1, 0), (64, 0), (300, 0), (300, 2)])
+def test_forward_graph_replays_the_layer(moe, T, flags):
+    # a captured forward, replayed after the inputs are rewritten in place, gives bitwise
+    # what a direct moe_forward gives on the new inputs
+    d, E, k, dff = 256, 16, 4, 384
+    w = moe_synth.custom(T, d, E, k, dff, seed=500 + T)
+    g = to_dev(moe_synth.generate(w))
+    x, logits = g["x"].clone(), g["logits"].clone()
+    out = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff), dtype=torch.uint8, device="cuda")
+    graph = moe.moe_forward_graph_create(x, logits, g["W1"], g["W3"], g["W2"], k, out, ws,
+                                         flags=flags)
+    try:
+        for rep in range(3):
+            gen = torch.Generator(device="cuda")
+            gen.manual_seed(rep)
+            x.copy_(torch.randn(T, d, generator=gen, device="cuda").to(torch.bfloat16))
+            logits.copy_(torch.randn(T, E, generator=gen, device="cuda"))
+            graph.launch()
+            ref, ws_ref = forward(moe, {**g, "x": x, "logits": logits}, k)
+            torch.cuda.synchronize()
+            assert moe.moe_get_error(ws) == 0 and moe.moe_get_error(ws_ref) == 0
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), rep
+    finally:
+        graph.close()
+
+
 def _device_workload(name):
     w = moe_synth.by_name(name)
     return w, moe_synth.generate(w, device="cuda")
