@@ -97,7 +97,8 @@ def dispatch(idx, E):
 
 
 def _unpack(inp):
-    x, logits, W1, W3, W2 = inp["x"], inp["logits"], inp["W1"], inp["W3"], inp["W2"]
+    # W3 absent or None: the cheap-activation expert, h = relu(x W1)^2
+    x, logits, W1, W3, W2 = inp["x"], inp["logits"], inp["W1"], inp.get("W3"), inp["W2"]
     T, d = x.shape
     E, _, dff = W1.shape
     return x, _logits64(logits), W1, W3, W2, T, d, E, dff
@@ -108,6 +109,8 @@ def _wtype(x):
 
 
 def _prep(a, wt):
+    if a is None:
+        return None
     return _c(a, np.uint16 if wt == "bf16" else np.float64)
 
 
@@ -130,7 +133,7 @@ def forward_permuted(inp, k, round_h=True):
     """Permuted forward (route, dispatch, row copy, per-row expert FFN, combine), bf16
     inputs.  Returns (y [T,d] f64, x_perm [T*k,d] uint16, o_perm [T*k,d] f64)."""
     x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
-    x, W1, W3, W2 = (_c(a, np.uint16) for a in (x, W1, W3, W2))
+    x, W1, W3, W2 = (_prep(a, "bf16") for a in (x, W1, W3, W2))
     y = np.empty((T, d), np.float64)
     xp = np.empty((T * k, d), np.uint16)
     op = np.empty((T * k, d), np.float64)
@@ -159,14 +162,14 @@ def backward_tokens(inp, dy, k, tokens=None, round_h=True, round_grad=True):
 
 def backward_dw(inp, dy, k, experts, round_h=True, round_grad=True):
     """Weight gradients of the listed experts: dW1, dW3 [n,d,dff] and dW2 [n,dff,d], f64
-    (round_grad as in backward_tokens)."""
+    (round_grad as in backward_tokens); dW3 is None for the cheap-activation expert."""
     x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
     wt = _wtype(x)
     x, W1, W3, W2, dy = (_prep(a, wt) for a in (x, W1, W3, W2, dy))
     ex = _c(experts, np.int32)
     n = len(ex)
     dW1 = np.empty((n, d, dff), np.float64)
-    dW3 = np.empty((n, d, dff), np.float64)
+    dW3 = np.empty((n, d, dff), np.float64) if W3 is not None else None
     dW2 = np.empty((n, dff, d), np.float64)
     fn = getattr(_load(), "oracle_backward_dw_" + wt)
     _check(fn(_ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), T, d, E, k, dff,
@@ -174,7 +177,8 @@ def backward_dw(inp, dy, k, experts, round_h=True, round_grad=True):
     return dW1, dW3, dW2
 
 
-def layer_flops(pairs: int, d: int, dff: int) -> int:
+def layer_flops(pairs: int, d: int, dff: int, gated: bool = True) -> int:
     """Algorithmic FLOP of the expert stage: 6*d*dff per token-expert pair (gate, up and
-    down projections: three d x dff multiply-adds), as the report's section 1.4 counts it."""
-    return 6 * d * dff * pairs
+    down projections: three d x dff multiply-adds), as the report's section 1.4 counts it;
+    4*d*dff without the gate projection (the cheap activation)."""
+    return (6 if gated else 4) * d * dff * pairs

@@ -12,6 +12,9 @@
 //  * DeepSeek-V4 report, Thai translation (itsolotime.com), section 1.4 "observations and
 //    suggestions": each token-expert pair costs 6hd FLOP covering the SwiGLU gate
 //    projection, the up projection and the down projection; the combine payload is BF16.
+//  * The same page, section 1.4, bullet on the activation function: a cheap element-wise
+//    activation without exponentials or divisions in place of SwiGLU, with the gating
+//    projection removed (the parameter budget then allows a wider intermediate).
 //  * The same page, section 3, and the 10100.com reading, section on batch-invariant and
 //    deterministic kernels: results must not depend on batch size or run.
 //
@@ -21,6 +24,8 @@
 //  * stable permute: permuted rows are ordered by (expert, token).
 //  * SwiGLU: h = silu(x W1) * (x W3), silu(a) = a / (1 + exp(-a)); h is rounded to bf16
 //    (round to nearest, ties to even) before the down projection when round_h != 0.
+//  * cheap activation (no W3 given): h = relu(x W1)^2, squared ReLU, an element-wise function
+//    with neither exponential nor division; h rounded to bf16 as above.
 //  * combine: y_t = sum_j g_j * o_j, here in fp64.
 //  * backward: the derivative of the bf16 rounding of h is taken as 1; with round_grad the
 //    matrix-product operands dO = g dy, da and db are rounded to bf16 (round to nearest
@@ -87,7 +92,8 @@ void route_token(const double* l, int E, int k, int32_t* idx, double* gate) {
   for (int j = 0; j < k; ++j) gate[j] = std::exp(l[idx[j]] - m) / s;
 }
 
-// One expert applied to one row x[0..d): a = x W1, b = x W3, h = silu(a) * b, o = h W2.
+// One expert applied to one row x[0..d): a = x W1, b = x W3, h = silu(a) * b, o = h W2;
+// without W3 (W3e null) the cheap activation: h = relu(a)^2 (b is left zero).
 // W1e, W3e are [d][dff] and W2e is [dff][d], row-major.
 template <class V>
 void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int dff, int round_h,
@@ -96,14 +102,20 @@ void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int df
   for (int c = 0; c < d; ++c) {
     const double xc = widen(x[c]);
     const V* w1 = W1e + static_cast<int64_t>(c) * dff;
-    const V* w3 = W3e + static_cast<int64_t>(c) * dff;
-    for (int f = 0; f < dff; ++f) {
-      a[f] += xc * widen(w1[f]);
-      b[f] += xc * widen(w3[f]);
+    for (int f = 0; f < dff; ++f) a[f] += xc * widen(w1[f]);
+    if (W3e) {
+      const V* w3 = W3e + static_cast<int64_t>(c) * dff;
+      for (int f = 0; f < dff; ++f) b[f] += xc * widen(w3[f]);
     }
   }
   for (int f = 0; f < dff; ++f) {
-    const double hv = a[f] / (1.0 + std::exp(-a[f])) * b[f];
+    double hv;
+    if (W3e) {
+      hv = a[f] / (1.0 + std::exp(-a[f])) * b[f];
+    } else {
+      const double r = a[f] > 0.0 ? a[f] : 0.0;
+      hv = r * r;
+    }
     h[f] = round_h ? round_bf16(hv) : hv;
   }
   for (int c = 0; c < d; ++c) o[c] = 0.0;
@@ -117,7 +129,8 @@ void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int df
 // the upstream gradient dy of the layer output:
 //   dgate = <o, dy>, dO = g dy, dh = dO W2^T,
 //   da = dh * b * silu'(a) with silu'(a) = s (1 + a (1 - s)), s = sigmoid(a),
-//   db = dh * silu(a),  dxp = da W1^T + db W3^T.
+//   db = dh * silu(a),  dxp = da W1^T + db W3^T;
+// without W3: da = dh * 2 relu(a) (the derivative of relu(a)^2), db = 0, dxp = da W1^T.
 // With round_grad != 0, dO, da and db are rounded to bf16 where they become operands of a
 // matrix product (dh, dxp and the weight gradients), the reading that every product of the
 // layer takes bf16 operands and accumulates exactly (here in fp64).
@@ -137,9 +150,14 @@ void ffn_row_bwd(const V* W1e, const V* W3e, const V* W2e, int d, int dff, doubl
     dh[f] = acc;
   }
   for (int f = 0; f < dff; ++f) {
-    const double sg = sigmoid(a[f]);
-    da[f] = dh[f] * b[f] * sg * (1.0 + a[f] * (1.0 - sg));
-    db[f] = dh[f] * a[f] * sg;
+    if (W3e) {
+      const double sg = sigmoid(a[f]);
+      da[f] = dh[f] * b[f] * sg * (1.0 + a[f] * (1.0 - sg));
+      db[f] = dh[f] * a[f] * sg;
+    } else {
+      da[f] = dh[f] * 2.0 * (a[f] > 0.0 ? a[f] : 0.0);
+      db[f] = 0.0;
+    }
     if (round_grad) {
       da[f] = round_bf16(da[f]);
       db[f] = round_bf16(db[f]);
@@ -147,9 +165,13 @@ void ffn_row_bwd(const V* W1e, const V* W3e, const V* W2e, int d, int dff, doubl
   }
   for (int c = 0; c < d; ++c) {
     const V* w1 = W1e + static_cast<int64_t>(c) * dff;
-    const V* w3 = W3e + static_cast<int64_t>(c) * dff;
     double acc = 0.0;
-    for (int f = 0; f < dff; ++f) acc += da[f] * widen(w1[f]) + db[f] * widen(w3[f]);
+    if (W3e) {
+      const V* w3 = W3e + static_cast<int64_t>(c) * dff;
+      for (int f = 0; f < dff; ++f) acc += da[f] * widen(w1[f]) + db[f] * widen(w3[f]);
+    } else {
+      for (int f = 0; f < dff; ++f) acc += da[f] * widen(w1[f]);
+    }
     dxp[c] = acc;
   }
 }
@@ -160,7 +182,9 @@ struct Dims {
 };
 
 template <class V>
-const V* w13(const V* W, const Dims& D, int e) { return W + static_cast<int64_t>(e) * D.d * D.dff; }
+const V* w13(const V* W, const Dims& D, int e) {
+  return W ? W + static_cast<int64_t>(e) * D.d * D.dff : nullptr;  // null: no W3
+}
 template <class V>
 const V* w2of(const V* W, const Dims& D, int e) { return W + static_cast<int64_t>(e) * D.dff * D.d; }
 
@@ -350,19 +374,18 @@ int backward_dw(const V* x, const double* logits, const V* W1, const V* W3, cons
       }
     }
     double* g1 = dW1 + static_cast<int64_t>(q) * D.d * D.dff;
-    double* g3 = dW3 + static_cast<int64_t>(q) * D.d * D.dff;
+    double* g3 = dW3 ? dW3 + static_cast<int64_t>(q) * D.d * D.dff : nullptr;  // null: no W3
     double* g2 = dW2 + static_cast<int64_t>(q) * D.dff * D.d;
 #pragma omp parallel for schedule(static)
     for (int c = 0; c < D.d; ++c) {
       double* r1 = g1 + static_cast<int64_t>(c) * D.dff;
-      double* r3 = g3 + static_cast<int64_t>(c) * D.dff;
-      for (int f = 0; f < D.dff; ++f) { r1[f] = 0.0; r3[f] = 0.0; }
+      double* r3 = g3 ? g3 + static_cast<int64_t>(c) * D.dff : nullptr;
+      for (int f = 0; f < D.dff; ++f) r1[f] = 0.0;
+      if (r3) for (int f = 0; f < D.dff; ++f) r3[f] = 0.0;
       for (int64_t r = 0; r < R; ++r) {
         const double xc = widen(x[(pairs[r] / D.k) * D.d + c]);
-        for (int f = 0; f < D.dff; ++f) {
-          r1[f] += xc * DA[r * D.dff + f];
-          r3[f] += xc * DB[r * D.dff + f];
-        }
+        for (int f = 0; f < D.dff; ++f) r1[f] += xc * DA[r * D.dff + f];
+        if (r3) for (int f = 0; f < D.dff; ++f) r3[f] += xc * DB[r * D.dff + f];
       }
     }
 #pragma omp parallel for schedule(static)

@@ -329,3 +329,101 @@ def test_layer_flops_is_six_h_d_per_pair():
     # the report's section 1.4 counts 6hd FLOP per token-expert pair (gate, up, down)
     assert oracle.layer_flops(1, 7168, 2048) == 6 * 7168 * 2048
     assert oracle.layer_flops(16384 * 8, 7168, 2048) == 11544872091648
+
+
+# ----------------------------------------------------------- cheap activation (no W3)
+
+
+def _no_w3(inp):
+    return {kk: v for kk, v in inp.items() if kk != "W3"}
+
+
+def _relu2(a):
+    return np.maximum(a, 0.0) ** 2
+
+
+def test_cheap_activation_k1_single_expert_is_dense_relu2_mlp():
+    # without the gate projection the expert is y = relu(x W1)^2 W2: with one expert and k = 1
+    # the layer is that dense MLP (numpy products)
+    rng = np.random.default_rng(41)
+    inp = _no_w3(_rand_inputs(rng, T=16, d=32, E=1, k=1, dff=48))
+    X = _bits_to_f64(inp["x"])
+    W1, W2 = (_bits_to_f64(inp[n])[0] for n in ("W1", "W2"))
+    h = _relu2(X @ W1)
+    assert (X @ W1 < 0).any() and (X @ W1 > 0).any()      # both sides of the kink occur
+    np.testing.assert_allclose(oracle.forward_tokens(inp, 1, round_h=False), h @ W2,
+                               rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(oracle.forward_tokens(inp, 1, round_h=True), _torch_bf16(h) @ W2,
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_cheap_activation_k_equals_E_and_permuted_forward():
+    from scipy.special import softmax
+    rng = np.random.default_rng(42)
+    T, d, E, dff = 10, 16, 5, 24
+    inp = _no_w3(_rand_inputs(rng, T=T, d=d, E=E, k=E, dff=dff))
+    X = _bits_to_f64(inp["x"])
+    p = softmax(inp["logits"].astype(np.float64), axis=1)
+    ref = np.zeros((T, d))
+    for e in range(E):
+        W1, W2 = (_bits_to_f64(inp[n])[e] for n in ("W1", "W2"))
+        ref += p[:, e:e + 1] * (_relu2(X @ W1) @ W2)
+    np.testing.assert_allclose(oracle.forward_tokens(inp, E, round_h=False), ref,
+                               rtol=1e-12, atol=1e-13)
+    k = 2
+    y_pm, _, _ = oracle.forward_permuted(inp, k)
+    np.testing.assert_allclose(y_pm, oracle.forward_tokens(inp, k), rtol=1e-13, atol=1e-14)
+
+
+def test_cheap_activation_backward_matches_central_finite_differences():
+    rng = np.random.default_rng(43)
+    T, d, E, k, dff = 3, 4, 3, 2, 5
+    inp = _no_w3(_rand_inputs(rng, T, d, E, k, dff, as_bf16=False))
+    inp["logits"] = inp["logits"].astype(np.float64)
+    dy = rng.standard_normal((T, d))
+    dx, dgate, dlog = oracle.backward_tokens(inp, dy, k, round_h=False, round_grad=False)
+    dW1, dW3, dW2 = oracle.backward_dw(inp, dy, k, np.arange(E), round_h=False, round_grad=False)
+    assert dW3 is None
+    # relu(a)^2 is continuously differentiable, so central differences converge at the kink too
+    tol = dict(rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dx, _fd(inp, dy, k, "x", 1e-6), **tol)
+    np.testing.assert_allclose(dW1, _fd(inp, dy, k, "W1", 1e-6), **tol)
+    np.testing.assert_allclose(dW2, _fd(inp, dy, k, "W2", 1e-6), **tol)
+    np.testing.assert_allclose(dlog, _fd(inp, dy, k, "logits", 1e-6), **tol)
+
+
+def test_cheap_activation_round_grad_rounds_exactly_the_product_operands():
+    from scipy.special import softmax
+    rng = np.random.default_rng(44)
+    T, d, E, k, dff = 12, 16, 3, 2, 24
+    inp = _no_w3(_rand_inputs(rng, T, d, E, k, dff))
+    dy = _bf16_bits(rng.standard_normal((T, d)))
+    X, DY = _bits_to_f64(inp["x"]), _bits_to_f64(dy)
+    W1, W2 = (_bits_to_f64(inp[n]) for n in ("W1", "W2"))
+    logits = inp["logits"].astype(np.float64)
+    order = np.argsort(-logits, axis=1, kind="stable")[:, :k]
+    gates = softmax(np.take_along_axis(logits, order, 1), axis=1)
+    e = 2
+    ref2 = np.zeros((dff, d)); ref1 = np.zeros((d, dff)); dx_ref = np.zeros((T, d))
+    for t in range(T):
+        for j in range(k):
+            ee = order[t, j]
+            a = X[t] @ W1[ee]
+            h = _torch_bf16(_relu2(a))
+            dO = _torch_bf16(gates[t, j] * DY[t])
+            da = _torch_bf16((W2[ee] @ dO) * 2.0 * np.maximum(a, 0.0))
+            dx_ref[t] += W1[ee] @ da
+            if ee == e:
+                ref2 += np.outer(h, dO)
+                ref1 += np.outer(X[t], da)
+    dW1, dW3, dW2 = oracle.backward_dw(inp, dy, k, [e])
+    np.testing.assert_allclose(dW2[0], ref2, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dW1[0], ref1, rtol=1e-10, atol=1e-12)
+    dx, _, _ = oracle.backward_tokens(inp, dy, k)
+    np.testing.assert_allclose(dx, dx_ref, rtol=1e-10, atol=1e-12)
+
+
+def test_layer_flops_without_the_gate_projection():
+    assert oracle.layer_flops(1, 7168, 3072, gated=False) == 4 * 7168 * 3072
+    # the same parameter budget (d_ff' = 1.5 d_ff) keeps the FLOP count
+    assert oracle.layer_flops(5, 7168, 3072, gated=False) == oracle.layer_flops(5, 7168, 2048)
