@@ -48,10 +48,14 @@ def _peaks():
 
 
 def _workload_config(w):
-    return {"workload": "%s: T=%d d=%d E=%d top-%d d_ff=%d, logits N(0,1) - %.1f ln(e+1)"
-                        % (w.name, w.T, w.d, w.E, w.k, w.dff, w.zipf_s),
+    return {"workload": "%s: T=%d d=%d E=%d top-%d d_ff=%d %s, logits N(0,1) - %.1f ln(e+1)"
+                        % (w.name, w.T, w.d, w.E, w.k, w.dff,
+                           "SwiGLU" if w.gated else "squared ReLU (no gate projection)",
+                           w.zipf_s),
             "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.dff,
-            "l2": "inputs larger than L2 (22.5 GB of expert weights read every step)",
+            "l2": "inputs larger than L2 (%.1f GB of expert weights read every step)"
+                  % (w.E * (3 if w.gated else 2) * w.d * w.dff * 2 / 1e9),
+            "activation": "SwiGLU" if w.gated else "squared ReLU",
             "parallelism": "replicas (one independent layer per GPU)"}
 
 
@@ -124,9 +128,10 @@ class ClockSampler:
 
 def _algorithmic(w, P):
     d, dff, T, E, k = w.d, w.dff, w.T, w.E, w.k
+    n1 = 2 if w.gated else 1  # projections in GEMM1: gate + up (SwiGLU) or up alone
     return dict(
-        gemm_flops=6 * d * dff * P,             # 6 d dff per token-expert pair
-        gemm1_flops=4 * d * dff * P,            # gate + up projections
+        gemm_flops=(2 * n1 + 2) * d * dff * P,  # 6 d dff per pair (4 d dff without the gate)
+        gemm1_flops=2 * n1 * d * dff * P,       # gate + up projections (or up alone)
         gemm2_flops=2 * d * dff * P,            # down projection
         # logits read; topk, gate, pos, perm written; x read; x_perm written
         dispatch_bytes=T * E * 4 + T * k * 16 + T * d * 2 + P * d * 2,
@@ -206,9 +211,9 @@ def bench_fwd_bwd(moe, dev, steps, warmup, shape=None):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nb)] for _ in range(steps)]
 
     def step(ev=None):
-        moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+        moe.moe_forward(g["x"], g["logits"], g["W1"], g.get("W3"), g["W2"], k, out, ws,
                         flags=moe.MOE_FWD_SAVE_FOR_BACKWARD, stream=stream)
-        moe.moe_backward(g["dy"], g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k,
+        moe.moe_backward(g["dy"], g["x"], g["logits"], g["W1"], g.get("W3"), g["W2"], k,
                          res["dx"], res["dW1"], res["dW3"], res["dW2"], res["dgate"],
                          res["dlogits"], ws, stage_events=ev, stream=stream)
 
@@ -308,7 +313,7 @@ def bench_native(args, w):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
 
     def step(ev=None):
-        moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+        moe.moe_forward(g["x"], g["logits"], g["W1"], g.get("W3"), g["W2"], k, out, ws,
                         stage_events=ev, stream=stream)
 
     for _ in range(args.warmup):
@@ -360,7 +365,7 @@ def bench_native(args, w):
 
     def e2e_step(i):
         j = i % 2
-        moe.moe_forward_host(hx[j], hl[j], g["W1"], g["W3"], g["W2"], k, ho[j], ws_io[j],
+        moe.moe_forward_host(hx[j], hl[j], g["W1"], g.get("W3"), g["W2"], k, ho[j], ws_io[j],
                              stream=io_streams[j])
 
     for i in range(max(2, args.warmup)):
@@ -388,7 +393,7 @@ def bench_native(args, w):
     del ws_io
 
     # the same step replayed from a captured CUDA graph (the launch-overhead path)
-    graph = moe.moe_forward_graph_create(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out,
+    graph = moe.moe_forward_graph_create(g["x"], g["logits"], g["W1"], g.get("W3"), g["W2"], k, out,
                                          ws)
     for _ in range(2):
         graph.launch(stream)
@@ -409,13 +414,13 @@ def bench_native(args, w):
     # timed for comparison; bitwise the same output
     wave_flags = moe.MOE_FWD_GATHER_ROWS | moe.MOE_FWD_FUSED_COMBINE
     for _ in range(2):
-        moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+        moe.moe_forward(g["x"], g["logits"], g["W1"], g.get("W3"), g["W2"], k, out, ws,
                         flags=wave_flags, stream=stream)
     barrier()
     n_wave = max(1, min(args.steps, 10))
     start.record(stream)
     for _ in range(n_wave):
-        moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+        moe.moe_forward(g["x"], g["logits"], g["W1"], g.get("W3"), g["W2"], k, out, ws,
                         flags=wave_flags, stream=stream)
     stop.record(stream)
     barrier()
@@ -436,11 +441,12 @@ def bench_native(args, w):
     counts = torch.bincount(torch.topk(g["logits"], k, dim=1).indices.flatten(),
                             minlength=E).double().cpu().numpy()
     active = counts > 0
-    w_bytes = 3 * 2 * d * dff  # per active expert
-    t_e = np.maximum(6 * d * dff * counts[active] / (peaks["bf16"] * 1e12), w_bytes / (peaks["hbm"] * 1e9))
+    w_bytes = (3 if w.gated else 2) * 2 * d * dff  # per active expert
+    fpr = (6 if w.gated else 4) * d * dff  # FLOP per routed row
+    t_e = np.maximum(fpr * counts[active] / (peaks["bf16"] * 1e12), w_bytes / (peaks["hbm"] * 1e9))
     gemm_ms = stages["gemm1_swiglu"] + stages["gemm2"]
     roof = {"per_expert_sum_ms": float(t_e.sum() * 1e3),
-            "overlapped_ms": float(max(6 * d * dff * counts.sum() / (peaks["bf16"] * 1e12),
+            "overlapped_ms": float(max(fpr * counts.sum() / (peaks["bf16"] * 1e12),
                                        active.sum() * w_bytes / (peaks["hbm"] * 1e9)) * 1e3),
             "active_experts": int(active.sum()),
             "weights_gb": float(active.sum() * w_bytes / 1e9),

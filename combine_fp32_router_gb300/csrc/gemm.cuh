@@ -47,6 +47,10 @@ struct KindTraits {
 };
 
 struct GemmParams {
+  // expert activation: 1 = SwiGLU (W1 and W3), 0 = squared ReLU on W1 alone (no gate
+  // projection): GEMM1 tiles then hold 256 columns of A = Xp W1, dH gives dA only, dX and
+  // dW1 take K = N = d_ff
+  int gated;
   // fp32 output tiles written by TMA stores (32 x 32 boxes, 128-byte swizzle) when tma_store:
   // c0 = out0, c1 = out1
   CUtensorMap mapC0, mapC1;
@@ -338,6 +342,29 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
   const int w0 = q * 32;  // first row of this warp
   auto clamp_rows = [&](int n) { return n - w0 < 0 ? 0 : (n - w0 > 32 ? 32 : n - w0); };
   if constexpr (KIND == kFwd1) {
+    if (!p.gated) {
+      // h = relu(a)^2 over the tile's 256 accumulator columns (h columns n0 ..)
+      const int64_t row0 = ti.row0 + w0;
+      char* H = reinterpret_cast<char*>(static_cast<uint16_t*>(p.out0) + row0 * p.dff + ti.n0);
+      const int nstore = clamp_rows(ti.nseg);      // pad rows are written as zeros
+      const int nsave = clamp_rows(ti.nvalid);
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        float a[32], h[32];
+        tmem_ld32(tacc + ch * 32, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float rl = fmaxf(a[i], 0.0f);
+          h[i] = valid ? rl * rl : 0.0f;
+        }
+        store_chunk<true>(buf, h, H + ch * 64, 2ll * p.dff, nstore, lane);
+        if (p.save_ab) {
+          char* SA = reinterpret_cast<char*>(p.save_a + row0 * p.dff + ti.n0 + ch * 32);
+          store_chunk<false>(buf, a, SA, 4ll * p.dff, nsave, lane);
+        }
+      }
+      return;
+    }
     constexpr int HALF = BN / 2;
     const int c0 = ti.n0 / 2;  // h column of this tile's first accumulator column
     const int64_t row0 = ti.row0 + w0;
@@ -418,7 +445,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         const int rr = 4 * i + rsub;
         if (rr < nval) {
           ua[i] = ld_v4(sa0 + rr * p.dff + ch * 32 + c4);
-          ub[i] = ld_v4(sb0 + rr * p.dff + ch * 32 + c4);
+          ub[i] = p.gated ? ld_v4(sb0 + rr * p.dff + ch * 32 + c4) : make_uint4(0u, 0u, 0u, 0u);
         }
       }
       float dh[32];
@@ -436,18 +463,25 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
                                  __uint_as_float(ua[i].z), __uint_as_float(ua[i].w)};
             const float bv[4] = {__uint_as_float(ub[i].x), __uint_as_float(ub[i].y),
                                  __uint_as_float(ub[i].z), __uint_as_float(ub[i].w)};
+            if (p.gated) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float g = buf[rr * 33 + c4 + q];
-              const float sg = 1.0f / (1.0f + expf(-av[q]));
-              da[q] = g * bv[q] * (sg * (1.0f + av[q] * (1.0f - sg)));
-              db[q] = g * (av[q] * sg);
+              for (int q = 0; q < 4; ++q) {
+                const float g = buf[rr * 33 + c4 + q];
+                const float sg = 1.0f / (1.0f + expf(-av[q]));
+                da[q] = g * bv[q] * (sg * (1.0f + av[q] * (1.0f - sg)));
+                db[q] = g * (av[q] * sg);
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)  // d relu(a)^2 / da = 2 relu(a)
+                da[q] = buf[rr * 33 + c4 + q] * (2.0f * fmaxf(av[q], 0.0f));
             }
           }
           uint16_t* o = dA0 + rr * (2 * p.dff) + ch * 32 + c4;
           *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(da[0], da[1]), pack_bf16x2(da[2], da[3]));
-          *reinterpret_cast<uint2*>(o + p.dff) =
-              make_uint2(pack_bf16x2(db[0], db[1]), pack_bf16x2(db[2], db[3]));
+          if (p.gated)
+            *reinterpret_cast<uint2*>(o + p.dff) =
+                make_uint2(pack_bf16x2(db[0], db[1]), pack_bf16x2(db[2], db[3]));
         }
       }
       __syncwarp();
@@ -654,7 +688,12 @@ __global__ void __launch_bounds__(256, 1)
           if (!p.gather_x) load_h(kL2HintA, sa, &mapA, fb, k0, ti.row0);
           const int wrow = ti.e * p.d + k0;
           const int h0 = ti.n0 / 2;  // first h column of the tile
-          if constexpr (PAIR) {
+          if (!p.gated) {
+            // squared ReLU: every B column comes from W1 (CTA rank r of a pair: its half)
+#pragma unroll
+            for (int i = 0; i < BL / 64; ++i)
+              load_h(kL2HintB, sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, wrow);
+          } else if constexpr (PAIR) {
             // rank 0 holds the W1 half of B, rank 1 the W3 half
             const CUtensorMap* wm = rank == 0 ? &mapB0 : &mapB1;
 #pragma unroll

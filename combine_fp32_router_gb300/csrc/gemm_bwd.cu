@@ -46,16 +46,19 @@ cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s) {
   const int BN = (L.d % 256 == 0) ? 256 : 128;
   const uint32_t brows = c.pair ? BN / 2 : BN;
   cudaError_t st = cudaSuccess;
-  // A = [dA|dB] rows (K = 2 dff); B = W1[e] / W3[e] viewed as [d rows][dff] (K-major)
-  const CUtensorMap a = make_map_2d(c.ws + L.dAB, 2ull * L.dff, L.P_pad, 4ull * L.dff, 64, 128, &st);
+  // A = [dA|dB] rows (K = 2 dff; squared ReLU: dA alone, K = dff); B = W1[e] / W3[e] viewed
+  // as [d rows][dff] (K-major)
+  const uint64_t kdim = (c.gated ? 2ull : 1ull) * L.dff;
+  const uint16_t* w3 = c.gated ? c.W3 : c.W1;  // never read without the gate projection
+  const CUtensorMap a = make_map_2d(c.ws + L.dAB, kdim, L.P_pad, 4ull * L.dff, 64, 128, &st);
   const CUtensorMap b0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, brows, &st);
-  const CUtensorMap b1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, brows, &st);
+  const CUtensorMap b1 = make_map_2d(w3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, brows, &st);
   const CUtensorMap sb0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, BN, &st);
-  const CUtensorMap sb1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, BN, &st);
+  const CUtensorMap sb1 = make_map_2d(w3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, BN, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = base_params(c);
   p.nb = L.d / BN;
-  p.nkb = 2 * L.dff / kBK;
+  p.nkb = static_cast<int>(kdim / kBK);
   p.out0 = c.ws + L.dXp;
   p.mapC0 = make_store_map_f32(c.ws + L.dXp, L.d, L.P_pad, 4ull * L.d, &st);
   if (st != cudaSuccess) return st;
@@ -98,11 +101,12 @@ cudaError_t launch_gemm_dw13(const GemmCtx& c, cudaStream_t s) {
   p.M = L.d;
   const int mrows = c.pair ? 2 * kBM : kBM;
   p.mb = (L.d + mrows - 1) / mrows;
-  p.nb = 2 * L.dff / BN;
+  p.nb = (c.gated ? 2 : 1) * L.dff / BN;  // squared ReLU: dW1 alone
   p.out0 = c.dW1;
   p.out1 = c.dW3;
   p.mapC0 = make_store_map_f32(c.dW1, L.dff, static_cast<uint64_t>(L.E) * L.d, 4ull * L.dff, &st);
-  p.mapC1 = make_store_map_f32(c.dW3, L.dff, static_cast<uint64_t>(L.E) * L.d, 4ull * L.dff, &st);
+  if (c.gated)
+    p.mapC1 = make_store_map_f32(c.dW3, L.dff, static_cast<uint64_t>(L.E) * L.d, 4ull * L.dff, &st);
   if (st != cudaSuccess) return st;
   p.tma_store = 1;
   const int64_t tiles = static_cast<int64_t>(L.E) * p.mb * p.nb;

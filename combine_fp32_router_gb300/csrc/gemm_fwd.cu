@@ -89,6 +89,7 @@ GemmParams base_params(const GemmCtx& c) {
   p.wait_ns = c.wait_ns;
   p.debug_flags = c.debug_flags;
   p.rows_cap = L.P_pad;
+  p.gated = c.gated ? 1 : 0;
   return p;
 }
 
@@ -108,10 +109,14 @@ cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
   // this map is not read)
   const CUtensorMap a = make_map_2d(c.ws + L.xperm, L.d, L.P_pad, 2ull * L.d, 64, 128, &st);
   const CUtensorMap b0 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 64, &st);
-  const CUtensorMap b1 = make_map_2d(c.W3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 64, &st);
+  // without W3 (squared ReLU) the second B map is never read
+  const CUtensorMap b1 = make_map_2d(c.gated ? c.W3 : c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d,
+                                     2ull * L.dff, 64, 64, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = base_params(c);
-  p.nb = L.dff / 128;  // 128 h columns per tile (W1 half + W3 half = 256 accumulator columns)
+  // SwiGLU: 128 h columns per tile (W1 half + W3 half = 256 accumulator columns);
+  // squared ReLU: 256 h columns of W1 per tile
+  p.nb = c.gated ? L.dff / 128 : L.dff / 256;
   p.nkb = L.d / kBK;
   p.out0 = c.ws + L.H;
   p.save_ab = c.save_ab;

@@ -79,6 +79,7 @@ struct GemmCtx {
   bool fuse_combine;     // GEMM2 also combines finished tokens into `out`
   bool gather_x;         // GEMM1 gathers its A rows from x (no x_perm)
   uint16_t* out;         // layer output [T, d] (fused combine)
+  bool gated;            // SwiGLU (W1, W3); false: squared ReLU on W1 alone
 };
 cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s);   // H = SwiGLU(Xp W1, Xp W3)
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s);   // Y = H W2

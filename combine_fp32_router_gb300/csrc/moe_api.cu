@@ -196,7 +196,8 @@ moe_status_t check_forward(const moe_bf16_t* x, const float* logits, const moe_b
                            size_t ws_bytes, int flags) {
   moe_status_t st = check_dims(T, d, E, k, d_ff, true);
   if (st != MOE_OK) return st;
-  if (!W1 || !W3 || !W2 || !ws) return MOE_ERR_INVALID_ARG;
+  if (!W1 || !W2 || !ws) return MOE_ERR_INVALID_ARG;
+  if (!W3 && d_ff % 256 != 0) return MOE_ERR_UNSUPPORTED;  // squared ReLU: 256-column tiles
   if (T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
   if (flags & ~(MOE_FWD_SAVE_FOR_BACKWARD | MOE_FWD_FUSED_COMBINE | MOE_FWD_GATHER_ROWS))
     return MOE_ERR_INVALID_ARG;
@@ -282,6 +283,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   // single-CTA launch per GEMM then covers every tile
   c.pair = use_pairs() && T > kTileRows;
   c.fuse_combine = (flags & MOE_FWD_FUSED_COMBINE) != 0;
+  c.gated = W3 != nullptr;
   c.gather_x = gather;
   c.out = out;
   MOE_TRY(launch_gemm_fwd1(c, stream));
@@ -404,7 +406,9 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
                           size_t ws_bytes, cudaEvent_t* stage_events, cudaStream_t stream) {
   moe_status_t st = check_dims(T, d, E, k, d_ff, true);
   if (st != MOE_OK) return st;
-  if (!W1 || !W3 || !W2 || !dW1 || !dW3 || !dW2 || !ws) return MOE_ERR_INVALID_ARG;
+  if (!W1 || !W2 || !dW1 || !dW2 || !ws) return MOE_ERR_INVALID_ARG;
+  if (!W3 != !dW3) return MOE_ERR_INVALID_ARG;  // no W3 (squared ReLU): no dW3 either
+  if (!W3 && d_ff % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if (T > 0 && (!dy || !x || !logits || !dx || !dgate)) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {dy, x, logits, W1, W3, W2, dx, dW1, dW3, dW2, dgate, dlogits};
   for (const void* p : ptrs)
@@ -419,7 +423,7 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   if (T == 0) {
     const size_t wb = static_cast<size_t>(E) * d * d_ff * 4;
     MOE_TRY(cudaMemsetAsync(dW1, 0, wb, stream));
-    MOE_TRY(cudaMemsetAsync(dW3, 0, wb, stream));
+    if (dW3) MOE_TRY(cudaMemsetAsync(dW3, 0, wb, stream));
     MOE_TRY(cudaMemsetAsync(dW2, 0, wb, stream));
     for (int i = 1; i < MOE_BWD_NUM_EVENTS; ++i) record(stage_events, i, stream);
     return MOE_OK;
@@ -452,6 +456,7 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   c.debug_flags = g_debug_flags.load();
   c.num_sms = num_sms_of_current_device();
   c.pair = use_pairs();
+  c.gated = W3 != nullptr;
   MOE_TRY(launch_gemm_dh(c, stream));
   record(stage_events, 2, stream);
   MOE_TRY(launch_gemm_dx(c, stream));

@@ -119,6 +119,10 @@ moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_
 
 /*
  * Forward of the whole layer: out [T,d] bf16.
+ * W3 = NULL selects the expert without the gate projection (report translation, section 1.4,
+ * activation bullet: a cheap element-wise activation with no exponential or division in
+ * place of SwiGLU; squared ReLU is this library's reading): h = bf16(relu(x W1[e])^2), then
+ * h W2[e] as below, with d_ff % 256 == 0 (else MOE_ERR_UNSUPPORTED).
  *   out_t = bf16( sum_j gate[t,j] * (h_tj W2[e_j]) ),  h_tj = bf16(silu(x_t W1[e_j]) * (x_t W3[e_j]))
  * with every matrix product accumulated in fp32 and the slot sum in fp32, in slot order.
  * ws must hold moe_workspace_bytes(T, d, E, k, d_ff, MOE_WS_BACKWARD if
@@ -171,7 +175,8 @@ moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host
                               cudaStream_t stream);
 
 /*
- * Backward of the layer for upstream gradient dy [T,d] bf16.  Precondition: ws holds the
+ * Backward of the layer for upstream gradient dy [T,d] bf16.  For the expert without the
+ * gate projection (forward with W3 = NULL) pass W3 = NULL and dW3 = NULL.  Precondition: ws holds the
  * state of a moe_forward call with MOE_FWD_SAVE_FOR_BACKWARD on the same x, logits, W1, W3,
  * W2 and sizes, with nothing else using ws in between.
  * Outputs (all overwritten, none accumulated into):

@@ -28,6 +28,8 @@ class Workload:
     zipf_s: float = 0.0          # 0: no bias; else logits += -s * ln(e + 1)
     seed: int = 1000
     sweep: tuple = field(default=())   # token counts of a batch-invariance sweep
+    gated: bool = True           # False: no W3 (squared-ReLU expert, d_ff = 1.5x for the
+                                 # same parameter count)
 
     @property
     def pairs(self) -> int:
@@ -43,6 +45,10 @@ WORKLOADS = [
              sweep=(1, 2, 4, 8, 16, 32, 64, 128)),
     Workload("large_skewed", T=16384, d=7168, E=256, k=8, dff=2048, zipf_s=1.2, seed=1003),
     Workload("fwd_bwd", T=8192, d=4096, E=128, k=8, dff=1536, seed=1004),
+    # the large skewed layer with the cheap activation: the same parameter budget (two
+    # projections of d_ff = 3072 instead of three of 2048)
+    Workload("large_skewed_relu2", T=16384, d=7168, E=256, k=8, dff=3072, zipf_s=1.2,
+             seed=1005, gated=False),
 ]
 
 
@@ -53,8 +59,8 @@ def by_name(name: str) -> Workload:
     raise KeyError(name)
 
 
-def custom(T, d, E, k, dff, seed=7, zipf_s=0.0, name="custom") -> Workload:
-    return Workload(name, T=T, d=d, E=E, k=k, dff=dff, zipf_s=zipf_s, seed=seed)
+def custom(T, d, E, k, dff, seed=7, zipf_s=0.0, name="custom", gated=True) -> Workload:
+    return Workload(name, T=T, d=d, E=E, k=k, dff=dff, zipf_s=zipf_s, seed=seed, gated=gated)
 
 
 def generate(w: Workload, device="cpu", with_dy=False):
@@ -81,7 +87,8 @@ def generate(w: Workload, device="cpu", with_dy=False):
         logits += bias.to(torch.float32).to(device)
     out["logits"] = logits
     out["W1"] = _randn_bf16(randn, (w.E, w.d, w.dff), 1.0 / math.sqrt(w.d))
-    out["W3"] = _randn_bf16(randn, (w.E, w.d, w.dff), 1.0 / math.sqrt(w.d))
+    if w.gated:
+        out["W3"] = _randn_bf16(randn, (w.E, w.d, w.dff), 1.0 / math.sqrt(w.d))
     out["W2"] = _randn_bf16(randn, (w.E, w.dff, w.d), 1.0 / math.sqrt(w.dff))
     if with_dy:
         out["dy"] = randn(w.T, w.d).to(torch.bfloat16)

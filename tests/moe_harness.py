@@ -86,7 +86,7 @@ def forward(moe, g, k, save=False, ws=None):
         ws = torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, save), dtype=torch.uint8,
                          device=x.device)
     out = torch.empty(T, d, dtype=torch.bfloat16, device=x.device)
-    moe.moe_forward(x, g["logits"], g["W1"], g["W3"], g["W2"], k, out, ws,
+    moe.moe_forward(x, g["logits"], g["W1"], g.get("W3"), g["W2"], k, out, ws,
                     flags=moe.MOE_FWD_SAVE_FOR_BACKWARD if save else 0)
     return out, ws
 
@@ -99,12 +99,12 @@ def backward(moe, g, k, ws):
     res = dict(
         dx=torch.empty(T, d, dtype=torch.bfloat16, device=dev),
         dW1=torch.empty(E, d, dff, dtype=torch.float32, device=dev),
-        dW3=torch.empty(E, d, dff, dtype=torch.float32, device=dev),
+        dW3=torch.empty(E, d, dff, dtype=torch.float32, device=dev) if "W3" in g else None,
         dW2=torch.empty(E, dff, d, dtype=torch.float32, device=dev),
         dgate=torch.empty(T, k, dtype=torch.float32, device=dev),
         dlogits=torch.empty(T, E, dtype=torch.float32, device=dev),
     )
-    moe.moe_backward(g["dy"], x, g["logits"], g["W1"], g["W3"], g["W2"], k, res["dx"],
+    moe.moe_backward(g["dy"], x, g["logits"], g["W1"], g.get("W3"), g["W2"], k, res["dx"],
                      res["dW1"], res["dW3"], res["dW2"], res["dgate"], res["dlogits"], ws)
     return res
 

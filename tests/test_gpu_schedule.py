@@ -1,9 +1,10 @@
 """The tile schedule changes no bit of the results.
 
-Forward and backward outputs must be bitwise the same whether the expert GEMMs run 256-row
-tiles on CTA pairs (with each expert's odd last tile on single CTAs) or 128-row tiles on
-single CTAs only (MOE_GEMM_PAIR=0), and the forward variant that gathers GEMM1's rows from x
-and fuses the combine into GEMM2 must match the default forward bitwise.  Each schedule runs
+Forward and backward outputs (SwiGLU and squared-ReLU experts) must be bitwise the same
+whether the expert GEMMs run 256-row tiles on CTA pairs (with each expert's odd last tile on
+single CTAs) or 128-row tiles on single CTAs only (MOE_GEMM_PAIR=0), and the forward variant
+that gathers GEMM1's rows from x and fuses the combine into GEMM2 must match the default
+forward bitwise.  Each schedule runs
 in its own process (the switch is read once per process).
 """
 import hashlib
@@ -25,17 +26,18 @@ import torch
 import moe_synth
 import combine_fp32_router_gb300 as moe
 from moe_harness import forward, backward, to_dev
-w = moe_synth.custom(T=3000, d=512, E=64, k=4, dff=384, seed=77, zipf_s=1.2)
+w = moe_synth.custom(T=3000, d=512, E=64, k=4, dff=%(dff)d, seed=77, zipf_s=1.2,
+                     gated=%(gated)s)
 inp = moe_synth.generate(w, with_dy=True)
 g = to_dev(inp)
 h = hashlib.sha256()
 out, ws = forward(moe, g, w.k, save=True)
 res = backward(moe, g, w.k, ws)
 assert moe.moe_get_error(ws) == 0
-for t in [out] + [res[k] for k in sorted(res)]:
+for t in [out] + [res[k] for k in sorted(res) if res[k] is not None]:
     h.update(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())
 o2 = torch.empty_like(out)
-moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], w.k, o2, ws,
+moe.moe_forward(g["x"], g["logits"], g["W1"], g.get("W3"), g["W2"], w.k, o2, ws,
                 flags=moe.MOE_FWD_GATHER_ROWS | moe.MOE_FWD_FUSED_COMBINE)
 assert moe.moe_get_error(ws) == 0
 assert torch.equal(o2.view(torch.int16), out.view(torch.int16))
@@ -43,15 +45,17 @@ print(h.hexdigest())
 """
 
 
-def _digest(env_extra):
+def _digest(env_extra, gated=True):
     env = dict(os.environ)
     env.update(env_extra)
-    r = subprocess.run([sys.executable, "-c", _SCRIPT % {"root": ROOT}], env=env,
+    script = _SCRIPT % {"root": ROOT, "gated": gated, "dff": 384 if gated else 512}
+    r = subprocess.run([sys.executable, "-c", script], env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
     return r.stdout.strip().splitlines()[-1]
 
 
-def test_schedule_does_not_change_results():
-    ref = _digest({})
-    assert _digest({"MOE_GEMM_PAIR": "0"}) == ref
+@pytest.mark.parametrize("gated", [True, False])   # SwiGLU, squared ReLU (no W3)
+def test_schedule_does_not_change_results(gated):
+    ref = _digest({}, gated)
+    assert _digest({"MOE_GEMM_PAIR": "0"}, gated) == ref
