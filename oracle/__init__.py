@@ -33,6 +33,11 @@ def _load():
         lib.oracle_round_bf16.restype = ctypes.c_double
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.oracle_route.argtypes = [_p, _i64, _int, _int, _p, _p]
+        lib.oracle_round_e4m3.restype = ctypes.c_double
+        lib.oracle_round_e4m3.argtypes = [ctypes.c_double]
+        lib.oracle_quantize_rows_e4m3.argtypes = [_p, _i64, _int, _p, _p]
+        lib.oracle_quantize_cols_e4m3.argtypes = [_p, _int, _int, _int, _p, _p]
+        lib.oracle_forward_tokens_fp8.argtypes = [_p] * 5 + dims + [_int, _p, _i64, _p]
         lib.oracle_dispatch.argtypes = [_p, _i64, _int, _int, _p, _p, _p, _p]
         for n in ("oracle_forward_tokens_bf16", "oracle_forward_tokens_f64"):
             getattr(lib, n).argtypes = [_p] * 5 + dims + [_int, _p, _i64, _p]
@@ -65,6 +70,47 @@ def num_threads() -> int:
 def round_bf16(v: float) -> float:
     """Nearest bf16 value of ``v`` (ties to even), as a float."""
     return _load().oracle_round_bf16(float(v))
+
+
+def round_e4m3(v: float) -> float:
+    """Nearest FP8 E4M3 value of ``v`` (ties to even, saturating at 448), as a float."""
+    return _load().oracle_round_e4m3(float(v))
+
+
+def quantize_rows_e4m3(x):
+    """Per-row E4M3 quantization of bf16 rows x [T, d] (raw uint16): returns the dequantized
+    values q*s [T, d] (float64) and the row scales s [T] (fp32 values as float64)."""
+    x = _c(x, np.uint16)
+    T, d = x.shape
+    xq = np.empty((T, d), np.float64)
+    s = np.empty(T, np.float64)
+    _check(_load().oracle_quantize_rows_e4m3(_ptr(x), T, d, _ptr(xq), _ptr(s)))
+    return xq, s
+
+
+def quantize_cols_e4m3(W):
+    """Per-(expert, column) E4M3 quantization of bf16 weights W [E, K, N] (raw uint16) over
+    K: returns the E4M3 values q [E, K, N] (float64) and the scales s [E, N]."""
+    W = _c(W, np.uint16)
+    E, K, N = W.shape
+    q = np.empty((E, K, N), np.float64)
+    s = np.empty((E, N), np.float64)
+    _check(_load().oracle_quantize_cols_e4m3(_ptr(W), E, K, N, _ptr(q), _ptr(s)))
+    return q, s
+
+
+def forward_tokens_fp8(inp, k, tokens=None, round_h=True):
+    """Forward with the FP8 dispatch payload (rows and W1 / W3 quantized to E4M3 with fp32
+    scales, then the SwiGLU expert on the dequantized values), bf16 inputs.  Returns [n, d]."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    x, W1, W3, W2 = (_prep(a, "bf16") for a in (x, W1, W3, W2))
+    tok = None if tokens is None else _c(tokens, np.int64)
+    n = T if tok is None else len(tok)
+    y = np.empty((n, d), np.float64)
+    _check(_load().oracle_forward_tokens_fp8(_ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2),
+                                             T, d, E, k, dff, int(round_h), _ptr(tok), n,
+                                             _ptr(y)))
+    return y
 
 
 def _logits64(logits):

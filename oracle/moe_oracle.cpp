@@ -12,6 +12,8 @@
 //  * DeepSeek-V4 report, Thai translation (itsolotime.com), section 1.4 "observations and
 //    suggestions": each token-expert pair costs 6hd FLOP covering the SwiGLU gate
 //    projection, the up projection and the down projection; the combine payload is BF16.
+//  * The same page, section 1.4, bullet on the compute-to-bandwidth ratio: the dispatch
+//    payload is FP8 (the combine payload BF16).
 //  * The same page, section 1.4, bullet on the activation function: a cheap element-wise
 //    activation without exponentials or divisions in place of SwiGLU, with the gating
 //    projection removed (the parameter budget then allows a wider intermediate).
@@ -27,6 +29,12 @@
 //  * cheap activation (no W3 given): h = relu(x W1)^2, squared ReLU, an element-wise function
 //    with neither exponential nor division; h rounded to bf16 as above.
 //  * combine: y_t = sum_j g_j * o_j, here in fp64.
+//  * FP8 dispatch: each token row is sent as FP8 E4M3 values with one fp32 scale per row,
+//    s_t = amax_c |x_tc| / 448 (448 = the largest E4M3 value; s_t = 1 for an all-zero row),
+//    q = e4m3(x / s_t) with x / s_t an fp32 division and e4m3() rounding to nearest even
+//    with saturation at 448.  The first projections use weights in the same format with one
+//    scale per (expert, output column), taken over the input dimension.  The expert then
+//    runs on the dequantized values q s, exactly as on bf16 inputs.
 //  * backward: the derivative of the bf16 rounding of h is taken as 1; with round_grad the
 //    matrix-product operands dO = g dy, da and db are rounded to bf16 (round to nearest
 //    even) like h, each product accumulating exactly (fp64).
@@ -71,6 +79,36 @@ double round_bf16(double v) {
 }
 
 double sigmoid(double a) { return 1.0 / (1.0 + std::exp(-a)); }
+
+// Nearest FP8 E4M3 value to v (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+// infinities): ties to even; magnitudes above 448, the largest finite value, saturate to it.
+double round_e4m3(double v) {
+  if (v == 0.0 || std::isnan(v)) return v;
+  const double a = std::fabs(v);
+  double r;
+  if (a < std::ldexp(1.0, -6)) {
+    // subnormal range: multiples of 2^-9
+    r = std::ldexp(std::nearbyint(std::ldexp(a, 9)), -9);
+  } else {
+    int ex;
+    const double m = std::frexp(a, &ex);  // a = m 2^ex, m in [0.5, 1)
+    r = std::ldexp(std::nearbyint(std::ldexp(m, 4)), ex - 4);  // 4 significant bits
+  }
+  if (r > 448.0) r = 448.0;
+  return v < 0 ? -r : r;
+}
+
+// fp32 scale of a block whose largest magnitude is amax (an fp32 value): amax / 448 as an
+// fp32 division (the double quotient rounded once to float is the correctly rounded fp32
+// quotient), 1 for an all-zero block.
+double e4m3_scale(double amax) {
+  if (amax == 0.0) return 1.0;
+  return static_cast<double>(static_cast<float>(amax / 448.0));
+}
+// x quantized with scale s: e4m3 of the fp32 quotient x / s
+double e4m3_quant(double x, double s) {
+  return round_e4m3(static_cast<double>(static_cast<float>(x / s)));
+}
 
 // Router for one token.  Experts are ordered by (logit descending, index ascending) and
 // the first k are kept; the gate is the softmax over those k logits.
@@ -401,6 +439,89 @@ int backward_dw(const V* x, const double* logits, const V* W1, const V* W3, cons
   return 0;
 }
 
+// ---------------------------------------------------------------------- FP8 dispatch
+// Per-row E4M3 quantization of x [T][d] (bf16 bits): dequantized values q s into xq, the
+// scales into s.
+void quantize_rows(const uint16_t* x, int64_t T, int d, double* xq, double* s) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    double amax = 0.0;
+    for (int c = 0; c < d; ++c) amax = std::fmax(amax, std::fabs(widen(x[t * d + c])));
+    const double st = e4m3_scale(amax);
+    s[t] = st;
+    if (xq)
+      for (int c = 0; c < d; ++c) xq[t * d + c] = e4m3_quant(widen(x[t * d + c]), st) * st;
+  }
+}
+
+// Per-column E4M3 scales of W [E][K][N] (bf16 bits), over K: s [E][N].
+void column_scales(const uint16_t* W, int E, int K, int N, double* s) {
+#pragma omp parallel for schedule(static)
+  for (int64_t en = 0; en < static_cast<int64_t>(E) * N; ++en) {
+    const int64_t e = en / N, n = en % N;
+    double amax = 0.0;
+    for (int c = 0; c < K; ++c)
+      amax = std::fmax(amax, std::fabs(widen(W[(e * K + c) * N + n])));
+    s[en] = e4m3_scale(amax);
+  }
+}
+
+// Forward with the FP8 dispatch payload: each token's row and the first projections' weights
+// quantized as above (weights quantized where they are used), SwiGLU, bf16 h, bf16 W2.
+int forward_tokens_fp8(const uint16_t* x, const double* logits, const uint16_t* W1,
+                       const uint16_t* W3, const uint16_t* W2, const Dims& D, int round_h,
+                       const int64_t* tokens, int64_t n, double* y) {
+  std::vector<double> s1(static_cast<size_t>(D.E) * D.dff), s3(s1.size());
+  column_scales(W1, D.E, D.d, D.dff, s1.data());
+  column_scales(W3, D.E, D.d, D.dff, s3.data());
+  int bad = 0;
+#pragma omp parallel
+  {
+    std::vector<int32_t> idx(D.k);
+    std::vector<double> gate(D.k), xq(D.d), a(D.dff), b(D.dff), h(D.dff), o(D.d);
+    double st;
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t t = tokens ? tokens[i] : i;
+      if (t < 0 || t >= D.T) {
+#pragma omp atomic write
+        bad = 1;
+        continue;
+      }
+      quantize_rows(x + t * D.d, 1, D.d, xq.data(), &st);
+      route_token(logits + t * D.E, D.E, D.k, idx.data(), gate.data());
+      double* yt = y + i * D.d;
+      for (int c = 0; c < D.d; ++c) yt[c] = 0.0;
+      for (int j = 0; j < D.k; ++j) {
+        const int e = idx[j];
+        const uint16_t* w1 = w13(W1, D, e);
+        const uint16_t* w3 = w13(W3, D, e);
+        const double* s1e = s1.data() + static_cast<int64_t>(e) * D.dff;
+        const double* s3e = s3.data() + static_cast<int64_t>(e) * D.dff;
+        for (int f = 0; f < D.dff; ++f) { a[f] = 0.0; b[f] = 0.0; }
+        for (int c = 0; c < D.d; ++c) {
+          const uint16_t* r1 = w1 + static_cast<int64_t>(c) * D.dff;
+          const uint16_t* r3 = w3 + static_cast<int64_t>(c) * D.dff;
+          for (int f = 0; f < D.dff; ++f) {
+            a[f] += xq[c] * (e4m3_quant(widen(r1[f]), s1e[f]) * s1e[f]);
+            b[f] += xq[c] * (e4m3_quant(widen(r3[f]), s3e[f]) * s3e[f]);
+          }
+        }
+        for (int f = 0; f < D.dff; ++f) {
+          const double hv = a[f] / (1.0 + std::exp(-a[f])) * b[f];
+          h[f] = round_h ? round_bf16(hv) : hv;
+        }
+        const uint16_t* w2 = w2of(W2, D, e);
+        for (int c = 0; c < D.d; ++c) o[c] = 0.0;
+        for (int f = 0; f < D.dff; ++f)
+          for (int c = 0; c < D.d; ++c) o[c] += h[f] * widen(w2[static_cast<int64_t>(f) * D.d + c]);
+        for (int c = 0; c < D.d; ++c) yt[c] += gate[j] * o[c];
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -408,6 +529,28 @@ extern "C" {
 int oracle_num_threads(void) { return omp_get_max_threads(); }
 
 double oracle_round_bf16(double v) { return round_bf16(v); }
+
+double oracle_round_e4m3(double v) { return round_e4m3(v); }
+
+// Row quantization of x [T][d] (bf16 bits): dequantized values (or NULL) and row scales.
+int oracle_quantize_rows_e4m3(const uint16_t* x, int64_t T, int d, double* xq, double* s) {
+  if (T < 0 || d <= 0) return -1;
+  quantize_rows(x, T, d, xq, s);
+  return 0;
+}
+
+// Column quantization of W [E][K][N] (bf16 bits): E4M3 values (not dequantized) and the
+// per-(expert, column) scales.
+int oracle_quantize_cols_e4m3(const uint16_t* W, int E, int K, int N, double* q, double* s) {
+  if (E <= 0 || K <= 0 || N <= 0) return -1;
+  column_scales(W, E, K, N, s);
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < static_cast<int64_t>(E) * K * N; ++i) {
+    const int64_t e = i / (static_cast<int64_t>(K) * N), n = i % N;
+    q[i] = e4m3_quant(widen(W[i]), s[e * N + n]);
+  }
+  return 0;
+}
 
 int oracle_route(const double* logits, int64_t T, int E, int k, int32_t* idx, double* gate) {
   if (!dims_ok(T, 1, E, k, 1)) return -1;
@@ -485,6 +628,13 @@ int oracle_backward_dw_f64(const double* x, const double* logits, const double* 
   if (!dims_ok(T, d, E, k, dff)) return -1;
   return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, round_grad,
                      experts, n_exp, dW1, dW3, dW2);
+}
+
+int oracle_forward_tokens_fp8(const uint16_t* x, const double* logits, const uint16_t* W1,
+                              const uint16_t* W3, const uint16_t* W2, ORACLE_DIMS, int round_h,
+                              const int64_t* tokens, int64_t n, double* y) {
+  if (!dims_ok(T, d, E, k, dff) || !W3) return -1;
+  return forward_tokens_fp8(x, logits, W1, W3, W2, Dims{T, d, E, k, dff}, round_h, tokens, n, y);
 }
 
 }  // extern "C"

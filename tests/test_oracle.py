@@ -427,3 +427,85 @@ def test_layer_flops_without_the_gate_projection():
     assert oracle.layer_flops(1, 7168, 3072, gated=False) == 4 * 7168 * 3072
     # the same parameter budget (d_ff' = 1.5 d_ff) keeps the FLOP count
     assert oracle.layer_flops(5, 7168, 3072, gated=False) == oracle.layer_flops(5, 7168, 2048)
+
+
+# ------------------------------------------------------------------ FP8 dispatch payload
+
+
+def _torch_e4m3(v):
+    return torch.tensor(np.asarray(v, np.float32)).to(torch.float8_e4m3fn).to(torch.float64) \
+        .numpy()
+
+
+def test_round_e4m3_matches_torch_float8_cast():
+    rng = np.random.default_rng(51)
+    v = np.concatenate([
+        rng.uniform(-448, 448, 4000),
+        rng.uniform(-2.0 ** -5, 2.0 ** -5, 2000),             # subnormals and the normal edge
+        np.ldexp(rng.integers(-16, 17, 400) + 0.5, -9),        # exact subnormal ties
+        np.array([0.0, -0.0, 448.0, -448.0, 1.0625, 1.1875, 2.0 ** -6, 2.0 ** -10]),
+    ]).astype(np.float32).astype(np.float64)
+    got = np.array([oracle.round_e4m3(x) for x in v])
+    np.testing.assert_array_equal(got, _torch_e4m3(v))
+    # saturation above the largest finite value (torch's cast gives NaN there)
+    assert oracle.round_e4m3(1000.0) == 448.0 and oracle.round_e4m3(-470.0) == -448.0
+
+
+def test_quantize_rows_e4m3_matches_float32_division_and_torch_cast():
+    rng = np.random.default_rng(52)
+    x = rng.standard_normal((9, 64)) * np.exp(rng.uniform(-6, 6, (9, 1)))
+    x[3] = 0.0                                                  # all-zero row: scale 1
+    xb = _bf16_bits(x)
+    xq, s = oracle.quantize_rows_e4m3(xb)
+    X32 = _bits_to_f64(xb).astype(np.float32)
+    amax = np.abs(X32).max(axis=1)
+    s_ref = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    np.testing.assert_array_equal(s, s_ref.astype(np.float64))
+    q_ref = _torch_e4m3(X32 / s_ref[:, None])
+    np.testing.assert_array_equal(xq, q_ref * s_ref[:, None].astype(np.float64))
+    assert np.abs(q_ref).max() == 448.0                         # each row's amax maps to 448
+
+
+def test_quantize_cols_e4m3_matches_float32_division_and_torch_cast():
+    rng = np.random.default_rng(53)
+    W = rng.standard_normal((3, 40, 24)) / 6.0
+    Wb = _bf16_bits(W)
+    q, s = oracle.quantize_cols_e4m3(Wb)
+    W32 = _bits_to_f64(Wb).astype(np.float32)
+    s_ref = (np.abs(W32).max(axis=1) / np.float32(448.0)).astype(np.float32)   # [E, N]
+    np.testing.assert_array_equal(s, s_ref.astype(np.float64))
+    np.testing.assert_array_equal(q, _torch_e4m3(W32 / s_ref[:, None, :]))
+
+
+def test_fp8_forward_k1_single_expert_is_dense_mlp_on_dequantized_values():
+    rng = np.random.default_rng(54)
+    inp = _rand_inputs(rng, T=12, d=32, E=1, k=1, dff=40)
+    xq, _ = oracle.quantize_rows_e4m3(inp["x"])
+    q1, s1 = oracle.quantize_cols_e4m3(inp["W1"])
+    q3, s3 = oracle.quantize_cols_e4m3(inp["W3"])
+    W1 = q1[0] * s1[0][None, :]
+    W3 = q3[0] * s3[0][None, :]
+    W2 = _bits_to_f64(inp["W2"])[0]
+    h = _silu(xq @ W1) * (xq @ W3)
+    np.testing.assert_allclose(oracle.forward_tokens_fp8(inp, 1, round_h=False), h @ W2,
+                               rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(oracle.forward_tokens_fp8(inp, 1), _torch_bf16(h) @ W2,
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_fp8_forward_equals_bf16_forward_when_quantization_is_exact():
+    # rows and weight columns whose largest magnitude is 448 and whose values are E4M3
+    # numbers quantize to themselves (scale 1): the FP8 forward is then the bf16 forward
+    rng = np.random.default_rng(55)
+    T, d, E, k, dff = 8, 16, 4, 2, 24
+    grid = np.unique(_torch_e4m3(rng.uniform(-448, 448, 5000)))
+    def pick(shape):
+        v = rng.choice(grid, size=shape)
+        return v
+    x = pick((T, d)); x[:, 0] = 448.0
+    W1 = pick((E, d, dff)); W1[:, 0, :] = 448.0
+    W3 = pick((E, d, dff)); W3[:, 0, :] = -448.0
+    W2 = rng.standard_normal((E, dff, d)) / 100
+    inp = dict(x=_bf16_bits(x), logits=rng.standard_normal((T, E)).astype(np.float32),
+               W1=_bf16_bits(W1), W3=_bf16_bits(W3), W2=_bf16_bits(W2))
+    np.testing.assert_array_equal(oracle.forward_tokens_fp8(inp, k), oracle.forward_tokens(inp, k))
