@@ -410,6 +410,34 @@ def bench_native(args, w):
     if st != 0:
         raise RuntimeError("device error (graph replay): " + moe.moe_status_string(st))
 
+    # the same step with the FP8 dispatch payload (E4M3 rows and W1 / W3, quantized outside
+    # the timed region), with its stage times
+    fp8 = None
+    if "W3" in g:
+        W1q, s1 = moe.moe_quantize_weights_fp8(g["W1"])
+        W3q, s3 = moe.moe_quantize_weights_fp8(g["W3"])
+        n_fp8 = max(1, min(args.steps, 20))
+        evf = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n_fp8)]
+        for _ in range(2):
+            moe.moe_forward_fp8(g["x"], g["logits"], W1q, W3q, s1, s3, g["W2"], k, out, ws,
+                                stream=stream)
+        barrier()
+        start.record(stream)
+        for i in range(n_fp8):
+            moe.moe_forward_fp8(g["x"], g["logits"], W1q, W3q, s1, s3, g["W2"], k, out, ws,
+                                stage_events=evf[i], stream=stream)
+        stop.record(stream)
+        barrier()
+        st = moe.moe_get_error(ws)
+        if st != 0:
+            raise RuntimeError("device error (fp8 forward): " + moe.moe_status_string(st))
+        f_ms = start.elapsed_time(stop) / n_fp8
+        f_st = [sum(e[j].elapsed_time(e[j + 1]) for e in evf) / n_fp8 for j in range(nev - 1)]
+        fp8 = {"ms_per_step": f_ms, "tokens_per_s": world * T / (f_ms * 1e-3),
+               "stages_ms": dict(zip(["dispatch", "gemm1_swiglu_fp8", "gemm2", "combine"], f_st)),
+               "gemm1_tflops": 4 * d * dff * T * k / (f_st[1] * 1e-3) / 1e12}
+        del W1q, W3q, s1, s3
+
     # the overlapped-wave variant (GEMM1 gathers rows from x, GEMM2 fuses the combine),
     # timed for comparison; bitwise the same output
     wave_flags = moe.MOE_FWD_GATHER_ROWS | moe.MOE_FWD_FUSED_COMBINE
@@ -477,6 +505,7 @@ def bench_native(args, w):
         "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
         "waved_forward_ms_per_step": waved_ms,
         "graph_forward_ms_per_step": graph_ms,
+        "fp8_forward": fp8,
         "clocks": clocks.summary(),
         "gpu_launches": fwd_launches(T) * args.steps,
     }

@@ -33,7 +33,8 @@ MOE_BWD_NUM_EVENTS = 7
 
 # Exported symbols of include/moe.h, in declaration order.
 EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispatch",
-           "moe_forward", "moe_forward_graph_create", "moe_forward_graph_launch",
+           "moe_forward", "moe_forward_fp8", "moe_quantize_weights_fp8",
+           "moe_forward_graph_create", "moe_forward_graph_launch",
            "moe_forward_graph_destroy", "moe_forward_host", "moe_backward",
            "moe_route_dispatch_noalloc", "moe_get_error", "moe_set_wait_timeout_ns",
            "moe_debug_set_flags", "moe_status_string")
@@ -58,6 +59,10 @@ def _load():
     lib.moe_route_dispatch.argtypes = [p, p, i64, i, i, i] + [p] * 7 + [p, sz, p]
     lib.moe_route_dispatch.restype = i
     lib.moe_forward.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i, p, p]
+    lib.moe_quantize_weights_fp8.restype = i
+    lib.moe_quantize_weights_fp8.argtypes = [p, i, i, i, p, p, p]
+    lib.moe_forward_fp8.restype = i
+    lib.moe_forward_fp8.argtypes = [p] * 7 + [i64, i, i, i, i, p, p, sz, p, p]
     lib.moe_forward_graph_create.restype = i
     lib.moe_forward_graph_create.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i,
                                                        ctypes.POINTER(ctypes.c_void_p)]
@@ -150,6 +155,28 @@ def moe_forward(x, logits, W1, W3, W2, k, out, ws, flags=0, stage_events=None, s
     _check(_lib.moe_forward(_ptr(x), _ptr(logits), _ptr(W1), _ptr(W3), _ptr(W2), T, d, E, k,
                             d_ff, _ptr(out), _ptr(ws), _nbytes(ws), int(flags),
                             _events(stage_events), _stream(stream)), "moe_forward")
+
+
+def moe_quantize_weights_fp8(W, stream=None):
+    """E4M3 copy of expert weights W [E, K, N] bf16 for moe_forward_fp8: returns
+    (Wq [E, N, K] uint8, scales [E, N] fp32) (one scale per output column)."""
+    E, K, N = W.shape
+    Wq = torch.empty(E, N, K, dtype=torch.uint8, device=W.device)
+    sc = torch.empty(E, N, dtype=torch.float32, device=W.device)
+    _check(_lib.moe_quantize_weights_fp8(_ptr(W), E, K, N, _ptr(Wq), _ptr(sc), _stream(stream)),
+           "moe_quantize_weights_fp8")
+    return Wq, sc
+
+
+def moe_forward_fp8(x, logits, W1q, W3q, w1_scale, w3_scale, W2, k, out, ws, stage_events=None,
+                    stream=None):
+    """Whole-layer forward with the FP8 dispatch payload (E4M3 rows and W1 / W3)."""
+    T, d = x.shape
+    E, d_ff, _ = W1q.shape
+    _check(_lib.moe_forward_fp8(_ptr(x), _ptr(logits), _ptr(W1q), _ptr(W3q), _ptr(w1_scale),
+                                _ptr(w3_scale), _ptr(W2), T, d, E, k, d_ff, _ptr(out), _ptr(ws),
+                                _nbytes(ws), _events(stage_events), _stream(stream)),
+           "moe_forward_fp8")
 
 
 class ForwardGraph:

@@ -37,13 +37,15 @@ enum GemmKind : int {
   kDx = 3,    // dXp = [dA|dB] [W1|W3]^T (fp32)                            (rows x d)
   kDw2 = 4,   // dW2[e] = H^T dO (fp32)                                    (dff x d)
   kDw13 = 5,  // [dW1|dW3][e] = Xp^T [dA|dB] (fp32)                         (d x 2dff)
+  kFwd1F8 = 6,  // GEMM1 + SwiGLU on the FP8 payload: Xp and W1 / W3 in E4M3 (K-major), the
+                // row and column scales applied in the epilogue                (rows x dff)
 };
 
 template <int KIND>
 struct KindTraits {
-  static constexpr bool kRowsM = (KIND <= kDx);      // M = permuted rows, K fixed
-  static constexpr int kAmn = (KIND >= kDw2) ? 1 : 0;  // A operand MN-major?
-  static constexpr int kBmn = (KIND == kDh || KIND == kDx) ? 0 : 1;
+  static constexpr bool kRowsM = (KIND <= kDx || KIND == kFwd1F8);  // M = permuted rows
+  static constexpr int kAmn = (KIND == kDw2 || KIND == kDw13) ? 1 : 0;  // A MN-major?
+  static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8) ? 0 : 1;
 };
 
 struct GemmParams {
@@ -51,6 +53,10 @@ struct GemmParams {
   // projection): GEMM1 tiles then hold 256 columns of A = Xp W1, dH gives dA only, dX and
   // dW1 take K = N = d_ff
   int gated;
+  // FP8 GEMM1: per-token row scales [T] and per-(expert, column) weight scales [E, dff]
+  const float* xscale;
+  const float* wscale1;
+  const float* wscale3;
   // fp32 output tiles written by TMA stores (32 x 32 boxes, 128-byte swizzle) when tma_store:
   // c0 = out0, c1 = out1
   CUtensorMap mapC0, mapC1;
@@ -341,8 +347,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
   const bool valid = r < ti.nvalid;
   const int w0 = q * 32;  // first row of this warp
   auto clamp_rows = [&](int n) { return n - w0 < 0 ? 0 : (n - w0 > 32 ? 32 : n - w0); };
-  if constexpr (KIND == kFwd1) {
-    if (!p.gated) {
+  if constexpr (KIND == kFwd1 || KIND == kFwd1F8) {
+    if (KIND == kFwd1 && !p.gated) {
       // h = relu(a)^2 over the tile's 256 accumulator columns (h columns n0 ..)
       const int64_t row0 = ti.row0 + w0;
       char* H = reinterpret_cast<char*>(static_cast<uint16_t*>(p.out0) + row0 * p.dff + ti.n0);
@@ -371,11 +377,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     char* H = reinterpret_cast<char*>(static_cast<uint16_t*>(p.out0) + row0 * p.dff + c0);
     const int nstore = clamp_rows(ti.nseg);      // pad rows are written as zeros
     const int nsave = clamp_rows(ti.nvalid);
+    float rscale = 1.0f;  // FP8: the row's (token's) scale
+    if (KIND == kFwd1F8 && valid) rscale = p.xscale[p.perm[ti.row0 + r] / p.k];
 #pragma unroll 1
     for (int ch = 0; ch < HALF / 32; ++ch) {
       float a[32], b[32], h[32];
       tmem_ld32(tacc + ch * 32, a);
       tmem_ld32(tacc + HALF + ch * 32, b);
+      if constexpr (KIND == kFwd1F8) {
+        // dequantize: A = (sum of E4M3 products) * row scale * column scale
+        const float* s1 = p.wscale1 + static_cast<int64_t>(ti.e) * p.dff + c0 + ch * 32;
+        const float* s3 = p.wscale3 + static_cast<int64_t>(ti.e) * p.dff + c0 + ch * 32;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          a[i] *= rscale * __ldg(s1 + i);
+          b[i] *= rscale * __ldg(s3 + i);
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 32; ++i) h[i] = valid ? silu_f(a[i]) * b[i] : 0.0f;
       store_chunk<true>(buf, h, H + ch * 64, 2ll * p.dff, nstore, lane);
@@ -550,7 +568,9 @@ __global__ void __launch_bounds__(256, 1)
   using Tr = KindTraits<KIND>;
   constexpr int S = Cfg::kStages;
   constexpr int BL = Cfg::kBLocal;  // B columns held by this CTA
-  constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN, Tr::kAmn, Tr::kBmn);
+  constexpr uint32_t IDESC = KIND == kFwd1F8
+                                 ? idesc_e4m3_f32(PAIR ? 2 * kBM : kBM, BN)
+                                 : idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN, Tr::kAmn, Tr::kBmn);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -706,6 +726,18 @@ __global__ void __launch_bounds__(256, 1)
               load_h(kL2HintB, sb + 8192u * (BN / 128 + i), &mapB1, fb, h0 + 64 * i, wrow);
             }
           }
+        } else if constexpr (KIND == kFwd1F8) {
+          // 128 K elements (bytes) per stage: A rows and the W1 / W3 rows (output columns) of
+          // the transposed E4M3 weights, all K-major
+          const int kb8 = kb * 128;
+          const int wrow = ti.e * p.dff + ti.n0 / 2;
+          load_h(kL2HintA, sa, &mapA, fb, kb8, ti.row0);
+          if constexpr (PAIR) {
+            load_h(kL2HintB, sb, rank == 0 ? &mapB0 : &mapB1, fb, kb8, wrow);
+          } else {
+            load_h(kL2HintB, sb, &mapB0, fb, kb8, wrow);
+            load_h(kL2HintB, sb + 16384u, &mapB1, fb, kb8, wrow);
+          }
         } else if constexpr (KIND == kFwd2) {
           load_h(kL2HintA, sa, &mapA, fb, k0, ti.row0);
 #pragma unroll
@@ -805,8 +837,16 @@ __global__ void __launch_bounds__(256, 1)
                                        : smem_desc_sw128(sa + kk * 32u, 16u, 1024u);
           const uint64_t bd = Tr::kBmn ? smem_desc_sw128(sb + kk * 2048u, 8192u, 1024u)
                                        : smem_desc_sw128(sb + kk * 32u, 16u, 1024u);
-          if constexpr (PAIR) umma_f16_pair(dtm, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-          else umma_f16(dtm, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          // bf16: K = 16 per instruction (32 bytes); E4M3: K = 32 (32 bytes), so the same
+          // 32-byte descriptor step covers both
+          const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+          if constexpr (KIND == kFwd1F8) {
+            if constexpr (PAIR) umma_f8_pair(dtm, ad, bd, IDESC, accum);
+            else umma_f8(dtm, ad, bd, IDESC, accum);
+          } else {
+            if constexpr (PAIR) umma_f16_pair(dtm, ad, bd, IDESC, accum);
+            else umma_f16(dtm, ad, bd, IDESC, accum);
+          }
         }
         if constexpr (PAIR) umma_commit_pair(empty_bar(s), 3);
         else umma_commit(empty_bar(s));

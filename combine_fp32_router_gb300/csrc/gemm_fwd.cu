@@ -46,6 +46,32 @@ CUtensorMap make_map_2d(const void* base, uint64_t inner, uint64_t rows, uint64_
   return m;
 }
 
+// 2-D byte (E4M3) tensor map with 128-byte swizzle: boxes of 128 bytes x box_rows rows.
+CUtensorMap make_map_2d_u8(const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                           uint32_t box_rows, cudaError_t* st) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof m);
+  auto enc = reinterpret_cast<Encode>(tensor_map_encoder());
+  if (!enc) {
+    *st = cudaErrorNotSupported;
+    return m;
+  }
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) *st = cudaErrorInvalidValue;
+  return m;
+}
+
 // 2-D fp32 tensor map for TMA stores of 32 x 32 boxes with 128-byte swizzle.
 CUtensorMap make_store_map_f32(void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                                cudaError_t* st) {
@@ -128,6 +154,29 @@ cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
   p.k = L.k;
   return run_rows_kind<kFwd1, 256>(c.pair, a, b0, b1, b0, b1, p, leftover_params(p, c), L.max_mt,
                                    L.E, c.num_sms, s);
+}
+
+cudaError_t launch_gemm_fwd1_fp8(const GemmCtx& c, cudaStream_t s) {
+  const WsLayout& L = *c.L;
+  cudaError_t st = cudaSuccess;
+  // A = E4M3 permuted rows [P_pad][d] bytes; B = E4M3 W1 / W3 transposed, [E * dff][d] bytes
+  // (one row per output column, K-major); 128 x 128-byte boxes for pairs and single CTAs
+  const CUtensorMap a = make_map_2d_u8(c.ws + L.xperm, L.d, L.P_pad, L.d, 128, &st);
+  const uint64_t wrows = static_cast<uint64_t>(L.E) * L.dff;
+  const CUtensorMap b0 = make_map_2d_u8(c.W1q, L.d, wrows, L.d, 128, &st);
+  const CUtensorMap b1 = make_map_2d_u8(c.W3q, L.d, wrows, L.d, 128, &st);
+  if (st != cudaSuccess) return st;
+  GemmParams p = base_params(c);
+  p.nb = L.dff / 128;  // 128 h columns per tile (W1 half + W3 half)
+  p.nkb = L.d / 128;   // 128 K elements per stage
+  p.out0 = c.ws + L.H;
+  p.perm = reinterpret_cast<const int32_t*>(c.ws + L.perm);
+  p.k = L.k;
+  p.xscale = reinterpret_cast<const float*>(c.ws + L.xscale);
+  p.wscale1 = c.wscale1;
+  p.wscale3 = c.wscale3;
+  return run_rows_kind<kFwd1F8, 256>(c.pair, a, b0, b1, b0, b1, p, leftover_params(p, c),
+                                     L.max_mt, L.E, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {

@@ -24,7 +24,7 @@ struct WsLayout {
          mt_expert = 0, mt_row0 = 0, n_pt = 0, pt_expert = 0, pt_row0 = 0, n_lo = 0,
          lo_expert = 0, lo_row0 = 0, topk = 0, gate = 0,
          pos = 0, perm = 0, xperm = 0, H = 0, Y = 0, Asave = 0, Bsave = 0, dO = 0, dAB = 0,
-         dXp = 0, seg = 0;
+         dXp = 0, seg = 0, xscale = 0;
   size_t route_total = 0, fwd_total = 0, bwd_total = 0;
 };
 
@@ -51,6 +51,14 @@ cudaError_t launch_scatter(const uint16_t* x, int64_t T, int d, int E, int k,
                            const int32_t* topk, const int32_t* bbase, const int32_t* poff,
                            int32_t* pos, int32_t* perm, uint16_t* x_perm, int64_t rows_cap,
                            DevErr* err, cudaStream_t s);
+// The stable permute with the FP8 payload: E4M3 rows (d bytes) and a row scale per token.
+cudaError_t launch_scatter_fp8(const uint16_t* x, int64_t T, int d, int E, int k,
+                               const int32_t* topk, const int32_t* bbase, const int32_t* poff,
+                               int32_t* pos, int32_t* perm, uint8_t* x_perm, float* xscale,
+                               int64_t rows_cap, DevErr* err, cudaStream_t s);
+// E4M3 weights, transposed to [E][N][K], with per-(expert, column) scales [E][N].
+cudaError_t launch_quantize_weights_fp8(const uint16_t* W, int E, int K, int N, uint8_t* Wq,
+                                        float* scales, cudaStream_t s);
 // Padding rows of every expert segment: perm = -1 and (if rows != null) zero bytes.
 cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, int32_t* perm,
                             void* rows, int64_t row_bytes, cudaStream_t s);
@@ -80,8 +88,12 @@ struct GemmCtx {
   bool gather_x;         // GEMM1 gathers its A rows from x (no x_perm)
   uint16_t* out;         // layer output [T, d] (fused combine)
   bool gated;            // SwiGLU (W1, W3); false: squared ReLU on W1 alone
+  // FP8 GEMM1: transposed E4M3 weights [E][dff][d] and their scales [E][dff]
+  const uint8_t *W1q, *W3q;
+  const float *wscale1, *wscale3;
 };
 cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s);   // H = SwiGLU(Xp W1, Xp W3)
+cudaError_t launch_gemm_fwd1_fp8(const GemmCtx& c, cudaStream_t s);  // H from E4M3 Xp, W1, W3
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s);   // Y = H W2
 cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s);     // dA,dB from dO W2^T
 cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s);     // dXp = dA W1^T + dB W3^T

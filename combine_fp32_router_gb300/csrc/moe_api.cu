@@ -122,6 +122,7 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   L.H = take(Pp * dff * 2);
   L.Y = take(Pp * d * 4);
   L.seg = take(P / (k > 0 ? k : 1) * static_cast<size_t>(d / 128) * 4);  // [T, d/128] counters
+  L.xscale = take(static_cast<size_t>(T) * 4);  // FP8 payload: one scale per token
   L.fwd_total = off;
   L.Asave = take(Pp * dff * 4);
   L.Bsave = take(Pp * dff * 4);
@@ -297,6 +298,96 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
     record(stage_events, 4, stream);
     return MOE_OK;
   }
+  MOE_TRY(launch_gemm_fwd2(c, stream));
+  record(stage_events, 3, stream);
+  MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,
+                         stream));
+  record(stage_events, 4, stream);
+  return MOE_OK;
+}
+
+moe_status_t moe_quantize_weights_fp8(const moe_bf16_t* W, int E, int K, int N, uint8_t* Wq,
+                                      float* scales, cudaStream_t stream) {
+  if (E < 1 || K < 1 || N < 1 || K % 128 != 0 || N % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!W || !Wq || !scales || !aligned16(W) || !aligned16(Wq) || !aligned16(scales))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(launch_quantize_weights_fp8(W, E, K, N, Wq, scales, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uint8_t* W1q,
+                             const uint8_t* W3q, const float* w1_scale, const float* w3_scale,
+                             const moe_bf16_t* W2, int64_t T, int d, int E, int k, int d_ff,
+                             moe_bf16_t* out, void* ws, size_t ws_bytes,
+                             cudaEvent_t* stage_events, cudaStream_t stream) {
+  moe_status_t st = check_dims(T, d, E, k, d_ff, true);
+  if (st != MOE_OK) return st;
+  if (!W1q || !W3q || !w1_scale || !w3_scale || !W2 || !ws) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, logits, W1q, W3q, w1_scale, w3_scale, W2, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_layout(T, d, E, k, d_ff);
+  if (ws_bytes < L.fwd_total) return MOE_ERR_WORKSPACE;
+
+  char* w = static_cast<char*>(ws);
+  DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
+  record(stage_events, 0, stream);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
+  if (T == 0) {
+    for (int i = 1; i < MOE_FWD_NUM_EVENTS; ++i) record(stage_events, i, stream);
+    return MOE_OK;
+  }
+  int32_t* hist = reinterpret_cast<int32_t*>(w + L.hist);
+  int32_t* bbase = reinterpret_cast<int32_t*>(w + L.bbase);
+  int32_t* counts = reinterpret_cast<int32_t*>(w + L.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  int32_t* poff = reinterpret_cast<int32_t*>(w + L.poff);
+  int32_t* topk = reinterpret_cast<int32_t*>(w + L.topk);
+  float* gate = reinterpret_cast<float*>(w + L.gate);
+  int32_t* pos = reinterpret_cast<int32_t*>(w + L.pos);
+  int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
+
+  // dispatch with the FP8 payload: route, count, prefix sums, E4M3 rows + row scales
+  MOE_TRY(launch_route_topk(logits, T, E, k, topk, gate, pos, hist, err, stream));
+  MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
+  TileTables tt;
+  tt.n_mt = reinterpret_cast<int32_t*>(w + L.n_mt);
+  tt.mt_expert = reinterpret_cast<int32_t*>(w + L.mt_expert);
+  tt.mt_row0 = reinterpret_cast<int32_t*>(w + L.mt_row0);
+  tt.n_pt = reinterpret_cast<int32_t*>(w + L.n_pt);
+  tt.pt_expert = reinterpret_cast<int32_t*>(w + L.pt_expert);
+  tt.pt_row0 = reinterpret_cast<int32_t*>(w + L.pt_row0);
+  tt.n_lo = reinterpret_cast<int32_t*>(w + L.n_lo);
+  tt.lo_expert = reinterpret_cast<int32_t*>(w + L.lo_expert);
+  tt.lo_row0 = reinterpret_cast<int32_t*>(w + L.lo_row0);
+  tt.max_mt = L.max_mt;
+  MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
+  MOE_TRY(launch_scatter_fp8(x, T, d, E, k, topk, bbase, poff, pos, perm,
+                             reinterpret_cast<uint8_t*>(w + L.xperm),
+                             reinterpret_cast<float*>(w + L.xscale), L.P_pad, err, stream));
+  MOE_TRY(launch_pad_rows(counts, poff, E, perm, nullptr, 0, stream));
+  record(stage_events, 1, stream);
+
+  GemmCtx c{};
+  c.L = &L;
+  c.ws = w;
+  c.x = x;
+  c.W2 = W2;
+  c.W1q = W1q;
+  c.W3q = W3q;
+  c.wscale1 = w1_scale;
+  c.wscale3 = w3_scale;
+  c.err = err;
+  c.wait_ns = g_wait_ns.load();
+  c.debug_flags = g_debug_flags.load();
+  c.num_sms = num_sms_of_current_device();
+  c.pair = use_pairs() && T > kTileRows;
+  c.gated = true;
+  c.out = out;
+  MOE_TRY(launch_gemm_fwd1_fp8(c, stream));
+  record(stage_events, 2, stream);
   MOE_TRY(launch_gemm_fwd2(c, stream));
   record(stage_events, 3, stream);
   MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,

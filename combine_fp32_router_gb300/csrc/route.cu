@@ -12,6 +12,8 @@
 #include <cfloat>
 #include <climits>
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -376,6 +378,128 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------ FP8 dispatch payload
+// E4M3 byte of v (round to nearest even, saturating at 448)
+__device__ __forceinline__ uint32_t e4m3_byte(float v) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+// E4M3 bytes of the 8 bf16 values in u, each divided by s (an fp32 division)
+__device__ __forceinline__ uint2 e4m3_pack8(uint4 u, float s) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    b[2 * i] = e4m3_byte(bf16lo(w[i]) / s);
+    b[2 * i + 1] = e4m3_byte(bf16hi(w[i]) / s);
+  }
+  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                    b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
+// Stable permute with the FP8 payload: as scatter_kernel, but the warp first takes the
+// token row's largest magnitude, stores the row scale s = amax / 448 (1 for a zero row) and
+// writes each permuted copy as E4M3 bytes of x / s (d bytes per row).
+__global__ void __launch_bounds__(256) scatter_fp8_kernel(const uint4* __restrict__ x, int64_t T,
+                                                          int d, int E, int k,
+                                                          const int32_t* __restrict__ topk,
+                                                          const int32_t* __restrict__ bbase,
+                                                          const int32_t* __restrict__ poff,
+                                                          int32_t* __restrict__ pos,
+                                                          int32_t* __restrict__ perm,
+                                                          uint8_t* __restrict__ x_perm,
+                                                          float* __restrict__ xscale,
+                                                          int64_t rows_cap, DevErr* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int n16 = d >> 3;  // 16-byte chunks of 8 bf16 per row
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += nwarps) {
+    int row = 0;
+    if (lane < k) {
+      const int64_t p = t * k + lane;
+      const int e = topk[p];
+      const int64_t b = t / kRouteTokensPerBlock;
+      row = poff[e] + bbase[b * E + e] + pos[p];
+      if (row < 0 || row >= rows_cap || e < 0 || e >= E) {
+        set_error(err, MOE_ERR_DEVICE_BOUNDS, 201);
+        row = -1;
+      } else {
+        pos[p] = row;
+        perm[row] = static_cast<int32_t>(p);
+      }
+    }
+    int rows[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
+    const uint4* src = x + t * n16;
+    float amax = 0.0f;
+    for (int c = lane; c < n16; c += 32) {
+      const uint4 u = ld_nc_v4(src + c);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16lo(w[i])), fabsf(bf16hi(w[i]))));
+    }
+    // the magnitudes are non-negative floats: their bit patterns order like the values
+    amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax)));
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    if (lane == 0) xscale[t] = s;
+    for (int c = lane; c < n16; c += 32) {
+      const uint2 q = e4m3_pack8(ld_nc_v4(src + c), s);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k && rows[j] >= 0)
+          *reinterpret_cast<uint2*>(x_perm + static_cast<int64_t>(rows[j]) * d + 8 * c) = q;
+    }
+  }
+}
+
+// E4M3 weights for the FP8 GEMM1: W [E][K][N] bf16 -> Wq [E][N][K] (transposed, so each
+// output column is a K-contiguous row) and scales [E][N], s = amax over K / 448 (1 for a
+// zero column), q = e4m3(w / s).  One CTA per (expert, 32 columns).
+__global__ void __launch_bounds__(256) quantize_weights_fp8_kernel(
+    const uint16_t* __restrict__ W, int K, int N, uint8_t* __restrict__ Wq,
+    float* __restrict__ scales) {
+  __shared__ float red[8][32];
+  __shared__ float sc[32];
+  __shared__ uint8_t tile[32][36];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int n0 = blockIdx.x * 32;
+  const int64_t e = blockIdx.y;
+  const uint16_t* We = W + e * K * static_cast<int64_t>(N);
+  float m = 0.0f;
+  for (int kk = w; kk < K; kk += 8)
+    m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(We[static_cast<int64_t>(kk) * N + n0 + lane]) << 16)));
+  red[w][lane] = m;
+  __syncthreads();
+  if (w == 0) {
+    float a = red[0][lane];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) a = fmaxf(a, red[i][lane]);
+    const float s = a > 0.0f ? a / 448.0f : 1.0f;
+    sc[lane] = s;
+    scales[e * N + n0 + lane] = s;
+  }
+  __syncthreads();
+  const float s = sc[lane];
+  uint8_t* out = Wq + (e * N + n0) * static_cast<int64_t>(K);
+  for (int k0 = 0; k0 < K; k0 += 32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int kk = k0 + w + 8 * i;
+      const float v = __uint_as_float(static_cast<uint32_t>(We[static_cast<int64_t>(kk) * N + n0 + lane]) << 16);
+      tile[w + 8 * i][lane] = static_cast<uint8_t>(e4m3_byte(v / s));
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int nn = w + 8 * i;
+      out[static_cast<int64_t>(nn) * K + k0 + lane] = tile[lane][nn];
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(256) pad_rows_kernel(const int32_t* __restrict__ counts,
                                                        const int32_t* __restrict__ poff,
                                                        int32_t* __restrict__ perm,
@@ -707,6 +831,23 @@ cudaError_t launch_scatter(const uint16_t* x, int64_t T, int d, int E, int k,
   scatter_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
       reinterpret_cast<const uint4*>(x), T, d, E, k, topk, bbase, poff, pos, perm,
       reinterpret_cast<uint4*>(x_perm), rows_cap, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_fp8(const uint16_t* x, int64_t T, int d, int E, int k,
+                               const int32_t* topk, const int32_t* bbase, const int32_t* poff,
+                               int32_t* pos, int32_t* perm, uint8_t* x_perm, float* xscale,
+                               int64_t rows_cap, DevErr* err, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  scatter_fp8_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(x), T, d, E, k, topk, bbase, poff, pos, perm, x_perm, xscale,
+      rows_cap, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weights_fp8(const uint16_t* W, int E, int K, int N, uint8_t* Wq,
+                                        float* scales, cudaStream_t s) {
+  quantize_weights_fp8_kernel<<<dim3(N / 32, E), 256, 0, s>>>(W, K, N, Wq, scales);
   return cudaGetLastError();
 }
 

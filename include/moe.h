@@ -136,6 +136,30 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
                          cudaEvent_t* stage_events, cudaStream_t stream);
 
 /*
+ * FP8 dispatch payload (report translation, section 1.4: FP8 dispatch, BF16 combine).  The
+ * readings of this library: each token row travels as E4M3 values with one fp32 scale per row,
+ * s_t = amax_c |x_tc| / 448 (1 for an all-zero row), q = e4m3(x / s_t) (fp32 division, round
+ * to nearest even, saturating at 448); the first projections use E4M3 weights with one fp32
+ * scale per (expert, output column) over the input dimension, in the same format.  GEMM1 runs
+ * on the tensor cores' FP8 path (tcgen05.mma kind::f8f6f4, fp32 accumulation) and applies the
+ * row and column scales in its epilogue; h, W2, GEMM2 and the combine are as in moe_forward.
+ * Forward only (no MOE_FWD_* flags).
+ *
+ * moe_quantize_weights_fp8: W [E,K,N] bf16 (device) -> Wq [E,N,K] E4M3 bytes (each output
+ * column a K-contiguous row) and scales [E,N] fp32.  K and N multiples of 128.
+ * moe_forward_fp8: x, logits, out and W2 as moe_forward; W1q, W3q [E,d_ff,d] and
+ * w1_scale, w3_scale [E,d_ff] from moe_quantize_weights_fp8 of W1 and W3; ws as for
+ * moe_forward without backward.
+ */
+moe_status_t moe_quantize_weights_fp8(const moe_bf16_t* W, int E, int K, int N, uint8_t* Wq,
+                                      float* scales, cudaStream_t stream);
+moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uint8_t* W1q,
+                             const uint8_t* W3q, const float* w1_scale, const float* w3_scale,
+                             const moe_bf16_t* W2, int64_t T, int d, int E, int k, int d_ff,
+                             moe_bf16_t* out, void* ws, size_t ws_bytes,
+                             cudaEvent_t* stage_events, cudaStream_t stream);
+
+/*
  * The launch-overhead path for small batches: one moe_forward captured into a CUDA graph and
  * replayed.  moe_forward_graph_create checks the arguments as moe_forward does, records
  * moe_forward(x, logits, W1, W3, W2, ..., out, ws, ws_bytes, flags) with exactly these
