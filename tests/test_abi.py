@@ -113,3 +113,36 @@ def test_forward_graph_validation(lib):
     assert st == lib.MOE_ERR_WORKSPACE and not h.value
     assert raw.moe_forward_graph_launch(None, None) == lib.MOE_ERR_INVALID_ARG
     raw.moe_forward_graph_destroy(None)                           # no-op
+
+
+def test_fp8_entry_points_validation(lib):
+    raw = lib.library()
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    need = lib.moe_workspace_bytes(64, 128, 8, 2, 256, False)
+    # weight quantization: K and N multiples of 128, non-null buffers
+    assert raw.moe_quantize_weights_fp8(fake, 4, 100, 256, fake, fake, None) == lib.MOE_ERR_UNSUPPORTED
+    assert raw.moe_quantize_weights_fp8(None, 4, 128, 256, fake, fake, None) == lib.MOE_ERR_INVALID_ARG
+    # forward: k > E, missing scales, small workspace
+    w = [fake] * 7
+    assert raw.moe_forward_fp8(*w, 64, 128, 8, 9, 256, fake, fake, need, None, None) == \
+        lib.MOE_ERR_INVALID_ARG
+    args = [fake, fake, fake, fake, None, fake, fake]
+    assert raw.moe_forward_fp8(*args, 64, 128, 8, 2, 256, fake, fake, need, None, None) == \
+        lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_forward_fp8(*w, 64, 128, 8, 2, 256, fake, fake, need - 256, None, None) == \
+        lib.MOE_ERR_WORKSPACE
+
+
+def test_relu2_validation(lib):
+    raw = lib.library()
+    fake = ctypes.c_void_p(1 << 20)
+    need = lib.moe_workspace_bytes(64, 128, 8, 2, 384, True)
+    # no W3 needs d_ff % 256 == 0
+    st = raw.moe_forward(fake, fake, fake, None, fake, 64, 128, 8, 2, 384, fake, fake, need, 0,
+                         None, None)
+    assert st == lib.MOE_ERR_UNSUPPORTED
+    # backward: W3 and dW3 both present or both absent
+    p = [fake] * 3
+    st = raw.moe_backward(*p, fake, None, fake, 64, 128, 8, 2, 256, fake, fake, fake, fake, fake,
+                          fake, fake, need, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG
