@@ -5,13 +5,17 @@
 // section 1.4: gate, up and down projections, 6hd FLOP per token-expert pair).  Every kind
 // below is one persistent, warp-specialised kernel:
 //   warp 0      TMA producer (one lane): operand tiles -> a ring of shared-memory stages
-//   warp 1      MMA issuer (one lane): tcgen05.mma 128 x BN x 16 into a TMEM accumulator
+//   warp 1      MMA issuer (one lane): tcgen05.mma 128 x BN x K into a TMEM accumulator
+//               (bf16: K = 16; E4M3: K = 32; with CTA pairs, rank 0 issues M = 256)
 //   warp 2      TMEM allocator
 //   warps 4..7  epilogue: tcgen05.ld of the accumulator, activation, global stores
 // Two TMEM accumulators alternate so the epilogue of tile i overlaps the MMAs of tile i+1.
+// GEMM1 with rows gathered from x (opt-in) adds warp 2 as a second row-copying warp next to
+// warp 0 and warp 3 (one lane) as the proxy-fence thread.
 //
 // Batch invariance and determinism (report translation, section 3; 10100.com reading):
-// the tile shape (128 x BN x 64), the K order and therefore each output element's
+// the tile shape (128 x BN x 64 bf16 or 128 E4M3 elements), the K order and therefore each
+// output element's
 // accumulation order are fixed by the model sizes alone, never by T or by the expert
 // loads; there is no split-K and no atomic accumulation; which CTA computes a tile does
 // not change its value.
