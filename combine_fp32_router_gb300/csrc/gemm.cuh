@@ -15,10 +15,9 @@
 //
 // Batch invariance and determinism (report translation, section 3; 10100.com reading):
 // the tile shape (128 x BN x 64 bf16 or 128 E4M3 elements), the K order and therefore each
-// output element's
-// accumulation order are fixed by the model sizes alone, never by T or by the expert
-// loads; there is no split-K and no atomic accumulation; which CTA computes a tile does
-// not change its value.
+// output element's accumulation order are fixed by the model sizes alone, never by T or by
+// the expert loads; there is no split-K and no atomic accumulation; which CTA computes a
+// tile does not change its value.
 //
 // Row layout: the permuted rows of every expert start at a multiple of 128 (padded
 // offsets), so each 128-row tile belongs to one expert; padding rows are masked in the
@@ -27,6 +26,7 @@
 
 #include <cuda.h>
 
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
@@ -109,7 +109,6 @@ constexpr int kEpiThreads = 128;
 // 1 = evict_last, 2 = evict_first.  A = permuted rows, B = expert weights.
 constexpr int kL2HintA = 0;
 constexpr int kL2HintB = 1;
-
 
 template <int BN, bool PAIR = false>
 struct GemmCfg {
@@ -270,11 +269,7 @@ __device__ __forceinline__ void combine_segment(const GemmParams& p, int seg, in
   }
 }
 
-// Each epilogue warp owns 32 accumulator rows (one per lane) and writes them 32 columns at a
-// time.  A lane holds 32 consecutive values of its own row; the warp transposes the 32 x 32
-// chunk through a padded shared buffer (32 x 33 floats, conflict-free both ways) so that every
-// global store instruction writes whole 128-byte lines of 4 (fp32) or 8 (bf16) rows.
-
+// 32 consecutive accumulator columns of this lane's row
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   float a[16], b[16];
   tmem_ld16x2(taddr, taddr + 16, a, b);
@@ -285,7 +280,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   }
 }
 
-// rows [0, nstore) of the chunk are written; base points at (row 0, first column of chunk)
+// Each epilogue warp owns 32 accumulator rows (one per lane) and writes them 32 columns at a
+// time.  A lane holds 32 consecutive values of its own row; the warp transposes the 32 x 32
+// chunk through a padded shared buffer (32 x 33 floats, conflict-free both ways) so that every
+// global store instruction writes whole 128-byte lines of 4 (fp32) or 8 (bf16) rows.
+// Rows [0, nstore) of the chunk are written; base points at (row 0, first column of chunk).
 template <bool BF16>
 __device__ __forceinline__ void store_chunk(float* buf, const float (&v)[32], char* base,
                                             int64_t row_bytes, int nstore, int lane) {
@@ -975,15 +974,17 @@ cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const 
   using Cfg = GemmCfg<BN, PAIR>;
   auto kern = grouped_gemm_kernel<KIND, BN, PAIR>;
   // the opt-in shared-memory size is a per-device function attribute: set it once per device
-  static unsigned long long attr_set_mask = 0ull;
+  // (two threads racing here both set the same value)
+  static std::atomic<unsigned long long> attr_set_mask{0ull};
   int dev = 0;
   cudaError_t st = cudaGetDevice(&dev);
   if (st != cudaSuccess) return st;
-  if (dev < 64 && !(attr_set_mask & (1ull << dev))) {
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit == 0ull || !(attr_set_mask.load(std::memory_order_acquire) & bit)) {
     st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(Cfg::kSmemBytes));
     if (st != cudaSuccess) return st;
-    attr_set_mask |= 1ull << dev;
+    attr_set_mask.fetch_or(bit, std::memory_order_release);
   }
   GemmParams pp = p;
   pp.max_tiles = max_tiles;

@@ -5,10 +5,12 @@
 // Dispatch -> Expert Compute -> Combine is the layer of "DeepSeek-V4 parallel strategy"
 // (blog.lpkt.cn, EP section).  On one GPU the combine reads the expert outputs as fp32 rows
 // and accumulates in fp32; the report translation's BF16 gather (itsolotime.com, section
-// 1.4) is a cross-GPU payload format and is not needed here.  Determinism follows the report's section 3
-// and the 10100.com reading: no floating-point atomics anywhere; counts come from
-// per-CTA shared-memory bit masks and histograms, positions from a fixed-order prefix sum,
-// and every floating-point reduction runs in a fixed order that depends only on d and k.
+// 1.4) is a cross-GPU payload format and is not needed here.  Determinism follows the
+// report's section 3 and the 10100.com reading: no floating-point atomics anywhere; counts
+// come from per-CTA shared-memory bit masks and histograms, positions from a fixed-order
+// prefix sum, and every floating-point reduction runs in a fixed order that depends only on
+// d and k.
+#include <atomic>
 #include <cfloat>
 #include <climits>
 
@@ -726,16 +728,17 @@ int grid_for_warps(int64_t warps, int warps_per_block) {
 // device and kernel; 0 if the query fails.
 template <typename K>
 int resident_blocks(K kern) {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev]) return cache[dev];
+  const int c = cache[dev].load(std::memory_order_relaxed);
+  if (c) return c;
   int per_sm = 0, sms = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 0;
-  cache[dev] = per_sm * sms;
-  return cache[dev];
+  cache[dev].store(per_sm * sms, std::memory_order_relaxed);
+  return per_sm * sms;
 }
 
 // Grid for a warp-per-unit kernel: one warp per unit, at most the resident capacity.
