@@ -28,9 +28,9 @@
  *   - Shapes: x [T,d], logits [T,E] fp32, W1 and W3 [E,d,d_ff], W2 [E,d_ff,d], out [T,d].
  *   - The library never allocates or frees device memory and never synchronises (except
  *     moe_get_error); only the graph entry points create (host and driver) objects.  Every
- *     launch is asynchronous on `stream`.  The workspace `ws`
- *     (device memory, 256-byte aligned, size from moe_workspace_bytes) is caller-owned;
- *     calls that share one ws must be ordered on the GPU (same stream, or synchronised).
+ *     launch is asynchronous on `stream`.  The workspace `ws` (device memory, 256-byte
+ *     aligned, size from moe_workspace_bytes) is caller-owned; calls that share one ws must
+ *     be ordered on the GPU (same stream, or synchronised).
  *   - Argument errors are detected on the host before anything is launched and returned as
  *     a status; nothing is written then.  Problems detected on the device (a bounded wait
  *     that ran out, an index out of range) are recorded in an error word inside `ws` and
@@ -127,8 +127,7 @@ moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_
  * with every matrix product accumulated in fp32 and the slot sum in fp32, in slot order.
  * ws must hold moe_workspace_bytes(T, d, E, k, d_ff, MOE_WS_BACKWARD if
  * MOE_FWD_SAVE_FOR_BACKWARD else 0) bytes; with MOE_FWD_SAVE_FOR_BACKWARD it keeps what
- * moe_backward needs.  stage_events:
- * NULL or MOE_FWD_NUM_EVENTS events (see above).
+ * moe_backward needs.  stage_events: NULL or MOE_FWD_NUM_EVENTS events (see above).
  */
 moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf16_t* W1,
                          const moe_bf16_t* W3, const moe_bf16_t* W2, int64_t T, int d, int E,
@@ -200,9 +199,9 @@ moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host
 
 /*
  * Backward of the layer for upstream gradient dy [T,d] bf16.  For the expert without the
- * gate projection (forward with W3 = NULL) pass W3 = NULL and dW3 = NULL.  Precondition: ws holds the
- * state of a moe_forward call with MOE_FWD_SAVE_FOR_BACKWARD on the same x, logits, W1, W3,
- * W2 and sizes, with nothing else using ws in between.
+ * gate projection (forward with W3 = NULL) pass W3 = NULL and dW3 = NULL.  Precondition: ws
+ * holds the state of a moe_forward call with MOE_FWD_SAVE_FOR_BACKWARD on the same x,
+ * logits, W1, W3, W2 and sizes, with nothing else using ws in between.
  * Outputs (all overwritten, none accumulated into):
  *   dx      [T,d]        bf16 : sum over slots j (in slot order, fp32) of dA W1^T + dB W3^T
  *   dW1,dW3 [E,d,d_ff]   fp32 : sum over the rows of each expert of x^T dA (resp. x^T dB)
@@ -210,8 +209,9 @@ moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host
  *   dgate   [T,k]        fp32 : <y_j, dy_t> with y_j the fp32 expert output
  *   dlogits [T,E]        fp32 : gradient through the top-k softmax (0 for unselected
  *                               experts); may be NULL
- * with dO = gate * dy, dH = dO W2^T, dA = dH * B * silu'(A), dB = dH * silu(A); dO, dA and dB
- * are rounded to bf16 as GEMM operands; every GEMM accumulates in fp32 in a fixed order.
+ * with dO = gate * dy, dH = dO W2^T, dA = dH * B * silu'(A), dB = dH * silu(A) (without the
+ * gate projection: dA = dH * 2 relu(A), no dB); dO, dA and dB are rounded to bf16 as GEMM
+ * operands; every GEMM accumulates in fp32 in a fixed order.
  * stage_events: NULL or MOE_BWD_NUM_EVENTS events.
  */
 moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float* logits,
