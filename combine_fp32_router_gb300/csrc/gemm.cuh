@@ -8,7 +8,9 @@
 //   warp 1      MMA issuer (one lane): tcgen05.mma 128 x BN x K into a TMEM accumulator
 //               (bf16: K = 16; E4M3: K = 32; with CTA pairs, rank 0 issues M = 256)
 //   warp 2      TMEM allocator
-//   warps 4..7  epilogue: tcgen05.ld of the accumulator, activation, global stores
+//   warps 4..7  epilogue: tcgen05.ld of the accumulator, activation, global stores (the dH
+//               pair launch: warps 4..11, two per TMEM lane quadrant, each taking half of
+//               the accumulator columns)
 // Two TMEM accumulators alternate so the epilogue of tile i overlaps the MMAs of tile i+1.
 // GEMM1 with rows gathered from x (opt-in) adds warp 2 as a second row-copying warp next to
 // warp 0 and warp 3 (one lane) as the proxy-fence thread.
@@ -50,6 +52,16 @@ struct KindTraits {
   static constexpr bool kRowsM = (KIND <= kDx || KIND == kFwd1F8);  // M = permuted rows
   static constexpr int kAmn = (KIND == kDw2 || KIND == kDw13) ? 1 : 0;  // A MN-major?
   static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8) ? 0 : 1;
+};
+
+// Epilogue warps of a launch: 4, one per TMEM lane quadrant, or 8 for the dH pair launch,
+// whose epilogue (saved A and B read from HBM, SwiGLU backward with exp and division per
+// element) is slower than its MMAs with 4 warps; two warps then share a lane quadrant and
+// split the accumulator columns.
+template <int KIND, bool PAIR>
+struct EpiCfg {
+  static constexpr int kWarps = (KIND == kDh && PAIR) ? 8 : 4;
+  static constexpr int kThreads = 128 + 32 * kWarps;  // + producer, MMA, TMEM, spare warps
 };
 
 struct GemmParams {
@@ -104,17 +116,18 @@ struct GemmParams {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
-constexpr int kEpiThreads = 128;
 // L2 eviction priority of the operand loads of the row-grouped forward GEMMs: 0 = default,
 // 1 = evict_last, 2 = evict_first.  A = permuted rows, B = expert weights.
 constexpr int kL2HintA = 0;
 constexpr int kL2HintB = 1;
 
-template <int BN, bool PAIR = false>
+template <int BN, bool PAIR = false, int EPI_WARPS = 4>
 struct GemmCfg {
   // a CTA pair holds half of the B tile in each CTA
   static constexpr int kBLocal = PAIR ? BN / 2 : BN;
-  static constexpr int kStages = (kABytes + kBLocal * kBK * 2 <= 32768) ? 6 : 4;
+  // 32 KB stages: 6 (5 with 8 epilogue warps); 48 KB stages: 4
+  static constexpr int kStages =
+      (kABytes + kBLocal * kBK * 2 <= 32768) ? (EPI_WARPS > 4 ? 5 : 6) : 4;
   static constexpr uint32_t kBBytes = kBLocal * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
@@ -123,10 +136,11 @@ struct GemmCfg {
   // one 1024-aligned 5 KB region per epilogue warp: a 32 x 33 fp32 transpose buffer, or the
   // 32 x 32 fp32 staging box of a TMA store
   static constexpr size_t kEpiWarpBytes = 5120;
-  static constexpr size_t kEpiBytes = 4 * kEpiWarpBytes;
+  static constexpr size_t kEpiBytes = EPI_WARPS * kEpiWarpBytes;
   static constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 1024 +
                                        kEpiBytes + 8 * kBars + 64;
   static_assert(kStageBytes % 1024 == 0, "stages keep the epilogue regions 1024-aligned");
+  static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of a CTA (227 KB)");
 };
 
 struct TileInfo {
@@ -342,10 +356,11 @@ __device__ __forceinline__ void store_chunk_tma(uint32_t stage, const float (&v)
 
 // Epilogue of one tile for one epilogue warp (rows q*32 .. q*32+31 of the accumulator).
 // `tacc` is the warp's TMEM address (lane base q*32, accumulator column 0); `r` = q*32 + lane.
+// `part` of `nparts` (dH with 8 epilogue warps: 2) selects the warp's share of the chunks.
 template <int KIND, int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& ti,
                                               uint32_t tacc, int q, int lane, float* buf,
-                                              uint32_t stage) {
+                                              uint32_t stage, int part, int nparts) {
   const int r = q * 32 + lane;
   const bool valid = r < ti.nvalid;
   const int w0 = q * 32;  // first row of this warp
@@ -456,8 +471,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     const int nstore = clamp_rows(ti.nseg);      // pad rows are written as zeros
     const int nval = clamp_rows(ti.nvalid);
     const int rsub = lane >> 3, c4 = (lane & 7) * 4;
+    const int ch_end = (part + 1) * (BN / 32) / nparts;
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 32; ++ch) {
+    for (int ch = part * (BN / 32) / nparts; ch < ch_end; ++ch) {
       // all 16 loads of the chunk in flight first; the accumulator read and the shared
       // transpose run under their latency
       uint4 ua[8], ub[8];
@@ -562,12 +578,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 // on; rank 0's commits arrive on both CTAs' empty / tmem-full barriers (multicast); both
 // epilogues release the accumulator on rank 0's tmem-empty barrier.
 template <int KIND, int BN, bool PAIR>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapB0,
                         const __grid_constant__ CUtensorMap mapB1,
                         const __grid_constant__ GemmParams p) {
-  using Cfg = GemmCfg<BN, PAIR>;
+  constexpr int EW = EpiCfg<KIND, PAIR>::kWarps;
+  using Cfg = GemmCfg<BN, PAIR, EW>;
   using Tr = KindTraits<KIND>;
   constexpr int S = Cfg::kStages;
   constexpr int BL = Cfg::kBLocal;  // B columns held by this CTA
@@ -615,7 +632,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
+      mbar_init(tempty_bar(a), PAIR ? 2 * EW : EW);  // one arrival per epilogue warp (both CTAs)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -891,7 +908,8 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
-    const int q = warp - 4;
+    const int ew = warp - 4;  // epilogue warp index
+    const int q = ew & 3;     // its TMEM lane quadrant (warp % 4)
     int it = 0;
     const uint32_t release_to = PAIR ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
     for (int tile = unit; tile < ntiles; tile += nunits) {
@@ -905,8 +923,9 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       epilogue_tile<KIND, BN>(p, ti, tacc, q, lane,
-                              epi_buf + q * (Cfg::kEpiWarpBytes / 4),
-                              epi0 + q * static_cast<uint32_t>(Cfg::kEpiWarpBytes));
+                              epi_buf + ew * (Cfg::kEpiWarpBytes / 4),
+                              epi0 + ew * static_cast<uint32_t>(Cfg::kEpiWarpBytes), ew >> 2,
+                              EW / 4);
       tc_fence_before();
       __syncwarp();
       // The accumulator is free once every lane's tcgen05.ld has completed (they have: the
@@ -971,7 +990,7 @@ template <int KIND, int BN, bool PAIR>
 cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                              const GemmParams& p, int64_t max_tiles, int num_sms,
                              cudaStream_t s) {
-  using Cfg = GemmCfg<BN, PAIR>;
+  using Cfg = GemmCfg<BN, PAIR, EpiCfg<KIND, PAIR>::kWarps>;
   auto kern = grouped_gemm_kernel<KIND, BN, PAIR>;
   // the opt-in shared-memory size is a per-device function attribute: set it once per device
   // (two threads racing here both set the same value)
@@ -993,7 +1012,7 @@ cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const 
   if (units < 1) units = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * units : units), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(EpiCfg<KIND, PAIR>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
