@@ -352,32 +352,37 @@ def bench_native(args, w):
     ms_step = ms / args.steps
     value = world * T * args.steps / (ms / 1e3)
 
-    # end to end through the public API with host buffers: moe_forward_host copies the step's
-    # x and logits from page-locked host memory into its workspace, runs the layer and copies
-    # the output back.  Two workspaces on two streams take alternate steps, so one step's
-    # copies overlap the other step's layer; every step still moves its own inputs and output.
+    # end to end through the public API with host buffers: each step copies its x and logits
+    # from page-locked host memory into a workspace, runs the layer and copies the output back
+    # (moe_forward_host_pipelined).  The layers run one after another on one compute stream;
+    # two workspaces, each with its own copy stream, take alternate steps, so one step's copies
+    # overlap its neighbours' layers.  Every step still moves its own inputs and output.
     ws_io = [torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, False, host_io=True),
                          dtype=torch.uint8, device=dev) for _ in range(2)]
-    io_streams = [torch.cuda.Stream(dev) for _ in range(2)]
+    compute = torch.cuda.Stream(dev)
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(2)]
+    copy_events = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(2)]
     hx = [g["x"].cpu().pin_memory() for _ in range(2)]
     hl = [g["logits"].cpu().pin_memory() for _ in range(2)]
     ho = [torch.empty(T, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
 
     def e2e_step(i):
         j = i % 2
-        moe.moe_forward_host(hx[j], hl[j], g["W1"], g.get("W3"), g["W2"], k, ho[j], ws_io[j],
-                             stream=io_streams[j])
+        moe.moe_forward_host_pipelined(hx[j], hl[j], g["W1"], g.get("W3"), g["W2"], k, ho[j],
+                                       ws_io[j], copy_stream=copy_streams[j],
+                                       events=copy_events[j], stream=compute)
 
     for i in range(max(2, args.warmup)):
         e2e_step(i)
     barrier()
-    ends = [torch.cuda.Event() for _ in range(2)]
+    used = [compute] + copy_streams
+    ends = [torch.cuda.Event() for _ in used]
     start.record(stream)
-    for s_ in io_streams:
+    for s_ in used:
         s_.wait_event(start)
     for i in range(args.steps):
         e2e_step(i)
-    for s_, e_ in zip(io_streams, ends):
+    for s_, e_ in zip(used, ends):
         e_.record(s_)
         stream.wait_event(e_)
     stop.record(stream)
@@ -459,7 +464,8 @@ def bench_native(args, w):
 
     e2e = {"value": world * T * args.steps / (ms_e2e / 1e3), "unit": UNIT,
            "h2d_bytes_per_step": T * d * 2 + T * E * 4, "d2h_bytes_per_step": T * d * 2,
-           "api": "moe_forward_host, page-locked host buffers, two streams taking alternate "
+           "api": "moe_forward_host_pipelined: page-locked host buffers; layers on one "
+                  "compute stream, two workspaces with a copy stream each taking alternate "
                   "steps"}
 
     names = ["dispatch", "gemm1_swiglu", "gemm2", "combine"]

@@ -35,7 +35,8 @@ MOE_BWD_NUM_EVENTS = 7
 EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispatch",
            "moe_forward", "moe_forward_fp8", "moe_quantize_weights_fp8",
            "moe_forward_graph_create", "moe_forward_graph_launch",
-           "moe_forward_graph_destroy", "moe_forward_host", "moe_backward",
+           "moe_forward_graph_destroy", "moe_forward_host", "moe_forward_host_pipelined",
+           "moe_backward",
            "moe_route_dispatch_noalloc", "moe_get_error", "moe_set_wait_timeout_ns",
            "moe_debug_set_flags", "moe_status_string")
 
@@ -72,6 +73,8 @@ def _load():
     lib.moe_forward_graph_destroy.argtypes = [p]
     lib.moe_forward_host.restype = i
     lib.moe_forward_host.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i, p, p]
+    lib.moe_forward_host_pipelined.restype = i
+    lib.moe_forward_host_pipelined.argtypes = [p] * 5 + [i64, i, i, i, i, p, p, sz, i, p] + [p] * 4
     lib.moe_forward.restype = i
     lib.moe_backward.argtypes = [p] * 6 + [i64, i, i, i, i] + [p] * 6 + [p, sz, p, p]
     lib.moe_backward.restype = i
@@ -227,6 +230,22 @@ def moe_forward_host(x_host, logits_host, W1, W3, W2, k, out_host, ws, flags=0,
                                  T, d, E, k, d_ff, _ptr(out_host), _ptr(ws), _nbytes(ws),
                                  int(flags), _events(stage_events), _stream(stream)),
            "moe_forward_host")
+
+
+def moe_forward_host_pipelined(x_host, logits_host, W1, W3, W2, k, out_host, ws, copy_stream,
+                               events, flags=0, stage_events=None, stream=None):
+    """moe_forward_host with the copies on ``copy_stream`` and the layer on ``stream``;
+    ``events`` holds the two torch.cuda.Event objects the call records and waits on
+    (inputs ready, layer done)."""
+    T, d = x_host.shape
+    E, _, d_ff = W1.shape
+    ev = _events(events)
+    if ev is None or len(ev) != 2:
+        raise ValueError("events must hold two torch.cuda.Event objects")
+    _check(_lib.moe_forward_host_pipelined(
+        _ptr(x_host), _ptr(logits_host), _ptr(W1), _ptr(W3), _ptr(W2), T, d, E, k, d_ff,
+        _ptr(out_host), _ptr(ws), _nbytes(ws), int(flags), _events(stage_events),
+        _stream(stream), _stream(copy_stream), ev[0], ev[1]), "moe_forward_host_pipelined")
 
 
 def moe_backward(dy, x, logits, W1, W3, W2, k, dx, dW1, dW3, dW2, dgate, dlogits, ws,

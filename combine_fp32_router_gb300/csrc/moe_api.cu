@@ -458,11 +458,16 @@ void moe_forward_graph_destroy(moe_forward_graph_t graph) {
   delete graph;
 }
 
-moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host,
-                              const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
-                              int64_t T, int d, int E, int k, int d_ff, moe_bf16_t* out_host,
-                              void* ws, size_t ws_bytes, int flags, cudaEvent_t* stage_events,
-                              cudaStream_t stream) {
+namespace {
+// moe_forward_host and moe_forward_host_pipelined: the input copies on `copy`, the layer on
+// `stream`, the output copy on `copy`.  With two streams, inputs_ready / layer_done order
+// them (recorded and waited on here); with one, stream order does.
+moe_status_t forward_host_impl(const moe_bf16_t* x_host, const float* logits_host,
+                               const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                               int64_t T, int d, int E, int k, int d_ff, moe_bf16_t* out_host,
+                               void* ws, size_t ws_bytes, int flags, cudaEvent_t* stage_events,
+                               cudaStream_t stream, cudaStream_t copy, cudaEvent_t inputs_ready,
+                               cudaEvent_t layer_done) {
   moe_status_t st = check_dims(T, d, E, k, d_ff, true);
   if (st != MOE_OK) return st;
   if (!ws) return MOE_ERR_INVALID_ARG;
@@ -483,14 +488,45 @@ moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host
       round_up(static_cast<size_t>(T) * E * 4, 256));
   const size_t xb = static_cast<size_t>(T) * d * 2, lb = static_cast<size_t>(T) * E * 4;
   if (T > 0) {
-    MOE_TRY(cudaMemcpyAsync(x, x_host, xb, cudaMemcpyHostToDevice, stream));
-    MOE_TRY(cudaMemcpyAsync(logits, logits_host, lb, cudaMemcpyHostToDevice, stream));
+    MOE_TRY(cudaMemcpyAsync(x, x_host, xb, cudaMemcpyHostToDevice, copy));
+    MOE_TRY(cudaMemcpyAsync(logits, logits_host, lb, cudaMemcpyHostToDevice, copy));
+  }
+  if (copy != stream) {
+    MOE_TRY(cudaEventRecord(inputs_ready, copy));
+    MOE_TRY(cudaStreamWaitEvent(stream, inputs_ready, 0));
   }
   st = moe_forward(x, logits, W1, W3, W2, T, d, E, k, d_ff, out, ws, io0, flags, stage_events,
                    stream);
   if (st != MOE_OK) return st;
-  if (T > 0) MOE_TRY(cudaMemcpyAsync(out_host, out, xb, cudaMemcpyDeviceToHost, stream));
+  if (copy != stream) {
+    MOE_TRY(cudaEventRecord(layer_done, stream));
+    MOE_TRY(cudaStreamWaitEvent(copy, layer_done, 0));
+  }
+  if (T > 0) MOE_TRY(cudaMemcpyAsync(out_host, out, xb, cudaMemcpyDeviceToHost, copy));
   return MOE_OK;
+}
+}  // namespace
+
+moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host,
+                              const moe_bf16_t* W1, const moe_bf16_t* W3, const moe_bf16_t* W2,
+                              int64_t T, int d, int E, int k, int d_ff, moe_bf16_t* out_host,
+                              void* ws, size_t ws_bytes, int flags, cudaEvent_t* stage_events,
+                              cudaStream_t stream) {
+  return forward_host_impl(x_host, logits_host, W1, W3, W2, T, d, E, k, d_ff, out_host, ws,
+                           ws_bytes, flags, stage_events, stream, stream, nullptr, nullptr);
+}
+
+moe_status_t moe_forward_host_pipelined(const moe_bf16_t* x_host, const float* logits_host,
+                                        const moe_bf16_t* W1, const moe_bf16_t* W3,
+                                        const moe_bf16_t* W2, int64_t T, int d, int E, int k,
+                                        int d_ff, moe_bf16_t* out_host, void* ws,
+                                        size_t ws_bytes, int flags, cudaEvent_t* stage_events,
+                                        cudaStream_t stream, cudaStream_t copy_stream,
+                                        cudaEvent_t inputs_ready, cudaEvent_t layer_done) {
+  if (!inputs_ready || !layer_done || inputs_ready == layer_done) return MOE_ERR_INVALID_ARG;
+  return forward_host_impl(x_host, logits_host, W1, W3, W2, T, d, E, k, d_ff, out_host, ws,
+                           ws_bytes, flags, stage_events, stream, copy_stream, inputs_ready,
+                           layer_done);
 }
 
 moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float* logits,

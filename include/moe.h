@@ -198,6 +198,28 @@ moe_status_t moe_forward_host(const moe_bf16_t* x_host, const float* logits_host
                               cudaStream_t stream);
 
 /*
+ * moe_forward_host for a loop that runs batches back to back: the input copies run on
+ * copy_stream, the layer on `stream` once they have landed, and the output copy on
+ * copy_stream once the layer has finished.  Successive calls on the same `stream` thus run
+ * their layers one after the other (each grouped GEMM fills the whole GPU), while a call's
+ * copies overlap the layers of the calls before and after it.  Two calls in flight need two
+ * workspaces; calls that share a ws must also share copy_stream, which orders a call's input
+ * copies after the previous call's output copy and hence after its layer.  inputs_ready and
+ * layer_done are two distinct events created by the caller (cudaEventDisableTiming is
+ * enough); the call records each and makes the other stream wait on it before returning, so
+ * the next call may reuse them.  Arguments, workspace size and stage_events as
+ * moe_forward_host (the events bracket the layer on `stream`).  copy_stream == stream gives
+ * moe_forward_host.
+ */
+moe_status_t moe_forward_host_pipelined(const moe_bf16_t* x_host, const float* logits_host,
+                                        const moe_bf16_t* W1, const moe_bf16_t* W3,
+                                        const moe_bf16_t* W2, int64_t T, int d, int E, int k,
+                                        int d_ff, moe_bf16_t* out_host, void* ws,
+                                        size_t ws_bytes, int flags, cudaEvent_t* stage_events,
+                                        cudaStream_t stream, cudaStream_t copy_stream,
+                                        cudaEvent_t inputs_ready, cudaEvent_t layer_done);
+
+/*
  * Backward of the layer for upstream gradient dy [T,d] bf16.  For the expert without the
  * gate projection (forward with W3 = NULL) pass W3 = NULL and dW3 = NULL.  Precondition: ws
  * holds the state of a moe_forward call with MOE_FWD_SAVE_FOR_BACKWARD on the same x,

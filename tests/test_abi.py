@@ -100,6 +100,29 @@ def test_forward_host_validation(lib):
     assert st == lib.MOE_ERR_UNSUPPORTED
 
 
+def test_forward_host_pipelined_validation(lib):
+    raw = lib.library()
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    ev0, ev1 = ctypes.c_void_p(1 << 21), ctypes.c_void_p(1 << 22)
+    w = [fake] * 3
+    need = lib.moe_workspace_bytes(64, 128, 8, 2, 256, False, host_io=True)
+    args = lambda: [fake, fake, *w, 64, 128, 8, 2, 256, fake, fake, need, 0, None, None, None]
+    # both events are required, and they must differ
+    assert raw.moe_forward_host_pipelined(*args(), None, ev1) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_forward_host_pipelined(*args(), ev0, None) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_forward_host_pipelined(*args(), ev0, ev0) == lib.MOE_ERR_INVALID_ARG
+    # the rest as moe_forward_host
+    a = args()
+    a[0] = None
+    assert raw.moe_forward_host_pipelined(*a, ev0, ev1) == lib.MOE_ERR_INVALID_ARG
+    a = args()
+    a[12] = lib.moe_workspace_bytes(64, 128, 8, 2, 256, False)
+    assert raw.moe_forward_host_pipelined(*a, ev0, ev1) == lib.MOE_ERR_WORKSPACE
+    a = args()
+    a[6] = 100
+    assert raw.moe_forward_host_pipelined(*a, ev0, ev1) == lib.MOE_ERR_UNSUPPORTED
+
+
 def test_forward_graph_validation(lib):
     raw = lib.library()
     fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first

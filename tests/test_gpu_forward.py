@@ -169,6 +169,39 @@ def test_forward_host_equals_device(moe, T, pinned, save):
             assert torch.equal(a, b), name
 
 
+def test_forward_host_pipelined_back_to_back(moe):
+    # six different batches through two workspaces, layers on one compute stream, copies on
+    # one copy stream per workspace: each output is bitwise the device forward of its batch
+    # (a copy that overtook a layer on a shared workspace would mix batches)
+    T, d, E, k, dff = 1024, 512, 32, 4, 384
+    nb = 6
+    w = moe_synth.custom(T * nb, d, E, k, dff, seed=91, zipf_s=1.2)
+    inp = moe_synth.generate(w)
+    g = to_dev(inp)
+    batches = [{"x": g["x"][i * T:(i + 1) * T].contiguous(),
+                "logits": g["logits"][i * T:(i + 1) * T].contiguous(),
+                "W1": g["W1"], "W3": g["W3"], "W2": g["W2"]} for i in range(nb)]
+    refs = [forward(moe, b, k)[0].cpu() for b in batches]
+    ws = [torch.empty(moe.moe_workspace_bytes(T, d, E, k, dff, False, host_io=True),
+                      dtype=torch.uint8, device="cuda") for _ in range(2)]
+    compute = torch.cuda.Stream()
+    copies = [torch.cuda.Stream() for _ in range(2)]
+    events = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(2)]
+    hx = [b["x"].cpu().pin_memory() for b in batches]
+    hl = [b["logits"].cpu().pin_memory() for b in batches]
+    ho = [torch.full((T, d), 7.0, dtype=torch.bfloat16).pin_memory() for _ in range(nb)]
+    torch.cuda.synchronize()
+    for i in range(nb):
+        j = i % 2
+        moe.moe_forward_host_pipelined(hx[i], hl[i], g["W1"], g["W3"], g["W2"], k, ho[i], ws[j],
+                                       copy_stream=copies[j], events=events[j], stream=compute)
+    torch.cuda.synchronize()
+    for x in ws:
+        assert moe.moe_get_error(x) == 0
+    for i in range(nb):
+        assert torch.equal(ho[i].view(torch.int16), refs[i].view(torch.int16)), i
+
+
 @pytest.mark.parametrize("T,flags", [(1, 0), (64, 0), (300, 0), (300, 2)])
 def test_forward_graph_replays_the_layer(moe, T, flags):
     # a captured forward, replayed after the inputs are rewritten in place, gives bitwise
