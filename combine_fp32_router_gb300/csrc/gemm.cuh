@@ -1025,21 +1025,21 @@ cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const 
   return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, pp);
 }
 
-// A rows-grouped GEMM: with pairs, every expert's full 256-row pair tiles run on CTA pairs
-// and its odd last 128-row tile on single CTAs (second launch); both give bitwise the same
-// rows.  `lo` carries the leftover tile table in place of the 128-row tile table; b0/b1 are
-// the B maps of the pair launch (a K-major B box holds BN/2 rows there), sb0/sb1 those of
-// single-CTA launches (BN rows).
+// A rows-grouped GEMM: with pairs, the 256-row pair tiles of the experts chosen for pairs
+// run on CTA pairs, and the rest (their odd last 128-row tiles, and every tile of the other
+// experts) on single CTAs in a second launch; both give bitwise the same rows.  `lo` carries
+// that launch's tile table in place of the 128-row tile table; b0/b1 are the B maps of the
+// pair launch (a K-major B box holds BN/2 rows there), sb0/sb1 those of single-CTA launches
+// (BN rows).
 template <int KIND, int BN>
 cudaError_t run_rows_kind(bool pair, const CUtensorMap& a, const CUtensorMap& b0,
                           const CUtensorMap& b1, const CUtensorMap& sb0, const CUtensorMap& sb1,
-                          const GemmParams& p, const GemmParams& lo, int64_t max_mt, int E,
+                          const GemmParams& p, const GemmParams& lo, int64_t max_mt,
                           int num_sms, cudaStream_t s) {
   if (!pair) return run_grouped_gemm<KIND, BN, false>(a, sb0, sb1, p, max_mt * p.nb, num_sms, s);
   cudaError_t st = run_grouped_gemm<KIND, BN, true>(a, b0, b1, p, max_mt * p.nb, num_sms, s);
   if (st != cudaSuccess) return st;
-  return run_grouped_gemm<KIND, BN, false>(a, sb0, sb1, lo, static_cast<int64_t>(E) * lo.nb,
-                                           num_sms, s);
+  return run_grouped_gemm<KIND, BN, false>(a, sb0, sb1, lo, max_mt * lo.nb, num_sms, s);
 }
 
 }  // namespace moe

@@ -37,8 +37,8 @@ cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s) {
   p.save_a = reinterpret_cast<float*>(c.ws + L.Asave);
   p.save_b = reinterpret_cast<float*>(c.ws + L.Bsave);
   const GemmParams lo = leftover_params(p, c);
-  if (BN == 256) return run_rows_kind<kDh, 256>(c.pair, a, b0, b0, sb0, sb0, p, lo, L.max_mt, L.E, c.num_sms, s);
-  return run_rows_kind<kDh, 128>(c.pair, a, b0, b0, sb0, sb0, p, lo, L.max_mt, L.E, c.num_sms, s);
+  if (BN == 256) return run_rows_kind<kDh, 256>(c.pair, a, b0, b0, sb0, sb0, p, lo, L.max_mt, c.num_sms, s);
+  return run_rows_kind<kDh, 128>(c.pair, a, b0, b0, sb0, sb0, p, lo, L.max_mt, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s) {
@@ -64,8 +64,8 @@ cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s) {
   if (st != cudaSuccess) return st;
   p.tma_store = 1;
   const GemmParams lo = leftover_params(p, c);
-  if (BN == 256) return run_rows_kind<kDx, 256>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, L.E, c.num_sms, s);
-  return run_rows_kind<kDx, 128>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, L.E, c.num_sms, s);
+  if (BN == 256) return run_rows_kind<kDx, 256>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, c.num_sms, s);
+  return run_rows_kind<kDx, 128>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s) {

@@ -153,7 +153,7 @@ cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s) {
   p.perm = reinterpret_cast<const int32_t*>(c.ws + L.perm);
   p.k = L.k;
   return run_rows_kind<kFwd1, 256>(c.pair, a, b0, b1, b0, b1, p, leftover_params(p, c), L.max_mt,
-                                   L.E, c.num_sms, s);
+                                   c.num_sms, s);
 }
 
 cudaError_t launch_gemm_fwd1_fp8(const GemmCtx& c, cudaStream_t s) {
@@ -176,7 +176,7 @@ cudaError_t launch_gemm_fwd1_fp8(const GemmCtx& c, cudaStream_t s) {
   p.wscale1 = c.wscale1;
   p.wscale3 = c.wscale3;
   return run_rows_kind<kFwd1F8, 256>(c.pair, a, b0, b1, b0, b1, p, leftover_params(p, c),
-                                     L.max_mt, L.E, c.num_sms, s);
+                                     L.max_mt, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
@@ -204,8 +204,8 @@ cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
   }
   const GemmParams lo = leftover_params(p, c);
   if (BN == 256)
-    return run_rows_kind<kFwd2, 256>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, L.E, c.num_sms, s);
-  return run_rows_kind<kFwd2, 128>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, L.E, c.num_sms, s);
+    return run_rows_kind<kFwd2, 256>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, c.num_sms, s);
+  return run_rows_kind<kFwd2, 128>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, c.num_sms, s);
 }
 
 }  // namespace moe

@@ -11,6 +11,7 @@ namespace moe {
 
 constexpr int kRouteTokensPerBlock = 128;  // tokens per routing CTA (4 ranking chunks of 32)
 constexpr int kTileRows = 128;             // rows of one expert GEMM tile; padded row unit
+constexpr int kPairOddMinTiles = 7;        // CTA pairs for an odd tile count from this many
 constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
 

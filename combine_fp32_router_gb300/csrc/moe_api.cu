@@ -115,8 +115,8 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   L.pt_expert = take(static_cast<size_t>(L.max_mt) * 4);
   L.pt_row0 = take(static_cast<size_t>(L.max_mt) * 4);
   L.n_lo = take(16);
-  L.lo_expert = take(static_cast<size_t>(E) * 4);
-  L.lo_row0 = take(static_cast<size_t>(E) * 4);
+  L.lo_expert = take(static_cast<size_t>(L.max_mt) * 4);
+  L.lo_row0 = take(static_cast<size_t>(L.max_mt) * 4);
   L.topk = take(P * 4);
   L.gate = take(P * 4);
   L.pos = take(P * 4);

@@ -283,10 +283,18 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   if (e < E) poff[e] = poffv;
   if (e == 0) poff[E] = tot_p;
   if (!with_tables) return;
-  // 128-row tiles; 256-row pair tiles (two consecutive 128-row tiles of one expert) with an
-  // odd last tile in the leftover table (computed by single-CTA tiles, same results)
+  // 128-row tiles (the single-CTA schedule) and, for CTA pairs, 256-row pair tiles (two
+  // consecutive 128-row tiles of one expert) plus a table for the single-CTA launch that runs
+  // beside them.  An expert runs on pairs when its tile count is even, or odd and at least
+  // kPairOddMinTiles; its odd last tile then goes to the single-CTA launch, which reads the
+  // expert's weights a second time, a cost that the pair tiles' higher MMA rate repays only
+  // from that many tiles on.  Every other expert runs all its tiles in the single-CTA launch
+  // and reads its weights once.  Pair and single-CTA tiles compute bitwise the same rows, so
+  // the choice changes no result.
   const int nm = pc / kTileRows;
-  const int np = nm / 2;
+  const bool paired = nm >= 2 && ((nm & 1) == 0 || nm >= kPairOddMinTiles);
+  const int np = paired ? nm / 2 : 0;
+  const int nlo = paired ? (nm & 1) : nm;  // tiles of the single-CTA launch
   const int ha = block_exclusive_scan(nm >= 2 ? nm : 0, warp_tot, &total) + (nm >= 2 ? nm : 0);
   const int H = total;
   const int lb = block_exclusive_scan(nm >= 2 ? 0 : nm, warp_tot, &total) + (nm >= 2 ? 0 : nm);
@@ -295,27 +303,30 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   const int PH = total;
   const int pb = block_exclusive_scan(np >= 2 ? 0 : np, warp_tot, &total) + (np >= 2 ? 0 : np);
   const int PL = total;
-  const int odd = nm & 1;
-  const int los = block_exclusive_scan(odd, warp_tot, &total);
+  const int los = block_exclusive_scan(nlo, warp_tot, &total);
   const int NLO = total;
+  // every table holds at most sum(nm) <= max_mt entries (the padded rows bound the tiles)
+  const bool fits = H + L <= tt.max_mt;
   if (e < E) {
     s_poff[e] = poffv;
     s_a[e] = ha;
     s_b[e] = lb;
     s_pa[e] = pa;
     s_pb[e] = pb;
-    if (odd) {
-      tt.lo_expert[los] = e;
-      tt.lo_row0[los] = poffv + (nm - 1) * kTileRows;
+    if (fits) {
+      for (int i = 0; i < nlo; ++i) {  // nlo <= kPairOddMinTiles - 2 for experts not paired
+        tt.lo_expert[los + i] = e;
+        tt.lo_row0[los + i] = poffv + (nm - nlo + i) * kTileRows;
+      }
     }
   }
   if (e == 0) {
-    tt.n_mt[0] = H + L;
-    tt.n_pt[0] = PH + PL;
-    tt.n_lo[0] = NLO;
+    tt.n_mt[0] = fits ? H + L : 0;
+    tt.n_pt[0] = fits ? PH + PL : 0;
+    tt.n_lo[0] = fits ? NLO : 0;
   }
   __syncthreads();
-  if (H + L > tt.max_mt) {
+  if (!fits) {
     if (e == 0) set_error(err, MOE_ERR_DEVICE_BOUNDS, 100);
     return;
   }
