@@ -171,21 +171,25 @@ def max_over_ranks(value, device):
     return float(t.item())
 
 
-def _pair():
-    return os.environ.get("MOE_GEMM_PAIR", "1") != "0"
+def _row_pairs(T, k, d, dff):
+    # the library's rule for CTA pairs in the row-grouped GEMMs (MOE_GEMM_PAIR: "0" never,
+    # "1" whenever T > 128, else T > 128 and T k d d_ff >= 2^37)
+    mode = os.environ.get("MOE_GEMM_PAIR", "")
+    if mode == "0" or T <= 128:
+        return False
+    return mode == "1" or T * k * d * dff >= 2 ** 37
 
 
-def fwd_launches(T=None):
+def fwd_launches(T, k, d, dff):
     # routing, column scan, offsets/tile tables, scatter, padding rows, GEMM1, GEMM2, combine;
-    # with CTA pairs (used when T > 128) each GEMM is a pair launch plus a single-CTA launch
-    # for leftover tiles
-    return 10 if _pair() and (T is None or T > 128) else 8
+    # with CTA pairs each GEMM is a pair launch plus a single-CTA launch for the other tiles
+    return 10 if _row_pairs(T, k, d, dff) else 8
 
 
-def bwd_launches():
-    # gate grads (rows + per token), dO padding, dH (+ leftover), dX (+ leftover), dX combine,
-    # dW2, dW1/dW3
-    return 10 if _pair() else 8
+def bwd_launches(T, k, d, dff):
+    # gate grads (rows + per token), dO padding, dH (+ single-CTA tiles), dX (+ single-CTA
+    # tiles), dX combine, dW2, dW1/dW3
+    return 10 if _row_pairs(T, k, d, dff) else 8
 
 
 def bench_fwd_bwd(moe, dev, steps, warmup, shape=None):
@@ -242,7 +246,7 @@ def bench_fwd_bwd(moe, dev, steps, warmup, shape=None):
             "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
             "backward_ms": bwd_ms, "backward_stages_ms": stages,
             "backward_tflops": bwd_flops / (bwd_ms * 1e-3) / 1e12,
-            "launches_per_step": fwd_launches() + bwd_launches()}
+            "launches_per_step": fwd_launches(T, k, d, dff) + bwd_launches(T, k, d, dff)}
 
 
 def run_cpu_baseline(w, inp_np, budget_s=15.0):
@@ -513,7 +517,7 @@ def bench_native(args, w):
         "graph_forward_ms_per_step": graph_ms,
         "fp8_forward": fp8,
         "clocks": clocks.summary(),
-        "gpu_launches": fwd_launches(T) * args.steps,
+        "gpu_launches": fwd_launches(T, k, d, dff) * args.steps,
     }
     if not args.no_backward:
         del ws

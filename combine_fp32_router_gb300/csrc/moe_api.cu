@@ -17,15 +17,32 @@ namespace {
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
 std::atomic<int> g_debug_flags{0};
 
-// Grouped GEMMs on CTA pairs (256-row tiles, tcgen05 cta_group::2) unless the environment
-// variable MOE_GEMM_PAIR is "0" (single-CTA 128-row tiles).  Both give bitwise identical
-// results; the switch exists to compare the two.
-bool use_pairs() {
-  static const bool v = [] {
+// CTA pairs (256-row tiles, tcgen05 cta_group::2) or single CTAs (128-row tiles) for the
+// grouped GEMMs; both give bitwise identical results.  The environment variable
+// MOE_GEMM_PAIR, read once per process, selects: "0" single CTAs only, "1" pairs wherever
+// an expert can fill a pair tile, unset (or anything else) the size rule of row_pairs.
+enum PairMode { kPairsOff = 0, kPairsOn = 1, kPairsAuto = 2 };
+PairMode pair_mode() {
+  static const PairMode v = [] {
     const char* e = std::getenv("MOE_GEMM_PAIR");
-    return !(e && e[0] == '0');
+    if (e && e[0] == '0' && e[1] == 0) return kPairsOff;
+    if (e && e[0] == '1' && e[1] == 0) return kPairsOn;
+    return kPairsAuto;
   }();
   return v;
+}
+bool use_pairs() { return pair_mode() != kPairsOff; }
+
+// CTA pairs for the row-grouped GEMMs (the experts' 256-row pair tiles, chosen per expert on
+// the device; the rest in a second, single-CTA launch): only when some expert can fill a pair
+// tile (T > 128) and the layer is large enough that the second launch's ramp and tail are
+// paid back, T k d d_ff >= 2^37 (GEMM1 >= 0.55 TFLOP).  Measured on GB300: T=4096, d=2048,
+// E=64, top-6, d_ff=1024 (T k d d_ff = 5.2e10) runs 7% faster on single CTAs alone;
+// T=8192, d=4096, E=128, top-8, d_ff=1536 (4.1e11) 3% faster with pairs.
+bool row_pairs(int64_t T, int k, int d, int dff) {
+  if (pair_mode() == kPairsOff || T <= kTileRows) return false;
+  const double work = static_cast<double>(T) * k * d * dff;
+  return pair_mode() == kPairsOn || work >= 137438953472.0;
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -283,9 +300,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.wait_ns = g_wait_ns.load();
   c.debug_flags = g_debug_flags.load();
   c.num_sms = num_sms_of_current_device();
-  // an expert has at most T rows, so with T <= 128 no expert fills a 256-row pair tile: one
-  // single-CTA launch per GEMM then covers every tile
-  c.pair = use_pairs() && T > kTileRows;
+  c.pair = row_pairs(T, k, d, d_ff);
   c.fuse_combine = (flags & MOE_FWD_FUSED_COMBINE) != 0;
   c.gated = W3 != nullptr;
   c.gather_x = gather;
@@ -386,7 +401,7 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uin
   c.wait_ns = g_wait_ns.load();
   c.debug_flags = g_debug_flags.load();
   c.num_sms = num_sms_of_current_device();
-  c.pair = use_pairs() && T > kTileRows;
+  c.pair = row_pairs(T, k, d, d_ff);
   c.gated = true;
   c.out = out;
   MOE_TRY(launch_gemm_fwd1_fp8(c, stream));
@@ -585,7 +600,7 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   c.wait_ns = g_wait_ns.load();
   c.debug_flags = g_debug_flags.load();
   c.num_sms = num_sms_of_current_device();
-  c.pair = use_pairs();
+  c.pair = row_pairs(T, k, d, d_ff);  // dH and dX: row-grouped like the forward
   c.gated = W3 != nullptr;
   MOE_TRY(launch_gemm_dh(c, stream));
   record(stage_events, 2, stream);
@@ -594,6 +609,7 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   MOE_TRY(launch_combine_f32(reinterpret_cast<const float*>(w + L.dXp), pos, T, k, d, dx,
                              stream));
   record(stage_events, 4, stream);
+  c.pair = use_pairs();  // the weight gradients pair on 256 output rows instead
   MOE_TRY(launch_gemm_dw2(c, stream));
   record(stage_events, 5, stream);
   MOE_TRY(launch_gemm_dw13(c, stream));

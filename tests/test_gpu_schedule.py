@@ -1,11 +1,12 @@
 """The tile schedule changes no bit of the results.
 
 Forward and backward outputs (SwiGLU and squared-ReLU experts) must be bitwise the same
-whether the expert GEMMs run 256-row tiles on CTA pairs (with each expert's odd last tile on
-single CTAs) or 128-row tiles on single CTAs only (MOE_GEMM_PAIR=0), and the forward variant
+whether the expert GEMMs run 256-row tiles on CTA pairs for the experts the tile tables pick
+(the rest on single CTAs; MOE_GEMM_PAIR=1), 128-row tiles on single CTAs only
+(MOE_GEMM_PAIR=0), or whatever the library's size rule picks (unset), and the forward variant
 that gathers GEMM1's rows from x and fuses the combine into GEMM2 must match the default
-forward bitwise.  Each schedule runs
-in its own process (the switch is read once per process).
+forward bitwise.  Each schedule runs in its own process (the switch is read once per
+process).
 """
 import hashlib
 import os
@@ -46,7 +47,7 @@ print(h.hexdigest())
 
 
 def _digest(env_extra, gated=True):
-    env = dict(os.environ)
+    env = {k: v for k, v in os.environ.items() if k != "MOE_GEMM_PAIR"}
     env.update(env_extra)
     script = _SCRIPT % {"root": ROOT, "gated": gated, "dff": 384 if gated else 512}
     r = subprocess.run([sys.executable, "-c", script], env=env,
@@ -57,5 +58,6 @@ def _digest(env_extra, gated=True):
 
 @pytest.mark.parametrize("gated", [True, False])   # SwiGLU, squared ReLU (no W3)
 def test_schedule_does_not_change_results(gated):
-    ref = _digest({}, gated)
+    ref = _digest({"MOE_GEMM_PAIR": "1"}, gated)
     assert _digest({"MOE_GEMM_PAIR": "0"}, gated) == ref
+    assert _digest({}, gated) == ref
