@@ -200,6 +200,17 @@ def test_forward_host_pipelined_back_to_back(moe):
         assert moe.moe_get_error(x) == 0
     for i in range(nb):
         assert torch.equal(ho[i].view(torch.int16), refs[i].view(torch.int16)), i
+    # an empty batch between full ones: nothing to copy, the events still order the streams
+    h0 = torch.empty(0, d, dtype=torch.bfloat16).pin_memory()
+    l0 = torch.empty(0, E, dtype=torch.float32).pin_memory()
+    moe.moe_forward_host_pipelined(h0, l0, g["W1"], g["W3"], g["W2"], k, h0, ws[0],
+                                   copy_stream=copies[0], events=events[0], stream=compute)
+    ho[0].fill_(7.0)
+    moe.moe_forward_host_pipelined(hx[0], hl[0], g["W1"], g["W3"], g["W2"], k, ho[0], ws[0],
+                                   copy_stream=copies[0], events=events[0], stream=compute)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(ws[0]) == 0
+    assert torch.equal(ho[0].view(torch.int16), refs[0].view(torch.int16))
 
 
 @pytest.mark.parametrize("T,flags", [(1, 0), (64, 0), (300, 0), (300, 2)])
