@@ -20,6 +20,29 @@
 #include "internal.h"
 
 namespace moe {
+
+// Programmatic dependent launch: the kernels of this file are launched with programmatic
+// stream serialization (launch_pdl), so a launch may start while the previous kernel in the
+// stream is still finishing; each kernel's first statement waits until that kernel has
+// completed and its writes are visible, before any global memory access.  This hides the
+// launch gap between back-to-back kernels; without the attribute the wait returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 namespace {
 
 // ------------------------------------------------------------------------------ routing
@@ -52,6 +75,7 @@ template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ topk,
     float* __restrict__ gate, int32_t* __restrict__ pos_local, int32_t* __restrict__ hist) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   constexpr int NB = EPL <= 8 ? 8 : (EPL <= 16 ? 4 : 2);
   static_assert(kRouteTokPerWarp % NB == 0, "");
   extern __shared__ uint32_t sm[];
@@ -156,6 +180,7 @@ __global__ void __launch_bounds__(256) scan_cols_kernel(const int32_t* __restric
                                                         int64_t nblk, int E,
                                                         int32_t* __restrict__ bbase,
                                                         int32_t* __restrict__ counts) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   __shared__ int part[8][32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int e = blockIdx.x * 32 + lane;
@@ -266,6 +291,7 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
                                                        int align, int32_t* __restrict__ offsets,
                                                        int32_t* __restrict__ poff, TileTables tt,
                                                        int with_tables, DevErr* err) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   __shared__ int warp_tot[32];
   __shared__ int total;
   __shared__ int s_poff[1024], s_a[1024], s_b[1024], s_pa[1024], s_pb[1024];
@@ -347,6 +373,7 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
                                                       int32_t* __restrict__ perm,
                                                       uint4* __restrict__ x_perm,
                                                       int64_t rows_cap, DevErr* err) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n16 = d >> 3;
@@ -422,6 +449,7 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const uint4* __restric
                                                           uint8_t* __restrict__ x_perm,
                                                           float* __restrict__ xscale,
                                                           int64_t rows_cap, DevErr* err) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n16 = d >> 3;  // 16-byte chunks of 8 bf16 per row
@@ -473,6 +501,7 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const uint4* __restric
 __global__ void __launch_bounds__(256) quantize_weights_fp8_kernel(
     const uint16_t* __restrict__ W, int K, int N, uint8_t* __restrict__ Wq,
     float* __restrict__ scales) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   __shared__ float red[8][32];
   __shared__ float sc[32];
   __shared__ uint8_t tile[32][36];
@@ -518,6 +547,7 @@ __global__ void __launch_bounds__(256) pad_rows_kernel(const int32_t* __restrict
                                                        int32_t* __restrict__ perm,
                                                        uint4* __restrict__ rows,
                                                        int64_t row16) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int e = blockIdx.x;
   const int64_t r0 = static_cast<int64_t>(poff[e]) + counts[e];
   const int64_t r1 = poff[e + 1];
@@ -545,6 +575,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
                                                       const int32_t* __restrict__ pos,
                                                       int64_t T, int k, int d,
                                                       uint4* __restrict__ out) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n8 = d >> 3;
@@ -597,6 +628,7 @@ __global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restri
                                                           const int32_t* __restrict__ pos,
                                                           int64_t T, int k, int d,
                                                           uint4* __restrict__ out) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n8 = d >> 3;
@@ -639,6 +671,7 @@ __global__ void __launch_bounds__(256) bwd_gate_rows_kernel(
     const uint4* __restrict__ dy, const float4* __restrict__ y, const float* __restrict__ gate,
     const int32_t* __restrict__ pos, int64_t T, int k, int d, uint4* __restrict__ dO,
     float* __restrict__ part) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n8 = d >> 3;
@@ -704,6 +737,7 @@ __global__ void __launch_bounds__(256) bwd_gate_finish_kernel(
     const float* __restrict__ part, const float* __restrict__ gate,
     const int32_t* __restrict__ topk, int64_t T, int k, int upt, int E,
     float* __restrict__ dgate, float* __restrict__ dlogits) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
@@ -774,27 +808,27 @@ template <int KC>
 cudaError_t launch_combine_kc(const float* y_rows, const float* gate, const int32_t* pos,
                               int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
   const int64_t units = T * ((d / 8 + kCombChunks - 1) / kCombChunks);
-  combine_kernel<KC><<<unit_grid(combine_kernel<KC>, units), 256, 0, s>>>(
-      reinterpret_cast<const float4*>(y_rows), gate, pos, T, k, d, reinterpret_cast<uint4*>(out));
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<KC>, dim3(unit_grid(combine_kernel<KC>, units)), dim3(256), 0,
+                    s, reinterpret_cast<const float4*>(y_rows), gate, pos, T, k, d,
+                    reinterpret_cast<uint4*>(out));
 }
 template <int KC>
 cudaError_t launch_combine_f32_kc(const float* rows, const int32_t* pos, int64_t T, int k, int d,
                                   uint16_t* out, cudaStream_t s) {
   const int64_t units = T * ((d / 8 + kCombChunks - 1) / kCombChunks);
-  combine_f32_kernel<KC><<<unit_grid(combine_f32_kernel<KC>, units), 256, 0, s>>>(
-      reinterpret_cast<const float4*>(rows), pos, T, k, d, reinterpret_cast<uint4*>(out));
-  return cudaGetLastError();
+  return launch_pdl(combine_f32_kernel<KC>, dim3(unit_grid(combine_f32_kernel<KC>, units)),
+                    dim3(256), 0, s, reinterpret_cast<const float4*>(rows), pos, T, k, d,
+                    reinterpret_cast<uint4*>(out));
 }
 template <int KC>
 cudaError_t launch_bwd_gate_kc(const uint16_t* dy, const float* y_rows, const float* gate,
                                const int32_t* pos, int64_t T, int k, int d, uint16_t* dO_rows,
                                float* part, cudaStream_t s) {
   const int64_t units = T * ((d / 8 + kCombChunks - 1) / kCombChunks);
-  bwd_gate_rows_kernel<KC><<<unit_grid(bwd_gate_rows_kernel<KC>, units), 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(dy), reinterpret_cast<const float4*>(y_rows), gate, pos, T,
-      k, d, reinterpret_cast<uint4*>(dO_rows), part);
-  return cudaGetLastError();
+  return launch_pdl(bwd_gate_rows_kernel<KC>, dim3(unit_grid(bwd_gate_rows_kernel<KC>, units)),
+                    dim3(256), 0, s, reinterpret_cast<const uint4*>(dy),
+                    reinterpret_cast<const float4*>(y_rows), gate, pos, T, k, d,
+                    reinterpret_cast<uint4*>(dO_rows), part);
 }
 
 }  // namespace
@@ -817,15 +851,14 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
   cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem));
   if (st != cudaSuccess) return st;
-  kern<<<static_cast<unsigned>(nblk), kRouteWarps * 32, smem, s>>>(logits, T, E, k, topk, gate,
-                                                                    pos_local, hist);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(static_cast<unsigned>(nblk)), dim3(kRouteWarps * 32), smem, s,
+                    logits, T, E, k, topk, gate, pos_local, hist);
 }
 
 cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* bbase,
                              int32_t* counts, cudaStream_t s) {
-  scan_cols_kernel<<<(E + 31) / 32, 256, 0, s>>>(hist, nblk, E, bbase, counts);
-  return cudaGetLastError();
+  return launch_pdl(scan_cols_kernel, dim3((E + 31) / 32), dim3(256), 0, s, hist, nblk, E, bbase,
+                    counts);
 }
 
 cudaError_t launch_offsets(const int32_t* counts, int E, int align, int32_t* offsets,
@@ -833,8 +866,8 @@ cudaError_t launch_offsets(const int32_t* counts, int E, int align, int32_t* off
                            cudaStream_t s) {
   TileTables tt{};
   if (tables) tt = *tables;
-  offsets_kernel<<<1, 1024, 0, s>>>(counts, E, align, offsets, poff, tt, tables ? 1 : 0, err);
-  return cudaGetLastError();
+  return launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, s, counts, E, align, offsets, poff, tt,
+                    tables ? 1 : 0, err);
 }
 
 cudaError_t launch_scatter(const uint16_t* x, int64_t T, int d, int E, int k,
@@ -842,10 +875,9 @@ cudaError_t launch_scatter(const uint16_t* x, int64_t T, int d, int E, int k,
                            int32_t* pos, int32_t* perm, uint16_t* x_perm, int64_t rows_cap,
                            DevErr* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  scatter_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(x), T, d, E, k, topk, bbase, poff, pos, perm,
-      reinterpret_cast<uint4*>(x_perm), rows_cap, err);
-  return cudaGetLastError();
+  return launch_pdl(scatter_kernel, dim3(grid_for_warps(T, 8)), dim3(256), 0, s,
+                    reinterpret_cast<const uint4*>(x), T, d, E, k, topk, bbase, poff, pos, perm,
+                    reinterpret_cast<uint4*>(x_perm), rows_cap, err);
 }
 
 cudaError_t launch_scatter_fp8(const uint16_t* x, int64_t T, int d, int E, int k,
@@ -853,23 +885,21 @@ cudaError_t launch_scatter_fp8(const uint16_t* x, int64_t T, int d, int E, int k
                                int32_t* pos, int32_t* perm, uint8_t* x_perm, float* xscale,
                                int64_t rows_cap, DevErr* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  scatter_fp8_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(x), T, d, E, k, topk, bbase, poff, pos, perm, x_perm, xscale,
-      rows_cap, err);
-  return cudaGetLastError();
+  return launch_pdl(scatter_fp8_kernel, dim3(grid_for_warps(T, 8)), dim3(256), 0, s,
+                    reinterpret_cast<const uint4*>(x), T, d, E, k, topk, bbase, poff, pos, perm,
+                    x_perm, xscale, rows_cap, err);
 }
 
 cudaError_t launch_quantize_weights_fp8(const uint16_t* W, int E, int K, int N, uint8_t* Wq,
                                         float* scales, cudaStream_t s) {
-  quantize_weights_fp8_kernel<<<dim3(N / 32, E), 256, 0, s>>>(W, K, N, Wq, scales);
-  return cudaGetLastError();
+  return launch_pdl(quantize_weights_fp8_kernel, dim3(N / 32, E), dim3(256), 0, s, W, K, N, Wq,
+                    scales);
 }
 
 cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, int32_t* perm,
                             void* rows, int64_t row_bytes, cudaStream_t s) {
-  pad_rows_kernel<<<E, 256, 0, s>>>(counts, poff, perm, reinterpret_cast<uint4*>(rows),
-                                    row_bytes / 16);
-  return cudaGetLastError();
+  return launch_pdl(pad_rows_kernel, dim3(E), dim3(256), 0, s, counts, poff, perm,
+                    reinterpret_cast<uint4*>(rows), row_bytes / 16);
 }
 
 cudaError_t launch_combine(const float* y_rows, const float* gate, const int32_t* pos,
@@ -887,9 +917,8 @@ cudaError_t launch_bwd_gate(const uint16_t* dy, const float* y_rows, const float
       MOE_DISPATCH_KC(k, launch_bwd_gate_kc, dy, y_rows, gate, pos, T, k, d, dO_rows, part, s);
   if (st != cudaSuccess) return st;
   const int upt = (d / 8 + kCombChunks - 1) / kCombChunks;
-  bwd_gate_finish_kernel<<<grid_for_warps(T, 8), 256, 0, s>>>(part, gate, topk, T, k, upt, E,
-                                                              dgate, dlogits);
-  return cudaGetLastError();
+  return launch_pdl(bwd_gate_finish_kernel, dim3(grid_for_warps(T, 8)), dim3(256), 0, s, part,
+                    gate, topk, T, k, upt, E, dgate, dlogits);
 }
 
 cudaError_t launch_combine_f32(const float* rows, const int32_t* pos, int64_t T, int k, int d,
