@@ -649,6 +649,9 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
   if constexpr (PAIR) cluster_sync_all();  // peer barriers initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Programmatic dependent launch: the set-up above (barriers, TMEM) may overlap the end of
+  // the previous kernel in the stream; global memory is touched only after it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   int64_t ntiles64;
   if constexpr (Tr::kRowsM) ntiles64 = static_cast<int64_t>(PAIR ? p.n_pt[0] : p.n_mt[0]) * p.nb;
@@ -1015,13 +1018,15 @@ cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const 
   cfg.blockDim = dim3(EpiCfg<KIND, PAIR>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 1 : 0;
+  cfg.numAttrs = PAIR ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, pp);
 }
 
