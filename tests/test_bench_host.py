@@ -1,0 +1,59 @@
+"""Host-side logic of bench.py, on the CPU: the algorithmic FLOP and byte counts behind the
+reported roofline fractions, and the launch counts that follow the library's rule for CTA
+pairs (MOE_GEMM_PAIR: "0" never, "1" whenever T > 128, unset T > 128 and T k d d_ff >= 2^37).
+"""
+import pytest
+
+import moe_synth
+
+
+@pytest.fixture(scope="module")
+def bench():
+    import bench as b
+    return b
+
+
+def test_algorithmic_counts_of_the_large_workload(bench):
+    w = moe_synth.by_name("large_skewed")
+    P = w.T * w.k
+    a = bench._algorithmic(w, P)
+    # SwiGLU expert: gate, up and down projections, 2 FLOP per multiply-add each, i.e. 6 d d_ff
+    # per token-expert pair (report translation, section 1.4)
+    assert a["gemm_flops"] == 6 * w.d * w.dff * P
+    assert a["gemm1_flops"] + a["gemm2_flops"] == a["gemm_flops"]
+    assert abs(a["gemm_flops"] / 1e12 - 11.545) < 5e-4
+    # dispatch: logits read (fp32), 16 B of routing results per pair, x read and x_perm written
+    assert a["dispatch_bytes"] == w.T * w.E * 4 + P * 16 + w.T * w.d * 2 + P * w.d * 2
+    assert abs(a["dispatch_bytes"] / 1e9 - 2.133) < 5e-4
+    # combine: fp32 expert rows read, gate + pos read, bf16 output written
+    assert a["combine_bytes"] == P * w.d * 4 + P * 8 + w.T * w.d * 2
+    assert abs(a["combine_bytes"] / 1e9 - 3.994) < 5e-4
+
+
+def test_algorithmic_counts_without_the_gate_projection(bench):
+    w = moe_synth.by_name("large_skewed_relu2")
+    P = w.T * w.k
+    a = bench._algorithmic(w, P)
+    assert a["gemm_flops"] == 4 * w.d * w.dff * P
+    assert a["gemm1_flops"] == a["gemm2_flops"] == 2 * w.d * w.dff * P
+
+
+@pytest.mark.parametrize("mode,name,pairs", [
+    (None, "large_skewed", True),    # T k d d_ff = 1.9e12
+    (None, "fwd_bwd", True),         # 4.1e11
+    (None, "mid", False),            # 5.2e10 < 2^37
+    (None, "tiny", False),           # T = 64 <= 128
+    ("0", "large_skewed", False),
+    ("1", "mid", True),
+    ("1", "tiny", False),            # no expert can fill a pair tile
+])
+def test_pair_rule_and_launch_counts(bench, monkeypatch, mode, name, pairs):
+    if mode is None:
+        monkeypatch.delenv("MOE_GEMM_PAIR", raising=False)
+    else:
+        monkeypatch.setenv("MOE_GEMM_PAIR", mode)
+    w = moe_synth.by_name(name)
+    assert bench._row_pairs(w.T, w.k, w.d, w.dff) == pairs
+    # each row-grouped GEMM adds a single-CTA launch beside its pair launch
+    assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)
+    assert bench.bwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)
