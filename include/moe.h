@@ -31,6 +31,11 @@
  *     launch is asynchronous on `stream`.  The workspace `ws` (device memory, 256-byte
  *     aligned, size from moe_workspace_bytes) is caller-owned; calls that share one ws must
  *     be ordered on the GPU (same stream, or synchronised).
+ *   - The kernels are launched with programmatic stream serialization and each waits for
+ *     the previous kernel in the stream to complete before touching global memory, so
+ *     stream order holds as usual: work the caller queues before a call is visible to it,
+ *     and a caller's own kernel queued after a call sees its outputs (a caller kernel that
+ *     itself opts into programmatic serialization must wait the same way).
  *   - Argument errors are detected on the host before anything is launched and returned as
  *     a status; nothing is written then.  Problems detected on the device (a bounded wait
  *     that ran out, an index out of range) are recorded in an error word inside `ws` and
