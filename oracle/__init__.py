@@ -46,6 +46,16 @@ def _load():
             getattr(lib, n).argtypes = [_p] * 6 + dims + [_int, _int, _p, _i64, _p, _p, _p]
         for n in ("oracle_backward_dw_bf16", "oracle_backward_dw_f64"):
             getattr(lib, n).argtypes = [_p] * 6 + dims + [_int, _int, _p, _int, _p, _p, _p]
+        lib.oracle_round_spread_bf16.restype = ctypes.c_double
+        lib.oracle_round_spread_bf16.argtypes = [ctypes.c_double, ctypes.c_double]
+        lib.oracle_sum_bound.restype = ctypes.c_double
+        lib.oracle_sum_bound.argtypes = [_p, _i64, ctypes.c_double, _p]
+        lib.oracle_forward_tokens_flip_bf16.argtypes = [_p] * 5 + dims + [_p, _p, _i64, _p, _p]
+        lib.oracle_backward_tokens_flip_bf16.argtypes = \
+            [_p] * 6 + dims + [_int, _p, _p, _i64] + [_p] * 6
+        lib.oracle_backward_dw_flip_bf16.argtypes = \
+            [_p] * 6 + dims + [_int, _p, _p, _int] + [_p] * 6
+        lib.oracle_pair_operands_bf16.argtypes = [_p] * 6 + dims + [_i64, _int] + [_p] * 12
         _lib = lib
     return _lib
 
@@ -228,3 +238,106 @@ def layer_flops(pairs: int, d: int, dff: int, gated: bool = True) -> int:
     down projections: three d x dff multiply-adds), as the report's section 1.4 counts it;
     4*d*dff without the gate projection (the cheap activation)."""
     return (6 if gated else 4) * d * dff * pairs
+
+
+# --------------------------------------------------------- rounding-flip allowance
+# Model of fp32 arithmetic behind the allowance (see the oracle's FlipModel): an fp32 sum lies
+# within ACC = lambda * eps * sqrt(sum of its squared running partial sums) of the exact sum,
+# with eps = 2^-23, twice the unit roundoff of round-to-nearest (a margin for the hardware's
+# order of accumulation), and lambda = 6, so that under the independent-error model a sum
+# leaves the bound with probability below 2 exp(-18) = 3e-8 (and far less with errors of at
+# most 2^-24); an element-wise fp32 evaluation lies within 16 eps of its value; the fp32
+# softmax gate within 32 eps.
+EPS32 = 2.0 ** -23
+FLIP_MODEL = (6 * EPS32, 16 * EPS32, 32 * EPS32)
+
+
+def _model(model):
+    m = np.asarray(FLIP_MODEL if model is None else model, np.float64)
+    assert m.shape == (3,)
+    return m
+
+
+def round_spread(v: float, dv: float) -> float:
+    """Largest change of the bf16 rounding of v when v moves by at most dv."""
+    return _load().oracle_round_spread_bf16(float(v), float(dv))
+
+
+def sum_bound(t, acc=FLIP_MODEL[0]):
+    """(exact sum of t in index order, the flip model's bound on an fp32 evaluation of it)."""
+    t = _c(t, np.float64)
+    s = ctypes.c_double(0.0)
+    b = _load().oracle_sum_bound(_ptr(t), t.size, float(acc), ctypes.byref(s))
+    return s.value, b
+
+
+def forward_tokens_flip(inp, k, tokens=None, model=None):
+    """forward_tokens (h rounded, bf16 inputs) plus the rounding-flip allowance of each output
+    element: returns (y [n,d], ay [n,d]), ay the largest change that h values which may round
+    the other way in fp32 arithmetic can cause in that element."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    x, W1, W3, W2 = (_prep(a, "bf16") for a in (x, W1, W3, W2))
+    tok = None if tokens is None else _c(tokens, np.int64)
+    n = T if tok is None else len(tok)
+    y = np.empty((n, d), np.float64)
+    ay = np.empty((n, d), np.float64)
+    m = _model(model)
+    _check(_load().oracle_forward_tokens_flip_bf16(
+        _ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), T, d, E, k, dff, _ptr(m), _ptr(tok),
+        n, _ptr(y), _ptr(ay)))
+    return y, ay
+
+
+def backward_tokens_flip(inp, dy, k, tokens=None, round_h=True, model=None):
+    """backward_tokens (round_grad on, bf16 inputs) plus the rounding-flip allowance of each
+    output: returns ((dx, dgate, dlogits), (adx, adgate, adlogits)).  An implementation that
+    rounds h, dO, da and db to bf16 after fp32 arithmetic obeying the flip model matches
+    within the stated tolerance plus these allowances."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    x, W1, W3, W2, dy = (_prep(a, "bf16") for a in (x, W1, W3, W2, dy))
+    tok = None if tokens is None else _c(tokens, np.int64)
+    n = T if tok is None else len(tok)
+    out = [np.empty(s, np.float64) for s in ((n, d), (n, k), (n, E)) * 2]
+    m = _model(model)
+    _check(_load().oracle_backward_tokens_flip_bf16(
+        _ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), T, d, E, k, dff,
+        int(round_h), _ptr(m), _ptr(tok), n, *[_ptr(a) for a in out]))
+    return tuple(out[:3]), tuple(out[3:])
+
+
+def backward_dw_flip(inp, dy, k, experts, round_h=True, model=None):
+    """backward_dw (round_grad on, bf16 inputs) plus the rounding-flip allowances: returns
+    ((dW1, dW3, dW2), (a1, a3, a2)); dW3 and a3 are None without W3."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    x, W1, W3, W2, dy = (_prep(a, "bf16") for a in (x, W1, W3, W2, dy))
+    ex = _c(experts, np.int32)
+    n = len(ex)
+    g = W3 is not None
+    dW1, a1 = np.empty((n, d, dff)), np.empty((n, d, dff))
+    dW3, a3 = (np.empty((n, d, dff)), np.empty((n, d, dff))) if g else (None, None)
+    dW2, a2 = np.empty((n, dff, d)), np.empty((n, dff, d))
+    m = _model(model)
+    _check(_load().oracle_backward_dw_flip_bf16(
+        _ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), T, d, E, k, dff,
+        int(round_h), _ptr(m), _ptr(ex), n, _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(a1),
+        _ptr(a3), _ptr(a2)))
+    return (dW1, dW3, dW2), (a1, a3, a2)
+
+
+def pair_operands(inp, dy, k, t, j, model=None):
+    """The bf16 operands of token t's slot-j pair and their flip intervals (test support): a
+    dict with e, g, h, vh (h before rounding), dO, da, db, and Dh, DdO, Dda, Ddb of shape
+    [n, 2]: the signed interval (lo <= 0 <= hi) within which another rounding may lie."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    x, W1, W3, W2, dy = (_prep(a, "bf16") for a in (x, W1, W3, W2, dy))
+    names = ("h", "vh", "Dh", "dO", "DdO", "da", "Dda", "db", "Ddb")
+    sizes = (dff, dff, (dff, 2), d, (d, 2), dff, (dff, 2), dff, (dff, 2))
+    r = {nm: np.empty(sz, np.float64) for nm, sz in zip(names, sizes)}
+    e = ctypes.c_int(0)
+    g = ctypes.c_double(0.0)
+    m = _model(model)
+    _check(_load().oracle_pair_operands_bf16(
+        _ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), T, d, E, k, dff, int(t),
+        int(j), _ptr(m), ctypes.byref(e), ctypes.byref(g), *[_ptr(r[nm]) for nm in names]))
+    r["e"], r["g"] = e.value, g.value
+    return r

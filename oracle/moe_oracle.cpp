@@ -38,6 +38,15 @@
 //  * backward: the derivative of the bf16 rounding of h is taken as 1; with round_grad the
 //    matrix-product operands dO = g dy, da and db are rounded to bf16 (round to nearest
 //    even) like h, each product accumulating exactly (fp64).
+//  * rounding-flip allowance (a test bound, not part of the layer): both the oracle and an
+//    fp32 implementation round h, dO, da and db to bf16, but from pre-rounding values that
+//    differ by the fp32 implementation's own rounding errors, so an operand whose value lies
+//    near a bf16 rounding midpoint may round to the neighbouring bf16 value there.  For each
+//    such operand the oracle computes, from its own fp64 values alone, the largest distance
+//    between the two roundings, on each side, using a model of fp32 arithmetic (FlipModel
+//    below); every gradient element then gets, on top of the stated tolerance, the largest
+//    change that those operands can cause together (each operand's signed deviation
+//    interval times what multiplies it in the element, summed over the element's terms).
 //
 // All arithmetic is fp64.  bf16 inputs are passed as their raw 16-bit patterns and
 // widened exactly.  Loops run in the plain order of the definitions; OpenMP only
@@ -133,17 +142,29 @@ void route_token(const double* l, int E, int k, int32_t* idx, double* gate) {
 // One expert applied to one row x[0..d): a = x W1, b = x W3, h = silu(a) * b, o = h W2;
 // without W3 (W3e null) the cheap activation: h = relu(a)^2 (b is left zero).
 // W1e, W3e are [d][dff] and W2e is [dff][d], row-major.
+// Optional by-products of ffn_row for the rounding-flip allowance: sa, sb = the sums of the
+// squared running partial sums of a and b (in the order the loops below form a and b), and
+// vh = h before its bf16 rounding.
+struct FwdTrace {
+  double* sa;
+  double* sb;
+  double* vh;
+};
+
 template <class V>
 void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int dff, int round_h,
-             double* a, double* b, double* h, double* o) {
+             double* a, double* b, double* h, double* o, const FwdTrace* tr = nullptr) {
   for (int f = 0; f < dff; ++f) { a[f] = 0.0; b[f] = 0.0; }
+  if (tr) for (int f = 0; f < dff; ++f) { tr->sa[f] = 0.0; tr->sb[f] = 0.0; }
   for (int c = 0; c < d; ++c) {
     const double xc = widen(x[c]);
     const V* w1 = W1e + static_cast<int64_t>(c) * dff;
     for (int f = 0; f < dff; ++f) a[f] += xc * widen(w1[f]);
+    if (tr) for (int f = 0; f < dff; ++f) tr->sa[f] += a[f] * a[f];
     if (W3e) {
       const V* w3 = W3e + static_cast<int64_t>(c) * dff;
       for (int f = 0; f < dff; ++f) b[f] += xc * widen(w3[f]);
+      if (tr) for (int f = 0; f < dff; ++f) tr->sb[f] += b[f] * b[f];
     }
   }
   for (int f = 0; f < dff; ++f) {
@@ -154,6 +175,7 @@ void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int df
       const double r = a[f] > 0.0 ? a[f] : 0.0;
       hv = r * r;
     }
+    if (tr) tr->vh[f] = hv;
     h[f] = round_h ? round_bf16(hv) : hv;
   }
   for (int c = 0; c < d; ++c) o[c] = 0.0;
@@ -172,20 +194,32 @@ void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int df
 // With round_grad != 0, dO, da and db are rounded to bf16 where they become operands of a
 // matrix product (dh, dxp and the weight gradients), the reading that every product of the
 // layer takes bf16 operands and accumulates exactly (here in fp64).
+// Optional by-products of ffn_row_bwd for the rounding-flip allowance: sdh = the sums of the
+// squared running partial sums of dh; vda, vdb = da and db before their bf16 rounding.
+struct BwdTrace {
+  double* sdh;
+  double* vda;
+  double* vdb;
+};
+
 template <class V>
 void ffn_row_bwd(const V* W1e, const V* W3e, const V* W2e, int d, int dff, double g,
                  const double* dy, const double* a, const double* b, const double* o,
                  int round_grad, double* dgate, double* dO, double* dh, double* da, double* db,
-                 double* dxp) {
+                 double* dxp, const BwdTrace* tr = nullptr) {
   double s = 0.0;
   for (int c = 0; c < d; ++c) s += o[c] * dy[c];
   *dgate = s;
   for (int c = 0; c < d; ++c) dO[c] = round_grad ? round_bf16(g * dy[c]) : g * dy[c];
   for (int f = 0; f < dff; ++f) {
     const V* w2 = W2e + static_cast<int64_t>(f) * d;
-    double acc = 0.0;
-    for (int c = 0; c < d; ++c) acc += dO[c] * widen(w2[c]);
+    double acc = 0.0, sq = 0.0;
+    for (int c = 0; c < d; ++c) {
+      acc += dO[c] * widen(w2[c]);
+      if (tr) sq += acc * acc;
+    }
     dh[f] = acc;
+    if (tr) tr->sdh[f] = sq;
   }
   for (int f = 0; f < dff; ++f) {
     if (W3e) {
@@ -195,6 +229,10 @@ void ffn_row_bwd(const V* W1e, const V* W3e, const V* W2e, int d, int dff, doubl
     } else {
       da[f] = dh[f] * 2.0 * (a[f] > 0.0 ? a[f] : 0.0);
       db[f] = 0.0;
+    }
+    if (tr) {
+      tr->vda[f] = da[f];
+      tr->vdb[f] = db[f];
     }
     if (round_grad) {
       da[f] = round_bf16(da[f]);
@@ -211,6 +249,117 @@ void ffn_row_bwd(const V* W1e, const V* W3e, const V* W2e, int d, int dff, doubl
       for (int f = 0; f < dff; ++f) acc += da[f] * widen(w1[f]);
     }
     dxp[c] = acc;
+  }
+}
+
+// ---------------------------------------------------------- rounding-flip allowance
+// Model of the fp32 arithmetic of an implementation that rounds the same operands to bf16
+// (the allowance's only parameters):
+//  * acc: an fp32 sum s = t_1 + ... + t_n lies within acc * sqrt(sum_j s_j^2) of the exact
+//    sum, s_j its running partial sums.  If each addition's rounding error is independent,
+//    zero-mean and at most eps relative, the Azuma-Hoeffding inequality bounds the sum's error
+//    by lambda * eps * sqrt(sum_j s_j^2) with probability at least 1 - 2 exp(-lambda^2 / 2)
+//    (the probabilistic rounding-error analysis of Higham and Mary, SIAM J. Sci. Comput.
+//    2019); acc = lambda * eps.
+//  * ev: an element-wise fp32 evaluation (a product, silu and its derivative, the rounding of
+//    an fp64-exact value to fp32) lies within ev * |value|.
+//  * gate: the fp32 softmax gate lies within gate * g.
+struct FlipModel {
+  double acc, ev, gate;
+};
+
+// Largest change of the bf16 rounding of v when v moves by at most dv.  Rounding is
+// monotone, so the extremes are the roundings of v - dv and v + dv.
+double round_spread(double v, double dv) {
+  const double r = round_bf16(v);
+  return std::fmax(std::fabs(round_bf16(v + dv) - r), std::fabs(round_bf16(v - dv) - r));
+}
+
+// Signed deviation interval of that rounding: round(v - dv) - round(v) <= 0 and
+// round(v + dv) - round(v) >= 0.
+struct Dev {
+  double lo, hi;
+  double mag() const { return std::fmax(-lo, hi); }
+};
+Dev round_dev(double v, double dv) {
+  const double r = round_bf16(v);
+  return Dev{round_bf16(v - dv) - r, round_bf16(v + dv) - r};
+}
+
+// Extremes of c * delta for delta in [lo, hi], added to an interval [dn, up].
+inline void add_scaled(double c, const Dev& dv, double* dn, double* up) {
+  const double p = c * dv.lo, q = c * dv.hi;
+  *dn += std::fmin(p, q);
+  *up += std::fmax(p, q);
+}
+
+// Lipschitz constants over the whole real line: |silu'(a)| <= 1.1, |silu''(a)| <= 0.5
+// (the largest values are 1.0998 near a = 2.4 and 0.5 at a = 0).
+constexpr double kSiluLip = 1.1;
+constexpr double kSiluPrimeLip = 0.5;
+
+// z = x y with x known to within dx and y to within dy: z is known to within
+// |x| dy + |y| dx + dx dy.
+inline double prod_unc(double x, double dx, double y, double dy) {
+  return std::fabs(x) * dy + std::fabs(y) * dx + dx * dy;
+}
+
+// Flip intervals of h = bf16(silu(a) b) (bf16(relu(a)^2) without W3) of one pair, from its
+// forward sums a, b [dff] and their trace: Dh [dff].
+void h_flip_bounds(int dff, bool gated, const double* a, const double* b, const FwdTrace& ft,
+                   const FlipModel& M, Dev* Dh) {
+  for (int f = 0; f < dff; ++f) {
+    const double dA = M.acc * std::sqrt(ft.sa[f]);
+    const double dB = gated ? M.acc * std::sqrt(ft.sb[f]) : 0.0;
+    const double s = gated ? a[f] * sigmoid(a[f]) : 0.0;  // silu(a)
+    const double r = a[f] > 0.0 ? a[f] : 0.0;              // relu(a)
+    const double dv = gated ? prod_unc(s, kSiluLip * dA, b[f], dB) : prod_unc(r, dA, r, dA);
+    Dh[f] = round_dev(ft.vh[f], dv + M.ev * std::fabs(ft.vh[f]));
+  }
+}
+
+// Flip bounds of one token-expert pair: the signed intervals within which the other
+// implementation's bf16 rounding of each operand lies around the oracle's.  In: the pair's
+// gate g and dy [d]; the forward's a, b [dff] and their trace; the backward's dh [dff] and its
+// trace.  Out: Dh [dff] (h), DdO [d] (dO = g dy), Dda [dff], Ddb [dff] (da, db; zero without
+// W3).
+template <class V>
+void pair_flip_bounds(const V* W2e, int d, int dff, bool gated, double g, const double* dy,
+                      const double* a, const double* b, const FwdTrace& ft, const double* dh,
+                      const BwdTrace& bt, const FlipModel& M, Dev* Dh, Dev* DdO, Dev* Dda,
+                      Dev* Ddb) {
+  // dO: the fp32 product of the fp32 gate and dy, then bf16
+  std::vector<int> flagged;  // columns c whose dO may round the other way
+  for (int c = 0; c < d; ++c) {
+    const double v = g * dy[c];
+    DdO[c] = round_dev(v, std::fabs(dy[c]) * M.gate * g + M.ev * std::fabs(v));
+    if (DdO[c].mag() != 0.0) flagged.push_back(c);
+  }
+  h_flip_bounds(dff, gated, a, b, ft, M, Dh);
+  for (int f = 0; f < dff; ++f) {
+    const double dA = M.acc * std::sqrt(ft.sa[f]);
+    const double dB = gated ? M.acc * std::sqrt(ft.sb[f]) : 0.0;
+    const double s = gated ? a[f] * sigmoid(a[f]) : 0.0;  // silu(a)
+    const double r = a[f] > 0.0 ? a[f] : 0.0;              // relu(a)
+    // dh = sum_c dO_c W2[f][c]: its accumulation error plus every dO flip times |W2|
+    const V* w2 = W2e + static_cast<int64_t>(f) * d;
+    double ddh = M.acc * std::sqrt(bt.sdh[f]);
+    for (int c : flagged) ddh += DdO[c].mag() * std::fabs(widen(w2[c]));
+    // da = dh q with q = b silu'(a) (2 relu(a) without W3); db = dh silu(a)
+    double q, dq;
+    if (gated) {
+      const double sg = sigmoid(a[f]);
+      const double sp = sg * (1.0 + a[f] * (1.0 - sg));
+      q = b[f] * sp;
+      dq = prod_unc(b[f], dB, sp, kSiluPrimeLip * dA);
+    } else {
+      q = 2.0 * r;
+      dq = 2.0 * dA;
+    }
+    Dda[f] = round_dev(bt.vda[f], prod_unc(dh[f], ddh, q, dq) + M.ev * std::fabs(bt.vda[f]));
+    Ddb[f] = gated ? round_dev(bt.vdb[f], prod_unc(dh[f], ddh, s, kSiluLip * dA) +
+                                              M.ev * std::fabs(bt.vdb[f]))
+                   : Dev{0.0, 0.0};
   }
 }
 
@@ -231,15 +380,28 @@ bool dims_ok(int64_t T, int d, int E, int k, int dff) {
 }
 
 // Brute-force forward for a list of tokens: route each token, run its k experts on its own
-// row, sum gate-weighted outputs.
+// row, sum gate-weighted outputs.  With a flip model M (round_h on), also the rounding-flip
+// allowance of each output element (ay [n,d]): the interval sum over j and f of
+// g_j W2[e_j][f][c] Dh_jf, reported as max(up, -down).
 template <class V>
 int forward_tokens(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
-                   const Dims& D, int round_h, const int64_t* tokens, int64_t n, double* y) {
+                   const Dims& D, int round_h, const int64_t* tokens, int64_t n, double* y,
+                   const FlipModel* M = nullptr, double* ay = nullptr) {
+  if (M && !round_h) return -1;
   int bad = 0;
 #pragma omp parallel
   {
     std::vector<int32_t> idx(D.k);
     std::vector<double> gate(D.k), a(D.dff), b(D.dff), h(D.dff), o(D.d);
+    std::vector<double> sa, sb, vh, ydn, yup;
+    std::vector<Dev> Dh;
+    if (M) {
+      for (auto* v : {&sa, &sb, &vh}) v->assign(D.dff, 0.0);
+      ydn.assign(D.d, 0.0);
+      yup.assign(D.d, 0.0);
+      Dh.resize(D.dff);
+    }
+    const FwdTrace ft{sa.data(), sb.data(), vh.data()};
 #pragma omp for schedule(dynamic, 1)
     for (int64_t i = 0; i < n; ++i) {
       const int64_t t = tokens ? tokens[i] : i;
@@ -251,12 +413,23 @@ int forward_tokens(const V* x, const double* logits, const V* W1, const V* W3, c
       route_token(logits + t * D.E, D.E, D.k, idx.data(), gate.data());
       double* yt = y + i * D.d;
       for (int c = 0; c < D.d; ++c) yt[c] = 0.0;
+      if (M) for (int c = 0; c < D.d; ++c) ydn[c] = yup[c] = 0.0;
       for (int j = 0; j < D.k; ++j) {
         const int e = idx[j];
         ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, round_h,
-                a.data(), b.data(), h.data(), o.data());
+                a.data(), b.data(), h.data(), o.data(), M ? &ft : nullptr);
         for (int c = 0; c < D.d; ++c) yt[c] += gate[j] * o[c];
+        if (!M) continue;
+        h_flip_bounds(D.dff, W3 != nullptr, a.data(), b.data(), ft, *M, Dh.data());
+        const V* W2e = w2of(W2, D, e);
+        for (int f = 0; f < D.dff; ++f) {
+          if (Dh[f].mag() == 0.0) continue;
+          const V* w2 = W2e + static_cast<int64_t>(f) * D.d;
+          for (int c = 0; c < D.d; ++c) add_scaled(gate[j] * widen(w2[c]), Dh[f], &ydn[c], &yup[c]);
+        }
       }
+      if (M && ay)
+        for (int c = 0; c < D.d; ++c) ay[i * D.d + c] = std::fmax(yup[c], -ydn[c]);
     }
   }
   return bad ? -1 : 0;
@@ -331,17 +504,44 @@ int forward_permuted(const V* x, const double* logits, const V* W1, const V* W3,
 
 // Per-token backward (brute force): dx_t = sum_j dxp_j, dgate_t, and dlogits_t through the
 // softmax over the selected logits: dl_{e_j} = g_j (dgate_j - sum_i g_i dgate_i), 0 elsewhere.
+// With a flip model M (round_grad on), also the rounding-flip allowance of each output
+// (adx [n,d], adg [n,k], adl [n,E]; null pointers skip one): the largest |change| of the
+// output when every flagged operand takes any value of its deviation interval, namely
+//   dx_t[c]:   sum_j sum_f W1[e_j][c][f] Dda_jf + W3[e_j][c][f] Ddb_jf,
+//   dgate_tj:  sum_f m_jf Dh_jf with m_jf = sum_c W2[e_j][f][c] dy_t[c] (the multiplier of
+//              h_f in <h W2, dy>),
+//   dl_{e_j}:  sum_i c_ji dgate_ti, c_jj = g_j (1 - g_j), c_ji = -g_j g_i,
+// each evaluated as an interval sum and reported as max(up, -down).
 template <class V, class G>
 int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
                     const G* dy, const Dims& D, int round_h, int round_grad,
                     const int64_t* tokens, int64_t n, double* dx, double* dgate,
-                    double* dlogits) {
+                    double* dlogits, const FlipModel* M = nullptr, double* adx = nullptr,
+                    double* adg = nullptr, double* adl = nullptr) {
+  if (M && !round_grad) return -1;
   int bad = 0;
 #pragma omp parallel
   {
     std::vector<int32_t> idx(D.k);
     std::vector<double> gate(D.k), a(D.dff), b(D.dff), h(D.dff), o(D.d), dyv(D.d), dO(D.d),
         dh(D.dff), da(D.dff), db(D.dff), dxp(D.d);
+    // flip-allowance work arrays
+    std::vector<double> sa, sb, vh, sdh, vda, vdb, xdn, xup, gdn, gup;
+    std::vector<Dev> Dh, DdO, Dda, Ddb;
+    std::vector<int> live;
+    if (M) {
+      for (auto* v : {&sa, &sb, &vh, &sdh, &vda, &vdb}) v->assign(D.dff, 0.0);
+      Dh.resize(D.dff);
+      Dda.resize(D.dff);
+      Ddb.resize(D.dff);
+      DdO.resize(D.d);
+      xdn.assign(D.d, 0.0);
+      xup.assign(D.d, 0.0);
+      gdn.assign(D.k, 0.0);
+      gup.assign(D.k, 0.0);
+    }
+    const FwdTrace ft{sa.data(), sb.data(), vh.data()};
+    const BwdTrace bt{sdh.data(), vda.data(), vdb.data()};
 #pragma omp for schedule(dynamic, 1)
     for (int64_t i = 0; i < n; ++i) {
       const int64_t t = tokens ? tokens[i] : i;
@@ -354,15 +554,44 @@ int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, 
       for (int c = 0; c < D.d; ++c) dyv[c] = widen(dy[t * D.d + c]);
       double* dxt = dx ? dx + i * D.d : nullptr;
       if (dxt) for (int c = 0; c < D.d; ++c) dxt[c] = 0.0;
+      if (M) {
+        for (int c = 0; c < D.d; ++c) xdn[c] = xup[c] = 0.0;
+      }
       std::vector<double> dg(D.k);
       for (int j = 0; j < D.k; ++j) {
         const int e = idx[j];
         ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, round_h,
-                a.data(), b.data(), h.data(), o.data());
+                a.data(), b.data(), h.data(), o.data(), M ? &ft : nullptr);
         ffn_row_bwd(w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, gate[j],
                     dyv.data(), a.data(), b.data(), o.data(), round_grad, &dg[j], dO.data(),
-                    dh.data(), da.data(), db.data(), dxp.data());
+                    dh.data(), da.data(), db.data(), dxp.data(), M ? &bt : nullptr);
         if (dxt) for (int c = 0; c < D.d; ++c) dxt[c] += dxp[c];
+        if (!M) continue;
+        const V* W1e = w13(W1, D, e);
+        const V* W3e = w13(W3, D, e);
+        const V* W2e = w2of(W2, D, e);
+        pair_flip_bounds(W2e, D.d, D.dff, W3e != nullptr, gate[j], dyv.data(), a.data(),
+                         b.data(), ft, dh.data(), bt, *M, Dh.data(), DdO.data(), Dda.data(),
+                         Ddb.data());
+        live.clear();  // columns f with a flagged da or db
+        for (int f = 0; f < D.dff; ++f)
+          if (Dda[f].mag() != 0.0 || Ddb[f].mag() != 0.0) live.push_back(f);
+        for (int c = 0; c < D.d; ++c) {
+          const V* w1 = W1e + static_cast<int64_t>(c) * D.dff;
+          const V* w3 = W3e ? W3e + static_cast<int64_t>(c) * D.dff : nullptr;
+          for (int f : live) {
+            add_scaled(widen(w1[f]), Dda[f], &xdn[c], &xup[c]);
+            if (w3) add_scaled(widen(w3[f]), Ddb[f], &xdn[c], &xup[c]);
+          }
+        }
+        gdn[j] = gup[j] = 0.0;
+        for (int f = 0; f < D.dff; ++f) {
+          if (Dh[f].mag() == 0.0) continue;
+          const V* w2 = W2e + static_cast<int64_t>(f) * D.d;
+          double m = 0.0;
+          for (int c = 0; c < D.d; ++c) m += widen(w2[c]) * dyv[c];
+          add_scaled(m, Dh[f], &gdn[j], &gup[j]);
+        }
       }
       if (dgate) for (int j = 0; j < D.k; ++j) dgate[i * D.k + j] = dg[j];
       if (dlogits) {
@@ -372,6 +601,24 @@ int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, 
         for (int j = 0; j < D.k; ++j) sgd += gate[j] * dg[j];
         for (int j = 0; j < D.k; ++j) dl[idx[j]] = gate[j] * (dg[j] - sgd);
       }
+      if (!M) continue;
+      if (adx)
+        for (int c = 0; c < D.d; ++c) adx[i * D.d + c] = std::fmax(xup[c], -xdn[c]);
+      if (adg)
+        for (int j = 0; j < D.k; ++j) adg[i * D.k + j] = std::fmax(gup[j], -gdn[j]);
+      if (adl) {
+        double* al = adl + i * D.E;
+        for (int e = 0; e < D.E; ++e) al[e] = 0.0;
+        for (int j = 0; j < D.k; ++j) {
+          double dn = 0.0, up = 0.0;
+          for (int q = 0; q < D.k; ++q) {
+            const double cq = q == j ? gate[j] * (1.0 - gate[j]) : -gate[j] * gate[q];
+            const Dev iv{gdn[q], gup[q]};
+            add_scaled(cq, iv, &dn, &up);
+          }
+          al[idx[j]] = std::fmax(up, -dn);
+        }
+      }
     }
   }
   return bad ? -1 : 0;
@@ -379,10 +626,16 @@ int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, 
 
 // Weight gradients of selected experts, summed over every pair routed to them:
 //   dW1[e] = sum x^T da, dW3[e] = sum x^T db, dW2[e] = sum h^T dO.
+// With a flip model M (round_grad on), also their rounding-flip allowances (null skips one),
+// interval sums over the expert's rows r:
+//   dW1[c][f]: x_rc Dda_rf;  dW3[c][f]: x_rc Ddb_rf;
+//   dW2[f][c]: (h_rf + dh) (dO_rc + ddO) - h_rf dO_rc over the corners of Dh_rf x DdO_rc.
 template <class V, class G>
 int backward_dw(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
                 const G* dy, const Dims& D, int round_h, int round_grad, const int32_t* experts,
-                int n_exp, double* dW1, double* dW3, double* dW2) {
+                int n_exp, double* dW1, double* dW3, double* dW2, const FlipModel* M = nullptr,
+                double* a1 = nullptr, double* a3 = nullptr, double* a2 = nullptr) {
+  if (M && !round_grad) return -1;
   const int64_t P = D.T * D.k;
   std::vector<int32_t> idx(P);
   std::vector<double> gate(P);
@@ -396,47 +649,180 @@ int backward_dw(const V* x, const double* logits, const V* W1, const V* W3, cons
     const int64_t R = static_cast<int64_t>(pairs.size());
     std::vector<double> A(R * D.dff), B(R * D.dff), H(R * D.dff), DO(R * D.d), DA(R * D.dff),
         DB(R * D.dff);
+    std::vector<Dev> fDh, fDdO, fDda, fDdb;  // per-row flip intervals
+    if (M) {
+      fDh.resize(R * D.dff);
+      fDdO.resize(R * D.d);
+      fDda.resize(R * D.dff);
+      fDdb.resize(R * D.dff);
+    }
 #pragma omp parallel
     {
       std::vector<double> o(D.d), dyv(D.d), dh(D.dff), dxp(D.d);
+      std::vector<double> sa, sb, vh, sdh, vda, vdb;
+      if (M)
+        for (auto* v : {&sa, &sb, &vh, &sdh, &vda, &vdb}) v->assign(D.dff, 0.0);
+      const FwdTrace ft{sa.data(), sb.data(), vh.data()};
+      const BwdTrace bt{sdh.data(), vda.data(), vdb.data()};
 #pragma omp for schedule(dynamic, 1)
       for (int64_t r = 0; r < R; ++r) {
         const int64_t p = pairs[r], t = p / D.k;
         ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, round_h,
-                &A[r * D.dff], &B[r * D.dff], &H[r * D.dff], o.data());
+                &A[r * D.dff], &B[r * D.dff], &H[r * D.dff], o.data(), M ? &ft : nullptr);
         for (int c = 0; c < D.d; ++c) dyv[c] = widen(dy[t * D.d + c]);
         double dg;
         ffn_row_bwd(w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, gate[p], dyv.data(),
                     &A[r * D.dff], &B[r * D.dff], o.data(), round_grad, &dg, &DO[r * D.d],
-                    dh.data(), &DA[r * D.dff], &DB[r * D.dff], dxp.data());
+                    dh.data(), &DA[r * D.dff], &DB[r * D.dff], dxp.data(), M ? &bt : nullptr);
+        if (M)
+          pair_flip_bounds(w2of(W2, D, e), D.d, D.dff, W3 != nullptr, gate[p], dyv.data(),
+                           &A[r * D.dff], &B[r * D.dff], ft, dh.data(), bt, *M,
+                           &fDh[r * D.dff], &fDdO[r * D.d], &fDda[r * D.dff], &fDdb[r * D.dff]);
       }
     }
     double* g1 = dW1 + static_cast<int64_t>(q) * D.d * D.dff;
     double* g3 = dW3 ? dW3 + static_cast<int64_t>(q) * D.d * D.dff : nullptr;  // null: no W3
     double* g2 = dW2 + static_cast<int64_t>(q) * D.dff * D.d;
-#pragma omp parallel for schedule(static)
-    for (int c = 0; c < D.d; ++c) {
-      double* r1 = g1 + static_cast<int64_t>(c) * D.dff;
-      double* r3 = g3 ? g3 + static_cast<int64_t>(c) * D.dff : nullptr;
-      for (int f = 0; f < D.dff; ++f) r1[f] = 0.0;
-      if (r3) for (int f = 0; f < D.dff; ++f) r3[f] = 0.0;
-      for (int64_t r = 0; r < R; ++r) {
-        const double xc = widen(x[(pairs[r] / D.k) * D.d + c]);
-        for (int f = 0; f < D.dff; ++f) r1[f] += xc * DA[r * D.dff + f];
-        if (r3) for (int f = 0; f < D.dff; ++f) r3[f] += xc * DB[r * D.dff + f];
+    double* h1 = M && a1 ? a1 + static_cast<int64_t>(q) * D.d * D.dff : nullptr;
+    double* h3 = M && a3 && W3 ? a3 + static_cast<int64_t>(q) * D.d * D.dff : nullptr;
+    double* h2 = M && a2 ? a2 + static_cast<int64_t>(q) * D.dff * D.d : nullptr;
+    // per row: the columns with a flagged da, db (f) and dO (c); only those add to an interval
+    std::vector<std::vector<int>> nz_a(M ? R : 0), nz_b(M ? R : 0), nz_o(M ? R : 0);
+    for (int64_t r = 0; M && r < R; ++r) {
+      for (int f = 0; f < D.dff; ++f) {
+        if (fDda[r * D.dff + f].mag() != 0.0) nz_a[r].push_back(f);
+        if (fDdb[r * D.dff + f].mag() != 0.0) nz_b[r].push_back(f);
+      }
+      for (int c = 0; c < D.d; ++c)
+        if (fDdO[r * D.d + c].mag() != 0.0) nz_o[r].push_back(c);
+    }
+#pragma omp parallel
+    {
+      std::vector<double> dn1, up1, dn3, up3;
+      if (h1) { dn1.assign(D.dff, 0.0); up1.assign(D.dff, 0.0); }
+      if (h3) { dn3.assign(D.dff, 0.0); up3.assign(D.dff, 0.0); }
+#pragma omp for schedule(static)
+      for (int c = 0; c < D.d; ++c) {
+        double* r1 = g1 + static_cast<int64_t>(c) * D.dff;
+        double* r3 = g3 ? g3 + static_cast<int64_t>(c) * D.dff : nullptr;
+        for (int f = 0; f < D.dff; ++f) r1[f] = 0.0;
+        if (r3) for (int f = 0; f < D.dff; ++f) r3[f] = 0.0;
+        if (h1) for (int f = 0; f < D.dff; ++f) dn1[f] = up1[f] = 0.0;
+        if (h3) for (int f = 0; f < D.dff; ++f) dn3[f] = up3[f] = 0.0;
+        for (int64_t r = 0; r < R; ++r) {
+          const double xc = widen(x[(pairs[r] / D.k) * D.d + c]);
+          for (int f = 0; f < D.dff; ++f) r1[f] += xc * DA[r * D.dff + f];
+          if (r3) for (int f = 0; f < D.dff; ++f) r3[f] += xc * DB[r * D.dff + f];
+          if (h1)
+            for (int f : nz_a[r]) add_scaled(xc, fDda[r * D.dff + f], &dn1[f], &up1[f]);
+          if (h3)
+            for (int f : nz_b[r]) add_scaled(xc, fDdb[r * D.dff + f], &dn3[f], &up3[f]);
+        }
+        if (h1)
+          for (int f = 0; f < D.dff; ++f)
+            h1[static_cast<int64_t>(c) * D.dff + f] = std::fmax(up1[f], -dn1[f]);
+        if (h3)
+          for (int f = 0; f < D.dff; ++f)
+            h3[static_cast<int64_t>(c) * D.dff + f] = std::fmax(up3[f], -dn3[f]);
       }
     }
-#pragma omp parallel for schedule(static)
-    for (int f = 0; f < D.dff; ++f) {
-      double* r2 = g2 + static_cast<int64_t>(f) * D.d;
-      for (int c = 0; c < D.d; ++c) r2[c] = 0.0;
-      for (int64_t r = 0; r < R; ++r) {
-        const double hf = H[r * D.dff + f];
-        for (int c = 0; c < D.d; ++c) r2[c] += hf * DO[r * D.d + c];
+#pragma omp parallel
+    {
+      std::vector<double> dn2, up2;
+      if (h2) { dn2.assign(D.d, 0.0); up2.assign(D.d, 0.0); }
+#pragma omp for schedule(static)
+      for (int f = 0; f < D.dff; ++f) {
+        double* r2 = g2 + static_cast<int64_t>(f) * D.d;
+        for (int c = 0; c < D.d; ++c) r2[c] = 0.0;
+        if (h2) for (int c = 0; c < D.d; ++c) dn2[c] = up2[c] = 0.0;
+        for (int64_t r = 0; r < R; ++r) {
+          const double hf = H[r * D.dff + f];
+          for (int c = 0; c < D.d; ++c) r2[c] += hf * DO[r * D.d + c];
+          if (!h2) continue;
+          const Dev dhf = fDh[r * D.dff + f];
+          // (h + u)(dO + w) - h dO = u dO + h w + u w, extremes at the corners
+          auto corners = [&](int c) {
+            const Dev ddo = fDdO[r * D.d + c];
+            const double dov = DO[r * D.d + c];
+            double lo = 0.0, hi = 0.0;
+            bool first = true;
+            for (double u : {dhf.lo, dhf.hi})
+              for (double w : {ddo.lo, ddo.hi}) {
+                const double z = u * dov + hf * w + u * w;
+                lo = first ? z : std::fmin(lo, z);
+                hi = first ? z : std::fmax(hi, z);
+                first = false;
+              }
+            dn2[c] += lo;
+            up2[c] += hi;
+          };
+          if (dhf.mag() != 0.0) {
+            for (int c = 0; c < D.d; ++c) corners(c);
+          } else {
+            for (int c : nz_o[r]) corners(c);  // only the dO flips of this row move dW2[f]
+          }
+        }
+        if (h2)
+          for (int c = 0; c < D.d; ++c)
+            h2[static_cast<int64_t>(f) * D.d + c] = std::fmax(up2[c], -dn2[c]);
       }
     }
   }
   return 0;
+}
+
+// Operands of one token-expert pair (token t, slot j) and their flip intervals, for the tests
+// of the allowance: h, its pre-rounding value vh and interval Dh [dff][2] (lo, hi); dO and
+// DdO [d][2]; da, db and Dda, Ddb [dff][2]; the expert index and gate through e_out, g_out.
+template <class V>
+int pair_operands(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
+                  const V* dy, const Dims& D, int64_t t, int j, const FlipModel& M, int* e_out,
+                  double* g_out, double* h, double* vh, double* Dh, double* dO, double* DdO,
+                  double* da, double* Dda, double* db, double* Ddb) {
+  if (t < 0 || t >= D.T || j < 0 || j >= D.k) return -1;
+  std::vector<int32_t> idx(D.k);
+  std::vector<double> gate(D.k), a(D.dff), b(D.dff), o(D.d), dyv(D.d), dh(D.dff), dxp(D.d),
+      sa(D.dff), sb(D.dff), sdh(D.dff), vda(D.dff), vdb(D.dff);
+  std::vector<Dev> ih(D.dff), io(D.d), ia(D.dff), ib(D.dff);
+  route_token(logits + t * D.E, D.E, D.k, idx.data(), gate.data());
+  const int e = idx[j];
+  const FwdTrace ft{sa.data(), sb.data(), vh};
+  const BwdTrace bt{sdh.data(), vda.data(), vdb.data()};
+  ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, 1, a.data(),
+          b.data(), h, o.data(), &ft);
+  for (int c = 0; c < D.d; ++c) dyv[c] = widen(dy[t * D.d + c]);
+  double dg;
+  ffn_row_bwd(w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, gate[j], dyv.data(),
+              a.data(), b.data(), o.data(), 1, &dg, dO, dh.data(), da, db, dxp.data(), &bt);
+  pair_flip_bounds(w2of(W2, D, e), D.d, D.dff, W3 != nullptr, gate[j], dyv.data(), a.data(),
+                   b.data(), ft, dh.data(), bt, M, ih.data(), io.data(), ia.data(), ib.data());
+  for (int f = 0; f < D.dff; ++f) {
+    Dh[2 * f] = ih[f].lo;
+    Dh[2 * f + 1] = ih[f].hi;
+    Dda[2 * f] = ia[f].lo;
+    Dda[2 * f + 1] = ia[f].hi;
+    Ddb[2 * f] = ib[f].lo;
+    Ddb[2 * f + 1] = ib[f].hi;
+  }
+  for (int c = 0; c < D.d; ++c) {
+    DdO[2 * c] = io[c].lo;
+    DdO[2 * c + 1] = io[c].hi;
+  }
+  *e_out = e;
+  *g_out = gate[j];
+  return 0;
+}
+
+// Flip-model accumulation bound of one plain sum: the running partial sums of t [n] (in index
+// order) give acc * sqrt(sum_j s_j^2); the exact sum goes to *sum.
+double sum_bound(const double* t, int64_t n, double acc, double* sum) {
+  double s = 0.0, sq = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    s += t[i];
+    sq += s * s;
+  }
+  *sum = s;
+  return acc * std::sqrt(sq);
 }
 
 // ---------------------------------------------------------------------- FP8 dispatch
@@ -628,6 +1014,58 @@ int oracle_backward_dw_f64(const double* x, const double* logits, const double* 
   if (!dims_ok(T, d, E, k, dff)) return -1;
   return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, round_grad,
                      experts, n_exp, dW1, dW3, dW2);
+}
+
+// ------------------------------------------------ rounding-flip allowance (test bound)
+// model = {acc, ev, gate} (FlipModel); round_grad is on.
+
+double oracle_round_spread_bf16(double v, double dv) { return round_spread(v, dv); }
+
+double oracle_sum_bound(const double* t, int64_t n, double acc, double* sum) {
+  return sum_bound(t, n, acc, sum);
+}
+
+int oracle_forward_tokens_flip_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
+                                    const uint16_t* W3, const uint16_t* W2, ORACLE_DIMS,
+                                    const double* model, const int64_t* tokens, int64_t n,
+                                    double* y, double* ay) {
+  if (!dims_ok(T, d, E, k, dff) || !model) return -1;
+  const FlipModel M{model[0], model[1], model[2]};
+  return forward_tokens(x, logits, W1, W3, W2, Dims{T, d, E, k, dff}, 1, tokens, n, y, &M, ay);
+}
+
+int oracle_backward_tokens_flip_bf16(const uint16_t* x, const double* logits,
+                                     const uint16_t* W1, const uint16_t* W3, const uint16_t* W2,
+                                     const uint16_t* dy, ORACLE_DIMS, int round_h,
+                                     const double* model, const int64_t* tokens, int64_t n,
+                                     double* dx, double* dgate, double* dlogits, double* adx,
+                                     double* adg, double* adl) {
+  if (!dims_ok(T, d, E, k, dff) || !model) return -1;
+  const FlipModel M{model[0], model[1], model[2]};
+  return backward_tokens(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, 1, tokens,
+                         n, dx, dgate, dlogits, &M, adx, adg, adl);
+}
+
+int oracle_backward_dw_flip_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
+                                 const uint16_t* W3, const uint16_t* W2, const uint16_t* dy,
+                                 ORACLE_DIMS, int round_h, const double* model,
+                                 const int32_t* experts, int n_exp, double* dW1, double* dW3,
+                                 double* dW2, double* a1, double* a3, double* a2) {
+  if (!dims_ok(T, d, E, k, dff) || !model) return -1;
+  const FlipModel M{model[0], model[1], model[2]};
+  return backward_dw(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, round_h, 1, experts,
+                     n_exp, dW1, dW3, dW2, &M, a1, a3, a2);
+}
+
+int oracle_pair_operands_bf16(const uint16_t* x, const double* logits, const uint16_t* W1,
+                              const uint16_t* W3, const uint16_t* W2, const uint16_t* dy,
+                              ORACLE_DIMS, int64_t t, int j, const double* model, int* e_out,
+                              double* g_out, double* h, double* vh, double* Dh, double* dO,
+                              double* DdO, double* da, double* Dda, double* db, double* Ddb) {
+  if (!dims_ok(T, d, E, k, dff) || !model) return -1;
+  const FlipModel M{model[0], model[1], model[2]};
+  return pair_operands(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, t, j, M, e_out, g_out,
+                       h, vh, Dh, dO, DdO, da, Dda, db, Ddb);
 }
 
 int oracle_forward_tokens_fp8(const uint16_t* x, const double* logits, const uint16_t* W1,

@@ -1,16 +1,18 @@
 """Backward of the layer on the GPU (moe_backward through the C ABI) against the oracle, and
 run-to-run bitwise determinism of forward + backward.
 
-Gradients use assert_close_grad: the stated bound |g - g_ref| <= 2e-2 |g_ref| + 2e-3 on all
-but a 1e-3 fraction of the elements, the rest within 1% of the tensor's rms: the residue of
-one-ulp bf16 rounding flips of the product operands (see moe_harness.assert_close_grad)."""
+Bar: every gradient element meets the stated bound |g - g_ref| <= 2e-2 |g_ref| + 2e-3 widened
+by the oracle's rounding-flip allowance for that element (moe_harness.assert_close_flip): the
+largest change that bf16 operands (h, dO, da, db) which may round the other way in fp32
+arithmetic can cause there, derived from oracle values alone.  The tiny workload also meets
+the stated bound alone."""
 import numpy as np
 import pytest
 import torch
 
 import moe_synth
 import oracle
-from moe_harness import (assert_close, assert_close_grad, backward, forward, np_of,
+from moe_harness import (assert_close, backward, check_backward, check_forward, forward, np_of,
                          sample_tokens, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -29,24 +31,26 @@ def _run(moe, g, k):
     return res
 
 
-def _check_all(moe, w, experts=None):
+def _check_all(moe, w, experts=None, plain=False):
     inp = moe_synth.generate(w, with_dy=True)
     g = to_dev(inp)
     res = _run(moe, g, w.k)
     npi = moe_synth.to_numpy(inp)
-    dx, dgate, dlog = oracle.backward_tokens(npi, npi["dy"], w.k)
-    assert_close_grad(np_of(res["dx"]), dx, "dx")
-    assert_close_grad(np_of(res["dgate"]), dgate, "dgate")
-    assert_close_grad(np_of(res["dlogits"]), dlog, "dlogits")
-    ex = np.arange(w.E) if experts is None else np.asarray(experts)
-    r1, r3, r2 = oracle.backward_dw(npi, npi["dy"], w.k, ex)
-    assert_close_grad(np_of(res["dW1"])[ex], r1, "dW1")
-    assert_close_grad(np_of(res["dW3"])[ex], r3, "dW3")
-    assert_close_grad(np_of(res["dW2"])[ex], r2, "dW2")
+    used = check_backward(res, npi, w.k, experts=experts)
+    print("%s: elements that needed the flip allowance: %s" % (w.name, used))
+    if plain:  # the stated bound alone
+        dx, dgate, dlog = oracle.backward_tokens(npi, npi["dy"], w.k)
+        assert_close(np_of(res["dx"]), dx, "dx")
+        assert_close(np_of(res["dgate"]), dgate, "dgate")
+        assert_close(np_of(res["dlogits"]), dlog, "dlogits")
+        r1, r3, r2 = oracle.backward_dw(npi, npi["dy"], w.k, np.arange(w.E))
+        assert_close(np_of(res["dW1"]), r1, "dW1")
+        assert_close(np_of(res["dW3"]), r3, "dW3")
+        assert_close(np_of(res["dW2"]), r2, "dW2")
 
 
 def test_backward_tiny_workload(moe):
-    _check_all(moe, moe_synth.by_name("tiny"))
+    _check_all(moe, moe_synth.by_name("tiny"), plain=True)
 
 
 @pytest.mark.parametrize("T,d,E,k,dff", [
@@ -89,15 +93,16 @@ def test_fwd_bwd_workload_sampled_and_deterministic(moe):
             assert torch.equal(a, b), kk
     assert moe.moe_get_error(ws) == 0
     npi = moe_synth.to_numpy(g)
-    tok = sample_tokens(w.T, 12, seed=2)
-    y = oracle.forward_tokens(npi, w.k, tokens=tok)
-    assert_close(np_of(ref["out"])[tok], y, "out (fwd_bwd, sampled tokens)")
-    dx, dgate, dlog = oracle.backward_tokens(npi, npi["dy"], w.k, tokens=tok)
-    assert_close_grad(np_of(ref["dx"])[tok], dx, "dx (sampled tokens)")
-    assert_close_grad(np_of(ref["dgate"])[tok], dgate, "dgate (sampled tokens)")
-    assert_close_grad(np_of(ref["dlogits"])[tok], dlog, "dlogits (sampled tokens)")
-    ex = np.array([0, 77])
-    r1, r3, r2 = oracle.backward_dw(npi, npi["dy"], w.k, ex)
-    assert_close_grad(np_of(ref["dW1"][ex.tolist()]), r1, "dW1 (experts 0, 77)")
-    assert_close_grad(np_of(ref["dW3"][ex.tolist()]), r3, "dW3 (experts 0, 77)")
-    assert_close_grad(np_of(ref["dW2"][ex.tolist()]), r2, "dW2 (experts 0, 77)")
+    tok = sample_tokens(w.T, 64, seed=2)
+    check_forward(ref["out"], npi, w.k, "out (fwd_bwd, sampled tokens)", tokens=tok)
+    # weight gradients of 10 experts: the most and the least loaded non-empty experts, and 8
+    # drawn at random
+    counts = np.bincount(oracle.route(npi["logits"], w.k)[0].reshape(-1), minlength=w.E)
+    hot, cold = int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
+    rng = np.random.default_rng(5)
+    ex = np.unique(np.concatenate([[hot, cold], rng.choice(w.E, 8, replace=False)]))
+    assert len(ex) >= 8 and counts[ex].min() > 0
+    used = check_backward(ref, npi, w.k, " (fwd_bwd)", tokens=tok, experts=ex)
+    exl = ex.tolist()
+    print("fwd_bwd: elements that needed the flip allowance:", used,
+          "experts", exl, "rows", counts[ex].tolist())

@@ -7,7 +7,7 @@ import torch
 
 import moe_synth
 import oracle
-from moe_harness import (assert_close, assert_close_grad, backward, forward, np_of,
+from moe_harness import (backward, check_backward, check_forward, forward, np_of,
                          sample_tokens, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +37,7 @@ def test_relu2_forward_matches_oracle(moe, T, d, E, k, dff):
     g = to_dev(inp)
     out, ws = forward(moe, g, k)
     assert moe.moe_get_error(ws) == 0
-    assert_close(np_of(out), oracle.forward_tokens(moe_synth.to_numpy(inp), k), "out (relu2)")
+    check_forward(out, moe_synth.to_numpy(inp), k, "out (relu2)")
 
 
 @pytest.mark.parametrize("T,d,E,k,dff", [
@@ -53,14 +53,8 @@ def test_relu2_backward_matches_oracle(moe, T, d, E, k, dff):
     res = backward(moe, g, k, ws)
     assert moe.moe_get_error(ws) == 0 and res["dW3"] is None
     npi = moe_synth.to_numpy(inp)
-    dx, dgate, dlog = oracle.backward_tokens(npi, npi["dy"], k)
-    assert_close_grad(np_of(res["dx"]), dx, "dx (relu2)")
-    assert_close_grad(np_of(res["dgate"]), dgate, "dgate (relu2)")
-    assert_close_grad(np_of(res["dlogits"]), dlog, "dlogits (relu2)")
-    r1, r3, r2 = oracle.backward_dw(npi, npi["dy"], k, np.arange(E))
-    assert r3 is None
-    assert_close_grad(np_of(res["dW1"]), r1, "dW1 (relu2)")
-    assert_close_grad(np_of(res["dW2"]), r2, "dW2 (relu2)")
+    used = check_backward(res, npi, k, " (relu2)")
+    print("relu2 backward: elements that needed the flip allowance:", used)
 
 
 def test_relu2_batch_invariance_and_determinism(moe):
@@ -102,5 +96,4 @@ def test_relu2_large_workload_sampled(moe):
     assert moe.moe_get_error(ws) == 0
     npi = moe_synth.to_numpy(g)
     tok = sample_tokens(w.T, 16, seed=4)
-    ref = oracle.forward_tokens(npi, w.k, tokens=tok)
-    assert_close(np_of(out)[tok], ref, "out (large relu2, sampled tokens)")
+    check_forward(out, npi, w.k, "out (large relu2, sampled tokens)", tokens=tok)
