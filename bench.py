@@ -135,8 +135,11 @@ def _algorithmic(w, P):
         gemm2_flops=2 * d * dff * P,            # down projection
         # logits read; topk, gate, pos, perm written; x read; x_perm written
         dispatch_bytes=T * E * 4 + T * k * 16 + T * d * 2 + P * d * 2,
-        # fp32 expert-output rows read; gate + pos read; out written (bf16)
-        combine_bytes=P * d * 4 + T * k * 8 + T * d * 2,
+        # algorithmic combine: bf16 expert-output rows read (the pages' BF16 gather), gate +
+        # pos read, out written (bf16)
+        combine_bytes=P * d * 2 + T * k * 8 + T * d * 2,
+        # what this build's combine moves: it reads the expert rows in fp32
+        combine_bytes_fp32_rows=P * d * 4 + T * k * 8 + T * d * 2,
     )
 
 
@@ -509,7 +512,9 @@ def bench_native(args, w):
     g_tflops = alg["gemm_flops"] / ((stages["gemm1_swiglu"] + stages["gemm2"]) * 1e-3) / 1e12
     disp_gbs = alg["dispatch_bytes"] / (stages["dispatch"] * 1e-3) / 1e9
     comb_gbs = alg["combine_bytes"] / (stages["combine"] * 1e-3) / 1e9
-    peak = peaks["bf16_sustained"]
+    comb_gbs_moved = alg["combine_bytes_fp32_rows"] / (stages["combine"] * 1e-3) / 1e9
+    # GEMM1 runs for milliseconds inside a sub-second timed loop: the burst peak applies
+    peak = peaks["bf16"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -519,7 +524,8 @@ def bench_native(args, w):
         "roofline": {"kernel": "grouped GEMM1 + SwiGLU (tcgen05)", "bound": "tensor",
                      "achieved": g1_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": g1_tflops / peak,
-                     "peak_source": "%s bf16 sustained (MEASURED_PEAKS.json)" % peaks["source"],
+                     "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peaks["source"],
+                     "frac_of_sustained": g1_tflops / peaks["bf16_sustained"],
                      "traffic": _traffic_of("gemm1")},
         "stages_ms": stages,
         "gemm_tflops": g_tflops,
@@ -527,6 +533,8 @@ def bench_native(args, w):
         "gemm_roofline_under_load": roof,
         "dispatch_gbs": disp_gbs, "dispatch_frac_of_hbm": disp_gbs / peaks["hbm"],
         "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
+        "combine_gbs_fp32_rows": comb_gbs_moved,
+        "combine_frac_of_hbm_fp32_rows": comb_gbs_moved / peaks["hbm"],
         "waved_forward_ms_per_step": waved_ms,
         "graph_forward_ms_per_step": graph_ms,
         "fp8_forward": fp8,
