@@ -37,8 +37,9 @@ EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispat
            "moe_forward_graph_create", "moe_forward_graph_launch",
            "moe_forward_graph_destroy", "moe_forward_host", "moe_forward_host_pipelined",
            "moe_backward",
-           "moe_route_dispatch_noalloc", "moe_get_error", "moe_set_wait_timeout_ns",
-           "moe_debug_set_flags", "moe_status_string")
+           "moe_route_dispatch_noalloc", "moe_route_dispatch_noalloc_get_error",
+           "moe_get_error", "moe_set_wait_timeout_ns", "moe_debug_set_flags",
+           "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -82,6 +83,8 @@ def _load():
     lib.moe_route_dispatch_noalloc.restype = i
     lib.moe_get_error.argtypes = [p, p]
     lib.moe_get_error.restype = i
+    lib.moe_route_dispatch_noalloc_get_error.argtypes = [p]
+    lib.moe_route_dispatch_noalloc_get_error.restype = i
     lib.moe_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.moe_set_wait_timeout_ns.restype = None
     lib.moe_debug_set_flags.argtypes = [i]
@@ -270,6 +273,12 @@ def moe_route_dispatch_noalloc(x, logits, k, topk_idx, gate, counts, offsets, pe
                                            _ptr(gate), _ptr(counts), _ptr(offsets), _ptr(perm),
                                            _ptr(pos), _ptr(x_perm), _stream(stream)),
            "moe_route_dispatch_noalloc")
+
+
+def moe_route_dispatch_noalloc_get_error(stream=None):
+    """Synchronise the stream and return the device error status the last
+    moe_route_dispatch_noalloc call on the current device recorded in the library's array."""
+    return int(_lib.moe_route_dispatch_noalloc_get_error(_stream(stream)))
 
 
 def moe_get_error(ws, stream=None):

@@ -45,13 +45,21 @@ enum GemmKind : int {
   kDw13 = 5,  // [dW1|dW3][e] = Xp^T [dA|dB] (fp32)                         (d x 2dff)
   kFwd1F8 = 6,  // GEMM1 + SwiGLU on the FP8 payload: Xp and W1 / W3 in E4M3 (K-major), the
                 // row and column scales applied in the epilogue                (rows x dff)
+  // The forward GEMMs with the operands swapped: the expert's weight columns are the M
+  // operand (256 per CTA pair, MN-major straight from the weights' row-major layout) and the
+  // expert's permuted rows the N operand (a block of up to 256 rows, K-major), so a tile's N
+  // follows the rows the block really holds (32, 64, 128 or 256) and an expert with few rows
+  // costs few MMAs; heavy and light experts then share one persistent CTA-pair launch.
+  kFwd1T = 7,   // H^T = [W1|W3]^T Xp^T -> SwiGLU -> H                      (dff x rows)
+  kFwd2T = 8,   // Y^T = W2^T H^T (fp32 rows)                                (d x rows)
 };
 
 template <int KIND>
 struct KindTraits {
   static constexpr bool kRowsM = (KIND <= kDx || KIND == kFwd1F8);  // M = permuted rows
-  static constexpr int kAmn = (KIND == kDw2 || KIND == kDw13) ? 1 : 0;  // A MN-major?
-  static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8) ? 0 : 1;
+  static constexpr bool kSwap = (KIND == kFwd1T || KIND == kFwd2T);  // N = permuted rows
+  static constexpr int kAmn = (KIND == kDw2 || KIND == kDw13 || kSwap) ? 1 : 0;  // A MN-major?
+  static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8 || kSwap) ? 0 : 1;
 };
 
 // Epilogue warps of a launch: 4, one per TMEM lane quadrant, or 8 for the dH pair launch,
@@ -111,6 +119,12 @@ struct GemmParams {
   int32_t* seg_count;        // [T, nb]: rows of (token, N block) written so far
   uint16_t* comb_out;        // [T, d] bf16 layer output
   int k;
+  // swapped forward kinds: the table of 256-row blocks (expert, first row) and tensor maps of
+  // the row operand with boxes of 16, 32, 64 and 128 rows (the rows a CTA takes of a block)
+  const int32_t* n_st;
+  const int32_t* st_expert;
+  const int32_t* st_row0;
+  CUtensorMap mapR[4];
 };
 
 constexpr int kBM = 128;
@@ -137,8 +151,10 @@ struct GemmCfg {
   // 32 x 32 fp32 staging box of a TMA store
   static constexpr size_t kEpiWarpBytes = 5120;
   static constexpr size_t kEpiBytes = EPI_WARPS * kEpiWarpBytes;
+  // + 128 bytes: TMEM address, abort flag, fill counters and the two rings of per-fill
+  // load bytes (this CTA's and, with pairs, the peer's)
   static constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + 1024 +
-                                       kEpiBytes + 8 * kBars + 64;
+                                       kEpiBytes + 8 * kBars + 128;
   static_assert(kStageBytes % 1024 == 0, "stages keep the epilogue regions 1024-aligned");
   static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of a CTA (227 KB)");
 };
@@ -154,6 +170,7 @@ struct TileInfo {
   int nseg;   // rows of this CTA inside the expert's padded row segment (rows-grouped kinds);
               // with PAIR the second half of an expert's last tile can lie past the segment,
               // on the next expert's rows, and must not be written
+  int box;    // swapped kinds: rows of the block each CTA loads (16, 32, 64 or 128); N = 2 box
   bool bad;   // tile tables out of range: every role skips the tile
 };
 
@@ -163,6 +180,7 @@ struct TileInfo {
 template <int KIND, int BN, bool PAIR>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, int rank) {
   TileInfo ti;
+  ti.box = kBM;
   if constexpr (KindTraits<KIND>::kRowsM) {
     const int mt = tile / p.nb;
     ti.n0 = (tile % p.nb) * BN;
@@ -178,6 +196,30 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, i
     }
     ti.nvalid = ti.bad ? 0 : p.poff[ti.e] + p.counts[ti.e] - ti.row0;
     ti.nseg = ti.bad ? 0 : p.poff[ti.e + 1] - ti.row0;
+    ti.m0 = 0;
+    ti.nk = p.nkb;
+    ti.mvalid = kBM;
+  } else if constexpr (KindTraits<KIND>::kSwap) {
+    // a block of up to 256 rows of one expert x one block of weight columns: 128 h columns
+    // (64 per CTA, each with its W1 and W3 column) for GEMM1, 256 without the gate
+    // projection or for GEMM2 (128 per CTA)
+    const int st = tile / p.nb;
+    ti.n0 = (tile % p.nb) * ((KIND == kFwd1T && p.gated) ? 128 : 256);
+    ti.e = p.st_expert[st];
+    ti.row0 = p.st_row0[st];
+    ti.bad = ti.e < 0 || ti.e >= p.E || ti.row0 < 0 || ti.row0 >= p.rows_cap;
+    ti.nvalid = 0;
+    ti.nseg = 0;
+    if (!ti.bad) {
+      const int nv = p.poff[ti.e] + p.counts[ti.e] - ti.row0;
+      const int ns = p.poff[ti.e + 1] - ti.row0;
+      ti.nvalid = nv < 2 * kBM ? nv : 2 * kBM;
+      ti.nseg = ns < 2 * kBM ? ns : 2 * kBM;
+      ti.bad = ti.nvalid < 1 || ti.nseg < ti.nvalid || ti.row0 + ti.nseg > p.rows_cap;
+      if (ti.bad) ti.nvalid = ti.nseg = 0;
+    }
+    const int half = (ti.nvalid + 1) / 2;
+    ti.box = half <= 16 ? 16 : (half <= 32 ? 32 : (half <= 64 ? 64 : 128));
     ti.m0 = 0;
     ti.nk = p.nkb;
     ti.mvalid = kBM;
@@ -570,6 +612,97 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
   }
 }
 
+// Epilogue of the swapped forward kinds for one epilogue warp: TMEM lanes are this CTA's
+// weight columns (one per lane of warp q's quadrant), TMEM columns the block's rows.  The
+// warp walks the rows 32 at a time; for each row, the 32 lanes write 32 consecutive output
+// columns.
+//  * kFwd1T with W3: lanes 0-63 hold A = Xp W1 and lanes 64-127 B = Xp W3 for the same 64 h
+//    columns, so warp q (A) and warp q + 2 (B) swap their 32 x 32 chunks through shared
+//    memory and each finishes half of the chunk's rows: h = bf16(silu(A) B).  Padding rows of
+//    the expert's segment get h = 0 (a later K-over-rows GEMM reads them).
+//  * kFwd1T without W3: h = bf16(relu(A)^2) over 128 W1 columns.
+//  * kFwd2T: Y rows (fp32) over 128 W2 columns (columns past d, when d is not a multiple of
+//    256, are neither loaded as real data nor stored).
+template <int KIND>
+__device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInfo& ti,
+                                              uint32_t tacc, int q, int lane, float* mine,
+                                              const float* partner, int rank) {
+  const int nch = (ti.nvalid + 31) / 32;
+  const int64_t row0 = ti.row0;
+  if constexpr (KIND == kFwd1T) {
+    uint16_t* H = static_cast<uint16_t*>(p.out0);
+    if (p.gated) {
+      const bool is_a = q < 2;
+      const int col = ti.n0 + 64 * rank + 32 * (q & 1) + lane;  // h column of this lane
+      float* save = is_a ? p.save_a : p.save_b;
+      const int bar = 1 + (q & 1);
+      const int j0 = is_a ? 0 : 16;
+#pragma unroll 1
+      for (int ch = 0; ch < nch; ++ch) {
+        float v[32];
+        tmem_ld32(tacc + ch * 32, v);
+        if (p.save_ab) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int r = ch * 32 + j;
+            if (r < ti.nvalid) save[(row0 + r) * p.dff + col] = v[j];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mine[lane * 33 + j] = v[j];
+        named_bar_sync(bar, 64);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j = j0 + jj, r = ch * 32 + j;
+          if (r < ti.nseg) {
+            float hv = 0.0f;
+            if (r < ti.nvalid) {
+              const float x0 = mine[lane * 33 + j], x1 = partner[lane * 33 + j];
+              hv = is_a ? silu_f(x0) * x1 : silu_f(x1) * x0;
+            }
+            H[(row0 + r) * p.dff + col] = bf16_bits(hv);
+          }
+        }
+        named_bar_sync(bar, 64);
+      }
+      if (is_a)
+        for (int r = nch * 32; r < ti.nseg; ++r) H[(row0 + r) * p.dff + col] = 0;
+    } else {
+      const int col = ti.n0 + 128 * rank + 32 * q + lane;
+#pragma unroll 1
+      for (int ch = 0; ch < nch; ++ch) {
+        float v[32];
+        tmem_ld32(tacc + ch * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int r = ch * 32 + j;
+          if (p.save_ab && r < ti.nvalid) p.save_a[(row0 + r) * p.dff + col] = v[j];
+          if (r < ti.nseg) {
+            const float rl = fmaxf(v[j], 0.0f);
+            H[(row0 + r) * p.dff + col] = bf16_bits(r < ti.nvalid ? rl * rl : 0.0f);
+          }
+        }
+      }
+      for (int r = nch * 32; r < ti.nseg; ++r) H[(row0 + r) * p.dff + col] = 0;
+    }
+  } else {
+    const int col = ti.n0 + 128 * rank + 32 * q + lane;
+    const bool live = ti.n0 + 128 * rank < p.d;  // warp-uniform: d is a multiple of 128
+    float* Y = static_cast<float*>(p.out0);
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+      float v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      if (!live) continue;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int r = ch * 32 + j;
+        if (r < ti.nvalid) Y[(row0 + r) * p.d + col] = v[j];
+      }
+    }
+  }
+}
+
 // PAIR: a cluster of two CTAs on two SMs computes one 256 x BN tile with
 // tcgen05.mma.cta_group::2.  Each CTA loads its own 128 rows of A and half of B into its own
 // shared memory; rank 0 issues the MMAs (M = 256), whose result lands in both CTAs' TMEM
@@ -609,6 +742,11 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   volatile uint32_t* consumed = reinterpret_cast<volatile uint32_t*>(misc + 8);
   volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(misc + 12);
+  // bytes this CTA's TMA loads of the fill in each stage bring (written by the producer as
+  // it arms / loads the stage), and the peer CTA's ring, sent over at exit (pairs)
+  volatile uint32_t* tx_ring = reinterpret_cast<volatile uint32_t*>(misc + 16);
+  volatile uint32_t* peer_tx = reinterpret_cast<volatile uint32_t*>(misc + 16 + 4 * S);
+  static_assert(16 + 8 * S <= 128, "misc region");
   float* epi_buf = reinterpret_cast<float*>(gbase + S * Cfg::kStageBytes);
   auto stage_a = [&](int s) { return base + s * Cfg::kStageBytes; };
   auto stage_b = [&](int s) { return base + s * Cfg::kStageBytes + kABytes; };
@@ -638,6 +776,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
     *abort_flag = 0;
     *consumed = 0u;
     *peer_issued = 0u;
+    for (int s = 0; s < S; ++s) tx_ring[s] = peer_tx[s] = Cfg::kStageBytes;
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -655,6 +794,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
 
   int64_t ntiles64;
   if constexpr (Tr::kRowsM) ntiles64 = static_cast<int64_t>(PAIR ? p.n_pt[0] : p.n_mt[0]) * p.nb;
+  else if constexpr (Tr::kSwap) ntiles64 = static_cast<int64_t>(p.n_st[0]) * p.nb;
   else ntiles64 = static_cast<int64_t>(p.E) * p.mb * p.nb;
   if (ntiles64 > p.max_tiles || ntiles64 < 0) {
     if (threadIdx.x == 0) set_error(p.err, MOE_ERR_DEVICE_BOUNDS, 10);
@@ -724,10 +864,34 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
       // lane 0: arm stage (fb) and issue the tile loads of K block kb (A too unless gathered)
       auto issue_stage = [&](int kb, uint32_t fb, uint32_t sa, uint32_t sb) {
         // rank 0 arms its barrier for both CTAs' bytes; rank 1 only loads
-        const uint32_t tx = gather ? Cfg::kBBytes : Cfg::kStageBytes;
+        uint32_t tx = gather ? Cfg::kBBytes : Cfg::kStageBytes;
+        if constexpr (Tr::kSwap) tx = kABytes + static_cast<uint32_t>(ti.box) * 128u;
+        tx_ring[(fb - full_bar(0)) / 8u] = tx;
         if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * tx : tx);
         const int k0 = kb * kBK;
-        if constexpr (KIND == kFwd1) {
+        if constexpr (Tr::kSwap) {
+          // A: this CTA's 128 weight columns as two 64-column boxes (MN-major); B: this CTA's
+          // `box` rows of the block (K-major), by the tensor map of that box height
+          if constexpr (KIND == kFwd1T) {
+            const int wrow = ti.e * p.d + k0;
+            if (p.gated) {
+              const int c0 = ti.n0 + 64 * rank;  // W1 columns -> lanes 0-63, W3 -> 64-127
+              load_h(kL2HintB, sa, &mapB0, fb, c0, wrow);
+              load_h(kL2HintB, sa + 8192u, &mapB1, fb, c0, wrow);
+            } else {
+              const int c0 = ti.n0 + 128 * rank;
+              load_h(kL2HintB, sa, &mapB0, fb, c0, wrow);
+              load_h(kL2HintB, sa + 8192u, &mapB0, fb, c0 + 64, wrow);
+            }
+          } else {
+            const int wrow = ti.e * p.dff + k0;
+            const int c0 = ti.n0 + 128 * rank;  // past d (d % 256 == 128): zero fill
+            load_h(kL2HintB, sa, &mapB0, fb, c0, wrow);
+            load_h(kL2HintB, sa + 8192u, &mapB0, fb, c0 + 64, wrow);
+          }
+          const int bi = ti.box == 16 ? 0 : (ti.box == 32 ? 1 : (ti.box == 64 ? 2 : 3));
+          load_h(kL2HintA, sb, &p.mapR[bi], fb, k0, ti.row0 + rank * ti.box);
+        } else if constexpr (KIND == kFwd1) {
           if (!p.gather_x) load_h(kL2HintA, sa, &mapA, fb, k0, ti.row0);
           const int wrow = ti.e * p.d + k0;
           const int h0 = ti.n0 / 2;  // first h column of the tile
@@ -845,6 +1009,8 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
       if (!wait_bar(tempty_bar(acc), aph ^ 1u, abort_flag, 2)) break;
       tc_fence_after();
       const uint32_t dtm = tmem_base + acc * BN;
+      // swapped kinds: M = 256 weight columns, N = the block's rows (2 box)
+      const uint32_t idesc = Tr::kSwap ? idesc_bf16_f32(2 * kBM, 2 * ti.box, 1, 0) : IDESC;
       for (int kb = 0; kb < ti.nk; ++kb) {
         const int s = fill % S;
         const uint32_t ph = (fill / S) & 1u;
@@ -867,8 +1033,8 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
             if constexpr (PAIR) umma_f8_pair(dtm, ad, bd, IDESC, accum);
             else umma_f8(dtm, ad, bd, IDESC, accum);
           } else {
-            if constexpr (PAIR) umma_f16_pair(dtm, ad, bd, IDESC, accum);
-            else umma_f16(dtm, ad, bd, IDESC, accum);
+            if constexpr (PAIR) umma_f16_pair(dtm, ad, bd, idesc, accum);
+            else umma_f16(dtm, ad, bd, idesc, accum);
           }
         }
         if constexpr (PAIR) umma_commit_pair(empty_bar(s), 3);
@@ -920,15 +1086,22 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
       if (ti.bad) continue;
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1u;
-      // warp-uniform decision: the tcgen05.ld below is .sync.aligned
-      const bool ok = wait_bar(tfull_bar(acc), aph, abort_flag, 5);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      // warp-uniform decision: the tcgen05.ld below is .sync.aligned; the warps of the
+      // swapped GEMM1 that exchange chunks (q, q + 2) decide together
+      bool ok = __all_sync(0xFFFFFFFFu, wait_bar(tfull_bar(acc), aph, abort_flag, 5));
+      if (KIND == kFwd1T && p.gated) ok = named_bar_and(1 + (q & 1), 64, ok);
+      if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      epilogue_tile<KIND, BN>(p, ti, tacc, q, lane,
-                              epi_buf + ew * (Cfg::kEpiWarpBytes / 4),
-                              epi0 + ew * static_cast<uint32_t>(Cfg::kEpiWarpBytes), ew >> 2,
-                              EW / 4);
+      if constexpr (Tr::kSwap) {
+        epilogue_swap<KIND>(p, ti, tacc, q, lane, epi_buf + ew * (Cfg::kEpiWarpBytes / 4),
+                            epi_buf + (ew ^ 2) * (Cfg::kEpiWarpBytes / 4), rank);
+      } else {
+        epilogue_tile<KIND, BN>(p, ti, tacc, q, lane,
+                                epi_buf + ew * (Cfg::kEpiWarpBytes / 4),
+                                epi0 + ew * static_cast<uint32_t>(Cfg::kEpiWarpBytes), ew >> 2,
+                                EW / 4);
+      }
       tc_fence_before();
       __syncwarp();
       // The accumulator is free once every lane's tcgen05.ld has completed (they have: the
@@ -949,8 +1122,12 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
   // fills it issued, rank 0 re-balances the expected bytes of fills only one CTA issued and
   // waits for them, then both CTAs leave together.
   if constexpr (PAIR) {
-    if (rank == 1 && warp == 0 && lane == 0)
+    if (rank == 1 && warp == 0 && lane == 0) {
       st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_issued)), 0), issued);
+      for (int s = 0; s < S; ++s)
+        st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_tx + s)), 0),
+                              tx_ring[s]);
+    }
     cluster_sync_all();
   }
   if (rank == 0 && warp == 0 && lane == 0) {
@@ -960,9 +1137,11 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
       const int s = f % S;
       const bool armed = f < issued && static_cast<int>(f) != skipped;
       if constexpr (PAIR) {
+        // a fill rank 0 armed for both CTAs but the peer never loaded: complete the peer's
+        // share (the same bytes: the same tile); a fill only the peer loaded: expect its bytes
         const bool peer_loaded = f < iss_p;
-        if (!armed) mbar_arrive_expect_tx(full_bar(s), peer_loaded ? Cfg::kStageBytes : 0u);
-        else if (!peer_loaded) mbar_complete_tx(full_bar(s), Cfg::kStageBytes);
+        if (!armed) mbar_arrive_expect_tx(full_bar(s), peer_loaded ? peer_tx[s] : 0u);
+        else if (!peer_loaded) mbar_complete_tx(full_bar(s), tx_ring[s]);
       } else {
         if (!armed) continue;
       }

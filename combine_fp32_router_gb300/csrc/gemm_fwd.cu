@@ -208,4 +208,59 @@ cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
   return run_rows_kind<kFwd2, 128>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, c.num_sms, s);
 }
 
+// Swapped forward GEMMs: one CTA-pair launch over every (row block, weight-column block).
+// The row operand has four tensor maps, with boxes of 16, 32, 64 and 128 rows: each CTA of a
+// pair loads half of the block's rows, rounded up to one of these.
+namespace {
+cudaError_t row_maps(GemmParams& p, const void* rows, uint64_t inner, uint64_t nrows,
+                     uint64_t row_bytes) {
+  cudaError_t st = cudaSuccess;
+  for (int i = 0; i < 4; ++i)
+    p.mapR[i] = make_map_2d(rows, inner, nrows, row_bytes, 64, 16u << i, &st);
+  return st;
+}
+GemmParams swap_params(const GemmCtx& c) {
+  GemmParams p = base_params(c);
+  p.n_st = reinterpret_cast<const int32_t*>(c.ws + c.L->n_st);
+  p.st_expert = reinterpret_cast<const int32_t*>(c.ws + c.L->st_expert);
+  p.st_row0 = reinterpret_cast<const int32_t*>(c.ws + c.L->st_row0);
+  return p;
+}
+}  // namespace
+
+cudaError_t launch_gemm_fwd1_swap(const GemmCtx& c, cudaStream_t s) {
+  const WsLayout& L = *c.L;
+  cudaError_t st = cudaSuccess;
+  // M operand: W1 and W3 viewed as [E d rows][dff] (64-column boxes of 64 K rows)
+  const CUtensorMap w1 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 64, &st);
+  const CUtensorMap w3 = make_map_2d(c.gated ? c.W3 : c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d,
+                                     2ull * L.dff, 64, 64, &st);
+  if (st != cudaSuccess) return st;
+  GemmParams p = swap_params(c);
+  st = row_maps(p, c.ws + L.xperm, L.d, L.P_pad, 2ull * L.d);
+  if (st != cudaSuccess) return st;
+  p.nb = c.gated ? L.dff / 128 : L.dff / 256;
+  p.nkb = L.d / kBK;
+  p.out0 = c.ws + L.H;
+  p.save_ab = c.save_ab;
+  p.save_a = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Asave) : nullptr;
+  p.save_b = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Bsave) : nullptr;
+  return run_grouped_gemm<kFwd1T, 256, true>(w1, w1, w3, p, L.max_mt * p.nb, c.num_sms, s);
+}
+
+cudaError_t launch_gemm_fwd2_swap(const GemmCtx& c, cudaStream_t s) {
+  const WsLayout& L = *c.L;
+  cudaError_t st = cudaSuccess;
+  // M operand: W2 viewed as [E dff rows][d] (64-column boxes of 64 K rows)
+  const CUtensorMap w2 = make_map_2d(c.W2, L.d, static_cast<uint64_t>(L.E) * L.dff, 2ull * L.d, 64, 64, &st);
+  if (st != cudaSuccess) return st;
+  GemmParams p = swap_params(c);
+  st = row_maps(p, c.ws + L.H, L.dff, L.P_pad, 2ull * L.dff);
+  if (st != cudaSuccess) return st;
+  p.nb = (L.d + 255) / 256;  // d % 256 == 128: the last block's second CTA has no columns
+  p.nkb = L.dff / kBK;
+  p.out0 = c.ws + L.Y;
+  return run_grouped_gemm<kFwd2T, 256, true>(w2, w2, w2, p, L.max_mt * p.nb, c.num_sms, s);
+}
+
 }  // namespace moe

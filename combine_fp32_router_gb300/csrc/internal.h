@@ -23,13 +23,20 @@ struct WsLayout {
   int d = 0, E = 0, k = 0, dff = 0;
   size_t err = 0, hist = 0, bbase = 0, counts = 0, offsets = 0, poff = 0, n_mt = 0,
          mt_expert = 0, mt_row0 = 0, n_pt = 0, pt_expert = 0, pt_row0 = 0, n_lo = 0,
-         lo_expert = 0, lo_row0 = 0, topk = 0, gate = 0,
+         lo_expert = 0, lo_row0 = 0, n_st = 0, st_expert = 0, st_row0 = 0, topk = 0, gate = 0,
          pos = 0, perm = 0, xperm = 0, H = 0, Y = 0, Asave = 0, Bsave = 0, dO = 0, dAB = 0,
          dXp = 0, seg = 0, xscale = 0;
   size_t route_total = 0, fwd_total = 0, bwd_total = 0;
 };
 
 WsLayout make_layout(int64_t T, int d, int E, int k, int dff);
+
+// Argument checks of the dispatch entry points (sizes, null pointers, 16-byte alignment),
+// shared by moe_route_dispatch and moe_route_dispatch_noalloc (moe_api.cu).
+moe_status_t check_route_args(const void* x, const void* logits, int64_t T, int d, int E, int k,
+                              const void* topk_idx, const void* gate, const void* counts,
+                              const void* offsets, const void* perm, const void* pos,
+                              const void* x_perm);
 
 // ---- routing / dispatch / combine launches (route.cu) -----------------------------------
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* topk,
@@ -39,12 +46,17 @@ cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* 
                              int32_t* counts, cudaStream_t s);
 // offsets (unpadded, may be null), poff (rows padded to `align`), and when align == 128
 // the tile tables: every 128-row tile (n_mt, mt_expert, mt_row0); the 256-row pair tiles
-// (n_pt, pt_expert, pt_row0: two consecutive 128-row tiles of one expert); and each
-// expert's odd last 128-row tile (n_lo, lo_expert, lo_row0), which pairs leave over.
+// (n_pt, pt_expert, pt_row0: two consecutive 128-row tiles of one expert); each expert's odd
+// last 128-row tile (n_lo, lo_expert, lo_row0), which pairs leave over; and the blocks of up
+// to 256 rows of the swapped forward GEMMs (n_st, st_expert, st_row0: every expert's rows
+// cut from its first row in 256-row steps, the last block partial).
 struct TileTables {
   int32_t *n_mt, *mt_expert, *mt_row0, *n_pt, *pt_expert, *pt_row0, *n_lo, *lo_expert, *lo_row0;
+  int32_t *n_st, *st_expert, *st_row0;
   int64_t max_mt;
 };
+// The tile tables of a workspace laid out by L.
+TileTables tile_tables(const WsLayout& L, char* ws);
 cudaError_t launch_offsets(const int32_t* counts, int E, int align, int32_t* offsets,
                            int32_t* poff, const TileTables* tables, DevErr* err,
                            cudaStream_t s);
@@ -85,6 +97,7 @@ struct GemmCtx {
   int debug_flags;
   int num_sms;
   bool pair;  // 256-row tiles on CTA pairs (tcgen05 cta_group::2)
+  bool swap;  // forward GEMMs with weight columns as M and row blocks as N (one pair launch)
   bool fuse_combine;     // GEMM2 also combines finished tokens into `out`
   bool gather_x;         // GEMM1 gathers its A rows from x (no x_perm)
   uint16_t* out;         // layer output [T, d] (fused combine)
@@ -96,6 +109,9 @@ struct GemmCtx {
 cudaError_t launch_gemm_fwd1(const GemmCtx& c, cudaStream_t s);   // H = SwiGLU(Xp W1, Xp W3)
 cudaError_t launch_gemm_fwd1_fp8(const GemmCtx& c, cudaStream_t s);  // H from E4M3 Xp, W1, W3
 cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s);   // Y = H W2
+// the same two GEMMs with swapped operands (weight columns x row blocks), CTA pairs
+cudaError_t launch_gemm_fwd1_swap(const GemmCtx& c, cudaStream_t s);
+cudaError_t launch_gemm_fwd2_swap(const GemmCtx& c, cudaStream_t s);
 cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s);     // dA,dB from dO W2^T
 cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s);     // dXp = dA W1^T + dB W3^T
 cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s);    // dW2 = H^T dO

@@ -33,6 +33,17 @@ PairMode pair_mode() {
 }
 bool use_pairs() { return pair_mode() != kPairsOff; }
 
+// Forward GEMMs with swapped operands (weight columns x row blocks, one CTA-pair launch each)
+// when MOE_FWD_SWAP is "1" and MOE_GEMM_PAIR is not "0"; otherwise the row-tile kernels (pairs
+// by the size rule or MOE_GEMM_PAIR); read once per process.
+bool forward_swap() {
+  static const bool v = [] {
+    const char* e = std::getenv("MOE_FWD_SWAP");
+    return e && e[0] == '1' && e[1] == 0;
+  }();
+  return v && use_pairs();
+}
+
 // CTA pairs for the row-grouped GEMMs (the experts' 256-row pair tiles, chosen per expert on
 // the device; the rest in a second, single-CTA launch): only when some expert can fill a pair
 // tile (T > 128) and the layer is large enough that the second launch's ramp and tail are
@@ -134,6 +145,9 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   L.n_lo = take(16);
   L.lo_expert = take(static_cast<size_t>(L.max_mt) * 4);
   L.lo_row0 = take(static_cast<size_t>(L.max_mt) * 4);
+  L.n_st = take(16);  // 256-row blocks: never more than the 128-row tiles
+  L.st_expert = take(static_cast<size_t>(L.max_mt) * 4);
+  L.st_row0 = take(static_cast<size_t>(L.max_mt) * 4);
   L.topk = take(P * 4);
   L.gate = take(P * 4);
   L.pos = take(P * 4);
@@ -153,6 +167,41 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   return L;
 }
 
+TileTables tile_tables(const WsLayout& L, char* w) {
+  TileTables tt;
+  tt.n_mt = reinterpret_cast<int32_t*>(w + L.n_mt);
+  tt.mt_expert = reinterpret_cast<int32_t*>(w + L.mt_expert);
+  tt.mt_row0 = reinterpret_cast<int32_t*>(w + L.mt_row0);
+  tt.n_pt = reinterpret_cast<int32_t*>(w + L.n_pt);
+  tt.pt_expert = reinterpret_cast<int32_t*>(w + L.pt_expert);
+  tt.pt_row0 = reinterpret_cast<int32_t*>(w + L.pt_row0);
+  tt.n_lo = reinterpret_cast<int32_t*>(w + L.n_lo);
+  tt.lo_expert = reinterpret_cast<int32_t*>(w + L.lo_expert);
+  tt.lo_row0 = reinterpret_cast<int32_t*>(w + L.lo_row0);
+  tt.n_st = reinterpret_cast<int32_t*>(w + L.n_st);
+  tt.st_expert = reinterpret_cast<int32_t*>(w + L.st_expert);
+  tt.st_row0 = reinterpret_cast<int32_t*>(w + L.st_row0);
+  tt.max_mt = L.max_mt;
+  return tt;
+}
+
+}  // namespace moe
+
+namespace moe {
+moe_status_t check_route_args(const void* x, const void* logits, int64_t T, int d, int E, int k,
+                              const void* topk_idx, const void* gate, const void* counts,
+                              const void* offsets, const void* perm, const void* pos,
+                              const void* x_perm) {
+  moe_status_t st = check_dims(T, d, E, k, 0, false);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !logits || !topk_idx || !gate || !perm || !pos || !x_perm))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, logits, topk_idx, gate, counts, offsets, perm, pos, x_perm};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
 }  // namespace moe
 
 using namespace moe;
@@ -177,14 +226,10 @@ moe_status_t moe_route_dispatch(const moe_bf16_t* x, const float* logits, int64_
                                 int32_t* offsets, int32_t* perm, int32_t* pos,
                                 moe_bf16_t* x_perm, void* ws, size_t ws_bytes,
                                 cudaStream_t stream) {
-  moe_status_t st = check_dims(T, d, E, k, 0, false);
+  moe_status_t st = check_route_args(x, logits, T, d, E, k, topk_idx, gate, counts, offsets,
+                                     perm, pos, x_perm);
   if (st != MOE_OK) return st;
-  if (!counts || !offsets || !ws) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!x || !logits || !topk_idx || !gate || !perm || !pos || !x_perm))
-    return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, logits, topk_idx, gate, counts, offsets, perm, pos, x_perm};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
   const WsLayout L = make_layout(T, d, E, k, 128);
   if (ws_bytes < L.route_total) return MOE_ERR_WORKSPACE;
@@ -266,17 +311,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   // dispatch: route, count, prefix sums (rows padded to 128 per expert), stable permute
   MOE_TRY(launch_route_topk(logits, T, E, k, topk, gate, pos, hist, err, stream));
   MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
-  TileTables tt;
-  tt.n_mt = reinterpret_cast<int32_t*>(w + L.n_mt);
-  tt.mt_expert = reinterpret_cast<int32_t*>(w + L.mt_expert);
-  tt.mt_row0 = reinterpret_cast<int32_t*>(w + L.mt_row0);
-  tt.n_pt = reinterpret_cast<int32_t*>(w + L.n_pt);
-  tt.pt_expert = reinterpret_cast<int32_t*>(w + L.pt_expert);
-  tt.pt_row0 = reinterpret_cast<int32_t*>(w + L.pt_row0);
-  tt.n_lo = reinterpret_cast<int32_t*>(w + L.n_lo);
-  tt.lo_expert = reinterpret_cast<int32_t*>(w + L.lo_expert);
-  tt.lo_row0 = reinterpret_cast<int32_t*>(w + L.lo_row0);
-  tt.max_mt = L.max_mt;
+  const TileTables tt = tile_tables(L, w);
   MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
   // With MOE_FWD_GATHER_ROWS (and no backward, which reads x_perm as a K operand) GEMM1
   // gathers its rows from x itself: the dispatch copy of the next tiles overlaps the MMAs of
@@ -305,7 +340,10 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.gated = W3 != nullptr;
   c.gather_x = gather;
   c.out = out;
-  MOE_TRY(launch_gemm_fwd1(c, stream));
+  // the plain forward runs both GEMMs with swapped operands on CTA pairs; the row-gather and
+  // fused-combine variants keep the row-tile kernels
+  c.swap = forward_swap() && !gather && !c.fuse_combine;
+  MOE_TRY(c.swap ? launch_gemm_fwd1_swap(c, stream) : launch_gemm_fwd1(c, stream));
   record(stage_events, 2, stream);
   if (c.fuse_combine) {
     // GEMM2 combines each token as soon as its k expert rows are written
@@ -316,7 +354,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
     record(stage_events, 4, stream);
     return MOE_OK;
   }
-  MOE_TRY(launch_gemm_fwd2(c, stream));
+  MOE_TRY(c.swap ? launch_gemm_fwd2_swap(c, stream) : launch_gemm_fwd2(c, stream));
   record(stage_events, 3, stream);
   MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,
                          stream));
@@ -370,17 +408,7 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uin
   // dispatch with the FP8 payload: route, count, prefix sums, E4M3 rows + row scales
   MOE_TRY(launch_route_topk(logits, T, E, k, topk, gate, pos, hist, err, stream));
   MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
-  TileTables tt;
-  tt.n_mt = reinterpret_cast<int32_t*>(w + L.n_mt);
-  tt.mt_expert = reinterpret_cast<int32_t*>(w + L.mt_expert);
-  tt.mt_row0 = reinterpret_cast<int32_t*>(w + L.mt_row0);
-  tt.n_pt = reinterpret_cast<int32_t*>(w + L.n_pt);
-  tt.pt_expert = reinterpret_cast<int32_t*>(w + L.pt_expert);
-  tt.pt_row0 = reinterpret_cast<int32_t*>(w + L.pt_row0);
-  tt.n_lo = reinterpret_cast<int32_t*>(w + L.n_lo);
-  tt.lo_expert = reinterpret_cast<int32_t*>(w + L.lo_expert);
-  tt.lo_row0 = reinterpret_cast<int32_t*>(w + L.lo_row0);
-  tt.max_mt = L.max_mt;
+  const TileTables tt = tile_tables(L, w);
   MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
   MOE_TRY(launch_scatter_fp8(x, T, d, E, k, topk, bbase, poff, pos, perm,
                              reinterpret_cast<uint8_t*>(w + L.xperm),

@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   griddep_wait();  // the previous kernel in the stream has finished (PDL)
   __shared__ int warp_tot[32];
   __shared__ int total;
-  __shared__ int s_poff[1024], s_a[1024], s_b[1024], s_pa[1024], s_pb[1024];
+  __shared__ int s_poff[1024], s_a[1024], s_b[1024], s_pa[1024], s_pb[1024], s_sa[1024],
+      s_sb[1024];
   const int e = threadIdx.x;
   const int c = e < E ? counts[e] : 0;
   const int pc = (c + align - 1) / align * align;
@@ -331,6 +332,14 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   const int PL = total;
   const int los = block_exclusive_scan(nlo, warp_tot, &total);
   const int NLO = total;
+  // blocks of up to 256 rows for the swapped forward GEMMs: experts with several blocks
+  // (bound by the tensor cores) merged in proportion with the one-block experts (bound by
+  // reading their weights)
+  const int ns = (c + 2 * kTileRows - 1) / (2 * kTileRows);
+  const int sa = block_exclusive_scan(ns >= 2 ? ns : 0, warp_tot, &total) + (ns >= 2 ? ns : 0);
+  const int SH = total;
+  const int sb = block_exclusive_scan(ns == 1 ? 1 : 0, warp_tot, &total) + (ns == 1 ? 1 : 0);
+  const int SL = total;
   // every table holds at most sum(nm) <= max_mt entries (the padded rows bound the tiles)
   const bool fits = H + L <= tt.max_mt;
   if (e < E) {
@@ -339,6 +348,8 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
     s_b[e] = lb;
     s_pa[e] = pa;
     s_pb[e] = pb;
+    s_sa[e] = sa;
+    s_sb[e] = sb;
     if (fits) {
       for (int i = 0; i < nlo; ++i) {  // nlo <= kPairOddMinTiles - 2 for experts not paired
         tt.lo_expert[los + i] = e;
@@ -350,6 +361,7 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
     tt.n_mt[0] = fits ? H + L : 0;
     tt.n_pt[0] = fits ? PH + PL : 0;
     tt.n_lo[0] = fits ? NLO : 0;
+    tt.n_st[0] = fits ? SH + SL : 0;
   }
   __syncthreads();
   if (!fits) {
@@ -358,6 +370,7 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   }
   fill_tile_table(s_a, s_b, s_poff, E, H, L, kTileRows, tt.mt_expert, tt.mt_row0);
   fill_tile_table(s_pa, s_pb, s_poff, E, PH, PL, 2 * kTileRows, tt.pt_expert, tt.pt_row0);
+  fill_tile_table(s_sa, s_sb, s_poff, E, SH, SL, 2 * kTileRows, tt.st_expert, tt.st_row0);
 }
 
 // Stable permute.  One warp per token: lanes j < k turn the CTA-local rank into the final
@@ -384,8 +397,9 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
       const int64_t p = t * k + lane;
       const int e = topk[p];
       const int64_t b = t / kRouteTokensPerBlock;
-      row = poff[e] + bbase[b * E + e] + pos[p];
-      if (row < 0 || row >= rows_cap || e < 0 || e >= E) {
+      // the expert index is checked before it indexes poff and bbase, the row after
+      row = (e >= 0 && e < E) ? poff[e] + bbase[b * E + e] + pos[p] : -1;
+      if (row < 0 || row >= rows_cap) {
         set_error(reinterpret_cast<DevErr*>(err), MOE_ERR_DEVICE_BOUNDS, 200);
         row = -1;
       } else {
@@ -460,8 +474,9 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const uint4* __restric
       const int64_t p = t * k + lane;
       const int e = topk[p];
       const int64_t b = t / kRouteTokensPerBlock;
-      row = poff[e] + bbase[b * E + e] + pos[p];
-      if (row < 0 || row >= rows_cap || e < 0 || e >= E) {
+      // the expert index is checked before it indexes poff and bbase, the row after
+      row = (e >= 0 && e < E) ? poff[e] + bbase[b * E + e] + pos[p] : -1;
+      if (row < 0 || row >= rows_cap) {
         set_error(err, MOE_ERR_DEVICE_BOUNDS, 201);
         row = -1;
       } else {

@@ -13,7 +13,10 @@
 // library, for the life of the process.  All calls share it and it keeps whatever the last
 // call left: the error record is cleared at the start of each call; the histograms and
 // bases are fully rewritten by every call.  Two calls that overlap on the GPU (different
-// streams without ordering, or different host threads) race on the array.
+// streams without ordering, or different host threads) race on the array.  The array's
+// device address is cached per device at the first call, so a device reset after that call
+// (cudaDeviceReset, or a new primary context) is not supported.
+// moe_route_dispatch_noalloc_get_error reads the error record the last call left.
 #include <mutex>
 
 #include "common.cuh"
@@ -50,8 +53,6 @@ void* scratch_on_current_device(cudaError_t* st) {
   return addr[dev];
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 }  // namespace moe
 
@@ -61,17 +62,10 @@ extern "C" moe_status_t moe_route_dispatch_noalloc(
     const moe_bf16_t* x, const float* logits, int64_t T, int d, int E, int k,
     int32_t* topk_idx, float* gate, int32_t* counts, int32_t* offsets, int32_t* perm,
     int32_t* pos, moe_bf16_t* x_perm, cudaStream_t stream) {
-  // same argument rules as moe_route_dispatch
-  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
-  if (E > kMaxE || k > kMaxK || d > 65536 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (T > (int64_t{1} << 31) / k) return MOE_ERR_UNSUPPORTED;
-  if (T * k + static_cast<int64_t>(kTileRows) * E >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED;
-  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!x || !logits || !topk_idx || !gate || !perm || !pos || !x_perm))
-    return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, logits, topk_idx, gate, counts, offsets, perm, pos, x_perm};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  // the argument rules of moe_route_dispatch, from the same function
+  const moe_status_t chk = check_route_args(x, logits, T, d, E, k, topk_idx, gate, counts,
+                                            offsets, perm, pos, x_perm);
+  if (chk != MOE_OK) return chk;
   // the fixed scratch holds an error record and two [ceil(T/128), E] int32 tables
   const int64_t nblk = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   const size_t table = round256(static_cast<size_t>(nblk) * E * 4);
@@ -100,4 +94,15 @@ extern "C" moe_status_t moe_route_dispatch_noalloc(
                      stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" moe_status_t moe_route_dispatch_noalloc_get_error(cudaStream_t stream) {
+  cudaError_t st = cudaSuccess;
+  const char* scratch = static_cast<const char*>(scratch_on_current_device(&st));
+  if (!scratch) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  DevErr e{};
+  if (cudaMemcpy(&e, scratch, sizeof e, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return static_cast<moe_status_t>(e.status);
 }

@@ -257,15 +257,25 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
  * GPU that loads the library until the process exits.  Limit: ceil(T/128) * E <= 262080
  * (for example T = 131072 tokens with E = 256, or T = 32640 with E = 1024); larger sizes
  * return MOE_ERR_UNSUPPORTED before anything is launched.  The first call on a device looks
- * up the array's device address (the device must be current); make that first call before
- * any stream capture.  Every call shares the array: calls that overlap on the GPU (unordered
- * streams, or several host threads) race and give undefined results.  Device-side checks of
- * this variant are recorded in the library's scratch and are not readable by the caller.
+ * up the array's device address (the device must be current) and keeps it for the life of
+ * the process: make that first call before any stream capture, and do not reset the device
+ * (cudaDeviceReset or a new primary context) after it.  Every call shares the array: calls
+ * that overlap on the GPU (unordered streams, or several host threads) race and give
+ * undefined results.  Device-side checks of this variant are recorded at the start of the
+ * library's array; moe_route_dispatch_noalloc_get_error reads them.
  */
 moe_status_t moe_route_dispatch_noalloc(const moe_bf16_t* x, const float* logits, int64_t T,
                                         int d, int E, int k, int32_t* topk_idx, float* gate,
                                         int32_t* counts, int32_t* offsets, int32_t* perm,
                                         int32_t* pos, moe_bf16_t* x_perm, cudaStream_t stream);
+
+/* The device-side error record of moe_route_dispatch_noalloc on the current device:
+ * synchronises `stream` (the stream of the last call), reads the record at the start of the
+ * library's fixed array and returns it: MOE_OK when the last call on this device recorded no
+ * device-side problem (each call clears the record first), MOE_ERR_DEVICE_BOUNDS when its
+ * scatter met an index out of range.  Returns MOE_ERR_CUDA if the stream reports an error.
+ * The pages have no counterpart; it belongs to the no-allocation dispatch. */
+moe_status_t moe_route_dispatch_noalloc_get_error(cudaStream_t stream);
 
 /* Synchronises `stream`, reads the device error word of `ws` and returns it (MOE_OK when
  * no device-side problem was recorded since the last moe_route_dispatch / moe_forward on

@@ -58,3 +58,42 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     with pytest.raises(moe.MoeError) as exc:
         _noalloc(moe, g, k)
     assert exc.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_error_record_reads_ok_after_a_normal_call():
+    import combine_fp32_router_gb300 as moe
+    g = to_dev(moe_synth.generate(moe_synth.custom(500, 128, 16, 4, 128, seed=31)))
+    _noalloc(moe, g, 4)
+    assert moe.moe_route_dispatch_noalloc_get_error() == moe.MOE_OK
+
+
+def test_noalloc_empty_batch_zeroes_counts_and_offsets():
+    import combine_fp32_router_gb300 as moe
+    E, k = 24, 3
+    g = {"x": torch.empty(0, 128, dtype=torch.bfloat16, device="cuda"),
+         "logits": torch.empty(0, E, dtype=torch.float32, device="cuda")}
+    out = _noalloc(moe, g, k)
+    assert (out["counts"] == 0).all() and (out["offsets"] == 0).all()
+    assert moe.moe_route_dispatch_noalloc_get_error() == moe.MOE_OK
+
+
+def test_noalloc_size_limit_is_exact():
+    # ceil(T/128) * E <= 262080 is accepted (T = 273 * 128, E = 960 reaches it exactly) and
+    # matches the workspace entry point; one more routing block is rejected
+    import combine_fp32_router_gb300 as moe
+    E, k, d = 960, 2, 8
+    T = 273 * 128
+    assert (T + 127) // 128 * E == 262080
+    w = moe_synth.custom(T, d, E, k, 128, seed=41)
+    g = to_dev(moe_synth.generate(w))
+    ref = route_dispatch(moe, g, k)
+    got = _noalloc(moe, g, k)
+    for key in ("topk_idx", "counts", "offsets", "perm", "pos"):
+        assert torch.equal(got[key], ref[key]), key
+    assert torch.equal(got["x_perm"].view(torch.int16), ref["x_perm"].view(torch.int16))
+    assert moe.moe_route_dispatch_noalloc_get_error() == moe.MOE_OK
+    big = {"x": torch.zeros(T + 1, d, dtype=torch.bfloat16, device="cuda"),
+           "logits": torch.zeros(T + 1, E, dtype=torch.float32, device="cuda")}
+    with pytest.raises(moe.MoeError) as exc:
+        _noalloc(moe, big, k)
+    assert exc.value.status == moe.MOE_ERR_UNSUPPORTED
