@@ -183,9 +183,22 @@ def _row_pairs(T, k, d, dff):
     return mode == "1" or T * k * d * dff >= 2 ** 37
 
 
+def _forward_swap(T, k, d, dff):
+    # the library's rule for the swapped forward GEMMs (MOE_FWD_SWAP: "0" never, "1" always,
+    # else T <= 128 or wherever the row-tile kernels would use CTA pairs); never with
+    # MOE_GEMM_PAIR "0"
+    mode = os.environ.get("MOE_FWD_SWAP", "")
+    if mode == "0" or os.environ.get("MOE_GEMM_PAIR", "") == "0":
+        return False
+    return mode == "1" or T <= 128 or _row_pairs(T, k, d, dff)
+
+
 def fwd_launches(T, k, d, dff):
     # routing, column scan, offsets/tile tables, scatter, padding rows, GEMM1, GEMM2, combine;
-    # with CTA pairs each GEMM is a pair launch plus a single-CTA launch for the other tiles
+    # with row-tile CTA pairs each GEMM is a pair launch plus a single-CTA launch for the
+    # other tiles (the swapped kernels take every tile in one pair launch)
+    if _forward_swap(T, k, d, dff):
+        return 8
     return 10 if _row_pairs(T, k, d, dff) else 8
 
 

@@ -651,19 +651,29 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
 #pragma unroll
         for (int j = 0; j < 32; ++j) mine[lane * 33 + j] = v[j];
         named_bar_sync(bar, 64);
+        float hv[16];
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
-          const int j = j0 + jj, r = ch * 32 + j;
-          if (r < ti.nseg) {
-            float hv = 0.0f;
-            if (r < ti.nvalid) {
-              const float x0 = mine[lane * 33 + j], x1 = partner[lane * 33 + j];
-              hv = is_a ? silu_f(x0) * x1 : silu_f(x1) * x0;
-            }
-            H[(row0 + r) * p.dff + col] = bf16_bits(hv);
-          }
+          const int j = j0 + jj;
+          const float x0 = mine[lane * 33 + j], x1 = partner[lane * 33 + j];
+          hv[jj] = ch * 32 + j < ti.nvalid ? (is_a ? silu_f(x0) * x1 : silu_f(x1) * x0) : 0.0f;
         }
-        named_bar_sync(bar, 64);
+        named_bar_sync(bar, 64);  // the partner has read `mine`
+        // the warp's 16 rows x 32 h columns as bf16 through `mine` (row pitch 64 bytes), then
+        // 16-byte stores: each instruction writes 8 rows x 64 bytes
+        uint16_t* hb = reinterpret_cast<uint16_t*>(mine);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) hb[jj * 32 + lane] = bf16_bits(hv[jj]);
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+          const int jj = (it * 32 + lane) >> 2, piece = lane & 3;
+          const int r = ch * 32 + j0 + jj;
+          if (r < ti.nseg)
+            st_v4(H + (row0 + r) * p.dff + (col - lane) + piece * 8,
+                  *reinterpret_cast<const uint4*>(hb + jj * 32 + piece * 8));
+        }
+        __syncwarp();  // stores have read `mine` before the next chunk rewrites it
       }
       if (is_a)
         for (int r = nch * 32; r < ti.nseg; ++r) H[(row0 + r) * p.dff + col] = 0;

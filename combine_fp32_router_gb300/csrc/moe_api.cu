@@ -33,16 +33,6 @@ PairMode pair_mode() {
 }
 bool use_pairs() { return pair_mode() != kPairsOff; }
 
-// Forward GEMMs with swapped operands (weight columns x row blocks, one CTA-pair launch each)
-// when MOE_FWD_SWAP is "1" and MOE_GEMM_PAIR is not "0"; otherwise the row-tile kernels (pairs
-// by the size rule or MOE_GEMM_PAIR); read once per process.
-bool forward_swap() {
-  static const bool v = [] {
-    const char* e = std::getenv("MOE_FWD_SWAP");
-    return e && e[0] == '1' && e[1] == 0;
-  }();
-  return v && use_pairs();
-}
 
 // CTA pairs for the row-grouped GEMMs (the experts' 256-row pair tiles, chosen per expert on
 // the device; the rest in a second, single-CTA launch): only when some expert can fill a pair
@@ -54,6 +44,25 @@ bool row_pairs(int64_t T, int k, int d, int dff) {
   if (pair_mode() == kPairsOff || T <= kTileRows) return false;
   const double work = static_cast<double>(T) * k * d * dff;
   return pair_mode() == kPairsOn || work >= 137438953472.0;
+}
+
+// Forward GEMMs with swapped operands (weight columns x row blocks, one CTA-pair launch each)
+// for small batches (T <= 128) and wherever the row-tile kernels would use CTA pairs; the
+// row-tile kernels on single CTAs in between (measured on GB300: T=4096, d=2048, E=64, top-6,
+// d_ff=1024 runs 0.37 ms on single-CTA row tiles, 0.44 ms swapped; T=1..128 with d=7168,
+// E=256, top-8, d_ff=2048 runs 2-18% faster swapped; the T=16384 layer of the same shape
+// and T=8192, d=4096, E=128, top-8, d_ff=1536 1-2%).  MOE_FWD_SWAP="0" turns the swapped
+// kernels off, "1" uses them for every size; MOE_GEMM_PAIR="0" (single CTAs only) turns
+// them off too.  Read once per process; every choice gives bitwise the same rows.
+bool forward_swap(int64_t T, int k, int d, int dff) {
+  static const int mode = [] {
+    const char* e = std::getenv("MOE_FWD_SWAP");
+    if (e && e[0] == '0' && e[1] == 0) return 0;
+    if (e && e[0] == '1' && e[1] == 0) return 1;
+    return 2;
+  }();
+  if (mode == 0 || !use_pairs()) return false;
+  return mode == 1 || T <= kTileRows || row_pairs(T, k, d, dff);
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -342,7 +351,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.out = out;
   // the plain forward runs both GEMMs with swapped operands on CTA pairs; the row-gather and
   // fused-combine variants keep the row-tile kernels
-  c.swap = forward_swap() && !gather && !c.fuse_combine;
+  c.swap = forward_swap(T, k, d, d_ff) && !gather && !c.fuse_combine;
   MOE_TRY(c.swap ? launch_gemm_fwd1_swap(c, stream) : launch_gemm_fwd1(c, stream));
   record(stage_events, 2, stream);
   if (c.fuse_combine) {

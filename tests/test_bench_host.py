@@ -57,6 +57,11 @@ def test_pair_rule_and_launch_counts(bench, monkeypatch, mode, name, pairs):
         monkeypatch.setenv("MOE_GEMM_PAIR", mode)
     w = moe_synth.by_name(name)
     assert bench._row_pairs(w.T, w.k, w.d, w.dff) == pairs
-    # each row-grouped GEMM adds a single-CTA launch beside its pair launch
+    # the backward's row-grouped GEMMs add a single-CTA launch beside each pair launch; the
+    # forward's swapped GEMMs (wherever row tiles would pair, and T <= 128) are one launch each
+    monkeypatch.setenv("MOE_FWD_SWAP", "0")
     assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)
+    monkeypatch.delenv("MOE_FWD_SWAP")
+    assert bench._forward_swap(w.T, w.k, w.d, w.dff) == (mode != "0" and (pairs or w.T <= 128))
+    assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == 8
     assert bench.bwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)

@@ -2,9 +2,9 @@
 
 Forward and backward outputs (SwiGLU and squared-ReLU experts) must be bitwise the same
 whether the forward GEMMs run with swapped operands (weight columns x blocks of up to 256
-rows, CTA pairs; the default), or as row tiles: 256-row tiles on CTA pairs for the experts the
-tile tables pick and the rest on single CTAs (MOE_FWD_SWAP=0, MOE_GEMM_PAIR=1), or 128-row
-tiles on single CTAs only (MOE_GEMM_PAIR=0); the backward's row-grouped GEMMs follow
+rows, CTA pairs; MOE_FWD_SWAP=1), or as row tiles: 256-row tiles on CTA pairs for the experts
+the tile tables pick and the rest on single CTAs (MOE_FWD_SWAP=0, MOE_GEMM_PAIR=1), or
+128-row tiles on single CTAs only (MOE_GEMM_PAIR=0); the backward's row-grouped GEMMs follow
 MOE_GEMM_PAIR or the library's size rule (unset).  The forward variant that gathers GEMM1's
 rows from x and fuses the combine into GEMM2 must match the default forward bitwise.  Each
 schedule runs in its own process (the switches are read once per process).
@@ -59,7 +59,7 @@ def _digest(env_extra, gated=True):
 
 @pytest.mark.parametrize("gated", [True, False])   # SwiGLU, squared ReLU (no W3)
 def test_schedule_does_not_change_results(gated):
-    ref = _digest({"MOE_GEMM_PAIR": "1"}, gated)
-    assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "0"}, gated) == ref
+    ref = _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "0"}, gated)
+    assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "1"}, gated) == ref
     assert _digest({"MOE_GEMM_PAIR": "0"}, gated) == ref
     assert _digest({}, gated) == ref
