@@ -38,6 +38,7 @@ EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispat
            "moe_forward_graph_destroy", "moe_forward_host", "moe_forward_host_pipelined",
            "moe_backward",
            "moe_route_dispatch_noalloc", "moe_route_dispatch_noalloc_get_error",
+           "moe_ep_first_expert", "moe_ep_plan", "moe_ep_return_plan", "moe_ep_copy_rows",
            "moe_get_error", "moe_set_wait_timeout_ns", "moe_debug_set_flags",
            "moe_status_string")
 
@@ -85,6 +86,14 @@ def _load():
     lib.moe_get_error.restype = i
     lib.moe_route_dispatch_noalloc_get_error.argtypes = [p]
     lib.moe_route_dispatch_noalloc_get_error.restype = i
+    lib.moe_ep_first_expert.argtypes = [i, i, i]
+    lib.moe_ep_first_expert.restype = i
+    lib.moe_ep_plan.argtypes = [p, i, i, i, i, i, p, p, p, p, p]
+    lib.moe_ep_plan.restype = i
+    lib.moe_ep_return_plan.argtypes = [p, i, i, i, i, p, p, p]
+    lib.moe_ep_return_plan.restype = i
+    lib.moe_ep_copy_rows.argtypes = [p, p, i, p, p, p, p, i, i64, p, i64, p, p]
+    lib.moe_ep_copy_rows.restype = i
     lib.moe_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.moe_set_wait_timeout_ns.restype = None
     lib.moe_debug_set_flags.argtypes = [i]
@@ -103,6 +112,11 @@ def _ptr(t):
     if not t.is_contiguous():
         raise ValueError("tensor arguments must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _nptr(a):
+    """Host numpy array -> pointer (the host-side planning entry points)."""
+    return ctypes.c_void_p(a.ctypes.data)
 
 
 def _nbytes(t):
@@ -279,6 +293,59 @@ def moe_route_dispatch_noalloc_get_error(stream=None):
     """Synchronise the stream and return the device error status the last
     moe_route_dispatch_noalloc call on the current device recorded in the library's array."""
     return int(_lib.moe_route_dispatch_noalloc_get_error(_stream(stream)))
+
+
+def moe_ep_first_expert(E, R, rank):
+    """First expert owned by `rank` of R (rank = R gives E)."""
+    return int(_lib.moe_ep_first_expert(int(E), int(R), int(rank)))
+
+
+def moe_ep_plan(counts_all, rank, row_align=128, wave_experts=4):
+    """Exchange plan of `rank` from every rank's per-expert counts (host int32 [R, E]):
+    returns dict(recv_off [n_local, R], rows (receive buffer rows), src_off [n_local, R],
+    recv_counts [n_local], waves (first local expert of each wave, plus n_local))."""
+    import numpy as np
+    c = np.ascontiguousarray(counts_all, dtype=np.int32)
+    R, E = c.shape
+    cap = -(-E // max(R, 1))                       # the most experts a rank can own
+    recv_off = np.zeros(cap * R + 1, np.int32)
+    src_off = np.zeros(cap * R, np.int32)
+    recv_counts = np.zeros(cap, np.int32)
+    wave_first = np.zeros(cap + 2, np.int32)
+    n_waves = np.zeros(1, np.int32)
+    _check(_lib.moe_ep_plan(_nptr(c), R, E, int(rank), int(row_align), int(wave_experts),
+                            _nptr(recv_off), _nptr(src_off), _nptr(recv_counts),
+                            _nptr(wave_first), _nptr(n_waves)), "moe_ep_plan")
+    nloc = moe_ep_first_expert(E, R, rank + 1) - moe_ep_first_expert(E, R, rank)
+    return dict(recv_off=recv_off[:nloc * R].reshape(nloc, R), rows=int(recv_off[nloc * R]),
+                src_off=src_off[:nloc * R].reshape(nloc, R), recv_counts=recv_counts[:nloc],
+                waves=wave_first[:int(n_waves[0]) + 1])
+
+
+def moe_ep_return_plan(counts_all, rank, row_align=128):
+    """For every expert: (owner rank, first row of this rank's rows in the owner's
+    receive-side buffers, first row in this rank's permuted buffer), int32 arrays [E]."""
+    import numpy as np
+    c = np.ascontiguousarray(counts_all, dtype=np.int32)
+    R, E = c.shape
+    owner, owner_row, own_row = (np.zeros(E, np.int32) for _ in range(3))
+    _check(_lib.moe_ep_return_plan(_nptr(c), R, E, int(rank), int(row_align), _nptr(owner),
+                                   _nptr(owner_row), _nptr(own_row)), "moe_ep_return_plan")
+    return owner, owner_row, own_row
+
+
+def moe_ep_copy_rows(peers, peer_rows, seg_src_rank, seg_src_row, seg_dst_row, seg_rows, dst,
+                     err_word, stream=None):
+    """Row segments from other ranks' buffers into ``dst`` (device tensors: ``peers`` an
+    int64 tensor of device addresses, ``peer_rows`` int64, the segment arrays int32);
+    row size = dst's row size."""
+    R = peers.numel()
+    n_seg = seg_rows.numel()
+    row_bytes = dst.stride(0) * dst.element_size()
+    _check(_lib.moe_ep_copy_rows(_ptr(peers), _ptr(peer_rows), R, _ptr(seg_src_rank),
+                                 _ptr(seg_src_row), _ptr(seg_dst_row), _ptr(seg_rows), n_seg,
+                                 row_bytes, _ptr(dst), dst.shape[0], _ptr(err_word),
+                                 _stream(stream)), "moe_ep_copy_rows")
 
 
 def moe_get_error(ws, stream=None):

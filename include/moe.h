@@ -277,6 +277,70 @@ moe_status_t moe_route_dispatch_noalloc(const moe_bf16_t* x, const float* logits
  * The pages have no counterpart; it belongs to the no-allocation dispatch. */
 moe_status_t moe_route_dispatch_noalloc_get_error(cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Fine-grained expert parallelism across R GPUs: the exchange plan and the pull-based row
+ * copies (DeepSeek-V4 report, Thai translation, itsolotime.com, section 1.2 and Figure 5:
+ * each GPU's experts run in waves, wave i+1's rows are fetched and wave i-1's outputs
+ * combined while wave i computes; section 1.4, communication-primitive bullet: the transfers
+ * are pull-based reads of the other GPUs' memory; 10100.com reading, section on
+ * fine-grained EP overlap).  Rank r of R owns experts [moe_ep_first_expert(E, R, r),
+ * moe_ep_first_expert(E, R, r + 1)).  Each rank dispatches its own tokens
+ * (moe_route_dispatch), all ranks exchange their per-expert counts ([R][E] int32, e.g. by an
+ * all-gather), each rank pulls the rows of its experts from the other ranks into its receive
+ * buffer (moe_ep_plan, moe_ep_copy_rows), runs the expert GEMMs on them, and each rank then
+ * pulls its own rows' expert outputs back (moe_ep_return_plan, moe_ep_copy_rows) and
+ * combines them as on one GPU.  The rows of an expert arrive ordered by (source rank, source
+ * row), i.e. by global token when the global batch is the ranks' batches concatenated, so
+ * every result is bitwise the single-GPU layer's on that batch.
+ * ------------------------------------------------------------------------------------- */
+
+/* First expert owned by `rank` of R (experts split into R contiguous blocks of floor/ceil
+ * E/R); rank = R gives E.  -1 for invalid arguments. */
+int moe_ep_first_expert(int E, int R, int rank);
+
+/* Exchange plan of `rank` (host function, host memory; nothing is launched).
+ * counts_all [R][E]: rows that each rank's dispatch routed to each expert.  For local expert
+ * i (global expert first + i) and source rank s:
+ *   recv_off[i*R + s]  first row of those rows in this rank's receive buffer; each expert's
+ *                      rows start at a multiple of row_align (128 for the grouped GEMMs);
+ *                      recv_off[n_local*R] = the receive buffer's row count,
+ *   src_off[i*R + s]   first row of those rows in rank s's permuted buffer (the exclusive
+ *                      prefix of s's counts: moe_route_dispatch's offsets on rank s),
+ *   recv_counts[i]     rows of local expert i from all ranks,
+ *   wave_first[w]      first local expert of wave w (waves of wave_experts experts),
+ *                      wave_first[*n_waves] = n_local.
+ * Output sizes: recv_off n_local*R + 1, src_off n_local*R, recv_counts n_local, wave_first
+ * ceil(n_local / wave_experts) + 1 (n_local <= ceil(E / R)).  Errors: MOE_ERR_INVALID_ARG
+ * (null pointer, R < 1, R > E, rank out of range, a negative count), MOE_ERR_UNSUPPORTED
+ * (more than 2^31 - 1 rows). */
+moe_status_t moe_ep_plan(const int32_t* counts_all, int R, int E, int rank, int row_align,
+                         int wave_experts, int32_t* recv_off, int32_t* src_off,
+                         int32_t* recv_counts, int32_t* wave_first, int32_t* n_waves);
+
+/* Return plan of `rank` (host function, host memory): for every expert e of the layer,
+ * owner[e] = the rank that computes it, owner_row[e] = the first row, in the owner's
+ * receive-side buffers, of the rows this rank sent it, own_row[e] = the first of those rows
+ * in this rank's permuted buffer.  Sizes E each.  Errors as moe_ep_plan. */
+moe_status_t moe_ep_return_plan(const int32_t* counts_all, int R, int E, int rank,
+                                int row_align, int32_t* owner, int32_t* owner_row,
+                                int32_t* own_row);
+
+/* Row segments copied into `dst` from other ranks' buffers with plain 16-byte loads and
+ * stores (no TMA, no multicast): segment i copies seg_rows[i] rows starting at row
+ * seg_src_row[i] of the buffer peers[seg_src_rank[i]] to rows starting at seg_dst_row[i]
+ * of dst.  peers [R] and peer_rows [R] (rows each peer buffer holds) and the four segment
+ * arrays [n_seg] are DEVICE arrays; each peers[s] is a device pointer this GPU can read (its
+ * own memory, or a peer GPU's mapped by the caller).  row_bytes: a multiple of 16; dst holds
+ * dst_rows rows.  A segment outside its source or destination records
+ * MOE_ERR_DEVICE_BOUNDS in the 16-byte error word `err_word` (device memory, e.g. the start
+ * of a workspace, read with moe_get_error) and is skipped.  Asynchronous on `stream`; the
+ * caller orders it after the source rows are written on their GPUs. */
+moe_status_t moe_ep_copy_rows(const void* const* peers, const int64_t* peer_rows, int R,
+                              const int32_t* seg_src_rank, const int32_t* seg_src_row,
+                              const int32_t* seg_dst_row, const int32_t* seg_rows, int n_seg,
+                              int64_t row_bytes, void* dst, int64_t dst_rows, void* err_word,
+                              cudaStream_t stream);
+
 /* Synchronises `stream`, reads the device error word of `ws` and returns it (MOE_OK when
  * no device-side problem was recorded since the last moe_route_dispatch / moe_forward on
  * this ws, which clear it).  Returns MOE_ERR_CUDA if the stream reports an error. */
