@@ -172,12 +172,19 @@ def _forward_swap(T, k, d, dff):
     return mode == "1" or T <= 128 or _row_pairs(T, k, d, dff)
 
 
+def _forward_fused(T, k, d, dff):
+    # both swapped GEMMs in one launch: the library's rule (MOE_FWD_FUSED "1" always, "0"
+    # never, else T <= 64)
+    mode = os.environ.get("MOE_FWD_FUSED", "")
+    return _forward_swap(T, k, d, dff) and mode != "0" and (mode == "1" or T <= 64)
+
+
 def fwd_launches(T, k, d, dff):
     # routing, column scan, offsets/tile tables, scatter, padding rows, GEMM1, GEMM2, combine;
     # with row-tile CTA pairs each GEMM is a pair launch plus a single-CTA launch for the
     # other tiles (the swapped kernels take every tile in one pair launch)
     if _forward_swap(T, k, d, dff):
-        return 8
+        return 7 if _forward_fused(T, k, d, dff) else 8
     return 10 if _row_pairs(T, k, d, dff) else 8
 
 
@@ -500,7 +507,11 @@ def bench_native(args, w):
             "weights_gbs": float(active.sum() * w_bytes / (gemm_ms * 1e-3) / 1e9)}
     roof["gemm_frac_of_per_expert_sum"] = roof["per_expert_sum_ms"] / gemm_ms
     roof["gemm_frac_of_overlapped"] = roof["overlapped_ms"] / gemm_ms
-    g1_tflops = alg["gemm1_flops"] / (stages["gemm1_swiglu"] * 1e-3) / 1e12
+    fused = _forward_fused(T, k, d, dff)
+    # the dominant kernel: GEMM1 + SwiGLU, or both GEMMs when they run as one launch (its
+    # stage then spans both and the GEMM2 stage is empty)
+    g1_flops = alg["gemm_flops"] if fused else alg["gemm1_flops"]
+    g1_tflops = g1_flops / (stages["gemm1_swiglu"] * 1e-3) / 1e12
     g_tflops = alg["gemm_flops"] / ((stages["gemm1_swiglu"] + stages["gemm2"]) * 1e-3) / 1e12
     disp_gbs = alg["dispatch_bytes"] / (stages["dispatch"] * 1e-3) / 1e9
     comb_gbs = alg["combine_bytes"] / (stages["combine"] * 1e-3) / 1e9
@@ -513,7 +524,8 @@ def bench_native(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": _workload_config(w),
         "e2e": e2e,
-        "roofline": {"kernel": "grouped GEMM1 + SwiGLU (tcgen05)", "bound": "tensor",
+        "roofline": {"kernel": ("grouped GEMM1 + SwiGLU + GEMM2, one tcgen05 launch" if fused
+                                else "grouped GEMM1 + SwiGLU (tcgen05)"), "bound": "tensor",
                      "achieved": g1_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": g1_tflops / peak,
                      "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peaks["source"],
@@ -553,6 +565,30 @@ def bench_native(args, w):
     return 0
 
 
+def probe_dram():
+    """Per-SM DRAM read rate against the number of streaming SMs (moe_probe_dram_read): one
+    JSON line per (path, SMs)."""
+    import combine_fp32_router_gb300 as moe
+    buf = torch.empty(6 << 30, dtype=torch.uint8, device="cuda")
+    buf.fill_(1)
+    out = torch.zeros(1024, dtype=torch.int32, device="cuda")
+    per_cta = (buf.numel() // 152) // 16384 * 16384
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for ctas in (4, 8, 16, 38, 76, 152):
+        for mode, name in ((0, "loads, 32 KB in flight"), (1, "bulk copies, 6 x 16 KB"),
+                           (2, "bulk copies, 12 x 16 KB")):
+            moe.moe_probe_dram_read(buf, ctas, mode, out)
+            a.record()
+            moe.moe_probe_dram_read(buf, ctas, mode, out)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            print(json.dumps({"path": name, "sms": ctas, "total_gbs": ctas * per_cta / ms / 1e6,
+                              "per_sm_gbs": per_cta / ms / 1e6,
+                              "timed_out": int(out[:ctas].sum().item())}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -569,7 +605,11 @@ def main():
                     help="T,d,E,k,d_ff of the forward + backward timing (profiling captures)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the forward + backward timing of the fwd_bwd workload")
+    ap.add_argument("--probe-dram", action="store_true",
+                    help="print the per-SM DRAM read rate by load path and SM count, then exit")
     args = ap.parse_args()
+    if args.probe_dram:
+        return probe_dram()
     if args.warmup < 3:
         args.warmup = 3
     if args.shape:

@@ -39,8 +39,8 @@ EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispat
            "moe_backward",
            "moe_route_dispatch_noalloc", "moe_route_dispatch_noalloc_get_error",
            "moe_ep_first_expert", "moe_ep_plan", "moe_ep_return_plan", "moe_ep_copy_rows",
-           "moe_get_error", "moe_set_wait_timeout_ns", "moe_debug_set_flags",
-           "moe_status_string")
+           "moe_probe_dram_read", "moe_get_error", "moe_set_wait_timeout_ns",
+           "moe_debug_set_flags", "moe_status_string")
 
 
 class MoeError(RuntimeError):
@@ -94,6 +94,8 @@ def _load():
     lib.moe_ep_return_plan.restype = i
     lib.moe_ep_copy_rows.argtypes = [p, p, i, p, p, p, p, i, i64, p, i64, p, p]
     lib.moe_ep_copy_rows.restype = i
+    lib.moe_probe_dram_read.argtypes = [p, sz, i, i, p, p]
+    lib.moe_probe_dram_read.restype = i
     lib.moe_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.moe_set_wait_timeout_ns.restype = None
     lib.moe_debug_set_flags.argtypes = [i]
@@ -346,6 +348,12 @@ def moe_ep_copy_rows(peers, peer_rows, seg_src_rank, seg_src_row, seg_dst_row, s
                                  _ptr(seg_src_row), _ptr(seg_dst_row), _ptr(seg_rows), n_seg,
                                  row_bytes, _ptr(dst), dst.shape[0], _ptr(err_word),
                                  _stream(stream)), "moe_ep_copy_rows")
+
+
+def moe_probe_dram_read(buf, ctas, mode, out, stream=None):
+    """Launch the per-SM DRAM read probe over ``buf`` (see include/moe.h)."""
+    _check(_lib.moe_probe_dram_read(_ptr(buf), _nbytes(buf), int(ctas), int(mode), _ptr(out),
+                                    _stream(stream)), "moe_probe_dram_read")
 
 
 def moe_get_error(ws, stream=None):

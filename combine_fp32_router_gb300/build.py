@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 
-SOURCES = ["route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "moe_api.cu", "route_noalloc.cu", "ep.cu"]
+SOURCES = ["route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "moe_api.cu", "route_noalloc.cu", "ep.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

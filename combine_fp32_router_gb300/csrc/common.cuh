@@ -133,6 +133,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------------------- counters
+// Device-scope release add (an arrival that publishes the thread's and, through a preceding
+// barrier and fence, its CTA's earlier stores).
+__device__ __forceinline__ void red_release_add(int32_t* p, int32_t v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait until *p >= target (acquire); on a timeout records MOE_ERR_TIMEOUT with `site`
+// and raises the abort flag (when given).  Returns true on success.
+__device__ __forceinline__ bool wait_count(const int32_t* p, int32_t target,
+                                           volatile int* abort_flag, DevErr* err, int site,
+                                           uint64_t limit_ns) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    __nanosleep(128);
+    if (ld_acquire(p) >= target) return true;
+    if (abort_flag && *abort_flag) return false;
+    if (global_ns() - t0 > limit_ns) {
+      if (abort_flag) *abort_flag = 1;
+      set_error(err, MOE_ERR_TIMEOUT, site);
+      return false;
+    }
+  }
+}
+// generic-proxy accesses to global memory are ordered before this thread's later async-proxy
+// (TMA) accesses
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

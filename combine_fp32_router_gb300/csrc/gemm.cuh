@@ -52,12 +52,17 @@ enum GemmKind : int {
   // costs few MMAs; heavy and light experts then share one persistent CTA-pair launch.
   kFwd1T = 7,   // H^T = [W1|W3]^T Xp^T -> SwiGLU -> H                      (dff x rows)
   kFwd2T = 8,   // Y^T = W2^T H^T (fp32 rows)                                (d x rows)
+  // Both swapped GEMMs in one persistent launch: every GEMM1 tile first, then every GEMM2
+  // tile; a GEMM2 tile of a row block starts loading H only when all GEMM1 tiles of that
+  // block have stored theirs (a per-block counter), so GEMM2 of the first blocks runs while
+  // GEMM1 of the last ones still computes, and one launch's ramp and tail serve both.
+  kFwdT = 9,
 };
 
 template <int KIND>
 struct KindTraits {
   static constexpr bool kRowsM = (KIND <= kDx || KIND == kFwd1F8);  // M = permuted rows
-  static constexpr bool kSwap = (KIND == kFwd1T || KIND == kFwd2T);  // N = permuted rows
+  static constexpr bool kSwap = (KIND == kFwd1T || KIND == kFwd2T || KIND == kFwdT);  // N = rows
   static constexpr int kAmn = (KIND == kDw2 || KIND == kDw13 || kSwap) ? 1 : 0;  // A MN-major?
   static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8 || kSwap) ? 0 : 1;
 };
@@ -125,6 +130,12 @@ struct GemmParams {
   const int32_t* st_expert;
   const int32_t* st_row0;
   CUtensorMap mapR[4];
+  // both GEMMs in one launch (kFwdT): GEMM2's column blocks and K blocks, the row maps of H
+  // (GEMM2's N operand), and the per-row-block count of GEMM1 tile halves (one per CTA of a
+  // pair) whose H rows are stored
+  int nb2, nkb2;
+  CUtensorMap mapR2[4];
+  int32_t* done1;
 };
 
 constexpr int kBM = 128;
@@ -171,6 +182,8 @@ struct TileInfo {
               // with PAIR the second half of an expert's last tile can lie past the segment,
               // on the next expert's rows, and must not be written
   int box;    // swapped kinds: rows of the block each CTA loads (16, 32, 64 or 128); N = 2 box
+  int part;   // swapped kinds: 1 = GEMM1 (+ SwiGLU) tile, 2 = GEMM2 tile
+  int st;     // swapped kinds: index of the row block in the block table
   bool bad;   // tile tables out of range: every role skips the tile
 };
 
@@ -203,8 +216,20 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, i
     // a block of up to 256 rows of one expert x one block of weight columns: 128 h columns
     // (64 per CTA, each with its W1 and W3 column) for GEMM1, 256 without the gate
     // projection or for GEMM2 (128 per CTA)
-    const int st = tile / p.nb;
-    ti.n0 = (tile % p.nb) * ((KIND == kFwd1T && p.gated) ? 128 : 256);
+    int part = KIND == kFwd2T ? 2 : 1, t = tile, nbp = p.nb, nk = p.nkb;
+    if constexpr (KIND == kFwdT) {
+      const int n1 = p.n_st[0] * p.nb;  // GEMM1 tiles come first
+      if (tile >= n1) {
+        part = 2;
+        t = tile - n1;
+        nbp = p.nb2;
+        nk = p.nkb2;
+      }
+    }
+    const int st = t / nbp;
+    ti.part = part;
+    ti.st = st;
+    ti.n0 = (t % nbp) * ((part == 1 && p.gated) ? 128 : 256);
     ti.e = p.st_expert[st];
     ti.row0 = p.st_row0[st];
     ti.bad = ti.e < 0 || ti.e >= p.E || ti.row0 < 0 || ti.row0 >= p.rows_cap;
@@ -221,7 +246,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, i
     const int half = (ti.nvalid + 1) / 2;
     ti.box = half <= 16 ? 16 : (half <= 32 ? 32 : (half <= 64 ? 64 : 128));
     ti.m0 = 0;
-    ti.nk = p.nkb;
+    ti.nk = nk;
     ti.mvalid = kBM;
   } else {
     const int per_e = p.mb * p.nb;
@@ -629,7 +654,7 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
                                               const float* partner, int rank) {
   const int nch = (ti.nvalid + 31) / 32;
   const int64_t row0 = ti.row0;
-  if constexpr (KIND == kFwd1T) {
+  if (ti.part == 1) {
     uint16_t* H = static_cast<uint16_t*>(p.out0);
     if (p.gated) {
       const bool is_a = q < 2;
@@ -698,7 +723,7 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
   } else {
     const int col = ti.n0 + 128 * rank + 32 * q + lane;
     const bool live = ti.n0 + 128 * rank < p.d;  // warp-uniform: d is a multiple of 128
-    float* Y = static_cast<float*>(p.out0);
+    float* Y = static_cast<float*>(KIND == kFwdT ? p.out1 : p.out0);
 #pragma unroll 1
     for (int ch = 0; ch < nch; ++ch) {
       float v[32];
@@ -804,7 +829,8 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
 
   int64_t ntiles64;
   if constexpr (Tr::kRowsM) ntiles64 = static_cast<int64_t>(PAIR ? p.n_pt[0] : p.n_mt[0]) * p.nb;
-  else if constexpr (Tr::kSwap) ntiles64 = static_cast<int64_t>(p.n_st[0]) * p.nb;
+  else if constexpr (Tr::kSwap)
+    ntiles64 = static_cast<int64_t>(p.n_st[0]) * (KIND == kFwdT ? p.nb + p.nb2 : p.nb);
   else ntiles64 = static_cast<int64_t>(p.E) * p.mb * p.nb;
   if (ntiles64 > p.max_tiles || ntiles64 < 0) {
     if (threadIdx.x == 0) set_error(p.err, MOE_ERR_DEVICE_BOUNDS, 10);
@@ -882,7 +908,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
         if constexpr (Tr::kSwap) {
           // A: this CTA's 128 weight columns as two 64-column boxes (MN-major); B: this CTA's
           // `box` rows of the block (K-major), by the tensor map of that box height
-          if constexpr (KIND == kFwd1T) {
+          if (ti.part == 1) {
             const int wrow = ti.e * p.d + k0;
             if (p.gated) {
               const int c0 = ti.n0 + 64 * rank;  // W1 columns -> lanes 0-63, W3 -> 64-127
@@ -896,11 +922,13 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
           } else {
             const int wrow = ti.e * p.dff + k0;
             const int c0 = ti.n0 + 128 * rank;  // past d (d % 256 == 128): zero fill
-            load_h(kL2HintB, sa, &mapB0, fb, c0, wrow);
-            load_h(kL2HintB, sa + 8192u, &mapB0, fb, c0 + 64, wrow);
+            const CUtensorMap* w2 = KIND == kFwdT ? &mapA : &mapB0;
+            load_h(kL2HintB, sa, w2, fb, c0, wrow);
+            load_h(kL2HintB, sa + 8192u, w2, fb, c0 + 64, wrow);
           }
           const int bi = ti.box == 16 ? 0 : (ti.box == 32 ? 1 : (ti.box == 64 ? 2 : 3));
-          load_h(kL2HintA, sb, &p.mapR[bi], fb, k0, ti.row0 + rank * ti.box);
+          const CUtensorMap* rows = (KIND == kFwdT && ti.part == 2) ? &p.mapR2[bi] : &p.mapR[bi];
+          load_h(kL2HintA, sb, rows, fb, k0, ti.row0 + rank * ti.box);
         } else if constexpr (KIND == kFwd1) {
           if (!p.gather_x) load_h(kL2HintA, sa, &mapA, fb, k0, ti.row0);
           const int wrow = ti.e * p.d + k0;
@@ -990,7 +1018,19 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
           ++fill;
         }
       } else if (lane == 0) {
-        for (int kb = 0; kb < ti.nk; ++kb) {
+        if constexpr (KIND == kFwdT) {
+          // a GEMM2 tile reads H rows that GEMM1 tiles of its block store: wait for all of
+          // them (each CTA of a pair counts once), then order those generic-proxy stores
+          // before this thread's async-proxy (TMA) loads
+          if (ti.part == 2) {
+            if (!wait_count(p.done1 + ti.st, 2 * p.nb, abort_flag, p.err, 9, p.wait_ns)) {
+              ok = false;
+            } else {
+              fence_proxy_async_global();
+            }
+          }
+        }
+        for (int kb = 0; kb < ti.nk && ok; ++kb) {
           const int s = fill % S;
           const uint32_t ph = (fill / S) & 1u;
           if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, 1)) {
@@ -1096,16 +1136,27 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
       if (ti.bad) continue;
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1u;
-      // warp-uniform decision: the tcgen05.ld below is .sync.aligned; the warps of the
-      // swapped GEMM1 that exchange chunks (q, q + 2) decide together
+      // warp-uniform decision: the tcgen05.ld below is .sync.aligned.  In the swapped kinds
+      // all epilogue warps decide together (an AND over a named barrier), because they meet
+      // at named barriers inside a tile (the chunk exchange of GEMM1, GEMM1's completion
+      // count) and a warp that left could leave the others waiting there
       bool ok = __all_sync(0xFFFFFFFFu, wait_bar(tfull_bar(acc), aph, abort_flag, 5));
-      if (KIND == kFwd1T && p.gated) ok = named_bar_and(1 + (q & 1), 64, ok);
+      if constexpr (Tr::kSwap) ok = named_bar_and(4, 32 * EW, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if constexpr (Tr::kSwap) {
         epilogue_swap<KIND>(p, ti, tacc, q, lane, epi_buf + ew * (Cfg::kEpiWarpBytes / 4),
                             epi_buf + (ew ^ 2) * (Cfg::kEpiWarpBytes / 4), rank);
+        if constexpr (KIND == kFwdT) {
+          if (ti.part == 1) {
+            // this CTA's H rows of the tile are stored: count them for the block's GEMM2
+            // tiles (every epilogue thread's stores are made visible device-wide first)
+            __threadfence();
+            named_bar_sync(3, 32 * EW);
+            if (ew == 0 && lane == 0) red_release_add(p.done1 + ti.st, 1);
+          }
+        }
       } else {
         epilogue_tile<KIND, BN>(p, ti, tacc, q, lane,
                                 epi_buf + ew * (Cfg::kEpiWarpBytes / 4),

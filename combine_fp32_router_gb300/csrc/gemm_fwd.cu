@@ -263,4 +263,33 @@ cudaError_t launch_gemm_fwd2_swap(const GemmCtx& c, cudaStream_t s) {
   return run_grouped_gemm<kFwd2T, 256, true>(w2, w2, w2, p, L.max_mt * p.nb, c.num_sms, s);
 }
 
+cudaError_t launch_gemm_fwd_fused(const GemmCtx& c, cudaStream_t s) {
+  const WsLayout& L = *c.L;
+  cudaError_t st = cudaSuccess;
+  // M operands: W1 / W3 viewed as [E d rows][dff], W2 as [E dff rows][d] (64-column boxes)
+  const CUtensorMap w1 = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 64, &st);
+  const CUtensorMap w3 = make_map_2d(c.gated ? c.W3 : c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d,
+                                     2ull * L.dff, 64, 64, &st);
+  const CUtensorMap w2 = make_map_2d(c.W2, L.d, static_cast<uint64_t>(L.E) * L.dff, 2ull * L.d, 64, 64, &st);
+  if (st != cudaSuccess) return st;
+  GemmParams p = swap_params(c);
+  st = row_maps(p, c.ws + L.xperm, L.d, L.P_pad, 2ull * L.d);
+  if (st != cudaSuccess) return st;
+  for (int i = 0; i < 4; ++i)
+    p.mapR2[i] = make_map_2d(c.ws + L.H, L.dff, L.P_pad, 2ull * L.dff, 64, 16u << i, &st);
+  if (st != cudaSuccess) return st;
+  p.nb = c.gated ? L.dff / 128 : L.dff / 256;
+  p.nkb = L.d / kBK;
+  p.nb2 = (L.d + 255) / 256;
+  p.nkb2 = L.dff / kBK;
+  p.out0 = c.ws + L.H;
+  p.out1 = c.ws + L.Y;
+  p.done1 = reinterpret_cast<int32_t*>(c.ws + L.done1);
+  p.save_ab = c.save_ab;
+  p.save_a = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Asave) : nullptr;
+  p.save_b = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Bsave) : nullptr;
+  return run_grouped_gemm<kFwdT, 256, true>(w2, w1, w3, p, L.max_mt * (p.nb + p.nb2), c.num_sms,
+                                            s);
+}
+
 }  // namespace moe

@@ -23,7 +23,8 @@ struct WsLayout {
   int d = 0, E = 0, k = 0, dff = 0;
   size_t err = 0, hist = 0, bbase = 0, counts = 0, offsets = 0, poff = 0, n_mt = 0,
          mt_expert = 0, mt_row0 = 0, n_pt = 0, pt_expert = 0, pt_row0 = 0, n_lo = 0,
-         lo_expert = 0, lo_row0 = 0, n_st = 0, st_expert = 0, st_row0 = 0, topk = 0, gate = 0,
+         lo_expert = 0, lo_row0 = 0, n_st = 0, st_expert = 0, st_row0 = 0, done1 = 0, topk = 0,
+         gate = 0,
          pos = 0, perm = 0, xperm = 0, H = 0, Y = 0, Asave = 0, Bsave = 0, dO = 0, dAB = 0,
          dXp = 0, seg = 0, xscale = 0;
   size_t route_total = 0, fwd_total = 0, bwd_total = 0;
@@ -53,6 +54,7 @@ cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* 
 struct TileTables {
   int32_t *n_mt, *mt_expert, *mt_row0, *n_pt, *pt_expert, *pt_row0, *n_lo, *lo_expert, *lo_row0;
   int32_t *n_st, *st_expert, *st_row0;
+  int32_t* done1;  // per 256-row block: GEMM1 halves stored (both GEMMs in one launch); zeroed
   int64_t max_mt;
 };
 // The tile tables of a workspace laid out by L.
@@ -112,6 +114,8 @@ cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s);   // Y = H W2
 // the same two GEMMs with swapped operands (weight columns x row blocks), CTA pairs
 cudaError_t launch_gemm_fwd1_swap(const GemmCtx& c, cudaStream_t s);
 cudaError_t launch_gemm_fwd2_swap(const GemmCtx& c, cudaStream_t s);
+// both swapped GEMMs in one persistent CTA-pair launch (GEMM2 of a block after its GEMM1)
+cudaError_t launch_gemm_fwd_fused(const GemmCtx& c, cudaStream_t s);
 cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s);     // dA,dB from dO W2^T
 cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s);     // dXp = dA W1^T + dB W3^T
 cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s);    // dW2 = H^T dO

@@ -65,6 +65,21 @@ bool forward_swap(int64_t T, int k, int d, int dff) {
   return mode == 1 || T <= kTileRows || row_pairs(T, k, d, dff);
 }
 
+// The swapped GEMMs as one persistent launch (GEMM2 of a row block after its GEMM1 tiles) for
+// T <= 64, where one launch's ramp and tail matter (measured on GB300: tiny 0.037 -> 0.034 ms,
+// T=1 at d=7168, E=256, top-8, d_ff=2048 0.158 -> 0.154 ms; T=8 and larger layers within
+// noise or slower, e.g. the T=16384 layer 9.67 -> 9.88 ms).  MOE_FWD_FUSED "1" forces it,
+// "0" turns it off; read once per process.  Bitwise the same rows as two launches.
+bool forward_fused(int64_t T) {
+  static const int mode = [] {
+    const char* e = std::getenv("MOE_FWD_FUSED");
+    if (e && e[0] == '0' && e[1] == 0) return 0;
+    if (e && e[0] == '1' && e[1] == 0) return 1;
+    return 2;
+  }();
+  return mode == 1 || (mode == 2 && T <= 64);
+}
+
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // moe_forward_host's staging at the end of the workspace: x, logits, out (256-byte aligned)
@@ -157,6 +172,7 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   L.n_st = take(16);  // 256-row blocks: never more than the 128-row tiles
   L.st_expert = take(static_cast<size_t>(L.max_mt) * 4);
   L.st_row0 = take(static_cast<size_t>(L.max_mt) * 4);
+  L.done1 = take(static_cast<size_t>(L.max_mt) * 4);
   L.topk = take(P * 4);
   L.gate = take(P * 4);
   L.pos = take(P * 4);
@@ -190,6 +206,7 @@ TileTables tile_tables(const WsLayout& L, char* w) {
   tt.n_st = reinterpret_cast<int32_t*>(w + L.n_st);
   tt.st_expert = reinterpret_cast<int32_t*>(w + L.st_expert);
   tt.st_row0 = reinterpret_cast<int32_t*>(w + L.st_row0);
+  tt.done1 = reinterpret_cast<int32_t*>(w + L.done1);
   tt.max_mt = L.max_mt;
   return tt;
 }
@@ -352,6 +369,16 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   // the plain forward runs both GEMMs with swapped operands on CTA pairs; the row-gather and
   // fused-combine variants keep the row-tile kernels
   c.swap = forward_swap(T, k, d, d_ff) && !gather && !c.fuse_combine;
+  if (c.swap && forward_fused(T)) {
+    // both GEMMs in one launch: the GEMM1 and GEMM2 stage events bracket it together
+    MOE_TRY(launch_gemm_fwd_fused(c, stream));
+    record(stage_events, 2, stream);
+    record(stage_events, 3, stream);
+    MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,
+                           stream));
+    record(stage_events, 4, stream);
+    return MOE_OK;
+  }
   MOE_TRY(c.swap ? launch_gemm_fwd1_swap(c, stream) : launch_gemm_fwd1(c, stream));
   record(stage_events, 2, stream);
   if (c.fuse_combine) {

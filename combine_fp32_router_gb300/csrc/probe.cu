@@ -1,0 +1,108 @@
+// Measurement probe: the DRAM read rate one SM sustains, by load path, for sizing the expert
+// GEMMs' schedule (how much weight streaming a CTA can do while others compute).  One CTA per
+// requested SM streams its own slice of a buffer much larger than L2:
+//   mode 0: 512 threads, four 16-byte loads in flight per thread (32 KB per SM);
+//   mode 1 / 2: one thread issues 16 KB bulk copies (cp.async.bulk) into 6 / 12 shared-memory
+//   stages, each completing on an mbarrier (96 / 192 KB in flight per SM).
+// Not part of the layer's path.
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(512) probe_ldg_kernel(const uint4* __restrict__ src,
+                                                        int64_t per_cta16, uint32_t* out) {
+  const uint4* p = src + blockIdx.x * per_cta16;
+  uint32_t acc = 0;
+  for (int64_t i = threadIdx.x; i < per_cta16; i += 4 * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t j = i + u * blockDim.x;
+      v[u] = j < per_cta16 ? ld_nc_v4(p + j) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  if (acc == 0x9E3779B9u) out[blockIdx.x] = acc;  // keeps the loads; practically never true
+}
+
+// bounded wait on an mbarrier phase (no error word: the probe reports through `out`)
+__device__ __forceinline__ bool probe_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+template <int S>
+__global__ void __launch_bounds__(32) probe_bulk_kernel(const char* __restrict__ src,
+                                                        int64_t per_cta, uint64_t wait_ns,
+                                                        uint32_t* out) {
+  constexpr uint32_t kChunk = 16384;
+  extern __shared__ __align__(1024) uint8_t stages[];
+  __shared__ __align__(8) uint64_t bar[S];
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bar[s]), 1);
+  fence_mbar_init();
+  const char* p = src + blockIdx.x * per_cta;
+  const int64_t n = per_cta / kChunk;
+  int64_t issued = 0, done = 0;
+  while (done < n) {
+    while (issued < n && issued - done < S) {
+      const int s = static_cast<int>(issued % S);
+      const uint32_t b = smem_u32(&bar[s]);
+      mbar_arrive_expect_tx(b, kChunk);
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+          ::"r"(smem_u32(stages + static_cast<size_t>(s) * kChunk)), "l"(p + issued * kChunk),
+          "r"(kChunk), "r"(b)
+          : "memory");
+      ++issued;
+    }
+    const int s = static_cast<int>(done % S);
+    // bounded wait; on a timeout the copies still in flight are waited for (bounded too)
+    if (!probe_wait(smem_u32(&bar[s]), static_cast<uint32_t>((done / S) & 1), wait_ns)) {
+      out[blockIdx.x] = 1u;
+      for (int64_t f = done + 1; f < issued; ++f)
+        probe_wait(smem_u32(&bar[f % S]), static_cast<uint32_t>((f / S) & 1), wait_ns);
+      return;
+    }
+    ++done;
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_probe_dram_read(const void* buf, size_t bytes, int ctas, int mode,
+                                            uint32_t* out, cudaStream_t stream) {
+  if (!buf || !out || ctas < 1 || ctas > 1024 || mode < 0 || mode > 2)
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(buf) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  // the same slice per CTA whatever the count, so rates compare across counts
+  const int64_t per_cta = static_cast<int64_t>(bytes / 152) / 16384 * 16384;
+  if (per_cta < 16384 || static_cast<size_t>(per_cta) * ctas > bytes) return MOE_ERR_INVALID_ARG;
+  cudaError_t e;
+  if (mode == 0) {
+    probe_ldg_kernel<<<ctas, 512, 0, stream>>>(static_cast<const uint4*>(buf), per_cta / 16,
+                                                out);
+    e = cudaGetLastError();
+  } else {
+    const int S = mode == 1 ? 6 : 12;
+    const size_t smem = static_cast<size_t>(S) * 16384;
+    auto k = mode == 1 ? probe_bulk_kernel<6> : probe_bulk_kernel<12>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e == cudaSuccess) {
+      k<<<ctas, 32, smem, stream>>>(static_cast<const char*>(buf), per_cta, 2000000000ull, out);
+      e = cudaGetLastError();
+    }
+  }
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

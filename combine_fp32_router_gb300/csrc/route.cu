@@ -349,6 +349,8 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
   fill_tile_table(s_a, s_b, s_poff, E, H, L, kTileRows, tt.mt_expert, tt.mt_row0);
   fill_tile_table(s_pa, s_pb, s_poff, E, PH, PL, 2 * kTileRows, tt.pt_expert, tt.pt_row0);
   fill_tile_table(s_sa, s_sb, s_poff, E, SH, SL, 2 * kTileRows, tt.st_expert, tt.st_row0);
+  if (tt.done1)
+    for (int i = threadIdx.x; i < SH + SL; i += blockDim.x) tt.done1[i] = 0;
 }
 
 // Stable permute.  One warp per token: lanes j < k turn the CTA-local rank into the final

@@ -341,6 +341,16 @@ moe_status_t moe_ep_copy_rows(const void* const* peers, const int64_t* peer_rows
                               int64_t row_bytes, void* dst, int64_t dst_rows, void* err_word,
                               cudaStream_t stream);
 
+/* Measurement probe (not part of the layer; the pages have no counterpart): the DRAM read
+ * rate one SM sustains by load path.  Launches `ctas` CTAs (one per SM when ctas <= the SM
+ * count), each streaming its own slice of floor(bytes / 152) bytes (rounded down to 16 KB)
+ * of `buf` (device memory, 16-byte aligned, much larger than L2): mode 0 with 16-byte loads
+ * by 512 threads, mode 1 / 2 with 16 KB bulk copies into 6 / 12 shared-memory stages.  The
+ * caller times the launch (events on `stream`); `out` (device, ctas uint32) receives 1 for a
+ * CTA whose bounded wait ran out.  MOE_ERR_INVALID_ARG when the slices do not fit in buf. */
+moe_status_t moe_probe_dram_read(const void* buf, size_t bytes, int ctas, int mode,
+                                 uint32_t* out, cudaStream_t stream);
+
 /* Synchronises `stream`, reads the device error word of `ws` and returns it (MOE_OK when
  * no device-side problem was recorded since the last moe_route_dispatch / moe_forward on
  * this ws, which clear it).  Returns MOE_ERR_CUDA if the stream reports an error. */

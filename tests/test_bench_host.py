@@ -63,5 +63,7 @@ def test_pair_rule_and_launch_counts(bench, monkeypatch, mode, name, pairs):
     assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)
     monkeypatch.delenv("MOE_FWD_SWAP")
     assert bench._forward_swap(w.T, w.k, w.d, w.dff) == (mode != "0" and (pairs or w.T <= 128))
-    assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == 8
+    # T <= 64: both swapped GEMMs in one launch
+    fused = mode != "0" and w.T <= 64
+    assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == (7 if fused else 8)
     assert bench.bwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)
