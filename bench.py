@@ -576,15 +576,24 @@ def probe_dram():
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for ctas in (4, 8, 16, 38, 76, 152):
         for mode, name in ((0, "loads, 32 KB in flight"), (1, "bulk copies, 6 x 16 KB"),
-                           (2, "bulk copies, 12 x 16 KB")):
+                           (2, "bulk copies, 12 x 16 KB"),
+                           (3, "64x64 boxes, rows 4 KB apart, 6 x 16 KB"),
+                           (4, "64x64 boxes, contiguous rows, 6 x 16 KB")):
             moe.moe_probe_dram_read(buf, ctas, mode, out)
             a.record()
             moe.moe_probe_dram_read(buf, ctas, mode, out)
             b.record()
             torch.cuda.synchronize()
             ms = a.elapsed_time(b)
-            print(json.dumps({"path": name, "sms": ctas, "total_gbs": ctas * per_cta / ms / 1e6,
-                              "per_sm_gbs": per_cta / ms / 1e6,
+            if mode < 3:
+                nbytes = per_cta
+            else:  # 256 bytes of each of the CTA's rows (the probe's split of the matrix)
+                cols = 2048 if mode == 3 else 128
+                nblk = cols // 128
+                rows = buf.numel() // (cols * 2)
+                nbytes = rows // ((152 + nblk - 1) // nblk) // 64 * 64 * 256
+            print(json.dumps({"path": name, "sms": ctas, "total_gbs": ctas * nbytes / ms / 1e6,
+                              "per_sm_gbs": nbytes / ms / 1e6,
                               "timed_out": int(out[:ctas].sum().item())}), flush=True)
     return 0
 

@@ -3,8 +3,13 @@
 // requested SM streams its own slice of a buffer much larger than L2:
 //   mode 0: 512 threads, four 16-byte loads in flight per thread (32 KB per SM);
 //   mode 1 / 2: one thread issues 16 KB bulk copies (cp.async.bulk) into 6 / 12 shared-memory
-//   stages, each completing on an mbarrier (96 / 192 KB in flight per SM).
+//   stages, each completing on an mbarrier (96 / 192 KB in flight per SM);
+//   mode 3 / 4: 2-D tensor-map loads of two 64 x 64 bf16 boxes per stage, as the expert GEMMs
+//   load a weight column block, from a matrix with 4 KB rows (a weight matrix's pattern) or
+//   with 256-byte rows (the same boxes over contiguous memory), 6 stages (96 KB in flight).
 // Not part of the layer's path.
+#include <cuda.h>
+
 #include <cstdint>
 
 #include "common.cuh"
@@ -75,20 +80,88 @@ __global__ void __launch_bounds__(32) probe_bulk_kernel(const char* __restrict__
   }
 }
 
+// 2-D tensor-map loads as the expert GEMMs issue them: per stage, two 64 x 64 bf16 boxes side
+// by side (128 columns) of consecutive rows; 6 stages.  The map's row pitch decides the DRAM
+// pattern: a weight matrix's 4 KB (128 bytes per box row, rows 4 KB apart) or 256 bytes
+// (the same boxes over contiguous memory).  CTA i takes column block i % nblk and its own
+// rows.
+__global__ void __launch_bounds__(32) probe_box_kernel(const __grid_constant__ CUtensorMap map,
+                                                       int nblk, int64_t rows_per_cta,
+                                                       uint64_t wait_ns, uint32_t* out) {
+  constexpr int S = 6;
+  constexpr uint32_t kStage = 16384;
+  extern __shared__ __align__(1024) uint8_t stages[];
+  __shared__ __align__(8) uint64_t bar[S];
+  if (threadIdx.x != 0) return;
+  const uint32_t base = (smem_u32(stages) + 1023u) & ~1023u;
+  for (int s = 0; s < S; ++s) mbar_init(smem_u32(&bar[s]), 1);
+  fence_mbar_init();
+  const int c0 = (blockIdx.x % nblk) * 128;
+  const int64_t r0 = (blockIdx.x / nblk) * rows_per_cta;
+  const int64_t n = rows_per_cta / 64;
+  int64_t issued = 0, done = 0;
+  while (done < n) {
+    while (issued < n && issued - done < S) {
+      const int s = static_cast<int>(issued % S);
+      const uint32_t b = smem_u32(&bar[s]);
+      mbar_arrive_expect_tx(b, kStage);
+      const int y = static_cast<int>(r0 + issued * 64);
+      tma_load_2d(base + s * kStage, &map, b, c0, y);
+      tma_load_2d(base + s * kStage + 8192u, &map, b, c0 + 64, y);
+      ++issued;
+    }
+    const int s = static_cast<int>(done % S);
+    if (!probe_wait(smem_u32(&bar[s]), static_cast<uint32_t>((done / S) & 1), wait_ns)) {
+      out[blockIdx.x] = 1u;
+      for (int64_t f = done + 1; f < issued; ++f)
+        probe_wait(smem_u32(&bar[f % S]), static_cast<uint32_t>((f / S) & 1), wait_ns);
+      return;
+    }
+    ++done;
+  }
+}
+
 }  // namespace
+
+CUtensorMap make_map_2d(const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_rows, cudaError_t* st);
+
 }  // namespace moe
 
 using namespace moe;
 
 extern "C" moe_status_t moe_probe_dram_read(const void* buf, size_t bytes, int ctas, int mode,
                                             uint32_t* out, cudaStream_t stream) {
-  if (!buf || !out || ctas < 1 || ctas > 1024 || mode < 0 || mode > 2)
+  if (!buf || !out || ctas < 1 || ctas > 1024 || mode < 0 || mode > 4)
     return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(buf) & 15u) != 0) return MOE_ERR_INVALID_ARG;
   // the same slice per CTA whatever the count, so rates compare across counts
   const int64_t per_cta = static_cast<int64_t>(bytes / 152) / 16384 * 16384;
   if (per_cta < 16384 || static_cast<size_t>(per_cta) * ctas > bytes) return MOE_ERR_INVALID_ARG;
   cudaError_t e;
+  if (mode >= 3) {
+    // the buffer as a bf16 matrix of 2048 columns (4 KB rows: 16 column blocks of 128) or of
+    // 128 columns (256-byte rows: one block); each CTA streams per_cta bytes of it
+    const uint64_t cols = mode == 3 ? 2048 : 128;
+    const int nblk = static_cast<int>(cols / 128);
+    const uint64_t rows = bytes / (cols * 2);
+    // the same rows per CTA whatever the count: the rows split among 152 CTAs' row ranges
+    const int64_t rows_per_cta =
+        static_cast<int64_t>(rows) / ((152 + nblk - 1) / nblk) / 64 * 64;
+    if ((ctas + nblk - 1) / nblk * rows_per_cta > static_cast<int64_t>(rows))
+      return MOE_ERR_INVALID_ARG;
+    cudaError_t st = cudaSuccess;
+    const CUtensorMap map = make_map_2d(buf, cols, rows, cols * 2, 64, 64, &st);
+    if (st != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t smem = 6 * 16384 + 1024;
+    e = cudaFuncSetAttribute(probe_box_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e == cudaSuccess) {
+      probe_box_kernel<<<ctas, 32, smem, stream>>>(map, nblk, rows_per_cta, 2000000000ull, out);
+      e = cudaGetLastError();
+    }
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   if (mode == 0) {
     probe_ldg_kernel<<<ctas, 512, 0, stream>>>(static_cast<const uint4*>(buf), per_cta / 16,
                                                 out);

@@ -345,7 +345,10 @@ moe_status_t moe_ep_copy_rows(const void* const* peers, const int64_t* peer_rows
  * rate one SM sustains by load path.  Launches `ctas` CTAs (one per SM when ctas <= the SM
  * count), each streaming its own slice of floor(bytes / 152) bytes (rounded down to 16 KB)
  * of `buf` (device memory, 16-byte aligned, much larger than L2): mode 0 with 16-byte loads
- * by 512 threads, mode 1 / 2 with 16 KB bulk copies into 6 / 12 shared-memory stages.  The
+ * by 512 threads, mode 1 / 2 with 16 KB bulk copies into 6 / 12 shared-memory stages, mode
+ * 3 / 4 with the expert GEMMs' 2-D tensor-map boxes (two 64 x 64 bf16 boxes per stage, 6
+ * stages) over the buffer viewed with 4 KB rows (a weight matrix's pattern) / 256-byte rows
+ * (contiguous; each CTA then streams 256 bytes of each of its rows).  The
  * caller times the launch (events on `stream`); `out` (device, ctas uint32) receives 1 for a
  * CTA whose bounded wait ran out.  MOE_ERR_INVALID_ARG when the slices do not fit in buf. */
 moe_status_t moe_probe_dram_read(const void* buf, size_t bytes, int ctas, int mode,
