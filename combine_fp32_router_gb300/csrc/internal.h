@@ -45,6 +45,17 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
                               cudaStream_t s);
 cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* bbase,
                              int32_t* counts, cudaStream_t s);
+struct TileTables;
+// The whole dispatch of T <= 128 tokens in one launch (route, counts, offsets and tables as
+// launch_offsets, pos, perm with -1 on padding rows, and the row copies unless x_perm is
+// null); E <= 1024.  Bitwise the results of the multi-kernel sequence.  It first clears the
+// error record `err`, so no memset precedes it.
+cudaError_t launch_dispatch_small(const float* logits, const uint16_t* x, int64_t T, int d,
+                                  int E, int k, int align, int32_t* topk, float* gate,
+                                  int32_t* pos, int32_t* perm, int32_t* counts,
+                                  int32_t* offsets, int32_t* poff, const TileTables* tables,
+                                  uint16_t* x_perm, int64_t rows_cap, int num_sms, DevErr* err,
+                                  cudaStream_t s);
 // offsets (unpadded, may be null), poff (rows padded to `align`), and when align == 128
 // the tile tables: every 128-row tile (n_mt, mt_expert, mt_row0); the 256-row pair tiles
 // (n_pt, pt_expert, pt_row0: two consecutive 128-row tiles of one expert); each expert's odd

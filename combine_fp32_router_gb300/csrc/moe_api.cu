@@ -318,7 +318,9 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   char* w = static_cast<char*>(ws);
   DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
   record(stage_events, 0, stream);
-  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
+  // a batch of T <= 128 is dispatched in one launch, which also clears the error record
+  const bool small = T > 0 && T <= kRouteTokensPerBlock && (g_debug_flags.load() & 2) == 0;
+  if (!small) MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
   if (T == 0) {
     for (int i = 1; i < MOE_FWD_NUM_EVENTS; ++i) record(stage_events, i, stream);
     return MOE_OK;
@@ -334,19 +336,29 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   int32_t* perm = reinterpret_cast<int32_t*>(w + L.perm);
   uint16_t* xperm = reinterpret_cast<uint16_t*>(w + L.xperm);
 
-  // dispatch: route, count, prefix sums (rows padded to 128 per expert), stable permute
-  MOE_TRY(launch_route_topk(logits, T, E, k, topk, gate, pos, hist, err, stream));
-  MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
-  const TileTables tt = tile_tables(L, w);
-  MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
+  // dispatch: route, count, prefix sums (rows padded to 128 per expert), stable permute.
   // With MOE_FWD_GATHER_ROWS (and no backward, which reads x_perm as a K operand) GEMM1
   // gathers its rows from x itself: the dispatch copy of the next tiles overlaps the MMAs of
   // the current ones.
   const bool gather = !save && (flags & MOE_FWD_GATHER_ROWS) != 0;
-  MOE_TRY(launch_scatter(x, T, d, E, k, topk, bbase, poff, pos, perm, gather ? nullptr : xperm,
-                         L.P_pad, err, stream));
-  // padding rows: perm = -1; zero x rows when the backward will read them as a K operand
-  MOE_TRY(launch_pad_rows(counts, poff, E, perm, save ? xperm : nullptr, 2ll * d, stream));
+  const TileTables tt = tile_tables(L, w);
+  const int num_sms = num_sms_of_current_device();
+  if (small) {
+    // one launch for the whole dispatch of a small batch
+    MOE_TRY(launch_dispatch_small(logits, x, T, d, E, k, kTileRows, topk, gate, pos, perm,
+                                  counts, offsets, poff, &tt, gather ? nullptr : xperm, L.P_pad,
+                                  num_sms, err, stream));
+    // zero x padding rows when the backward will read them as a K operand
+    if (save) MOE_TRY(launch_pad_rows(counts, poff, E, nullptr, xperm, 2ll * d, stream));
+  } else {
+    MOE_TRY(launch_route_topk(logits, T, E, k, topk, gate, pos, hist, err, stream));
+    MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
+    MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
+    MOE_TRY(launch_scatter(x, T, d, E, k, topk, bbase, poff, pos, perm,
+                           gather ? nullptr : xperm, L.P_pad, err, stream));
+    // padding rows: perm = -1; zero x rows when the backward will read them as a K operand
+    MOE_TRY(launch_pad_rows(counts, poff, E, perm, save ? xperm : nullptr, 2ll * d, stream));
+  }
   record(stage_events, 1, stream);
 
   GemmCtx c{};
@@ -360,7 +372,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.err = err;
   c.wait_ns = g_wait_ns.load();
   c.debug_flags = g_debug_flags.load();
-  c.num_sms = num_sms_of_current_device();
+  c.num_sms = num_sms;
   c.pair = row_pairs(T, k, d, d_ff);
   c.fuse_combine = (flags & MOE_FWD_FUSED_COMBINE) != 0;
   c.gated = W3 != nullptr;
@@ -426,7 +438,9 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uin
   char* w = static_cast<char*>(ws);
   DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
   record(stage_events, 0, stream);
-  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
+  // a batch of T <= 128 is dispatched in one launch, which also clears the error record
+  const bool small = T > 0 && T <= kRouteTokensPerBlock && (g_debug_flags.load() & 2) == 0;
+  if (!small) MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
   if (T == 0) {
     for (int i = 1; i < MOE_FWD_NUM_EVENTS; ++i) record(stage_events, i, stream);
     return MOE_OK;

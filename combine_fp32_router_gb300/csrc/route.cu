@@ -40,15 +40,88 @@ constexpr int kRouteWarps = 16;                                     // warps per
 constexpr int kRouteTokPerWarp = kRouteTokensPerBlock / kRouteWarps;  // top-k tokens per warp
 static_assert(kRouteTokensPerBlock == 128 && kRouteTokPerWarp * kRouteWarps == 128, "");
 
-// One CTA = 128 consecutive tokens.
-// Top-k: 16 warps x 8 tokens.  A warp first loads the logits of NB of its tokens (EPL per
-// lane each) so that their loads are in flight together, then per token runs k rounds of a
-// warp arg-max: one warp max-reduction of the order keys, one min-reduction of the expert
-// indices holding that key (ties -> lower index), and the winner is marked taken.
-// Ranking: per 32-token chunk (warps 0..3), a bit mask per expert (bit i = token i of the
-// chunk chose it) gives each pair its rank among the chunk's earlier tokens; the masks'
-// popcounts then give per-chunk bases and the CTA's histogram row.  pos_local receives the
-// pair's rank among the CTA's tokens routed to the same expert.
+// Top-k and gate of one token, by one warp: k rounds of a warp arg-max (a max-reduction of
+// the order keys, then a min-reduction of the expert indices holding that key, so ties go
+// to the lower index; the winner is marked taken), then a softmax over the k selected logits
+// in fp32, summed in slot order.  v[c] is the logit of expert lane + 32 c.  Lane j < k
+// receives slot j's expert and gate.
+template <int EPL>
+__device__ __forceinline__ void topk_token(const float (&v)[EPL], int E, int k, int lane,
+                                           int* sel_e_out, float* gate_out) {
+  uint32_t key[EPL];
+#pragma unroll
+  for (int c = 0; c < EPL; ++c) key[c] = order_key(v[c]);
+  uint32_t live = 0;  // bit c: expert lane + 32c exists and is not yet taken
+#pragma unroll
+  for (int c = 0; c < EPL; ++c)
+    if (lane + 32 * c < E) live |= 1u << c;
+  int sel_e = 0;
+  float sel_v = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    uint32_t best = 0u;  // a lane with no live expert offers 0, never above a live key
+#pragma unroll
+    for (int c = 0; c < EPL; ++c)
+      if (((live >> c) & 1u) && key[c] > best) best = key[c];
+    const uint32_t bk = __reduce_max_sync(0xFFFFFFFFu, best);
+    uint32_t mine = 0xFFFFFFFFu;
+#pragma unroll
+    for (int c = EPL - 1; c >= 0; --c)
+      if (((live >> c) & 1u) && key[c] == bk) mine = static_cast<uint32_t>(lane + 32 * c);
+    const uint32_t ew = __reduce_min_sync(0xFFFFFFFFu, mine);
+    if ((ew & 31u) == static_cast<uint32_t>(lane)) live &= ~(1u << (ew >> 5));
+    if (lane == j) {
+      sel_e = static_cast<int>(ew);
+      sel_v = order_value(bk);
+    }
+  }
+  const float v0 = __shfl_sync(0xFFFFFFFFu, sel_v, 0);
+  const float ex = (lane < k) ? expf(sel_v - v0) : 0.0f;
+  float s = 0.0f;
+  for (int j = 0; j < k; ++j) s += __shfl_sync(0xFFFFFFFFu, ex, j);
+  *sel_e_out = sel_e;
+  *gate_out = ex / s;
+}
+
+// Ranks inside one block of nt <= 128 tokens whose experts are in tok_e ([128][kMaxK]):
+// per 32-token chunk (warps 0..3), a bit mask per expert (bit i = token i of the chunk chose
+// it; `mask` [4][E] zeroed beforehand) gives each pair its rank among the chunk's earlier
+// tokens, and the masks' popcounts the chunk bases.  On return tok_r[i][j] is pair (i, j)'s
+// rank among the block's tokens routed to the same expert, and count[e] (shared or global
+// memory) the block's tokens routed to e.  Every thread of the block calls it, after a
+// barrier that follows the writes of tok_e; it ends with a barrier.
+__device__ __forceinline__ void rank_block(uint32_t* mask, int32_t* wbase, const int32_t* tok_e,
+                                           int32_t* tok_r, int nt, int E, int k,
+                                           int32_t* count) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int i = w * 32 + lane;
+  const bool valid = w < kRouteTokensPerBlock / 32 && i < nt;
+  const int32_t* my_e = tok_e + i * kMaxK;
+  int32_t* my_r = tok_r + i * kMaxK;
+  if (valid)
+    for (int j = 0; j < k; ++j) atomicOr(&mask[w * E + my_e[j]], 1u << lane);
+  __syncwarp();
+  if (valid)
+    for (int j = 0; j < k; ++j) my_r[j] = __popc(mask[w * E + my_e[j]] & ((1u << lane) - 1u));
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int ww = 0; ww < kRouteTokensPerBlock / 32; ++ww) {
+      wbase[ww * E + e] = run;
+      run += __popc(mask[ww * E + e]);
+    }
+    count[e] = run;
+  }
+  __syncthreads();
+  if (valid)
+    for (int j = 0; j < k; ++j) my_r[j] += wbase[w * E + my_e[j]];
+  __syncthreads();
+}
+
+// One CTA = 128 consecutive tokens.  Top-k: 16 warps x 8 tokens; a warp first loads the
+// logits of NB of its tokens (EPL per lane each) so that their loads are in flight together,
+// then runs topk_token per token.  rank_block then gives each pair its rank among the CTA's
+// tokens routed to the same expert (pos_local) and the CTA's histogram row.
 template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ topk,
@@ -82,74 +155,22 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     for (int i = 0; i < NB; ++i) {
       const int64_t t = blk0 + wt0 + b0 + i;
       if (t >= T) break;
-      uint32_t key[EPL];
-#pragma unroll
-      for (int c = 0; c < EPL; ++c) key[c] = order_key(v[i][c]);
-      uint32_t live = 0;  // bit c: expert lane + 32c exists and is not yet taken
-#pragma unroll
-      for (int c = 0; c < EPL; ++c)
-        if (lane + 32 * c < E) live |= 1u << c;
-      int sel_e = 0;
-      float sel_v = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        uint32_t best = 0u;  // a lane with no live expert offers 0, never above a live key
-#pragma unroll
-        for (int c = 0; c < EPL; ++c)
-          if (((live >> c) & 1u) && key[c] > best) best = key[c];
-        const uint32_t bk = __reduce_max_sync(0xFFFFFFFFu, best);
-        uint32_t mine = 0xFFFFFFFFu;
-#pragma unroll
-        for (int c = EPL - 1; c >= 0; --c)
-          if (((live >> c) & 1u) && key[c] == bk) mine = static_cast<uint32_t>(lane + 32 * c);
-        const uint32_t ew = __reduce_min_sync(0xFFFFFFFFu, mine);
-        if ((ew & 31u) == static_cast<uint32_t>(lane)) live &= ~(1u << (ew >> 5));
-        if (lane == j) {
-          sel_e = static_cast<int>(ew);
-          sel_v = order_value(bk);
-        }
-      }
-      // softmax over the k selected logits, fp32, summed in slot order
-      const float v0 = __shfl_sync(0xFFFFFFFFu, sel_v, 0);
-      const float ex = (lane < k) ? expf(sel_v - v0) : 0.0f;
-      float s = 0.0f;
-      for (int j = 0; j < k; ++j) s += __shfl_sync(0xFFFFFFFFu, ex, j);
+      int sel_e;
+      float g;
+      topk_token<EPL>(v[i], E, k, lane, &sel_e, &g);
       if (lane < k) {
         topk[t * k + lane] = sel_e;
-        gate[t * k + lane] = ex / s;
+        gate[t * k + lane] = g;
         tok_e[(wt0 + b0 + i) * kMaxK + lane] = sel_e;
       }
     }
   }
   __syncthreads();
-  // ranks inside each 32-token chunk
-  const int64_t t = blk0 + w * 32 + lane;
-  const bool ranker = w < kRouteTokensPerBlock / 32;
-  const bool valid = ranker && t < T;
-  int32_t* my_e = tok_e + w * 32 * kMaxK;
-  int32_t* my_r = tok_r + w * 32 * kMaxK;
-  if (valid)
-    for (int j = 0; j < k; ++j) atomicOr(&mask[w * E + my_e[lane * kMaxK + j]], 1u << lane);
-  __syncwarp();
-  if (valid)
-    for (int j = 0; j < k; ++j)
-      my_r[lane * kMaxK + j] =
-          __popc(mask[w * E + my_e[lane * kMaxK + j]] & ((1u << lane) - 1u));
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-#pragma unroll
-    for (int ww = 0; ww < kRouteTokensPerBlock / 32; ++ww) {
-      wbase[ww * E + e] = run;
-      run += __popc(mask[ww * E + e]);
-    }
-    hist[static_cast<int64_t>(blockIdx.x) * E + e] = run;
-  }
-  __syncthreads();
-  if (valid)
-    for (int j = 0; j < k; ++j) {
-      const int e = my_e[lane * kMaxK + j];
-      pos_local[t * k + j] = wbase[w * E + e] + my_r[lane * kMaxK + j];
-    }
+  const int64_t left = T - blk0;
+  const int nt = left < kRouteTokensPerBlock ? static_cast<int>(left) : kRouteTokensPerBlock;
+  rank_block(mask, wbase, tok_e, tok_r, nt, E, k, hist + static_cast<int64_t>(blockIdx.x) * E);
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x)
+    pos_local[blk0 * k + i] = tok_r[(i / k) * kMaxK + i % k];
 }
 
 // Column prefix over the routing CTAs: bbase[b][e] = sum_{b' < b} hist[b'][e], counts[e].
@@ -265,17 +286,18 @@ __device__ __forceinline__ void fill_tile_table(const int* a_incl, const int* b_
   }
 }
 
-__global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E,
-                                                       int align, int32_t* __restrict__ offsets,
-                                                       int32_t* __restrict__ poff, TileTables tt,
-                                                       int with_tables, DevErr* err) {
-  griddep_wait();  // the previous kernel in the stream has finished (PDL)
+// Offsets and tile tables of the expert counts, one CTA of 1024 threads (thread e holds
+// expert e's count c, 0 past E): offsets (unpadded exclusive prefix and total, unless null),
+// poff (rows padded to multiples of `align`, with the total), and with_tables the GEMM tile
+// tables.  Every thread of the CTA calls it.
+__device__ __forceinline__ void offsets_block(int c, int E, int align, int32_t* __restrict__ offsets,
+                                              int32_t* __restrict__ poff, const TileTables& tt,
+                                              int with_tables, DevErr* err) {
   __shared__ int warp_tot[32];
   __shared__ int total;
   __shared__ int s_poff[1024], s_a[1024], s_b[1024], s_pa[1024], s_pb[1024], s_sa[1024],
       s_sb[1024];
   const int e = threadIdx.x;
-  const int c = e < E ? counts[e] : 0;
   const int pc = (c + align - 1) / align * align;
   const int off = block_exclusive_scan(c, warp_tot, &total);
   const int tot_c = total;
@@ -353,6 +375,15 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict
     for (int i = threadIdx.x; i < SH + SL; i += blockDim.x) tt.done1[i] = 0;
 }
 
+__global__ void __launch_bounds__(1024) offsets_kernel(const int32_t* __restrict__ counts, int E,
+                                                       int align, int32_t* __restrict__ offsets,
+                                                       int32_t* __restrict__ poff, TileTables tt,
+                                                       int with_tables, DevErr* err) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
+  const int e = threadIdx.x;
+  offsets_block(e < E ? counts[e] : 0, E, align, offsets, poff, tt, with_tables, err);
+}
+
 // Stable permute.  One warp per token: lanes j < k turn the CTA-local rank into the final
 // row (padded expert offset + rank of earlier routing CTAs + local rank), write pos/perm,
 // then (unless x_perm is null) the warp copies the token's row once from x and stores it k
@@ -408,6 +439,115 @@ __global__ void __launch_bounds__(256) scatter_kernel(const uint4* __restrict__ 
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j)
         if (j < k && rows[j] >= 0) st_v4(x_perm + static_cast<int64_t>(rows[j]) * n16 + c, v0);
+    }
+  }
+}
+
+// Single-launch dispatch for T <= 128 (one routing block): every CTA routes all T tokens
+// itself (topk_token, rank_block: the same arithmetic as route_topk_kernel) and scans the
+// counts, so no CTA waits for another.  CTA 0 clears the error record and writes the
+// routing outputs (topk, gate, pos,
+// perm of the tokens' rows, counts, and offsets_block's offsets, poff and tile tables); the
+// other CTAs (CTA 0 too in a grid of one) set perm = -1 on the padding rows, a warp per
+// expert, and copy the token rows to their permuted rows, work split by 16-byte column chunks
+// (each chunk loaded once, stored k times).  Results equal those of route_topk, scan_cols,
+// offsets, scatter and pad_rows's perm part.  1024 threads; dynamic shared memory as
+// small_dispatch_smem.
+template <int EPL>
+__global__ void __launch_bounds__(1024) dispatch_small_kernel(
+    const float* __restrict__ logits, const uint4* __restrict__ x, int T, int d, int E, int k,
+    int align, int32_t* __restrict__ topk, float* __restrict__ gate, int32_t* __restrict__ pos,
+    int32_t* __restrict__ perm, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ poff, TileTables tt, int with_tables, uint4* __restrict__ x_perm,
+    int64_t rows_cap, DevErr* err) {
+  griddep_wait();  // the previous kernel in the stream has finished (PDL)
+  constexpr int NB = EPL <= 8 ? 4 : 1;  // tokens whose loads fly together (no spills)
+  extern __shared__ uint32_t sm[];
+  uint32_t* mask = sm;                                        // [4][E]
+  int32_t* wbase = reinterpret_cast<int32_t*>(sm + 4 * E);   // [4][E]
+  int32_t* tok_e = wbase + 4 * E;                             // [128][kMaxK]
+  int32_t* tok_r = tok_e + kRouteTokensPerBlock * kMaxK;     // [128][kMaxK]: rank, then row
+  int32_t* s_cnt = tok_r + kRouteTokensPerBlock * kMaxK;     // [E]
+  int32_t* s_poff = s_cnt + E;                                // [E + 1]
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const bool lead = blockIdx.x == 0;
+  const bool mover = !lead || gridDim.x == 1;  // pads perm and copies rows
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  // the launch begins the layer's device work: CTA 0, the only one that records errors
+  // here, clears the error record (ordered before its first record by the barriers below)
+  if (lead && threadIdx.x == 0) *err = DevErr{};
+  for (int i = threadIdx.x; i < 4 * E; i += blockDim.x) mask[i] = 0u;
+  for (int t0 = w; t0 < T; t0 += 32 * NB) {
+    float v[NB][EPL];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int t = t0 + 32 * b;
+#pragma unroll
+      for (int c = 0; c < EPL; ++c) {
+        const int e = lane + 32 * c;
+        v[b][c] = (t < T && e < E) ? __ldg(logits + static_cast<int64_t>(t) * E + e) : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int t = t0 + 32 * b;
+      if (t >= T) break;
+      int sel_e;
+      float g;
+      topk_token<EPL>(v[b], E, k, lane, &sel_e, &g);
+      if (lane < k) {
+        tok_e[t * kMaxK + lane] = sel_e;
+        if (lead) {
+          topk[t * k + lane] = sel_e;
+          gate[t * k + lane] = g;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  rank_block(mask, wbase, tok_e, tok_r, T, E, k, s_cnt);
+  const int c = threadIdx.x < E ? s_cnt[threadIdx.x] : 0;
+  if (lead) {
+    if (threadIdx.x < E) counts[threadIdx.x] = c;
+    offsets_block(c, E, align, offsets, poff, tt, with_tables, err);
+  }
+  // this CTA's copy of the padded offsets (the same scan as offsets_block's)
+  const int pv = block_exclusive_scan((c + align - 1) / align * align, warp_tot, &total);
+  if (threadIdx.x < E) s_poff[threadIdx.x] = pv;
+  if (threadIdx.x == 0) s_poff[E] = total;
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    const int t = i / k, j = i - t * k;
+    int row = s_poff[tok_e[t * kMaxK + j]] + tok_r[t * kMaxK + j];
+    if (row >= rows_cap) {
+      if (lead) set_error(err, MOE_ERR_DEVICE_BOUNDS, 210);
+      row = -1;
+    } else if (lead) {
+      pos[i] = row;
+      perm[row] = i;
+    }
+    tok_r[t * kMaxK + j] = row;
+  }
+  if (!mover) return;
+  const int nmov = gridDim.x > 1 ? gridDim.x - 1 : 1;
+  const int mrank = gridDim.x > 1 ? blockIdx.x - 1 : 0;
+  for (int e = mrank * 32 + w; e < E; e += nmov * 32) {
+    const int64_t r1 = s_poff[e + 1] < rows_cap ? s_poff[e + 1] : rows_cap;
+    for (int64_t r = s_poff[e] + s_cnt[e] + lane; r < r1; r += 32) perm[r] = -1;
+  }
+  __syncthreads();  // every row of tok_r is final
+  if (!x_perm) return;
+  const int n16 = d >> 3;
+  const int64_t nchunks = static_cast<int64_t>(T) * n16;
+  for (int64_t q = static_cast<int64_t>(mrank) * blockDim.x + threadIdx.x; q < nchunks;
+       q += static_cast<int64_t>(nmov) * blockDim.x) {
+    const int t = static_cast<int>(q / n16);
+    const int col = static_cast<int>(q - static_cast<int64_t>(t) * n16);
+    const uint4 v = ld_nc_v4(x + q);
+    for (int j = 0; j < k; ++j) {
+      const int row = tok_r[t * kMaxK + j];
+      if (row >= 0) st_v4(x_perm + static_cast<int64_t>(row) * n16 + col, v);
     }
   }
 }
@@ -564,21 +704,23 @@ constexpr int kCombChunks = 128;  // 8-column chunks per unit (1024 columns, 4 p
 // Combine: out[t] = bf16( sum_j gate[t,j] * y[pos[t,j]] ) over the fp32 expert-output rows,
 // fp32 fused multiply-adds in slot order j = 0..k-1, one rounding at the end.  Each lane owns
 // 8 consecutive columns per step (two 16-byte loads per slot).  KC >= k bounds the slots.
+// `cpu` chunks per work unit: kCombChunks, or 32 (one step per lane) for small batches,
+// whose few units would otherwise leave each warp several dependent load rounds.
 template <int KC>
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y,
                                                       const float* __restrict__ gate,
                                                       const int32_t* __restrict__ pos,
-                                                      int64_t T, int k, int d,
+                                                      int64_t T, int k, int d, int cpu,
                                                       uint4* __restrict__ out) {
   griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n8 = d >> 3;
-  const int upt = (n8 + kCombChunks - 1) / kCombChunks;
+  const int upt = (n8 + cpu - 1) / cpu;
   for (int64_t u = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
        u < T * upt; u += nwarps) {
     const int64_t t = u / upt;
-    const int c0 = static_cast<int>(u - t * upt) * kCombChunks;
+    const int c0 = static_cast<int>(u - t * upt) * cpu;
     int row = 0;
     float g = 0.0f;
     if (lane < k) {
@@ -593,7 +735,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
       gs[j] = __shfl_sync(0xFFFFFFFFu, g, j);
     }
 #pragma unroll 1
-    for (int c = c0 + lane; c < c0 + kCombChunks && c < n8; c += 32) {
+    for (int c = c0 + lane; c < c0 + cpu && c < n8; c += 32) {
       float acc[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
@@ -802,9 +944,12 @@ int unit_grid(K kern, int64_t units) {
 template <int KC>
 cudaError_t launch_combine_kc(const float* y_rows, const float* gate, const int32_t* pos,
                               int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
-  const int64_t units = T * ((d / 8 + kCombChunks - 1) / kCombChunks);
+  // one step per lane while the units do not fill the GPU's warps a few times over
+  const int64_t small_units = T * ((d / 8 + 31) / 32);
+  const int cpu = small_units <= 8192 ? 32 : kCombChunks;
+  const int64_t units = T * ((d / 8 + cpu - 1) / cpu);
   return launch_pdl(combine_kernel<KC>, dim3(unit_grid(combine_kernel<KC>, units)), dim3(256), 0,
-                    s, reinterpret_cast<const float4*>(y_rows), gate, pos, T, k, d,
+                    s, reinterpret_cast<const float4*>(y_rows), gate, pos, T, k, d, cpu,
                     reinterpret_cast<uint4*>(out));
 }
 template <int KC>
@@ -848,6 +993,44 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
   if (st != cudaSuccess) return st;
   return launch_pdl(kern, dim3(static_cast<unsigned>(nblk)), dim3(kRouteWarps * 32), smem, s,
                     logits, T, E, k, topk, gate, pos_local, hist);
+}
+
+size_t small_dispatch_smem(int E) {
+  return (10 * static_cast<size_t>(E) + 1 + 2 * kRouteTokensPerBlock * kMaxK) * 4;
+}
+
+cudaError_t launch_dispatch_small(const float* logits, const uint16_t* x, int64_t T, int d,
+                                  int E, int k, int align, int32_t* topk, float* gate,
+                                  int32_t* pos, int32_t* perm, int32_t* counts,
+                                  int32_t* offsets, int32_t* poff, const TileTables* tables,
+                                  uint16_t* x_perm, int64_t rows_cap, int num_sms, DevErr* err,
+                                  cudaStream_t s) {
+  if (T <= 0 || T > kRouteTokensPerBlock || E > 1024) return cudaErrorInvalidValue;
+  const size_t smem = small_dispatch_smem(E);
+  const int epl = (E + 31) / 32;
+  void (*kern)(const float*, const uint4*, int, int, int, int, int, int32_t*, float*, int32_t*,
+               int32_t*, int32_t*, int32_t*, int32_t*, TileTables, int, uint4*, int64_t,
+               DevErr*);
+  if (epl <= 1) kern = dispatch_small_kernel<1>;
+  else if (epl <= 2) kern = dispatch_small_kernel<2>;
+  else if (epl <= 4) kern = dispatch_small_kernel<4>;
+  else if (epl <= 8) kern = dispatch_small_kernel<8>;
+  else if (epl <= 16) kern = dispatch_small_kernel<16>;
+  else kern = dispatch_small_kernel<32>;
+  cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+  if (st != cudaSuccess) return st;
+  TileTables tt{};
+  if (tables) tt = *tables;
+  // CTA 0 for the routing outputs and tables, then one CTA per 1024 16-byte chunks of the
+  // token rows (at least one), at most one CTA per SM
+  const int64_t chunks = x_perm ? T * (d / 8) : 0;
+  int64_t g = 1 + (chunks > 0 ? (chunks + 1023) / 1024 : 1);
+  if (g > num_sms) g = num_sms;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(g)), dim3(1024), smem, s, logits,
+                    reinterpret_cast<const uint4*>(x), static_cast<int>(T), d, E, k, align, topk,
+                    gate, pos, perm, counts, offsets, poff, tt, tables ? 1 : 0,
+                    reinterpret_cast<uint4*>(x_perm), rows_cap, err);
 }
 
 cudaError_t launch_scan_cols(const int32_t* hist, int64_t nblk, int E, int32_t* bbase,

@@ -366,7 +366,9 @@ void moe_set_wait_timeout_ns(uint64_t ns);
 
 /* Test hook, process-wide, 0 by default.  Bit 0: the first CTA of the next grouped-GEMM
  * launches skips its first operand load so that the matching wait runs out (used to test
- * the timeout path on a tiny problem with a short timeout). */
+ * the timeout path on a tiny problem with a short timeout).  Bit 1: moe_forward dispatches
+ * batches of T <= 128 with the multi-kernel sequence of larger batches instead of its
+ * single launch (both give bitwise the same workspace contents and output). */
 void moe_debug_set_flags(int flags);
 
 /* Short English description of a status code. */
