@@ -179,13 +179,21 @@ def _forward_fused(T, k, d, dff):
     return _forward_swap(T, k, d, dff) and mode != "0" and (mode == "1" or T <= 64)
 
 
-def fwd_launches(T, k, d, dff):
-    # routing, column scan, offsets/tile tables, scatter, padding rows, GEMM1, GEMM2, combine;
-    # with row-tile CTA pairs each GEMM is a pair launch plus a single-CTA launch for the
-    # other tiles (the swapped kernels take every tile in one pair launch)
+def fwd_launches(T, k, d, dff, save=False):
+    # dispatch: routing, column scan, offsets/tile tables, scatter, padding rows; or, for
+    # T <= 128, the library's single dispatch launch (plus the zeroing of the padding rows
+    # when saving for the backward).  GEMM1 and GEMM2: one swapped launch each, or one
+    # together for T <= 64; with row-tile CTA pairs each is a pair launch plus a single-CTA
+    # launch for the other tiles.  Then the combine.
+    if 0 < T <= 128:
+        dispatch = 2 if save else 1
+    else:
+        dispatch = 5
     if _forward_swap(T, k, d, dff):
-        return 7 if _forward_fused(T, k, d, dff) else 8
-    return 10 if _row_pairs(T, k, d, dff) else 8
+        gemms = 1 if _forward_fused(T, k, d, dff) else 2
+    else:
+        gemms = 4 if _row_pairs(T, k, d, dff) else 2
+    return dispatch + gemms + 1
 
 
 def bwd_launches(T, k, d, dff):
@@ -253,7 +261,7 @@ def bench_fwd_bwd(moe, dev, steps, warmup, shape=None):
             "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
             "backward_ms": bwd_ms, "backward_stages_ms": stages,
             "backward_tflops": bwd_flops / (bwd_ms * 1e-3) / 1e12,
-            "launches_per_step": fwd_launches(T, k, d, dff) + bwd_launches(T, k, d, dff)}
+            "launches_per_step": fwd_launches(T, k, d, dff, save=True) + bwd_launches(T, k, d, dff)}
 
 
 def run_cpu_baseline(w, inp_np, budget_s=15.0):

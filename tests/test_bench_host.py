@@ -58,12 +58,17 @@ def test_pair_rule_and_launch_counts(bench, monkeypatch, mode, name, pairs):
     w = moe_synth.by_name(name)
     assert bench._row_pairs(w.T, w.k, w.d, w.dff) == pairs
     # the backward's row-grouped GEMMs add a single-CTA launch beside each pair launch; the
-    # forward's swapped GEMMs (wherever row tiles would pair, and T <= 128) are one launch each
+    # forward's swapped GEMMs (wherever row tiles would pair, and T <= 128) are one launch
+    # each; a batch of T <= 128 is dispatched in one launch instead of five
+    small = w.T <= 128
     monkeypatch.setenv("MOE_FWD_SWAP", "0")
-    assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)
+    assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else (4 if small else 8))
     monkeypatch.delenv("MOE_FWD_SWAP")
-    assert bench._forward_swap(w.T, w.k, w.d, w.dff) == (mode != "0" and (pairs or w.T <= 128))
+    assert bench._forward_swap(w.T, w.k, w.d, w.dff) == (mode != "0" and (pairs or small))
     # T <= 64: both swapped GEMMs in one launch
     fused = mode != "0" and w.T <= 64
-    assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == (7 if fused else 8)
+    expect = (3 if fused else 4) if small else 8
+    assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == expect
+    # saving for the backward adds the zeroing of the padding rows to the single dispatch
+    assert bench.fwd_launches(w.T, w.k, w.d, w.dff, save=True) == expect + (1 if small else 0)
     assert bench.bwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)
