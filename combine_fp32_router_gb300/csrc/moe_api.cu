@@ -438,9 +438,7 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uin
   char* w = static_cast<char*>(ws);
   DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
   record(stage_events, 0, stream);
-  // a batch of T <= 128 is dispatched in one launch, which also clears the error record
-  const bool small = T > 0 && T <= kRouteTokensPerBlock && (g_debug_flags.load() & 2) == 0;
-  if (!small) MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
   if (T == 0) {
     for (int i = 1; i < MOE_FWD_NUM_EVENTS; ++i) record(stage_events, i, stream);
     return MOE_OK;

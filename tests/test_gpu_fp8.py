@@ -115,3 +115,18 @@ def test_fp8_large_workload_sampled(moe):
     tok = sample_tokens(w.T, 6, seed=5)
     ref = oracle.forward_tokens_fp8(npi, w.k, tokens=tok)
     assert_close(np_of(out)[tok], ref, "out (fp8, large workload, sampled tokens)")
+
+
+@pytest.mark.parametrize("T", [5, 200])   # single dispatch launch for moe_forward / five kernels
+def test_every_forward_clears_the_error_record(moe, T):
+    # a workspace full of stale bytes: each forward entry point starts from a clean record
+    w = moe_synth.custom(T, 128, 8, 2, 256, seed=T + 11)
+    g = to_dev(moe_synth.generate(w))
+    ws = torch.full((moe.moe_workspace_bytes(T, 128, 8, 2, 256),), 0x7F, dtype=torch.uint8,
+                    device=g["x"].device)
+    out = torch.empty(T, 128, dtype=torch.bfloat16, device=g["x"].device)
+    moe.moe_forward(g["x"], g["logits"], g["W1"], g["W3"], g["W2"], 2, out, ws)
+    assert moe.moe_get_error(ws) == moe.MOE_OK
+    ws.fill_(0x7F)
+    _fp8_forward(moe, g, 2, ws=ws)
+    assert moe.moe_get_error(ws) == moe.MOE_OK
