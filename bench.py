@@ -135,11 +135,9 @@ def _algorithmic(w, P):
         gemm2_flops=2 * d * dff * P,            # down projection
         # logits read; topk, gate, pos, perm written; x read; x_perm written
         dispatch_bytes=T * E * 4 + T * k * 16 + T * d * 2 + P * d * 2,
-        # algorithmic combine: bf16 expert-output rows read (the pages' BF16 gather), gate +
-        # pos read, out written (bf16)
+        # combine: bf16 expert-output rows read (the pages' BF16 gather), gate + pos read,
+        # out written (bf16)
         combine_bytes=P * d * 2 + T * k * 8 + T * d * 2,
-        # what this build's combine moves: it reads the expert rows in fp32
-        combine_bytes_fp32_rows=P * d * 4 + T * k * 8 + T * d * 2,
     )
 
 
@@ -523,7 +521,6 @@ def bench_native(args, w):
     g_tflops = alg["gemm_flops"] / ((stages["gemm1_swiglu"] + stages["gemm2"]) * 1e-3) / 1e12
     disp_gbs = alg["dispatch_bytes"] / (stages["dispatch"] * 1e-3) / 1e9
     comb_gbs = alg["combine_bytes"] / (stages["combine"] * 1e-3) / 1e9
-    comb_gbs_moved = alg["combine_bytes_fp32_rows"] / (stages["combine"] * 1e-3) / 1e9
     # GEMM1 runs for milliseconds inside a sub-second timed loop: the burst peak applies
     peak = peaks["bf16"]
     line = {
@@ -548,8 +545,6 @@ def bench_native(args, w):
         "gemm_roofline_under_load": roof,
         "dispatch_gbs": disp_gbs, "dispatch_frac_of_hbm": disp_gbs / peaks["hbm"],
         "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
-        "combine_gbs_fp32_rows": comb_gbs_moved,
-        "combine_frac_of_hbm_fp32_rows": comb_gbs_moved / peaks["hbm"],
         "waved_forward_ms_per_step": waved_ms,
         "graph_forward_ms_per_step": graph_ms,
         "fp8_forward": fp8,

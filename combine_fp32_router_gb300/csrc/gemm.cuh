@@ -38,7 +38,7 @@ namespace moe {
 
 enum GemmKind : int {
   kFwd1 = 0,  // H = bf16(silu(Xp W1) * (Xp W3)), optional fp32 A/B save   (rows x dff)
-  kFwd2 = 1,  // Y = H W2 (fp32 rows for the fp32 combine)                  (rows x d)
+  kFwd2 = 1,  // Y = H W2 (bf16 rows, the combine's payload)                (rows x d)
   kDh = 2,    // dH = dO W2^T -> dA, dB (bf16) through the SwiGLU backward (rows x dff)
   kDx = 3,    // dXp = [dA|dB] [W1|W3]^T (fp32)                            (rows x d)
   kDw2 = 4,   // dW2[e] = H^T dO (fp32)                                    (dff x d)
@@ -51,7 +51,7 @@ enum GemmKind : int {
   // follows the rows the block really holds (32, 64, 128 or 256) and an expert with few rows
   // costs few MMAs; heavy and light experts then share one persistent CTA-pair launch.
   kFwd1T = 7,   // H^T = [W1|W3]^T Xp^T -> SwiGLU -> H                      (dff x rows)
-  kFwd2T = 8,   // Y^T = W2^T H^T (fp32 rows)                                (d x rows)
+  kFwd2T = 8,   // Y^T = W2^T H^T (bf16 rows)                                (d x rows)
   // Both swapped GEMMs in one persistent launch: every GEMM1 tile first, then every GEMM2
   // tile; a GEMM2 tile of a row block starts loading H only when all GEMM1 tiles of that
   // block have stored theirs (a per-block counter), so GEMM2 of the first blocks runs while
@@ -299,6 +299,7 @@ __device__ __forceinline__ void ld_f32x16(const float* p, float (&v)[16]) {
 // each row's lane counts one more finished row of its (token, N block) segment (integer
 // atomics: exact whatever their order).  A lane that brings a segment to k rows has the
 // whole warp combine it right away: out[t, cols] = bf16(sum_j gate[t,j] * Y[pos[t,j], cols])
+// over the bf16 output rows Y
 // with fp32 fused multiply-adds in slot order, the same arithmetic as the stand-alone
 // combine, so the result is bitwise identical.  The combine of earlier experts' tokens thus
 // runs under the MMAs of later experts (the accumulator is double-buffered, so the epilogue
@@ -314,15 +315,18 @@ __device__ __forceinline__ void combine_segment(const GemmParams& p, int seg, in
     g = p.gate[static_cast<int64_t>(t) * p.k + lane];
   }
   const int col = nblk * BN + lane * CPL;
-  const float* Y = static_cast<const float*>(p.out0);
+  const uint16_t* Y = static_cast<const uint16_t*>(p.out0);  // bf16 output rows
   float4 y[kMaxK][CPL / 4];
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
     const int rj = __shfl_sync(0xFFFFFFFFu, row, j);
     if (j < p.k) {
-      const float4* src = reinterpret_cast<const float4*>(Y + static_cast<int64_t>(rj) * p.d + col);
+      const uint16_t* src = Y + static_cast<int64_t>(rj) * p.d + col;
 #pragma unroll
-      for (int c4 = 0; c4 < CPL / 4; ++c4) y[j][c4] = __ldcg(src + c4);
+      for (int c4 = 0; c4 < CPL / 4; ++c4) {
+        const uint2 u = __ldcg(reinterpret_cast<const uint2*>(src) + c4);
+        y[j][c4] = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+      }
     }
   }
   float acc[CPL];
@@ -491,21 +495,32 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     }
   } else if constexpr (KIND == kFwd2 || KIND == kDx) {
     const int64_t row0 = ti.row0 + w0;
-    char* out = reinterpret_cast<char*>(static_cast<float*>(p.out0) + row0 * p.d + ti.n0);
     const int nstore = clamp_rows(ti.nvalid);
-    // TMA stores write all 32 rows of the warp: rows past the expert's count are padding rows
-    // of its own segment (zeros: their A rows are zero), which nothing reads
-    const bool tma = p.tma_store && !p.fuse_combine && clamp_rows(ti.nseg) == 32;
+    if constexpr (KIND == kFwd2) {
+      // bf16 output rows (the combine's payload), through the bf16 transpose
+      char* out = reinterpret_cast<char*>(static_cast<uint16_t*>(p.out0) + row0 * p.d + ti.n0);
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 32; ++ch) {
-      float v[32];
-      tmem_ld32(tacc + ch * 32, v);
-      if (tma) {
-        store_chunk_tma(stage, v, &p.mapC0, ti.n0 + ch * 32, static_cast<int>(row0), lane);
-      } else {
-        if (p.tma_store && lane == 0) bulk_wait_read_all();  // the region may still be read
-        __syncwarp();
-        store_chunk<false>(buf, v, out + ch * 128, 4ll * p.d, nstore, lane);
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        float v[32];
+        tmem_ld32(tacc + ch * 32, v);
+        store_chunk<true>(buf, v, out + ch * 64, 2ll * p.d, nstore, lane);
+      }
+    } else {
+      // fp32 dX rows.  TMA stores write all 32 rows of the warp: rows past the expert's count
+      // are padding rows of its own segment (zeros: their A rows are zero), which nothing reads
+      char* out = reinterpret_cast<char*>(static_cast<float*>(p.out0) + row0 * p.d + ti.n0);
+      const bool tma = p.tma_store && clamp_rows(ti.nseg) == 32;
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        float v[32];
+        tmem_ld32(tacc + ch * 32, v);
+        if (tma) {
+          store_chunk_tma(stage, v, &p.mapC0, ti.n0 + ch * 32, static_cast<int>(row0), lane);
+        } else {
+          if (p.tma_store && lane == 0) bulk_wait_read_all();  // the region may still be read
+          __syncwarp();
+          store_chunk<false>(buf, v, out + ch * 128, 4ll * p.d, nstore, lane);
+        }
       }
     }
     if constexpr (KIND == kFwd2) {
@@ -646,7 +661,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 //    memory and each finishes half of the chunk's rows: h = bf16(silu(A) B).  Padding rows of
 //    the expert's segment get h = 0 (a later K-over-rows GEMM reads them).
 //  * kFwd1T without W3: h = bf16(relu(A)^2) over 128 W1 columns.
-//  * kFwd2T: Y rows (fp32) over 128 W2 columns (columns past d, when d is not a multiple of
+//  * kFwd2T: Y rows (bf16) over 128 W2 columns (columns past d, when d is not a multiple of
 //    256, are neither loaded as real data nor stored).
 template <int KIND>
 __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInfo& ti,
@@ -721,19 +736,29 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
       for (int r = nch * 32; r < ti.nseg; ++r) H[(row0 + r) * p.dff + col] = 0;
     }
   } else {
-    const int col = ti.n0 + 128 * rank + 32 * q + lane;
+    const int c0 = ti.n0 + 128 * rank + 32 * q;  // first output column of this warp
     const bool live = ti.n0 + 128 * rank < p.d;  // warp-uniform: d is a multiple of 128
-    float* Y = static_cast<float*>(KIND == kFwdT ? p.out1 : p.out0);
+    uint16_t* Y = static_cast<uint16_t*>(KIND == kFwdT ? p.out1 : p.out0);
+    uint16_t* yb = reinterpret_cast<uint16_t*>(mine);
 #pragma unroll 1
     for (int ch = 0; ch < nch; ++ch) {
       float v[32];
       tmem_ld32(tacc + ch * 32, v);
       if (!live) continue;
+      // bf16 rows (the combine's payload): the warp's 32 rows x 32 columns through `mine`
+      // (row pitch 64 bytes), then 16-byte stores, each instruction 8 rows x 64 bytes
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 32; ++j) yb[j * 32 + lane] = bf16_bits(v[j]);
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int j = (it * 32 + lane) >> 2, piece = lane & 3;
         const int r = ch * 32 + j;
-        if (r < ti.nvalid) Y[(row0 + r) * p.d + col] = v[j];
+        if (r < ti.nvalid)
+          st_v4(Y + (row0 + r) * p.d + c0 + piece * 8,
+                *reinterpret_cast<const uint4*>(yb + j * 32 + piece * 8));
       }
+      __syncwarp();  // stores have read `mine` before the next chunk rewrites it
     }
   }
 }

@@ -197,11 +197,6 @@ cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
   p.seg_count = reinterpret_cast<int32_t*>(c.ws + L.seg);
   p.comb_out = c.out;
   p.k = L.k;
-  if (!c.fuse_combine) {
-    p.mapC0 = make_store_map_f32(c.ws + L.Y, L.d, L.P_pad, 4ull * L.d, &st);
-    if (st != cudaSuccess) return st;
-    p.tma_store = 1;
-  }
   const GemmParams lo = leftover_params(p, c);
   if (BN == 256)
     return run_rows_kind<kFwd2, 256>(c.pair, a, b0, b0, b0, b0, p, lo, L.max_mt, c.num_sms, s);

@@ -88,10 +88,10 @@ cudaError_t launch_quantize_weights_fp8(const uint16_t* W, int E, int K, int N, 
 // Padding rows of every expert segment: perm = -1 and (if rows != null) zero bytes.
 cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, int32_t* perm,
                             void* rows, int64_t row_bytes, cudaStream_t s);
-cudaError_t launch_combine(const float* y_rows, const float* gate, const int32_t* pos,
+cudaError_t launch_combine(const uint16_t* y_rows, const float* gate, const int32_t* pos,
                            int64_t T, int k, int d, uint16_t* out, cudaStream_t s);
 // `part`: scratch of T * ceil(d / 1024) * k floats (per-block partial dot products).
-cudaError_t launch_bwd_gate(const uint16_t* dy, const float* y_rows, const float* gate,
+cudaError_t launch_bwd_gate(const uint16_t* dy, const uint16_t* y_rows, const float* gate,
                             const int32_t* pos, const int32_t* topk, int64_t T, int k, int d,
                             int E, uint16_t* dO_rows, float* dgate, float* dlogits, float* part,
                             cudaStream_t s);

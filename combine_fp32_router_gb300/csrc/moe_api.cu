@@ -179,7 +179,7 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int dff) {
   L.perm = take(Pp * 4);
   L.xperm = take(Pp * d * 2);
   L.H = take(Pp * dff * 2);
-  L.Y = take(Pp * d * 4);
+  L.Y = take(Pp * d * 2);  // bf16 expert output rows
   L.seg = take(P / (k > 0 ? k : 1) * static_cast<size_t>(d / 128) * 4);  // [T, d/128] counters
   L.xscale = take(static_cast<size_t>(T) * 4);  // FP8 payload: one scale per token
   L.fwd_total = off;
@@ -386,7 +386,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
     MOE_TRY(launch_gemm_fwd_fused(c, stream));
     record(stage_events, 2, stream);
     record(stage_events, 3, stream);
-    MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,
+    MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), gate, pos, T, k, d, out,
                            stream));
     record(stage_events, 4, stream);
     return MOE_OK;
@@ -404,7 +404,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   }
   MOE_TRY(c.swap ? launch_gemm_fwd2_swap(c, stream) : launch_gemm_fwd2(c, stream));
   record(stage_events, 3, stream);
-  MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,
+  MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), gate, pos, T, k, d, out,
                          stream));
   record(stage_events, 4, stream);
   return MOE_OK;
@@ -484,7 +484,7 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uin
   record(stage_events, 2, stream);
   MOE_TRY(launch_gemm_fwd2(c, stream));
   record(stage_events, 3, stream);
-  MOE_TRY(launch_combine(reinterpret_cast<const float*>(w + L.Y), gate, pos, T, k, d, out,
+  MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), gate, pos, T, k, d, out,
                          stream));
   record(stage_events, 4, stream);
   return MOE_OK;
@@ -657,7 +657,7 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   uint16_t* dO = reinterpret_cast<uint16_t*>(w + L.dO);
 
   // the dX rows' buffer is free until the dX GEMM: it holds the gate grads' partial sums
-  MOE_TRY(launch_bwd_gate(dy, reinterpret_cast<const float*>(w + L.Y), gate, pos, topk, T, k,
+  MOE_TRY(launch_bwd_gate(dy, reinterpret_cast<const uint16_t*>(w + L.Y), gate, pos, topk, T, k,
                           d, E, dO, dgate, dlogits, reinterpret_cast<float*>(w + L.dXp), stream));
   MOE_TRY(launch_pad_rows(counts, poff, E, nullptr, dO, 2ll * d, stream));
   record(stage_events, 1, stream);

@@ -3,9 +3,9 @@
 // gate-weighted combine, and the per-token part of the backward.
 //
 // Dispatch -> Expert Compute -> Combine is the layer of "DeepSeek-V4 parallel strategy"
-// (blog.lpkt.cn, EP section).  On one GPU the combine reads the expert outputs as fp32 rows
-// and accumulates in fp32; the report translation's BF16 gather (itsolotime.com, section
-// 1.4) is a cross-GPU payload format and is not needed here.  Determinism follows the
+// (blog.lpkt.cn, EP section).  The combine reads the expert outputs as bf16 rows, the BF16
+// combine payload of the report translation (itsolotime.com, section 1.4), and accumulates
+// in fp32.  Determinism follows the
 // report's section 3 and the 10100.com reading: no floating-point atomics anywhere; counts
 // come from per-CTA shared-memory bit masks and histograms, positions from a fixed-order
 // prefix sum, and every floating-point reduction runs in a fixed order that depends only on
@@ -701,13 +701,14 @@ __global__ void __launch_bounds__(256) pad_rows_kernel(const int32_t* __restrict
 // at most one unit per warp instead of a partial wave of whole blocks.
 constexpr int kCombChunks = 128;  // 8-column chunks per unit (1024 columns, 4 per lane)
 
-// Combine: out[t] = bf16( sum_j gate[t,j] * y[pos[t,j]] ) over the fp32 expert-output rows,
-// fp32 fused multiply-adds in slot order j = 0..k-1, one rounding at the end.  Each lane owns
-// 8 consecutive columns per step (two 16-byte loads per slot).  KC >= k bounds the slots.
-// `cpu` chunks per work unit: kCombChunks, or 32 (one step per lane) for small batches,
+// Combine: out[t] = bf16( sum_j gate[t,j] * y[pos[t,j]] ) over the bf16 expert-output rows
+// (the BF16 combine payload of the report translation, section 1.4), fp32 fused multiply-adds
+// in slot order j = 0..k-1, one rounding at the end.  Each lane owns 8 consecutive columns per
+// step (one 16-byte load per slot).  KC >= k bounds the slots.
+// `cpu` chunks per work unit: kCombChunks, or 64 (one iteration per lane) for small batches,
 // whose few units would otherwise leave each warp several dependent load rounds.
 template <int KC>
-__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ y,
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y,
                                                       const float* __restrict__ gate,
                                                       const int32_t* __restrict__ pos,
                                                       int64_t T, int k, int d, int cpu,
@@ -734,27 +735,42 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
       rows[j] = __shfl_sync(0xFFFFFFFFu, row, j);
       gs[j] = __shfl_sync(0xFFFFFFFFu, g, j);
     }
+    // two column steps (c and c + 32) per iteration: every slot's two 16-byte loads are in
+    // flight together
 #pragma unroll 1
-    for (int c = c0 + lane; c < c0 + cpu && c < n8; c += 32) {
-      float acc[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+    for (int c = c0 + lane; c < c0 + cpu && c < n8; c += 64) {
+      const bool two = c + 32 < c0 + cpu && c + 32 < n8;
+      uint4 v[2][KC];
 #pragma unroll
       for (int j = 0; j < KC; ++j)
         if (j < k) {
-          const float4* src = y + (static_cast<int64_t>(rows[j]) * n8 + c) * 2;
-          const float4 a = __ldg(src), b = __ldg(src + 1);
-          acc[0] = __fmaf_rn(gs[j], a.x, acc[0]);
-          acc[1] = __fmaf_rn(gs[j], a.y, acc[1]);
-          acc[2] = __fmaf_rn(gs[j], a.z, acc[2]);
-          acc[3] = __fmaf_rn(gs[j], a.w, acc[3]);
-          acc[4] = __fmaf_rn(gs[j], b.x, acc[4]);
-          acc[5] = __fmaf_rn(gs[j], b.y, acc[5]);
-          acc[6] = __fmaf_rn(gs[j], b.z, acc[6]);
-          acc[7] = __fmaf_rn(gs[j], b.w, acc[7]);
+          const uint4* src = y + static_cast<int64_t>(rows[j]) * n8 + c;
+          v[0][j] = __ldg(src);
+          if (two) v[1][j] = __ldg(src + 32);
         }
-      st_v4(out + t * n8 + c, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        if (s2 == 1 && !two) break;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KC; ++j)
+          if (j < k) {
+            const uint4 u = v[s2][j];
+            acc[0] = __fmaf_rn(gs[j], bf16lo(u.x), acc[0]);
+            acc[1] = __fmaf_rn(gs[j], bf16hi(u.x), acc[1]);
+            acc[2] = __fmaf_rn(gs[j], bf16lo(u.y), acc[2]);
+            acc[3] = __fmaf_rn(gs[j], bf16hi(u.y), acc[3]);
+            acc[4] = __fmaf_rn(gs[j], bf16lo(u.z), acc[4]);
+            acc[5] = __fmaf_rn(gs[j], bf16hi(u.z), acc[5]);
+            acc[6] = __fmaf_rn(gs[j], bf16lo(u.w), acc[6]);
+            acc[7] = __fmaf_rn(gs[j], bf16hi(u.w), acc[7]);
+          }
+        st_v4(out + t * n8 + c + 32 * s2,
+              make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+      }
     }
   }
 }
@@ -805,7 +821,7 @@ __global__ void __launch_bounds__(256) combine_f32_kernel(const float4* __restri
 // dlogits[t, e_j] = g_j (dgate_j - sum_i g_i dgate_i), 0 for unselected experts.
 template <int KC>
 __global__ void __launch_bounds__(256) bwd_gate_rows_kernel(
-    const uint4* __restrict__ dy, const float4* __restrict__ y, const float* __restrict__ gate,
+    const uint4* __restrict__ dy, const uint4* __restrict__ y, const float* __restrict__ gate,
     const int32_t* __restrict__ pos, int64_t T, int k, int d, uint4* __restrict__ dO,
     float* __restrict__ part) {
   griddep_wait();  // the previous kernel in the stream has finished (PDL)
@@ -844,9 +860,9 @@ __global__ void __launch_bounds__(256) bwd_gate_rows_kernel(
 #pragma unroll
       for (int j = 0; j < KC; ++j)
         if (j < k) {
-          const float4* ys = y + (static_cast<int64_t>(rows[j]) * n8 + c) * 2;
-          const float4 ya = __ldg(ys), yb = __ldg(ys + 1);
-          const float yf[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+          const uint4 yv = __ldg(y + static_cast<int64_t>(rows[j]) * n8 + c);  // bf16 row
+          const float yf[8] = {bf16lo(yv.x), bf16hi(yv.x), bf16lo(yv.y), bf16hi(yv.y),
+                               bf16lo(yv.z), bf16hi(yv.z), bf16lo(yv.w), bf16hi(yv.w)};
 #pragma unroll
           for (int q = 0; q < 8; ++q) dot[j] = __fmaf_rn(yf[q], dyf[q], dot[j]);
           uint4 o;
@@ -942,14 +958,15 @@ int unit_grid(K kern, int64_t units) {
               : KERNEL<16>(__VA_ARGS__))
 
 template <int KC>
-cudaError_t launch_combine_kc(const float* y_rows, const float* gate, const int32_t* pos,
+cudaError_t launch_combine_kc(const uint16_t* y_rows, const float* gate, const int32_t* pos,
                               int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
-  // one step per lane while the units do not fill the GPU's warps a few times over
-  const int64_t small_units = T * ((d / 8 + 31) / 32);
-  const int cpu = small_units <= 8192 ? 32 : kCombChunks;
+  // one iteration per lane (two column steps) while the units do not fill the GPU's warps a
+  // few times over
+  const int64_t small_units = T * ((d / 8 + 63) / 64);
+  const int cpu = small_units <= 8192 ? 64 : kCombChunks;
   const int64_t units = T * ((d / 8 + cpu - 1) / cpu);
   return launch_pdl(combine_kernel<KC>, dim3(unit_grid(combine_kernel<KC>, units)), dim3(256), 0,
-                    s, reinterpret_cast<const float4*>(y_rows), gate, pos, T, k, d, cpu,
+                    s, reinterpret_cast<const uint4*>(y_rows), gate, pos, T, k, d, cpu,
                     reinterpret_cast<uint4*>(out));
 }
 template <int KC>
@@ -961,13 +978,13 @@ cudaError_t launch_combine_f32_kc(const float* rows, const int32_t* pos, int64_t
                     reinterpret_cast<uint4*>(out));
 }
 template <int KC>
-cudaError_t launch_bwd_gate_kc(const uint16_t* dy, const float* y_rows, const float* gate,
+cudaError_t launch_bwd_gate_kc(const uint16_t* dy, const uint16_t* y_rows, const float* gate,
                                const int32_t* pos, int64_t T, int k, int d, uint16_t* dO_rows,
                                float* part, cudaStream_t s) {
   const int64_t units = T * ((d / 8 + kCombChunks - 1) / kCombChunks);
   return launch_pdl(bwd_gate_rows_kernel<KC>, dim3(unit_grid(bwd_gate_rows_kernel<KC>, units)),
                     dim3(256), 0, s, reinterpret_cast<const uint4*>(dy),
-                    reinterpret_cast<const float4*>(y_rows), gate, pos, T, k, d,
+                    reinterpret_cast<const uint4*>(y_rows), gate, pos, T, k, d,
                     reinterpret_cast<uint4*>(dO_rows), part);
 }
 
@@ -1080,13 +1097,13 @@ cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, i
                     reinterpret_cast<uint4*>(rows), row_bytes / 16);
 }
 
-cudaError_t launch_combine(const float* y_rows, const float* gate, const int32_t* pos,
+cudaError_t launch_combine(const uint16_t* y_rows, const float* gate, const int32_t* pos,
                            int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   return MOE_DISPATCH_KC(k, launch_combine_kc, y_rows, gate, pos, T, k, d, out, s);
 }
 
-cudaError_t launch_bwd_gate(const uint16_t* dy, const float* y_rows, const float* gate,
+cudaError_t launch_bwd_gate(const uint16_t* dy, const uint16_t* y_rows, const float* gate,
                             const int32_t* pos, const int32_t* topk, int64_t T, int k, int d,
                             int E, uint16_t* dO_rows, float* dgate, float* dlogits, float* part,
                             cudaStream_t s) {

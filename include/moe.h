@@ -18,9 +18,9 @@
  *     fp32; slot j = 0..k-1 follows descending logit;
  *   - the permutation orders rows by (expert, token);
  *   - h = bf16(silu(x W1) * (x W3)) with silu(a) = a / (1 + exp(-a)); A = x W1 and B = x W3
- *     stay fp32; the expert outputs y_j = h W2 stay fp32 (on one GPU the combine reads them
- *     from HBM, so the pages' BF16 gather, a cross-GPU payload format, is not used) and are
- *     combined as out_t = bf16(sum_j gate[t,j] * y_j), an fp32 accumulation in slot order.
+ *     stay fp32; the expert outputs y_j = bf16(h W2) are bf16 rows (the BF16 combine payload
+ *     of the report translation, section 1.4), combined as
+ *     out_t = bf16(sum_j gate[t,j] * y_j), an fp32 accumulation in slot order.
  *
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller, row-major, 16-byte
@@ -233,7 +233,7 @@ moe_status_t moe_forward_host_pipelined(const moe_bf16_t* x_host, const float* l
  *   dx      [T,d]        bf16 : sum over slots j (in slot order, fp32) of dA W1^T + dB W3^T
  *   dW1,dW3 [E,d,d_ff]   fp32 : sum over the rows of each expert of x^T dA (resp. x^T dB)
  *   dW2     [E,d_ff,d]   fp32 : sum over the rows of each expert of h^T dO
- *   dgate   [T,k]        fp32 : <y_j, dy_t> with y_j the fp32 expert output
+ *   dgate   [T,k]        fp32 : <y_j, dy_t> with y_j the bf16 expert output row
  *   dlogits [T,E]        fp32 : gradient through the top-k softmax (0 for unselected
  *                               experts); may be NULL
  * with dO = gate * dy, dH = dO W2^T, dA = dH * B * silu'(A), dB = dH * silu(A) (without the

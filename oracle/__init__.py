@@ -51,11 +51,12 @@ def _load():
         lib.oracle_sum_bound.restype = ctypes.c_double
         lib.oracle_sum_bound.argtypes = [_p, _i64, ctypes.c_double, _p]
         lib.oracle_forward_tokens_flip_bf16.argtypes = [_p] * 5 + dims + [_p, _p, _i64, _p, _p]
+        lib.oracle_forward_tokens_fp8_flip.argtypes = [_p] * 5 + dims + [_p, _p, _i64, _p, _p]
         lib.oracle_backward_tokens_flip_bf16.argtypes = \
             [_p] * 6 + dims + [_int, _p, _p, _i64] + [_p] * 6
         lib.oracle_backward_dw_flip_bf16.argtypes = \
             [_p] * 6 + dims + [_int, _p, _p, _int] + [_p] * 6
-        lib.oracle_pair_operands_bf16.argtypes = [_p] * 6 + dims + [_i64, _int] + [_p] * 12
+        lib.oracle_pair_operands_bf16.argtypes = [_p] * 6 + dims + [_i64, _int] + [_p] * 14
         _lib = lib
     return _lib
 
@@ -271,10 +272,27 @@ def sum_bound(t, acc=FLIP_MODEL[0]):
     return s.value, b
 
 
+def forward_tokens_fp8_flip(inp, k, tokens=None, model=None):
+    """forward_tokens_fp8 (h and the output rows rounded) plus the rounding-flip allowance of
+    each output element, as forward_tokens_flip: returns (y [n,d], ay [n,d])."""
+    x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
+    x, W1, W3, W2 = (_prep(a, "bf16") for a in (x, W1, W3, W2))
+    tok = None if tokens is None else _c(tokens, np.int64)
+    n = T if tok is None else len(tok)
+    y = np.empty((n, d), np.float64)
+    ay = np.empty((n, d), np.float64)
+    m = _model(model)
+    _check(_load().oracle_forward_tokens_fp8_flip(
+        _ptr(x), _ptr(l64), _ptr(W1), _ptr(W3), _ptr(W2), T, d, E, k, dff, _ptr(m), _ptr(tok),
+        n, _ptr(y), _ptr(ay)))
+    return y, ay
+
+
 def forward_tokens_flip(inp, k, tokens=None, model=None):
-    """forward_tokens (h rounded, bf16 inputs) plus the rounding-flip allowance of each output
-    element: returns (y [n,d], ay [n,d]), ay the largest change that h values which may round
-    the other way in fp32 arithmetic can cause in that element."""
+    """forward_tokens (h and the output rows rounded, bf16 inputs) plus the rounding-flip
+    allowance of each output element: returns (y [n,d], ay [n,d]), ay the largest change that
+    output-row values which may round the other way in fp32 arithmetic (taking in the h values
+    that may) can cause in that element."""
     x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
     x, W1, W3, W2 = (_prep(a, "bf16") for a in (x, W1, W3, W2))
     tok = None if tokens is None else _c(tokens, np.int64)
@@ -326,12 +344,13 @@ def backward_dw_flip(inp, dy, k, experts, round_h=True, model=None):
 
 def pair_operands(inp, dy, k, t, j, model=None):
     """The bf16 operands of token t's slot-j pair and their flip intervals (test support): a
-    dict with e, g, h, vh (h before rounding), dO, da, db, and Dh, DdO, Dda, Ddb of shape
-    [n, 2]: the signed interval (lo <= 0 <= hi) within which another rounding may lie."""
+    dict with e, g, h, vh (h before rounding), dO, da, db, o (the bf16 output row), and Dh,
+    DdO, Dda, Ddb, Do of shape [n, 2]: the signed interval (lo <= 0 <= hi) within which
+    another rounding may lie."""
     x, l64, W1, W3, W2, T, d, E, dff = _unpack(inp)
     x, W1, W3, W2, dy = (_prep(a, "bf16") for a in (x, W1, W3, W2, dy))
-    names = ("h", "vh", "Dh", "dO", "DdO", "da", "Dda", "db", "Ddb")
-    sizes = (dff, dff, (dff, 2), d, (d, 2), dff, (dff, 2), dff, (dff, 2))
+    names = ("h", "vh", "Dh", "dO", "DdO", "da", "Dda", "db", "Ddb", "o", "Do")
+    sizes = (dff, dff, (dff, 2), d, (d, 2), dff, (dff, 2), dff, (dff, 2), d, (d, 2))
     r = {nm: np.empty(sz, np.float64) for nm, sz in zip(names, sizes)}
     e = ctypes.c_int(0)
     g = ctypes.c_double(0.0)

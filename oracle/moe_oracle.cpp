@@ -26,6 +26,9 @@
 //  * stable permute: permuted rows are ordered by (expert, token).
 //  * SwiGLU: h = silu(x W1) * (x W3), silu(a) = a / (1 + exp(-a)); h is rounded to bf16
 //    (round to nearest, ties to even) before the down projection when round_h != 0.
+//  * expert output rows: with round_h != 0 each row o = h W2 is rounded to bf16 as well (the
+//    BF16 combine payload of the report translation, section 1.4), and the combine and the
+//    gate gradient read those bf16 rows.
 //  * cheap activation (no W3 given): h = relu(x W1)^2, squared ReLU, an element-wise function
 //    with neither exponential nor division; h rounded to bf16 as above.
 //  * combine: y_t = sum_j g_j * o_j, here in fp64.
@@ -39,7 +42,7 @@
 //    matrix-product operands dO = g dy, da and db are rounded to bf16 (round to nearest
 //    even) like h, each product accumulating exactly (fp64).
 //  * rounding-flip allowance (a test bound, not part of the layer): both the oracle and an
-//    fp32 implementation round h, dO, da and db to bf16, but from pre-rounding values that
+//    fp32 implementation round h, o, dO, da and db to bf16, but from pre-rounding values that
 //    differ by the fp32 implementation's own rounding errors, so an operand whose value lies
 //    near a bf16 rounding midpoint may round to the neighbouring bf16 value there.  For each
 //    such operand the oracle computes, from its own fp64 values alone, the largest distance
@@ -140,15 +143,17 @@ void route_token(const double* l, int E, int k, int32_t* idx, double* gate) {
 }
 
 // One expert applied to one row x[0..d): a = x W1, b = x W3, h = silu(a) * b, o = h W2;
-// without W3 (W3e null) the cheap activation: h = relu(a)^2 (b is left zero).
-// W1e, W3e are [d][dff] and W2e is [dff][d], row-major.
+// without W3 (W3e null) the cheap activation: h = relu(a)^2 (b is left zero).  With round_h,
+// h and o are rounded to bf16.  W1e, W3e are [d][dff] and W2e is [dff][d], row-major.
 // Optional by-products of ffn_row for the rounding-flip allowance: sa, sb = the sums of the
 // squared running partial sums of a and b (in the order the loops below form a and b), and
-// vh = h before its bf16 rounding.
+// vh = h before its bf16 rounding; so, vo = the same for o (null: not traced).
 struct FwdTrace {
   double* sa;
   double* sb;
   double* vh;
+  double* so = nullptr;
+  double* vo = nullptr;
 };
 
 template <class V>
@@ -179,9 +184,16 @@ void ffn_row(const V* x, const V* W1e, const V* W3e, const V* W2e, int d, int df
     h[f] = round_h ? round_bf16(hv) : hv;
   }
   for (int c = 0; c < d; ++c) o[c] = 0.0;
+  const bool tro = tr && tr->so;
+  if (tro) for (int c = 0; c < d; ++c) tr->so[c] = 0.0;
   for (int f = 0; f < dff; ++f) {
     const V* w2 = W2e + static_cast<int64_t>(f) * d;
     for (int c = 0; c < d; ++c) o[c] += h[f] * widen(w2[c]);
+    if (tro) for (int c = 0; c < d; ++c) tr->so[c] += o[c] * o[c];
+  }
+  for (int c = 0; c < d; ++c) {
+    if (tr && tr->vo) tr->vo[c] = o[c];
+    if (round_h) o[c] = round_bf16(o[c]);
   }
 }
 
@@ -318,6 +330,23 @@ void h_flip_bounds(int dff, bool gated, const double* a, const double* b, const 
   }
 }
 
+// Flip intervals of the pair's bf16 output row o = bf16(h W2): Do [d].  The other
+// implementation's pre-rounding o differs from the oracle's by its fp32 accumulation error and
+// by every h flip times |W2| (its h is the oracle's up to those flips).
+template <class V>
+void o_flip_bounds(const V* W2e, int d, int dff, const FwdTrace& ft, const Dev* Dh,
+                   const FlipModel& M, Dev* Do) {
+  std::vector<double> dv(d);
+  for (int c = 0; c < d; ++c) dv[c] = M.acc * std::sqrt(ft.so[c]);
+  for (int f = 0; f < dff; ++f) {
+    const double m = Dh[f].mag();
+    if (m == 0.0) continue;
+    const V* w2 = W2e + static_cast<int64_t>(f) * d;
+    for (int c = 0; c < d; ++c) dv[c] += m * std::fabs(widen(w2[c]));
+  }
+  for (int c = 0; c < d; ++c) Do[c] = round_dev(ft.vo[c], dv[c]);
+}
+
 // Flip bounds of one token-expert pair: the signed intervals within which the other
 // implementation's bf16 rounding of each operand lies around the oracle's.  In: the pair's
 // gate g and dy [d]; the forward's a, b [dff] and their trace; the backward's dh [dff] and its
@@ -381,8 +410,9 @@ bool dims_ok(int64_t T, int d, int E, int k, int dff) {
 
 // Brute-force forward for a list of tokens: route each token, run its k experts on its own
 // row, sum gate-weighted outputs.  With a flip model M (round_h on), also the rounding-flip
-// allowance of each output element (ay [n,d]): the interval sum over j and f of
-// g_j W2[e_j][f][c] Dh_jf, reported as max(up, -down).
+// allowance of each output element (ay [n,d]): the interval sum over j of g_j Do_jc, the flip
+// interval of the pair's bf16 output row (which takes in the h flips), reported as
+// max(up, -down).
 template <class V>
 int forward_tokens(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
                    const Dims& D, int round_h, const int64_t* tokens, int64_t n, double* y,
@@ -393,15 +423,15 @@ int forward_tokens(const V* x, const double* logits, const V* W1, const V* W3, c
   {
     std::vector<int32_t> idx(D.k);
     std::vector<double> gate(D.k), a(D.dff), b(D.dff), h(D.dff), o(D.d);
-    std::vector<double> sa, sb, vh, ydn, yup;
-    std::vector<Dev> Dh;
+    std::vector<double> sa, sb, vh, so, vo, ydn, yup;
+    std::vector<Dev> Dh, Do;
     if (M) {
       for (auto* v : {&sa, &sb, &vh}) v->assign(D.dff, 0.0);
-      ydn.assign(D.d, 0.0);
-      yup.assign(D.d, 0.0);
+      for (auto* v : {&so, &vo, &ydn, &yup}) v->assign(D.d, 0.0);
       Dh.resize(D.dff);
+      Do.resize(D.d);
     }
-    const FwdTrace ft{sa.data(), sb.data(), vh.data()};
+    const FwdTrace ft{sa.data(), sb.data(), vh.data(), so.data(), vo.data()};
 #pragma omp for schedule(dynamic, 1)
     for (int64_t i = 0; i < n; ++i) {
       const int64_t t = tokens ? tokens[i] : i;
@@ -421,12 +451,8 @@ int forward_tokens(const V* x, const double* logits, const V* W1, const V* W3, c
         for (int c = 0; c < D.d; ++c) yt[c] += gate[j] * o[c];
         if (!M) continue;
         h_flip_bounds(D.dff, W3 != nullptr, a.data(), b.data(), ft, *M, Dh.data());
-        const V* W2e = w2of(W2, D, e);
-        for (int f = 0; f < D.dff; ++f) {
-          if (Dh[f].mag() == 0.0) continue;
-          const V* w2 = W2e + static_cast<int64_t>(f) * D.d;
-          for (int c = 0; c < D.d; ++c) add_scaled(gate[j] * widen(w2[c]), Dh[f], &ydn[c], &yup[c]);
-        }
+        o_flip_bounds(w2of(W2, D, e), D.d, D.dff, ft, Dh.data(), *M, Do.data());
+        for (int c = 0; c < D.d; ++c) add_scaled(gate[j], Do[c], &ydn[c], &yup[c]);
       }
       if (M && ay)
         for (int c = 0; c < D.d; ++c) ay[i * D.d + c] = std::fmax(yup[c], -ydn[c]);
@@ -508,8 +534,8 @@ int forward_permuted(const V* x, const double* logits, const V* W1, const V* W3,
 // (adx [n,d], adg [n,k], adl [n,E]; null pointers skip one): the largest |change| of the
 // output when every flagged operand takes any value of its deviation interval, namely
 //   dx_t[c]:   sum_j sum_f W1[e_j][c][f] Dda_jf + W3[e_j][c][f] Ddb_jf,
-//   dgate_tj:  sum_f m_jf Dh_jf with m_jf = sum_c W2[e_j][f][c] dy_t[c] (the multiplier of
-//              h_f in <h W2, dy>),
+//   dgate_tj:  sum_c dy_t[c] Do_jc (dgate reads the pair's bf16 output row o, whose flip
+//              interval Do takes in the h flips),
 //   dl_{e_j}:  sum_i c_ji dgate_ti, c_jj = g_j (1 - g_j), c_ji = -g_j g_i,
 // each evaluated as an interval sum and reported as max(up, -down).
 template <class V, class G>
@@ -526,11 +552,14 @@ int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, 
     std::vector<double> gate(D.k), a(D.dff), b(D.dff), h(D.dff), o(D.d), dyv(D.d), dO(D.d),
         dh(D.dff), da(D.dff), db(D.dff), dxp(D.d);
     // flip-allowance work arrays
-    std::vector<double> sa, sb, vh, sdh, vda, vdb, xdn, xup, gdn, gup;
-    std::vector<Dev> Dh, DdO, Dda, Ddb;
+    std::vector<double> sa, sb, vh, so, vo, sdh, vda, vdb, xdn, xup, gdn, gup;
+    std::vector<Dev> Dh, Do, DdO, Dda, Ddb;
     std::vector<int> live;
     if (M) {
       for (auto* v : {&sa, &sb, &vh, &sdh, &vda, &vdb}) v->assign(D.dff, 0.0);
+      so.assign(D.d, 0.0);
+      vo.assign(D.d, 0.0);
+      Do.resize(D.d);
       Dh.resize(D.dff);
       Dda.resize(D.dff);
       Ddb.resize(D.dff);
@@ -540,7 +569,7 @@ int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, 
       gdn.assign(D.k, 0.0);
       gup.assign(D.k, 0.0);
     }
-    const FwdTrace ft{sa.data(), sb.data(), vh.data()};
+    const FwdTrace ft{sa.data(), sb.data(), vh.data(), so.data(), vo.data()};
     const BwdTrace bt{sdh.data(), vda.data(), vdb.data()};
 #pragma omp for schedule(dynamic, 1)
     for (int64_t i = 0; i < n; ++i) {
@@ -585,13 +614,8 @@ int backward_tokens(const V* x, const double* logits, const V* W1, const V* W3, 
           }
         }
         gdn[j] = gup[j] = 0.0;
-        for (int f = 0; f < D.dff; ++f) {
-          if (Dh[f].mag() == 0.0) continue;
-          const V* w2 = W2e + static_cast<int64_t>(f) * D.d;
-          double m = 0.0;
-          for (int c = 0; c < D.d; ++c) m += widen(w2[c]) * dyv[c];
-          add_scaled(m, Dh[f], &gdn[j], &gup[j]);
-        }
+        o_flip_bounds(W2e, D.d, D.dff, ft, Dh.data(), *M, Do.data());
+        for (int c = 0; c < D.d; ++c) add_scaled(dyv[c], Do[c], &gdn[j], &gup[j]);
       }
       if (dgate) for (int j = 0; j < D.k; ++j) dgate[i * D.k + j] = dg[j];
       if (dlogits) {
@@ -778,24 +802,29 @@ template <class V>
 int pair_operands(const V* x, const double* logits, const V* W1, const V* W3, const V* W2,
                   const V* dy, const Dims& D, int64_t t, int j, const FlipModel& M, int* e_out,
                   double* g_out, double* h, double* vh, double* Dh, double* dO, double* DdO,
-                  double* da, double* Dda, double* db, double* Ddb) {
+                  double* da, double* Dda, double* db, double* Ddb, double* o, double* Do) {
   if (t < 0 || t >= D.T || j < 0 || j >= D.k) return -1;
   std::vector<int32_t> idx(D.k);
-  std::vector<double> gate(D.k), a(D.dff), b(D.dff), o(D.d), dyv(D.d), dh(D.dff), dxp(D.d),
-      sa(D.dff), sb(D.dff), sdh(D.dff), vda(D.dff), vdb(D.dff);
-  std::vector<Dev> ih(D.dff), io(D.d), ia(D.dff), ib(D.dff);
+  std::vector<double> gate(D.k), a(D.dff), b(D.dff), dyv(D.d), dh(D.dff), dxp(D.d),
+      sa(D.dff), sb(D.dff), so(D.d), vo(D.d), sdh(D.dff), vda(D.dff), vdb(D.dff);
+  std::vector<Dev> ih(D.dff), io(D.d), ia(D.dff), ib(D.dff), iy(D.d);
   route_token(logits + t * D.E, D.E, D.k, idx.data(), gate.data());
   const int e = idx[j];
-  const FwdTrace ft{sa.data(), sb.data(), vh};
+  const FwdTrace ft{sa.data(), sb.data(), vh, so.data(), vo.data()};
   const BwdTrace bt{sdh.data(), vda.data(), vdb.data()};
   ffn_row(x + t * D.d, w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, 1, a.data(),
-          b.data(), h, o.data(), &ft);
+          b.data(), h, o, &ft);
   for (int c = 0; c < D.d; ++c) dyv[c] = widen(dy[t * D.d + c]);
   double dg;
   ffn_row_bwd(w13(W1, D, e), w13(W3, D, e), w2of(W2, D, e), D.d, D.dff, gate[j], dyv.data(),
-              a.data(), b.data(), o.data(), 1, &dg, dO, dh.data(), da, db, dxp.data(), &bt);
+              a.data(), b.data(), o, 1, &dg, dO, dh.data(), da, db, dxp.data(), &bt);
   pair_flip_bounds(w2of(W2, D, e), D.d, D.dff, W3 != nullptr, gate[j], dyv.data(), a.data(),
                    b.data(), ft, dh.data(), bt, M, ih.data(), io.data(), ia.data(), ib.data());
+  o_flip_bounds(w2of(W2, D, e), D.d, D.dff, ft, ih.data(), M, iy.data());
+  for (int c = 0; c < D.d; ++c) {
+    Do[2 * c] = iy[c].lo;
+    Do[2 * c + 1] = iy[c].hi;
+  }
   for (int f = 0; f < D.dff; ++f) {
     Dh[2 * f] = ih[f].lo;
     Dh[2 * f + 1] = ih[f].hi;
@@ -853,10 +882,15 @@ void column_scales(const uint16_t* W, int E, int K, int N, double* s) {
 }
 
 // Forward with the FP8 dispatch payload: each token's row and the first projections' weights
-// quantized as above (weights quantized where they are used), SwiGLU, bf16 h, bf16 W2.
+// quantized as above (weights quantized where they are used), SwiGLU, bf16 h, bf16 W2, and
+// (round_h) the bf16 output row, as in ffn_row.  With a flip model M (round_h on), also the
+// rounding-flip allowance of each output element (ay [n,d]), as in forward_tokens: a and b
+// are the sums of the dequantized products, traced like ffn_row's.
 int forward_tokens_fp8(const uint16_t* x, const double* logits, const uint16_t* W1,
                        const uint16_t* W3, const uint16_t* W2, const Dims& D, int round_h,
-                       const int64_t* tokens, int64_t n, double* y) {
+                       const int64_t* tokens, int64_t n, double* y,
+                       const FlipModel* M = nullptr, double* ay = nullptr) {
+  if (M && !round_h) return -1;
   std::vector<double> s1(static_cast<size_t>(D.E) * D.dff), s3(s1.size());
   column_scales(W1, D.E, D.d, D.dff, s1.data());
   column_scales(W3, D.E, D.d, D.dff, s3.data());
@@ -865,6 +899,9 @@ int forward_tokens_fp8(const uint16_t* x, const double* logits, const uint16_t* 
   {
     std::vector<int32_t> idx(D.k);
     std::vector<double> gate(D.k), xq(D.d), a(D.dff), b(D.dff), h(D.dff), o(D.d);
+    std::vector<double> sa(D.dff), sb(D.dff), vh(D.dff), so(D.d), vo(D.d), ydn(D.d), yup(D.d);
+    std::vector<Dev> Dh(D.dff), Do(D.d);
+    const FwdTrace ft{sa.data(), sb.data(), vh.data(), so.data(), vo.data()};
     double st;
 #pragma omp for schedule(dynamic, 1)
     for (int64_t i = 0; i < n; ++i) {
@@ -877,14 +914,14 @@ int forward_tokens_fp8(const uint16_t* x, const double* logits, const uint16_t* 
       quantize_rows(x + t * D.d, 1, D.d, xq.data(), &st);
       route_token(logits + t * D.E, D.E, D.k, idx.data(), gate.data());
       double* yt = y + i * D.d;
-      for (int c = 0; c < D.d; ++c) yt[c] = 0.0;
+      for (int c = 0; c < D.d; ++c) yt[c] = ydn[c] = yup[c] = 0.0;
       for (int j = 0; j < D.k; ++j) {
         const int e = idx[j];
         const uint16_t* w1 = w13(W1, D, e);
         const uint16_t* w3 = w13(W3, D, e);
         const double* s1e = s1.data() + static_cast<int64_t>(e) * D.dff;
         const double* s3e = s3.data() + static_cast<int64_t>(e) * D.dff;
-        for (int f = 0; f < D.dff; ++f) { a[f] = 0.0; b[f] = 0.0; }
+        for (int f = 0; f < D.dff; ++f) { a[f] = 0.0; b[f] = 0.0; sa[f] = 0.0; sb[f] = 0.0; }
         for (int c = 0; c < D.d; ++c) {
           const uint16_t* r1 = w1 + static_cast<int64_t>(c) * D.dff;
           const uint16_t* r3 = w3 + static_cast<int64_t>(c) * D.dff;
@@ -892,17 +929,34 @@ int forward_tokens_fp8(const uint16_t* x, const double* logits, const uint16_t* 
             a[f] += xq[c] * (e4m3_quant(widen(r1[f]), s1e[f]) * s1e[f]);
             b[f] += xq[c] * (e4m3_quant(widen(r3[f]), s3e[f]) * s3e[f]);
           }
+          if (M)
+            for (int f = 0; f < D.dff; ++f) {
+              sa[f] += a[f] * a[f];
+              sb[f] += b[f] * b[f];
+            }
         }
         for (int f = 0; f < D.dff; ++f) {
           const double hv = a[f] / (1.0 + std::exp(-a[f])) * b[f];
+          vh[f] = hv;
           h[f] = round_h ? round_bf16(hv) : hv;
         }
         const uint16_t* w2 = w2of(W2, D, e);
-        for (int c = 0; c < D.d; ++c) o[c] = 0.0;
-        for (int f = 0; f < D.dff; ++f)
+        for (int c = 0; c < D.d; ++c) o[c] = so[c] = 0.0;
+        for (int f = 0; f < D.dff; ++f) {
           for (int c = 0; c < D.d; ++c) o[c] += h[f] * widen(w2[static_cast<int64_t>(f) * D.d + c]);
-        for (int c = 0; c < D.d; ++c) yt[c] += gate[j] * o[c];
+          if (M) for (int c = 0; c < D.d; ++c) so[c] += o[c] * o[c];
+        }
+        for (int c = 0; c < D.d; ++c) {
+          vo[c] = o[c];
+          yt[c] += gate[j] * (round_h ? round_bf16(o[c]) : o[c]);
+        }
+        if (!M) continue;
+        h_flip_bounds(D.dff, true, a.data(), b.data(), ft, *M, Dh.data());
+        o_flip_bounds(w2, D.d, D.dff, ft, Dh.data(), *M, Do.data());
+        for (int c = 0; c < D.d; ++c) add_scaled(gate[j], Do[c], &ydn[c], &yup[c]);
       }
+      if (M && ay)
+        for (int c = 0; c < D.d; ++c) ay[i * D.d + c] = std::fmax(yup[c], -ydn[c]);
     }
   }
   return bad ? -1 : 0;
@@ -1061,11 +1115,12 @@ int oracle_pair_operands_bf16(const uint16_t* x, const double* logits, const uin
                               const uint16_t* W3, const uint16_t* W2, const uint16_t* dy,
                               ORACLE_DIMS, int64_t t, int j, const double* model, int* e_out,
                               double* g_out, double* h, double* vh, double* Dh, double* dO,
-                              double* DdO, double* da, double* Dda, double* db, double* Ddb) {
+                              double* DdO, double* da, double* Dda, double* db, double* Ddb,
+                              double* o, double* Do) {
   if (!dims_ok(T, d, E, k, dff) || !model) return -1;
   const FlipModel M{model[0], model[1], model[2]};
   return pair_operands(x, logits, W1, W3, W2, dy, Dims{T, d, E, k, dff}, t, j, M, e_out, g_out,
-                       h, vh, Dh, dO, DdO, da, Dda, db, Ddb);
+                       h, vh, Dh, dO, DdO, da, Dda, db, Ddb, o, Do);
 }
 
 int oracle_forward_tokens_fp8(const uint16_t* x, const double* logits, const uint16_t* W1,
@@ -1073,6 +1128,17 @@ int oracle_forward_tokens_fp8(const uint16_t* x, const double* logits, const uin
                               const int64_t* tokens, int64_t n, double* y) {
   if (!dims_ok(T, d, E, k, dff) || !W3) return -1;
   return forward_tokens_fp8(x, logits, W1, W3, W2, Dims{T, d, E, k, dff}, round_h, tokens, n, y);
+}
+
+// forward_tokens_fp8 (h and the output rows rounded) with its rounding-flip allowance ay [n,d]
+int oracle_forward_tokens_fp8_flip(const uint16_t* x, const double* logits, const uint16_t* W1,
+                                   const uint16_t* W3, const uint16_t* W2, ORACLE_DIMS,
+                                   const double* model, const int64_t* tokens, int64_t n,
+                                   double* y, double* ay) {
+  if (!dims_ok(T, d, E, k, dff) || !W3 || !model) return -1;
+  const FlipModel M{model[0], model[1], model[2]};
+  return forward_tokens_fp8(x, logits, W1, W3, W2, Dims{T, d, E, k, dff}, 1, tokens, n, y, &M,
+                            ay);
 }
 
 }  // extern "C"

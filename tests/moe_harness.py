@@ -25,8 +25,9 @@ def assert_close(got, ref, what, rtol=RTOL, atol=ATOL):
 
 def assert_close_flip(got, ref, allow, what, rtol=RTOL, atol=ATOL):
     """The stated bound, widened element by element by the oracle's rounding-flip allowance
-    (oracle.backward_tokens_flip / backward_dw_flip): both sides round h, dO, da and db to
-    bf16, and an operand whose pre-rounding value lies near a bf16 rounding midpoint may
+    (oracle.forward_tokens_flip, backward_tokens_flip, ...): both sides round h, the expert
+    output rows, dO, da and db to bf16, and an operand whose pre-rounding value lies near a
+    bf16 rounding midpoint may
     round the other way on the GPU (its value comes from fp32 accumulation, the oracle's from
     fp64).  `allow` is, per element, the largest change those operands can cause there,
     computed from oracle values alone.  Returns how many elements needed it."""
@@ -47,8 +48,8 @@ def assert_close_flip(got, ref, allow, what, rtol=RTOL, atol=ATOL):
 
 def check_forward(out, npi, k, what, tokens=None):
     """Layer output (rows `tokens` of the batch, or all) against the oracle: the stated bound
-    plus the oracle's per-element rounding-flip allowance of h.  Returns how many elements
-    needed the allowance."""
+    plus the oracle's per-element rounding-flip allowance of h and the bf16 expert output
+    rows.  Returns how many elements needed the allowance."""
     import oracle
     y, ay = oracle.forward_tokens_flip(npi, k, tokens=tokens)
     got = np_of(out) if tokens is None else np_of(out)[tokens]

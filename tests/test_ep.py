@@ -102,7 +102,7 @@ def _rank_main(rank, R, port, shape, q):
                     n = counts_all[s, e0 + i]
                     a, b = plan["recv_off"][i, s], plan["src_off"][i, s]
                     recv[a:a + n] = allx[s][b:b + n]
-        # 3: the experts on the received rows (fp64 outputs, as the GPU keeps fp32 rows)
+        # 3: the experts on the received rows (the oracle's bf16 output rows, held as fp64)
         y_recv = np.zeros((plan["rows"], d))
         for i in range(nloc):
             a, n = plan["recv_off"][i, 0], plan["recv_counts"][i]

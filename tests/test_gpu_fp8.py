@@ -1,6 +1,7 @@
 """The FP8 dispatch payload on the GPU against the oracle: the E4M3 weight copies and their
-scales bitwise, the forward within the stated tolerance, batch invariance and run-to-run
-determinism bitwise, and CTA-pair vs single-CTA schedules bitwise."""
+scales bitwise, the forward within the stated tolerance plus the oracle's rounding-flip
+allowance of the bf16 h and output rows, batch invariance and run-to-run determinism bitwise,
+and CTA-pair vs single-CTA schedules bitwise."""
 import os
 import subprocess
 import sys
@@ -11,7 +12,7 @@ import torch
 
 import moe_synth
 import oracle
-from moe_harness import assert_close, np_of, sample_tokens, to_dev
+from moe_harness import assert_close_flip, np_of, sample_tokens, to_dev
 
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -60,8 +61,8 @@ def test_fp8_forward_matches_oracle(moe, T, d, E, k, dff):
     inp = moe_synth.generate(w)
     out, ws = _fp8_forward(moe, to_dev(inp), k)
     assert moe.moe_get_error(ws) == 0
-    ref = oracle.forward_tokens_fp8(moe_synth.to_numpy(inp), k)
-    assert_close(np_of(out), ref, "out (fp8)")
+    ref, allow = oracle.forward_tokens_fp8_flip(moe_synth.to_numpy(inp), k)
+    assert_close_flip(np_of(out), ref, allow, "out (fp8)")
 
 
 def test_fp8_batch_invariance_and_determinism(moe):
@@ -113,8 +114,8 @@ def test_fp8_large_workload_sampled(moe):
     assert moe.moe_get_error(ws) == 0
     npi = moe_synth.to_numpy(g)
     tok = sample_tokens(w.T, 6, seed=5)
-    ref = oracle.forward_tokens_fp8(npi, w.k, tokens=tok)
-    assert_close(np_of(out)[tok], ref, "out (fp8, large workload, sampled tokens)")
+    ref, allow = oracle.forward_tokens_fp8_flip(npi, w.k, tokens=tok)
+    assert_close_flip(np_of(out)[tok], ref, allow, "out (fp8, large workload, sampled tokens)")
 
 
 @pytest.mark.parametrize("T", [5, 200])   # single dispatch launch for moe_forward / five kernels

@@ -170,10 +170,12 @@ def test_k1_single_expert_is_dense_swiglu_mlp():
     h = _silu(X @ W1) * (X @ W3)
     np.testing.assert_allclose(oracle.forward_tokens(inp, 1, round_h=False), h @ W2,
                                rtol=1e-12, atol=1e-13)
-    # rounding h to bf16 (h is a float64 here; rounding via float32 first can only differ
-    # on exact float32 ties, which this random draw does not produce)
+    # rounding h, then the expert's output row, to bf16 (the BF16 combine payload); with one
+    # expert and k = 1 the gate is 1 and the output is that row (the values are float64 here;
+    # rounding via float32 first can only differ on exact float32 ties, which this random draw
+    # does not produce)
     y = oracle.forward_tokens(inp, 1, round_h=True)
-    np.testing.assert_allclose(y, _torch_bf16(h) @ W2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(y, _torch_bf16(_torch_bf16(h) @ W2))
 
 
 def test_k_equals_E_is_softmax_weighted_dense_sum():
@@ -353,8 +355,8 @@ def test_cheap_activation_k1_single_expert_is_dense_relu2_mlp():
     assert (X @ W1 < 0).any() and (X @ W1 > 0).any()      # both sides of the kink occur
     np.testing.assert_allclose(oracle.forward_tokens(inp, 1, round_h=False), h @ W2,
                                rtol=1e-12, atol=1e-13)
-    np.testing.assert_allclose(oracle.forward_tokens(inp, 1, round_h=True), _torch_bf16(h) @ W2,
-                               rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(oracle.forward_tokens(inp, 1, round_h=True),
+                                  _torch_bf16(_torch_bf16(h) @ W2))
 
 
 def test_cheap_activation_k_equals_E_and_permuted_forward():
@@ -489,8 +491,9 @@ def test_fp8_forward_k1_single_expert_is_dense_mlp_on_dequantized_values():
     h = _silu(xq @ W1) * (xq @ W3)
     np.testing.assert_allclose(oracle.forward_tokens_fp8(inp, 1, round_h=False), h @ W2,
                                rtol=1e-12, atol=1e-13)
-    np.testing.assert_allclose(oracle.forward_tokens_fp8(inp, 1), _torch_bf16(h) @ W2,
-                               rtol=1e-12, atol=1e-13)
+    # bf16 h, then the bf16 output row (gate 1 with one expert and k = 1)
+    np.testing.assert_array_equal(oracle.forward_tokens_fp8(inp, 1),
+                                  _torch_bf16(_torch_bf16(h) @ W2))
 
 
 def test_fp8_forward_equals_bf16_forward_when_quantization_is_exact():

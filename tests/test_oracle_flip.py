@@ -1,7 +1,8 @@
 """Pins of the oracle's rounding-flip allowance (CPU only).
 
-The oracle and an fp32 implementation both round h, dO = g dy, da and db to bf16, from
-pre-rounding values that differ by the fp32 implementation's own rounding errors.  The oracle
+The oracle and an fp32 implementation both round h, the expert output rows o = h W2 (the
+combine's bf16 payload), dO = g dy, da and db to bf16, from pre-rounding values that differ by
+the fp32 implementation's own rounding errors (and, for o, by the flips of h).  The oracle
 bounds, from its fp64 values alone, how far the two roundings of each operand can lie apart
 (a model of fp32 arithmetic: a probabilistic accumulation bound and an element-wise
 evaluation bound), and turns that into an allowance for every gradient element.  These tests
@@ -115,7 +116,8 @@ def test_sum_bound_covers_real_fp32_sums():
 
 def _emulate_fp32(inp, dy, k, gated):
     """The layer in float32 arithmetic with products accumulated in order (as a tensor core
-    with fp32 accumulation would, up to the order), h, dO, da, db rounded to bf16 by torch."""
+    with fp32 accumulation would, up to the order), h, the output rows Y, dO, da, db rounded
+    to bf16 by torch."""
     x = _bits_to_f64(inp["x"]).astype(F32)
     W1 = _bits_to_f64(inp["W1"]).astype(F32)
     W3 = _bits_to_f64(inp["W3"]).astype(F32) if gated else None
@@ -150,6 +152,7 @@ def _emulate_fp32(inp, dy, k, gated):
     Y = np.zeros((P, d), F32)
     for f in range(dff):
         Y += h[:, f:f + 1] * W2[ep, f, :]
+    Y = _bf16_round32(Y)
     dyp = dyf[tok]
     dO = _bf16_round32(g.reshape(-1)[:, None] * dyp)
     dH = np.zeros((P, dff), F32)
@@ -186,8 +189,8 @@ def _emulate_fp32(inp, dy, k, gated):
     out = np.zeros((T, d), F32)
     for j in range(k):
         out += g[:, j:j + 1] * Y[j::k]
-    return dict(h=h, dO=dO, da=da, db=db, dx=dx, dgate=dgate.reshape(T, k), dW1=dW1, dW3=dW3,
-                dW2=dW2, idx=idx, out=out)
+    return dict(h=h, o=Y, dO=dO, da=da, db=db, dx=dx, dgate=dgate.reshape(T, k), dW1=dW1,
+                dW3=dW3, dW2=dW2, idx=idx, out=out)
 
 
 def _within(got, ref, allow, what):
@@ -204,14 +207,15 @@ def test_fp32_emulation_flips_only_where_allowed(gated):
     dff = 256
     inp, dy = _inputs(11 if gated else 12, T, d, E, k, dff, gated)
     emu = _emulate_fp32(inp, dy, k, gated)
-    flips = {"h": 0, "dO": 0, "da": 0, "db": 0}
+    flips = {"h": 0, "o": 0, "dO": 0, "da": 0, "db": 0}
     unflagged_flips_without_model = 0
     for t in range(T):
         for j in range(k):
             op = oracle.pair_operands(inp, dy, k, t, j)
             off = oracle.pair_operands(inp, dy, k, t, j, model=(0.0, 0.0, 0.0))
             p = t * k + j
-            for name, D in (("h", "Dh"), ("dO", "DdO"), ("da", "Dda"), ("db", "Ddb")):
+            for name, D in (("h", "Dh"), ("o", "Do"), ("dO", "DdO"), ("da", "Dda"),
+                            ("db", "Ddb")):
                 diff = emu[name][p].astype(np.float64) - op[name]
                 lo, hi = op[D][:, 0], op[D][:, 1]
                 assert (lo <= 0).all() and (hi >= 0).all()
@@ -320,7 +324,7 @@ def test_extreme_operand_choices_stay_inside_the_allowance(gated):
             h, dO = o["h"] + choose(o["Dh"]), o["dO"] + choose(o["DdO"])
             da, db = o["da"] + choose(o["Dda"]), o["db"] + choose(o["Ddb"])
             pdx[t] += W1[e] @ da + (W3[e] @ db if gated else 0.0)
-            pdg[t, j] = (h @ W2[e]) @ dyf[t]
+            pdg[t, j] = (o["o"] + choose(o["Do"])) @ dyf[t]   # dgate reads the bf16 output row
             pW1[e] += np.outer(x[t], da)
             if gated:
                 pW3[e] += np.outer(x[t], db)
@@ -330,20 +334,26 @@ def test_extreme_operand_choices_stay_inside_the_allowance(gated):
     def random_end(D):
         return np.where(rng.random(len(D)) < 0.5, D[:, 0], D[:, 1])
 
-    # forward: out = sum_j g_j (h_j W2[e_j]); only the h flips move it
+    # forward: out = sum_j g_j o_j with o_j the bf16 output row; its flip interval Do takes in
+    # the h flips (any h choice moves the pre-rounding row by at most sum_f |W2| |Dh|)
     y, ay = oracle.forward_tokens_flip(inp, k, model=model)
     for trial in range(6):
         py = np.zeros((T, d))
         for (t, j), o in ops.items():
-            py[t] += o["g"] * ((o["h"] + random_end(o["Dh"])) @ W2[o["e"]])
+            py[t] += o["g"] * (o["o"] + random_end(o["Do"]))
         assert (np.abs(py - y) <= ay + slack).all()
+    for (t, j), o in ops.items():   # the h flips' reach stays inside the row's interval
+        hb = o["h"] + random_end(o["Dh"])
+        pre = hb @ W2[o["e"]]
+        assert (np.abs(pre - (o["h"] @ W2[o["e"]])) <= np.abs(W2[o["e"]]).T @ np.maximum(
+            -o["Dh"][:, 0], o["Dh"][:, 1]) + slack).all()
     t, c = 4, 9
     up = dn = 0.0
     for j in range(k):
         o = ops[(t, j)]
-        prod = (o["g"] * W2[o["e"]][:, c])[:, None] * o["Dh"]
-        up += prod.max(axis=1).sum()
-        dn += prod.min(axis=1).sum()
+        prod = o["g"] * o["Do"][c]
+        up += prod.max()
+        dn += prod.min()
     assert math.isclose(max(up, -dn), ay[t, c], rel_tol=1e-12, abs_tol=1e-15)
 
     for trial in range(6):
@@ -368,12 +378,46 @@ def test_extreme_operand_choices_stay_inside_the_allowance(gated):
                 up += prod.max(axis=1).sum()
                 dn += prod.min(axis=1).sum()
         assert math.isclose(max(up, -dn), adx[t, c], rel_tol=1e-12, abs_tol=1e-15)
-    # attainment for dgate[t, j]: the multiplier of h_f is (W2 dy)_f
+    # attainment for dgate[t, j]: the multiplier of o_c is dy_t[c]
     for t, j in ((1, 0), (7, 1)):
         o = ops[(t, j)]
-        m = W2[o["e"]] @ dyf[t]
-        prod = m[:, None] * o["Dh"]
+        prod = dyf[t][:, None] * o["Do"]
         want = max(prod.max(axis=1).sum(), -prod.min(axis=1).sum())
         assert math.isclose(want, adg[t, j], rel_tol=1e-12, abs_tol=1e-15)
     # dlogits: a linear map of the dgate intervals through the softmax Jacobian
     assert (adl >= 0).all() and (adl[dlog == 0] == 0).all()
+
+
+def test_fp8_forward_allowance_values_and_zero_model():
+    # the FP8 forward's allowance comes with values equal to the plain FP8 forward; a model that
+    # allows nothing gives none; an fp32 emulation of the FP8 expert (dequantized operands,
+    # fp32 sums, torch's bf16 rounding of h and the output rows) stays inside it
+    inp, _ = _inputs(31, 20, 256, 4, 2, 256)
+    y0 = oracle.forward_tokens_fp8(inp, 2)
+    y, ay = oracle.forward_tokens_fp8_flip(inp, 2)
+    assert np.array_equal(y0, y)
+    _, az = oracle.forward_tokens_fp8_flip(inp, 2, model=(0.0, 0.0, 0.0))
+    assert not az.any()
+    xq, _ = oracle.quantize_rows_e4m3(inp["x"])
+    q1, s1 = oracle.quantize_cols_e4m3(inp["W1"])
+    q3, s3 = oracle.quantize_cols_e4m3(inp["W3"])
+    W2 = _bits_to_f64(inp["W2"]).astype(F32)
+    idx, g = oracle.route(inp["logits"], 2)
+    out = np.zeros(y.shape, F32)
+    for t in range(y.shape[0]):
+        for j in range(2):
+            e = idx[t, j]
+            W1 = (q1[e] * s1[e][None, :]).astype(F32)
+            W3 = (q3[e] * s3[e][None, :]).astype(F32)
+            xr = xq[t].astype(F32)
+            A = np.zeros(W1.shape[1], F32)
+            B = np.zeros(W1.shape[1], F32)
+            for c in range(xr.shape[0]):
+                A += xr[c] * W1[c]
+                B += xr[c] * W3[c]
+            h = _bf16_round32((A / (F32(1) + np.exp(-A))) * B)
+            o = np.zeros(W2.shape[2], F32)
+            for f in range(h.shape[0]):
+                o += h[f] * W2[e, f]
+            out[t] += F32(g[t, j]) * _bf16_round32(o)
+    _within(out, y, ay, "out (fp8 emulation)")
