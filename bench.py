@@ -536,8 +536,8 @@ def bench_native(args, w):
                      "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peaks["source"],
                      "frac_of_sustained": g1_tflops / peaks["bf16_sustained"],
                      # DRAM bytes of one full-size launch are not captured (over the
-                     # capture-size rule) and do not scale with the units; a skewed
-                     # T=8192 d=4096 E=64 capture read 1.28x its algorithmic bytes
+                     # capture-size rule) and do not scale with the units; skewed
+                     # T=8192 d=4096 E=64 captures read 1.28-1.45x their algorithmic bytes
                      "traffic": None},
         "stages_ms": stages,
         "gemm_tflops": g_tflops,
