@@ -847,31 +847,47 @@ __global__ void __launch_bounds__(256) bwd_gate_rows_kernel(
       gs[j] = __shfl_sync(0xFFFFFFFFu, g, j);
       dot[j] = 0.0f;
     }
+    // two column steps (c and c + 32) per iteration: their dy and bf16 row loads are in
+    // flight together; each slot's dot product still adds step c, then step c + 32
 #pragma unroll 1
-    for (int c = c0 + lane; c < c0 + kCombChunks && c < n8; c += 32) {
-      const uint4 dv = ld_nc_v4(dy + t * n8 + c);
-      const uint32_t du[4] = {dv.x, dv.y, dv.z, dv.w};
-      float dyf[8];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        dyf[2 * q] = bf16lo(du[q]);
-        dyf[2 * q + 1] = bf16hi(du[q]);
-      }
+    for (int c = c0 + lane; c < c0 + kCombChunks && c < n8; c += 64) {
+      const bool two = c + 32 < c0 + kCombChunks && c + 32 < n8;
+      uint4 dv[2], yv[2][KC];
+      dv[0] = ld_nc_v4(dy + t * n8 + c);
+      if (two) dv[1] = ld_nc_v4(dy + t * n8 + c + 32);
 #pragma unroll
       for (int j = 0; j < KC; ++j)
         if (j < k) {
-          const uint4 yv = __ldg(y + static_cast<int64_t>(rows[j]) * n8 + c);  // bf16 row
-          const float yf[8] = {bf16lo(yv.x), bf16hi(yv.x), bf16lo(yv.y), bf16hi(yv.y),
-                               bf16lo(yv.z), bf16hi(yv.z), bf16lo(yv.w), bf16hi(yv.w)};
-#pragma unroll
-          for (int q = 0; q < 8; ++q) dot[j] = __fmaf_rn(yf[q], dyf[q], dot[j]);
-          uint4 o;
-          o.x = pack_bf16x2(gs[j] * dyf[0], gs[j] * dyf[1]);
-          o.y = pack_bf16x2(gs[j] * dyf[2], gs[j] * dyf[3]);
-          o.z = pack_bf16x2(gs[j] * dyf[4], gs[j] * dyf[5]);
-          o.w = pack_bf16x2(gs[j] * dyf[6], gs[j] * dyf[7]);
-          st_v4(dO + static_cast<int64_t>(rows[j]) * n8 + c, o);
+          const uint4* src = y + static_cast<int64_t>(rows[j]) * n8 + c;  // bf16 row
+          yv[0][j] = __ldg(src);
+          if (two) yv[1][j] = __ldg(src + 32);
         }
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        if (s2 == 1 && !two) break;
+        const uint32_t du[4] = {dv[s2].x, dv[s2].y, dv[s2].z, dv[s2].w};
+        float dyf[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          dyf[2 * q] = bf16lo(du[q]);
+          dyf[2 * q + 1] = bf16hi(du[q]);
+        }
+#pragma unroll
+        for (int j = 0; j < KC; ++j)
+          if (j < k) {
+            const uint4 u4 = yv[s2][j];
+            const float yf[8] = {bf16lo(u4.x), bf16hi(u4.x), bf16lo(u4.y), bf16hi(u4.y),
+                                 bf16lo(u4.z), bf16hi(u4.z), bf16lo(u4.w), bf16hi(u4.w)};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) dot[j] = __fmaf_rn(yf[q], dyf[q], dot[j]);
+            uint4 o;
+            o.x = pack_bf16x2(gs[j] * dyf[0], gs[j] * dyf[1]);
+            o.y = pack_bf16x2(gs[j] * dyf[2], gs[j] * dyf[3]);
+            o.z = pack_bf16x2(gs[j] * dyf[4], gs[j] * dyf[5]);
+            o.w = pack_bf16x2(gs[j] * dyf[6], gs[j] * dyf[7]);
+            st_v4(dO + static_cast<int64_t>(rows[j]) * n8 + c + 32 * s2, o);
+          }
+      }
     }
     float mine = 0.0f;
 #pragma unroll
