@@ -266,6 +266,17 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, i
 
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
 
+// What the forward saves for the backward's dH epilogue, per h element: the multipliers of dh
+// in dA = dh * b silu'(a) and dB = dh * silu(a), with silu'(a) = s (1 + a (1 - s)) and
+// s = sigmoid(a); without the gate projection dA = dh * 2 relu(a).  The backward then needs one
+// multiply per output instead of an exp and a division.
+__device__ __forceinline__ void swiglu_bwd_mults(float a, float b, float* ma, float* mb) {
+  const float sg = 1.0f / (1.0f + expf(-a));
+  *ma = b * (sg * (1.0f + a * (1.0f - sg)));
+  *mb = a * sg;
+}
+__device__ __forceinline__ float relu2_bwd_mult(float a) { return 2.0f * fmaxf(a, 0.0f); }
+
 __device__ __forceinline__ void st_zero32(void* p) {  // 32 bytes of zeros
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   st_v4(p, z);
@@ -454,6 +465,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
         }
         store_chunk<true>(buf, h, H + ch * 64, 2ll * p.dff, nstore, lane);
         if (p.save_ab) {
+          // dA's multiplier 2 relu(a)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = relu2_bwd_mult(a[i]);
           char* SA = reinterpret_cast<char*>(p.save_a + row0 * p.dff + ti.n0 + ch * 32);
           store_chunk<false>(buf, a, SA, 4ll * p.dff, nsave, lane);
         }
@@ -487,6 +501,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       for (int i = 0; i < 32; ++i) h[i] = valid ? silu_f(a[i]) * b[i] : 0.0f;
       store_chunk<true>(buf, h, H + ch * 64, 2ll * p.dff, nstore, lane);
       if (p.save_ab) {
+        // dA's and dB's multipliers b silu'(a) and silu(a), in place of a and b
+#pragma unroll
+        for (int i = 0; i < 32; ++i) swiglu_bwd_mults(a[i], b[i], &a[i], &b[i]);
         char* SA = reinterpret_cast<char*>(p.save_a + row0 * p.dff + c0 + ch * 32);
         char* SB = reinterpret_cast<char*>(p.save_b + row0 * p.dff + c0 + ch * 32);
         store_chunk<false>(buf, a, SA, 4ll * p.dff, nsave, lane);
@@ -544,8 +561,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     }
   } else if constexpr (KIND == kDh) {
     // The warp puts its 32 x 32 chunk of dH through the padded shared buffer, then works row
-    // by row: 8 lanes per row read the row's saved A and B (16 bytes each, whole 128-byte
-    // lines), apply the SwiGLU backward and store dA and dB (8 bytes each).
+    // by row: 8 lanes per row read the row's saved multipliers of dA and dB (16 bytes each,
+    // whole 128-byte lines), multiply and store dA and dB (8 bytes each).
     const int64_t row0 = ti.row0 + w0;
     uint16_t* dA0 = static_cast<uint16_t*>(p.out0) + row0 * (2 * p.dff) + ti.n0;
     const float* sa0 = p.save_a + row0 * p.dff + ti.n0;
@@ -582,18 +599,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
                                  __uint_as_float(ua[i].z), __uint_as_float(ua[i].w)};
             const float bv[4] = {__uint_as_float(ub[i].x), __uint_as_float(ub[i].y),
                                  __uint_as_float(ub[i].z), __uint_as_float(ub[i].w)};
-            if (p.gated) {
+            // the forward saved dA's and dB's multipliers (b silu'(a) and silu(a), or
+            // 2 relu(a) without the gate projection) in place of a and b
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float g = buf[rr * 33 + c4 + q];
-                const float sg = 1.0f / (1.0f + expf(-av[q]));
-                da[q] = g * bv[q] * (sg * (1.0f + av[q] * (1.0f - sg)));
-                db[q] = g * (av[q] * sg);
-              }
-            } else {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)  // d relu(a)^2 / da = 2 relu(a)
-                da[q] = buf[rr * 33 + c4 + q] * (2.0f * fmaxf(av[q], 0.0f));
+            for (int q = 0; q < 4; ++q) {
+              const float g = buf[rr * 33 + c4 + q];
+              da[q] = g * av[q];
+              db[q] = g * bv[q];
             }
           }
           uint16_t* o = dA0 + rr * (2 * p.dff) + ch * 32 + c4;
@@ -674,20 +686,12 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
     if (p.gated) {
       const bool is_a = q < 2;
       const int col = ti.n0 + 64 * rank + 32 * (q & 1) + lane;  // h column of this lane
-      float* save = is_a ? p.save_a : p.save_b;
       const int bar = 1 + (q & 1);
       const int j0 = is_a ? 0 : 16;
 #pragma unroll 1
       for (int ch = 0; ch < nch; ++ch) {
         float v[32];
         tmem_ld32(tacc + ch * 32, v);
-        if (p.save_ab) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int r = ch * 32 + j;
-            if (r < ti.nvalid) save[(row0 + r) * p.dff + col] = v[j];
-          }
-        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) mine[lane * 33 + j] = v[j];
         named_bar_sync(bar, 64);
@@ -696,7 +700,16 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
         for (int jj = 0; jj < 16; ++jj) {
           const int j = j0 + jj;
           const float x0 = mine[lane * 33 + j], x1 = partner[lane * 33 + j];
-          hv[jj] = ch * 32 + j < ti.nvalid ? (is_a ? silu_f(x0) * x1 : silu_f(x1) * x0) : 0.0f;
+          const float av = is_a ? x0 : x1, bv = is_a ? x1 : x0;
+          const int r = ch * 32 + j;
+          hv[jj] = r < ti.nvalid ? silu_f(av) * bv : 0.0f;
+          if (p.save_ab && r < ti.nvalid) {
+            // dA's and dB's multipliers for the backward, of this warp's half of the rows
+            float ma, mb;
+            swiglu_bwd_mults(av, bv, &ma, &mb);
+            p.save_a[(row0 + r) * p.dff + col] = ma;
+            p.save_b[(row0 + r) * p.dff + col] = mb;
+          }
         }
         named_bar_sync(bar, 64);  // the partner has read `mine`
         // the warp's 16 rows x 32 h columns as bf16 through `mine` (row pitch 64 bytes), then
@@ -726,7 +739,8 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int r = ch * 32 + j;
-          if (p.save_ab && r < ti.nvalid) p.save_a[(row0 + r) * p.dff + col] = v[j];
+          if (p.save_ab && r < ti.nvalid)
+            p.save_a[(row0 + r) * p.dff + col] = relu2_bwd_mult(v[j]);  // dA's multiplier
           if (r < ti.nseg) {
             const float rl = fmaxf(v[j], 0.0f);
             H[(row0 + r) * p.dff + col] = bf16_bits(r < ti.nvalid ? rl * rl : 0.0f);

@@ -70,7 +70,9 @@ typedef enum moe_status {
 } moe_status_t;
 
 /* Flags of moe_forward. */
-#define MOE_FWD_SAVE_FOR_BACKWARD 1 /* keep A = x W1 and B = x W3 (fp32) in ws for moe_backward */
+#define MOE_FWD_SAVE_FOR_BACKWARD 1 /* keep, per h element, dA's and dB's multipliers b silu'(a)
+                                       * and silu(a) (fp32; 2 relu(a) without W3) in ws for
+                                       * moe_backward */
 #define MOE_FWD_FUSED_COMBINE 2     /* GEMM2 combines each token as soon as its k expert rows are
                                        written (the single-GPU form of the overlapped combine of
                                        waves); bitwise the same output as the default separate
