@@ -194,10 +194,21 @@ def fwd_launches(T, k, d, dff, save=False):
     return dispatch + gemms + 1
 
 
+def _backward_swap(T, k, d, dff):
+    # the library's rule for the backward's swapped dX GEMM (MOE_BWD_SWAP: "0" never, "1"
+    # always, else as the forward's swapped GEMMs); never with MOE_GEMM_PAIR "0"
+    mode = os.environ.get("MOE_BWD_SWAP", "")
+    if mode == "0" or os.environ.get("MOE_GEMM_PAIR", "") == "0":
+        return False
+    return mode == "1" or T <= 128 or _row_pairs(T, k, d, dff)
+
+
 def bwd_launches(T, k, d, dff):
     # gate grads (rows + per token), dO padding, dH (+ single-CTA tiles), dX (+ single-CTA
-    # tiles), dX combine, dW2, dW1/dW3
-    return 10 if _row_pairs(T, k, d, dff) else 8
+    # tiles, or one swapped launch), dX combine, dW2, dW1/dW3
+    pairs = _row_pairs(T, k, d, dff)
+    dx = 1 if _backward_swap(T, k, d, dff) or not pairs else 2
+    return 6 + (2 if pairs else 1) + dx
 
 
 def bench_fwd_bwd(moe, dev, steps, warmup, shape=None):

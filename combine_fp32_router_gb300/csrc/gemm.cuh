@@ -57,13 +57,20 @@ enum GemmKind : int {
   // block have stored theirs (a per-block counter), so GEMM2 of the first blocks runs while
   // GEMM1 of the last ones still computes, and one launch's ramp and tail serve both.
   kFwdT = 9,
+  // The backward's dX rows swapped the same way: the expert's W1 / W3 rows (d of them, 256
+  // per CTA pair) are the M operand, K-major as stored ([d][dff]: K = dff contiguous), and a
+  // block of up to 256 rows of [dA|dB] the N operand, so every expert runs on CTA pairs in
+  // one launch whatever its tile count.
+  kDxT = 10,    // dXp^T = [W1|W3] [dA|dB]^T (fp32 rows)                     (d x rows)
 };
 
 template <int KIND>
 struct KindTraits {
   static constexpr bool kRowsM = (KIND <= kDx || KIND == kFwd1F8);  // M = permuted rows
-  static constexpr bool kSwap = (KIND == kFwd1T || KIND == kFwd2T || KIND == kFwdT);  // N = rows
-  static constexpr int kAmn = (KIND == kDw2 || KIND == kDw13 || kSwap) ? 1 : 0;  // A MN-major?
+  static constexpr bool kSwap =
+      (KIND == kFwd1T || KIND == kFwd2T || KIND == kFwdT || KIND == kDxT);  // N = rows
+  static constexpr int kAmn =
+      (KIND == kDw2 || KIND == kDw13 || (kSwap && KIND != kDxT)) ? 1 : 0;  // A MN-major?
   static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8 || kSwap) ? 0 : 1;
 };
 
@@ -216,7 +223,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, i
     // a block of up to 256 rows of one expert x one block of weight columns: 128 h columns
     // (64 per CTA, each with its W1 and W3 column) for GEMM1, 256 without the gate
     // projection or for GEMM2 (128 per CTA)
-    int part = KIND == kFwd2T ? 2 : 1, t = tile, nbp = p.nb, nk = p.nkb;
+    // part: 1 GEMM1, 2 GEMM2, 3 the backward's dX
+    int part = KIND == kFwd2T ? 2 : (KIND == kDxT ? 3 : 1), t = tile, nbp = p.nb, nk = p.nkb;
     if constexpr (KIND == kFwdT) {
       const int n1 = p.n_st[0] * p.nb;  // GEMM1 tiles come first
       if (tile >= n1) {
@@ -673,6 +681,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 //    memory and each finishes half of the chunk's rows: h = bf16(silu(A) B).  Padding rows of
 //    the expert's segment get h = 0 (a later K-over-rows GEMM reads them).
 //  * kFwd1T without W3: h = bf16(relu(A)^2) over 128 W1 columns.
+//  * kDxT: fp32 dX rows over 128 d columns (as kFwd2T, columns past d are not stored).
 //  * kFwd2T: Y rows (bf16) over 128 W2 columns (columns past d, when d is not a multiple of
 //    256, are neither loaded as real data nor stored).
 template <int KIND>
@@ -681,6 +690,25 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
                                               const float* partner, int rank) {
   const int nch = (ti.nvalid + 31) / 32;
   const int64_t row0 = ti.row0;
+  if constexpr (KIND == kDxT) {
+    // fp32 dX rows over this CTA's 128 d columns: per chunk of 32 rows, each row's 32
+    // columns of the warp in one 128-byte store (lane = column)
+    const int col = ti.n0 + 128 * rank + 32 * q + lane;
+    const bool live = ti.n0 + 128 * rank < p.d;  // warp-uniform: d is a multiple of 128
+    float* X = static_cast<float*>(p.out0);
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+      float v[32];
+      tmem_ld32(tacc + ch * 32, v);
+      if (!live) continue;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int r = ch * 32 + j;
+        if (r < ti.nvalid) X[(row0 + r) * p.d + col] = v[j];
+      }
+    }
+    return;
+  }
   if (ti.part == 1) {
     uint16_t* H = static_cast<uint16_t*>(p.out0);
     if (p.gated) {
@@ -947,7 +975,14 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
         if constexpr (Tr::kSwap) {
           // A: this CTA's 128 weight columns as two 64-column boxes (MN-major); B: this CTA's
           // `box` rows of the block (K-major), by the tensor map of that box height
-          if (ti.part == 1) {
+          if constexpr (KIND == kDxT) {
+            // A: this CTA's 128 W1 (K < d_ff) or W3 rows, K-major: one box of 64 K x 128 rows;
+            // past d (d % 256 == 128) the rows belong to the next expert or are zero fill, and
+            // their results are not stored
+            const int wrow = ti.e * p.d + ti.n0 + 128 * rank;
+            if (k0 < p.dff) load_h(kL2HintB, sa, &mapB0, fb, k0, wrow);
+            else load_h(kL2HintB, sa, &mapB1, fb, k0 - p.dff, wrow);
+          } else if (ti.part == 1) {
             const int wrow = ti.e * p.d + k0;
             if (p.gated) {
               const int c0 = ti.n0 + 64 * rank;  // W1 columns -> lanes 0-63, W3 -> 64-127
@@ -1099,7 +1134,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
       tc_fence_after();
       const uint32_t dtm = tmem_base + acc * BN;
       // swapped kinds: M = 256 weight columns, N = the block's rows (2 box)
-      const uint32_t idesc = Tr::kSwap ? idesc_bf16_f32(2 * kBM, 2 * ti.box, 1, 0) : IDESC;
+      const uint32_t idesc = Tr::kSwap ? idesc_bf16_f32(2 * kBM, 2 * ti.box, Tr::kAmn, 0) : IDESC;
       for (int kb = 0; kb < ti.nk; ++kb) {
         const int s = fill % S;
         const uint32_t ph = (fill / S) & 1u;

@@ -5,6 +5,9 @@ namespace moe {
 
 GemmParams base_params(const GemmCtx& c);
 GemmParams leftover_params(const GemmParams& p, const GemmCtx& c);
+GemmParams swap_params(const GemmCtx& c);
+cudaError_t row_maps(GemmParams& p, const void* rows, uint64_t inner, uint64_t nrows,
+                     uint64_t row_bytes);
 
 namespace {
 template <int KIND>
@@ -66,6 +69,27 @@ cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s) {
   const GemmParams lo = leftover_params(p, c);
   if (BN == 256) return run_rows_kind<kDx, 256>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, c.num_sms, s);
   return run_rows_kind<kDx, 128>(c.pair, a, b0, b1, sb0, sb1, p, lo, L.max_mt, c.num_sms, s);
+}
+
+// dX rows with swapped operands: one CTA-pair launch over every (block of up to 256 rows,
+// 256 d columns), the M operand W1 / W3 rows (K-major, K = d_ff each), the N operand the
+// block's [dA|dB] rows.
+cudaError_t launch_gemm_dx_swap(const GemmCtx& c, cudaStream_t s) {
+  const WsLayout& L = *c.L;
+  cudaError_t st = cudaSuccess;
+  const uint64_t kdim = (c.gated ? 2ull : 1ull) * L.dff;
+  const uint16_t* w3 = c.gated ? c.W3 : c.W1;  // never read without the gate projection
+  // W1 / W3 viewed as [E d rows][dff]: boxes of 64 K columns x 128 rows
+  const CUtensorMap w1m = make_map_2d(c.W1, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 128, &st);
+  const CUtensorMap w3m = make_map_2d(w3, L.dff, static_cast<uint64_t>(L.E) * L.d, 2ull * L.dff, 64, 128, &st);
+  if (st != cudaSuccess) return st;
+  GemmParams p = swap_params(c);
+  st = row_maps(p, c.ws + L.dAB, kdim, L.P_pad, 4ull * L.dff);
+  if (st != cudaSuccess) return st;
+  p.nb = (L.d + 255) / 256;  // d % 256 == 128: the last block's second CTA has no columns
+  p.nkb = static_cast<int>(kdim / kBK);
+  p.out0 = c.ws + L.dXp;
+  return run_grouped_gemm<kDxT, 256, true>(w1m, w1m, w3m, p, L.max_mt * p.nb, c.num_sms, s);
 }
 
 cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s) {

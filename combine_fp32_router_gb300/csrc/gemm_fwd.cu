@@ -206,7 +206,6 @@ cudaError_t launch_gemm_fwd2(const GemmCtx& c, cudaStream_t s) {
 // Swapped forward GEMMs: one CTA-pair launch over every (row block, weight-column block).
 // The row operand has four tensor maps, with boxes of 16, 32, 64 and 128 rows: each CTA of a
 // pair loads half of the block's rows, rounded up to one of these.
-namespace {
 cudaError_t row_maps(GemmParams& p, const void* rows, uint64_t inner, uint64_t nrows,
                      uint64_t row_bytes) {
   cudaError_t st = cudaSuccess;
@@ -221,7 +220,6 @@ GemmParams swap_params(const GemmCtx& c) {
   p.st_row0 = reinterpret_cast<const int32_t*>(c.ws + c.L->st_row0);
   return p;
 }
-}  // namespace
 
 cudaError_t launch_gemm_fwd1_swap(const GemmCtx& c, cudaStream_t s) {
   const WsLayout& L = *c.L;

@@ -65,6 +65,22 @@ bool forward_swap(int64_t T, int k, int d, int dff) {
   return mode == 1 || T <= kTileRows || row_pairs(T, k, d, dff);
 }
 
+// The backward's dX GEMM with swapped operands (every expert on CTA pairs in one launch) by the
+// same rule as the forward's (measured on GB300: the fwd_bwd workload, T=8192, d=4096, E=128,
+// top-8, d_ff=1536, whose 5-tile experts otherwise run on single CTAs in a second launch).
+// MOE_BWD_SWAP="0" keeps the row-tile kernels, "1" swaps at every size; read once per process.
+// Bitwise the same dX rows either way.
+bool backward_swap(int64_t T, int k, int d, int dff) {
+  static const int mode = [] {
+    const char* e = std::getenv("MOE_BWD_SWAP");
+    if (e && e[0] == '0' && e[1] == 0) return 0;
+    if (e && e[0] == '1' && e[1] == 0) return 1;
+    return 2;
+  }();
+  if (mode == 0 || !use_pairs()) return false;
+  return mode == 1 || T <= kTileRows || row_pairs(T, k, d, dff);
+}
+
 // The swapped GEMMs as one persistent launch (GEMM2 of a row block after its GEMM1 tiles) for
 // T <= 64, where one launch's ramp and tail matter (measured on GB300: tiny 0.037 -> 0.034 ms,
 // T=1 at d=7168, E=256, top-8, d_ff=2048 0.158 -> 0.154 ms; T=8 and larger layers within
@@ -680,7 +696,8 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   c.gated = W3 != nullptr;
   MOE_TRY(launch_gemm_dh(c, stream));
   record(stage_events, 2, stream);
-  MOE_TRY(launch_gemm_dx(c, stream));
+  MOE_TRY(backward_swap(T, k, d, d_ff) ? launch_gemm_dx_swap(c, stream)
+                                       : launch_gemm_dx(c, stream));
   record(stage_events, 3, stream);
   MOE_TRY(launch_combine_f32(reinterpret_cast<const float*>(w + L.dXp), pos, T, k, d, dx,
                              stream));
