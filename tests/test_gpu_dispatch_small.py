@@ -50,6 +50,8 @@ def _scratch_end(E):
     (37, 384, 33, 3, 256),      # two logits per lane, ragged expert count
     (128, 256, 256, 8, 256),    # the largest batch of the single launch
     (100, 128, 1000, 16, 128),  # 32 logits per lane, the largest k
+    (90, 128, 100, 5, 128),     # 4 logits per lane
+    (33, 128, 300, 6, 128),     # 16 logits per lane
     (64, 256, 1, 1, 256),       # one expert
 ])
 @pytest.mark.parametrize("flags", [0, 1, 4])  # plain, save for backward, row gather
