@@ -203,12 +203,22 @@ def _backward_swap(T, k, d, dff):
     return mode == "1" or T <= 128 or _row_pairs(T, k, d, dff)
 
 
+def _backward_swap_dh(T, k, d, dff):
+    # the library's rule for the backward's swapped dH GEMM (MOE_BWD_DH_SWAP: "0" never, "1"
+    # always, else as the swapped dX); never with MOE_GEMM_PAIR "0"
+    mode = os.environ.get("MOE_BWD_DH_SWAP", "")
+    if mode == "0" or os.environ.get("MOE_GEMM_PAIR", "") == "0":
+        return False
+    return mode == "1" or _backward_swap(T, k, d, dff)
+
+
 def bwd_launches(T, k, d, dff):
-    # gate grads (rows + per token), dO padding, dH (+ single-CTA tiles), dX (+ single-CTA
+    # gate grads (rows + per token), dO padding, dH and dX (each: pair tiles + single-CTA
     # tiles, or one swapped launch), dX combine, dW2, dW1/dW3
     pairs = _row_pairs(T, k, d, dff)
+    dh = 1 if _backward_swap_dh(T, k, d, dff) or not pairs else 2
     dx = 1 if _backward_swap(T, k, d, dff) or not pairs else 2
-    return 6 + (2 if pairs else 1) + dx
+    return 6 + dh + dx
 
 
 def bench_fwd_bwd(moe, dev, steps, warmup, shape=None):

@@ -62,25 +62,28 @@ enum GemmKind : int {
   // block of up to 256 rows of [dA|dB] the N operand, so every expert runs on CTA pairs in
   // one launch whatever its tile count.
   kDxT = 10,    // dXp^T = [W1|W3] [dA|dB]^T (fp32 rows)                     (d x rows)
+  // and dH: the expert's W2 rows (d_ff of them, K = d contiguous) as the M operand, a block of
+  // dO rows as N; the epilogue applies the saved multipliers per (row, d_ff column)
+  kDhT = 11,    // dH^T = W2 dO^T -> dA, dB (bf16)                            (dff x rows)
 };
 
 template <int KIND>
 struct KindTraits {
   static constexpr bool kRowsM = (KIND <= kDx || KIND == kFwd1F8);  // M = permuted rows
-  static constexpr bool kSwap =
-      (KIND == kFwd1T || KIND == kFwd2T || KIND == kFwdT || KIND == kDxT);  // N = rows
+  static constexpr bool kSwap = (KIND == kFwd1T || KIND == kFwd2T || KIND == kFwdT ||
+                                 KIND == kDxT || KIND == kDhT);  // N = rows
   static constexpr int kAmn =
-      (KIND == kDw2 || KIND == kDw13 || (kSwap && KIND != kDxT)) ? 1 : 0;  // A MN-major?
+      (KIND == kDw2 || KIND == kDw13 || (kSwap && KIND != kDxT && KIND != kDhT)) ? 1 : 0;
   static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8 || kSwap) ? 0 : 1;
 };
 
-// Epilogue warps of a launch: 4, one per TMEM lane quadrant, or 8 for the dH pair launch,
-// whose epilogue (saved A and B read from HBM, SwiGLU backward with exp and division per
-// element) is slower than its MMAs with 4 warps; two warps then share a lane quadrant and
-// split the accumulator columns.
+// Epilogue warps of a launch: 4, one per TMEM lane quadrant, or 8 for the dH pair launches,
+// whose epilogue (the saved multipliers of dA and dB read from HBM, 12 bytes of traffic per
+// accumulator element) is slower than their MMAs with 4 warps; two warps then share a lane
+// quadrant and split the accumulator columns.
 template <int KIND, bool PAIR>
 struct EpiCfg {
-  static constexpr int kWarps = (KIND == kDh && PAIR) ? 8 : 4;
+  static constexpr int kWarps = ((KIND == kDh || KIND == kDhT) && PAIR) ? 8 : 4;
   static constexpr int kThreads = 128 + 32 * kWarps;  // + producer, MMA, TMEM, spare warps
 };
 
@@ -223,8 +226,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, i
     // a block of up to 256 rows of one expert x one block of weight columns: 128 h columns
     // (64 per CTA, each with its W1 and W3 column) for GEMM1, 256 without the gate
     // projection or for GEMM2 (128 per CTA)
-    // part: 1 GEMM1, 2 GEMM2, 3 the backward's dX
-    int part = KIND == kFwd2T ? 2 : (KIND == kDxT ? 3 : 1), t = tile, nbp = p.nb, nk = p.nkb;
+    // part: 1 GEMM1, 2 GEMM2, 3 the backward's dX, 4 its dH
+    int part = KIND == kFwd2T ? 2 : (KIND == kDxT ? 3 : (KIND == kDhT ? 4 : 1)), t = tile,
+        nbp = p.nb, nk = p.nkb;
     if constexpr (KIND == kFwdT) {
       const int n1 = p.n_st[0] * p.nb;  // GEMM1 tiles come first
       if (tile >= n1) {
@@ -682,14 +686,83 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 //    the expert's segment get h = 0 (a later K-over-rows GEMM reads them).
 //  * kFwd1T without W3: h = bf16(relu(A)^2) over 128 W1 columns.
 //  * kDxT: fp32 dX rows over 128 d columns (as kFwd2T, columns past d are not stored).
+//  * kDhT: dA and dB rows (bf16) over 128 d_ff columns; the two warps of a lane quadrant
+//    (`half` 0 and 1 of 2) take alternate 32-row chunks.
 //  * kFwd2T: Y rows (bf16) over 128 W2 columns (columns past d, when d is not a multiple of
 //    256, are neither loaded as real data nor stored).
 template <int KIND>
 __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInfo& ti,
                                               uint32_t tacc, int q, int lane, float* mine,
-                                              const float* partner, int rank) {
+                                              const float* partner, int rank, int half,
+                                              int nhalves) {
   const int nch = (ti.nvalid + 31) / 32;
   const int64_t row0 = ti.row0;
+  if constexpr (KIND == kDhT) {
+    // Each 32 x 32 chunk (lane = d_ff column, register = row) goes through `mine` transposed;
+    // then 8 lanes per row read the row's saved multipliers of dA and dB (16 bytes each, whole
+    // 128-byte lines), multiply and store 8 bytes of dA and of dB.  Padding rows of the
+    // expert's segment get zeros (dW1 / dW3 read them as K rows).
+    const int c0 = ti.n0 + 128 * rank + 32 * q;  // first d_ff column of this warp
+    if (c0 >= p.dff) return;  // warp-uniform: d_ff % 256 == 128, rank 1's last columns
+    uint16_t* dA0 = static_cast<uint16_t*>(p.out0) + row0 * (2 * p.dff) + c0;
+    const float* sa0 = p.save_a + row0 * p.dff + c0;
+    const float* sb0 = p.save_b + row0 * p.dff + c0;
+    const int rsub = lane >> 3, c4 = (lane & 7) * 4;
+#pragma unroll 1
+    for (int ch = half; ch < nch; ch += nhalves) {
+      const int nval = ti.nvalid - ch * 32, nstore = ti.nseg - ch * 32;  // may exceed 32
+      // all 16 loads of the chunk in flight first; the accumulator read and the shared
+      // transpose run under their latency
+      uint4 ua[8], ub[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int64_t r = ch * 32 + 4 * i + rsub;
+        ua[i] = ub[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (4 * i + rsub < nval) {
+          ua[i] = ld_v4(sa0 + r * p.dff + c4);
+          if (p.gated) ub[i] = ld_v4(sb0 + r * p.dff + c4);
+        }
+      }
+      float v[32];
+      tmem_ld32(tacc + ch * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) mine[j * 33 + lane] = v[j];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + rsub;
+        if (rr < nstore) {
+          // rows past the valid ones multiply zeros (their saved multipliers are not read)
+          const float av[4] = {__uint_as_float(ua[i].x), __uint_as_float(ua[i].y),
+                               __uint_as_float(ua[i].z), __uint_as_float(ua[i].w)};
+          const float bv[4] = {__uint_as_float(ub[i].x), __uint_as_float(ub[i].y),
+                               __uint_as_float(ub[i].z), __uint_as_float(ub[i].w)};
+          float da[4], db[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float g = mine[rr * 33 + c4 + u];
+            da[u] = rr < nval ? g * av[u] : 0.0f;
+            db[u] = rr < nval ? g * bv[u] : 0.0f;
+          }
+          uint16_t* o = dA0 + (ch * 32 + rr) * static_cast<int64_t>(2 * p.dff) + c4;
+          *reinterpret_cast<uint2*>(o) =
+              make_uint2(pack_bf16x2(da[0], da[1]), pack_bf16x2(da[2], da[3]));
+          if (p.gated)
+            *reinterpret_cast<uint2*>(o + p.dff) =
+                make_uint2(pack_bf16x2(db[0], db[1]), pack_bf16x2(db[2], db[3]));
+        }
+      }
+      __syncwarp();  // the stores' reads of `mine` are done before the next chunk rewrites it
+    }
+    // padding rows of the segment past the last chunk: 4 rows per instruction
+    const uint2 z = make_uint2(0u, 0u);
+    for (int r = nch * 32 + 4 * half + rsub; r < ti.nseg; r += 4 * nhalves) {
+      uint16_t* o = dA0 + r * static_cast<int64_t>(2 * p.dff) + c4;
+      *reinterpret_cast<uint2*>(o) = z;
+      if (p.gated) *reinterpret_cast<uint2*>(o + p.dff) = z;
+    }
+    return;
+  }
   if constexpr (KIND == kDxT) {
     // fp32 dX rows over this CTA's 128 d columns: per chunk of 32 rows, each row's 32
     // columns of the warp in one 128-byte store (lane = column)
@@ -982,6 +1055,10 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
             const int wrow = ti.e * p.d + ti.n0 + 128 * rank;
             if (k0 < p.dff) load_h(kL2HintB, sa, &mapB0, fb, k0, wrow);
             else load_h(kL2HintB, sa, &mapB1, fb, k0 - p.dff, wrow);
+          } else if constexpr (KIND == kDhT) {
+            // A: this CTA's 128 W2 rows (d_ff index), K-major (K = d): one box of 64 K x 128
+            // rows; past d_ff (d_ff % 256 == 128) as for kDxT
+            load_h(kL2HintB, sa, &mapB0, fb, k0, ti.e * p.dff + ti.n0 + 128 * rank);
           } else if (ti.part == 1) {
             const int wrow = ti.e * p.d + k0;
             if (p.gated) {
@@ -1221,7 +1298,8 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if constexpr (Tr::kSwap) {
         epilogue_swap<KIND>(p, ti, tacc, q, lane, epi_buf + ew * (Cfg::kEpiWarpBytes / 4),
-                            epi_buf + (ew ^ 2) * (Cfg::kEpiWarpBytes / 4), rank);
+                            epi_buf + (ew ^ 2) * (Cfg::kEpiWarpBytes / 4), rank, ew >> 2,
+                            EW / 4);
         if constexpr (KIND == kFwdT) {
           if (ti.part == 1) {
             // this CTA's H rows of the tile are stored: count them for the block's GEMM2

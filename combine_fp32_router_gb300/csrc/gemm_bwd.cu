@@ -92,6 +92,26 @@ cudaError_t launch_gemm_dx_swap(const GemmCtx& c, cudaStream_t s) {
   return run_grouped_gemm<kDxT, 256, true>(w1m, w1m, w3m, p, L.max_mt * p.nb, c.num_sms, s);
 }
 
+// dH with swapped operands: one CTA-pair launch over every (block of up to 256 rows, 256 d_ff
+// columns), the M operand W2 rows (K-major, K = d), the N operand the block's dO rows; the
+// epilogue applies the saved multipliers and writes dA and dB.
+cudaError_t launch_gemm_dh_swap(const GemmCtx& c, cudaStream_t s) {
+  const WsLayout& L = *c.L;
+  cudaError_t st = cudaSuccess;
+  // W2 viewed as [E dff rows][d]: boxes of 64 K columns x 128 rows
+  const CUtensorMap w2m = make_map_2d(c.W2, L.d, static_cast<uint64_t>(L.E) * L.dff, 2ull * L.d, 64, 128, &st);
+  if (st != cudaSuccess) return st;
+  GemmParams p = swap_params(c);
+  st = row_maps(p, c.ws + L.dO, L.d, L.P_pad, 2ull * L.d);
+  if (st != cudaSuccess) return st;
+  p.nb = (L.dff + 255) / 256;  // d_ff % 256 == 128: the last block's second CTA has no columns
+  p.nkb = L.d / kBK;
+  p.out0 = c.ws + L.dAB;
+  p.save_a = reinterpret_cast<float*>(c.ws + L.Asave);
+  p.save_b = reinterpret_cast<float*>(c.ws + L.Bsave);
+  return run_grouped_gemm<kDhT, 256, true>(w2m, w2m, w2m, p, L.max_mt * p.nb, c.num_sms, s);
+}
+
 cudaError_t launch_gemm_dw2(const GemmCtx& c, cudaStream_t s) {
   const WsLayout& L = *c.L;
   const int BN = (L.d % 256 == 0) ? 256 : 128;

@@ -128,6 +128,8 @@ cudaError_t launch_gemm_fwd2_swap(const GemmCtx& c, cudaStream_t s);
 // both swapped GEMMs in one persistent CTA-pair launch (GEMM2 of a block after its GEMM1)
 cudaError_t launch_gemm_fwd_fused(const GemmCtx& c, cudaStream_t s);
 cudaError_t launch_gemm_dh(const GemmCtx& c, cudaStream_t s);     // dA,dB from dO W2^T
+// the same with swapped operands (W2 rows x row blocks), CTA pairs, one launch
+cudaError_t launch_gemm_dh_swap(const GemmCtx& c, cudaStream_t s);
 cudaError_t launch_gemm_dx(const GemmCtx& c, cudaStream_t s);     // dXp = dA W1^T + dB W3^T
 // the same with swapped operands ([W1|W3] rows x row blocks), CTA pairs, one launch
 cudaError_t launch_gemm_dx_swap(const GemmCtx& c, cudaStream_t s);

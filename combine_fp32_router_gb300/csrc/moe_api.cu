@@ -81,6 +81,19 @@ bool backward_swap(int64_t T, int k, int d, int dff) {
   return mode == 1 || T <= kTileRows || row_pairs(T, k, d, dff);
 }
 
+// The backward's dH GEMM with swapped operands, by the same rule unless MOE_BWD_DH_SWAP ("0"
+// or "1") overrides it; read once per process.  Bitwise the same dA and dB rows either way.
+bool backward_swap_dh(int64_t T, int k, int d, int dff) {
+  static const int mode = [] {
+    const char* e = std::getenv("MOE_BWD_DH_SWAP");
+    if (e && e[0] == '0' && e[1] == 0) return 0;
+    if (e && e[0] == '1' && e[1] == 0) return 1;
+    return 2;
+  }();
+  if (mode == 0 || !use_pairs()) return false;
+  return mode == 1 || backward_swap(T, k, d, dff);
+}
+
 // The swapped GEMMs as one persistent launch (GEMM2 of a row block after its GEMM1 tiles) for
 // T <= 64, where one launch's ramp and tail matter (measured on GB300: tiny 0.037 -> 0.034 ms,
 // T=1 at d=7168, E=256, top-8, d_ff=2048 0.158 -> 0.154 ms; T=8 and larger layers within
@@ -694,7 +707,8 @@ moe_status_t moe_backward(const moe_bf16_t* dy, const moe_bf16_t* x, const float
   c.num_sms = num_sms_of_current_device();
   c.pair = row_pairs(T, k, d, d_ff);  // dH and dX: row-grouped like the forward
   c.gated = W3 != nullptr;
-  MOE_TRY(launch_gemm_dh(c, stream));
+  MOE_TRY(backward_swap_dh(T, k, d, d_ff) ? launch_gemm_dh_swap(c, stream)
+                                          : launch_gemm_dh(c, stream));
   record(stage_events, 2, stream);
   MOE_TRY(backward_swap(T, k, d, d_ff) ? launch_gemm_dx_swap(c, stream)
                                        : launch_gemm_dx(c, stream));

@@ -68,8 +68,12 @@ def test_pair_rule_and_launch_counts(bench, monkeypatch, mode, name, pairs):
     assert bench.fwd_launches(w.T, w.k, w.d, w.dff) == expect
     # saving for the backward adds the zeroing of the padding rows to the single dispatch
     assert bench.fwd_launches(w.T, w.k, w.d, w.dff, save=True) == expect + (1 if small else 0)
-    # the backward's dX runs swapped (one launch) wherever the forward's GEMMs would
+    # the backward's dH and dX run swapped (one launch each) wherever the forward's GEMMs
+    # would; MOE_BWD_DH_SWAP overrides the rule for dH alone
     monkeypatch.setenv("MOE_BWD_SWAP", "0")
     assert bench.bwd_launches(w.T, w.k, w.d, w.dff) == (10 if pairs else 8)
-    monkeypatch.delenv("MOE_BWD_SWAP")
+    monkeypatch.setenv("MOE_BWD_DH_SWAP", "1")
     assert bench.bwd_launches(w.T, w.k, w.d, w.dff) == (9 if pairs else 8)
+    monkeypatch.delenv("MOE_BWD_DH_SWAP")
+    monkeypatch.delenv("MOE_BWD_SWAP")
+    assert bench.bwd_launches(w.T, w.k, w.d, w.dff) == 8
