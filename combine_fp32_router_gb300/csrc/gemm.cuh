@@ -77,13 +77,15 @@ struct KindTraits {
   static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8 || kSwap) ? 0 : 1;
 };
 
-// Epilogue warps of a launch: 4, one per TMEM lane quadrant, or 8 for the dH pair launches,
-// whose epilogue (the saved multipliers of dA and dB read from HBM, 12 bytes of traffic per
-// accumulator element) is slower than their MMAs with 4 warps; two warps then share a lane
-// quadrant and split the accumulator columns.
+// Epilogue warps of a launch: 4, one per TMEM lane quadrant, or 8 for the row-tile dH pair
+// launch, whose epilogue (the saved multipliers of dA and dB read from HBM, 12 bytes of
+// traffic per accumulator element) is slower than its MMAs with 4 warps; two warps then share
+// a lane quadrant and split the accumulator columns.  (The swapped dH runs faster with 4
+// warps and the sixth stage they leave room for: measured on GB300, 0.697 -> 0.662 ms at the
+// fwd_bwd workload, T=8192, d=4096, E=128, top-8, d_ff=1536.)
 template <int KIND, bool PAIR>
 struct EpiCfg {
-  static constexpr int kWarps = ((KIND == kDh || KIND == kDhT) && PAIR) ? 8 : 4;
+  static constexpr int kWarps = (KIND == kDh && PAIR) ? 8 : 4;
   static constexpr int kThreads = 128 + 32 * kWarps;  // + producer, MMA, TMEM, spare warps
 };
 
@@ -686,8 +688,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
 //    the expert's segment get h = 0 (a later K-over-rows GEMM reads them).
 //  * kFwd1T without W3: h = bf16(relu(A)^2) over 128 W1 columns.
 //  * kDxT: fp32 dX rows over 128 d columns (as kFwd2T, columns past d are not stored).
-//  * kDhT: dA and dB rows (bf16) over 128 d_ff columns; the two warps of a lane quadrant
-//    (`half` 0 and 1 of 2) take alternate 32-row chunks.
+//  * kDhT: dA and dB rows (bf16) over 128 d_ff columns; where a launch runs two warps per lane
+//    quadrant, they take alternate 32-row chunks (`half` of `nhalves`).
 //  * kFwd2T: Y rows (bf16) over 128 W2 columns (columns past d, when d is not a multiple of
 //    256, are neither loaded as real data nor stored).
 template <int KIND>
