@@ -160,14 +160,21 @@ def _row_pairs(T, k, d, dff):
     return mode == "1" or T * k * d * dff >= 2 ** 37
 
 
+def _swap_size(T, k, d, dff):
+    # the library's size rule for the swapped-operand GEMMs: T <= 128, wherever row tiles
+    # would pair, and (unless MOE_GEMM_PAIR is set) from T k d d_ff >= 2^36
+    if T <= 128 or _row_pairs(T, k, d, dff):
+        return True
+    return os.environ.get("MOE_GEMM_PAIR", "") not in ("0", "1") and T * k * d * dff >= 2 ** 36
+
+
 def _forward_swap(T, k, d, dff):
     # the library's rule for the swapped forward GEMMs (MOE_FWD_SWAP: "0" never, "1" always,
-    # else T <= 128 or wherever the row-tile kernels would use CTA pairs); never with
-    # MOE_GEMM_PAIR "0"
+    # else the size rule); never with MOE_GEMM_PAIR "0"
     mode = os.environ.get("MOE_FWD_SWAP", "")
     if mode == "0" or os.environ.get("MOE_GEMM_PAIR", "") == "0":
         return False
-    return mode == "1" or T <= 128 or _row_pairs(T, k, d, dff)
+    return mode == "1" or _swap_size(T, k, d, dff)
 
 
 def _forward_fused(T, k, d, dff):
@@ -196,11 +203,11 @@ def fwd_launches(T, k, d, dff, save=False):
 
 def _backward_swap(T, k, d, dff):
     # the library's rule for the backward's swapped dX GEMM (MOE_BWD_SWAP: "0" never, "1"
-    # always, else as the forward's swapped GEMMs); never with MOE_GEMM_PAIR "0"
+    # always, else the forward's size rule); never with MOE_GEMM_PAIR "0"
     mode = os.environ.get("MOE_BWD_SWAP", "")
     if mode == "0" or os.environ.get("MOE_GEMM_PAIR", "") == "0":
         return False
-    return mode == "1" or T <= 128 or _row_pairs(T, k, d, dff)
+    return mode == "1" or _swap_size(T, k, d, dff)
 
 
 def _backward_swap_dh(T, k, d, dff):

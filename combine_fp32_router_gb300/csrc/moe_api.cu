@@ -46,14 +46,25 @@ bool row_pairs(int64_t T, int k, int d, int dff) {
   return pair_mode() == kPairsOn || work >= 137438953472.0;
 }
 
-// Forward GEMMs with swapped operands (weight columns x row blocks, one CTA-pair launch each)
-// for small batches (T <= 128) and wherever the row-tile kernels would use CTA pairs; the
-// row-tile kernels on single CTAs in between (measured on GB300: T=4096, d=2048, E=64, top-6,
-// d_ff=1024 runs 0.37 ms on single-CTA row tiles, 0.44 ms swapped; T=1..128 with d=7168,
-// E=256, top-8, d_ff=2048 runs 2-18% faster swapped; the T=16384 layer of the same shape
-// and T=8192, d=4096, E=128, top-8, d_ff=1536 1-2%).  MOE_FWD_SWAP="0" turns the swapped
-// kernels off, "1" uses them for every size; MOE_GEMM_PAIR="0" (single CTAs only) turns
-// them off too.  Read once per process; every choice gives bitwise the same rows.
+// The size rule of the swapped-operand kinds (weight columns or rows x row blocks, every expert
+// on CTA pairs in one launch): small batches (T <= 128), wherever the row-tile kernels would use
+// CTA pairs, and from T k d d_ff >= 2^36 (half the row-pair threshold).  Measured on GB300:
+//  * T=4096, d=2048, E=64, top-6, d_ff=1024 (5.2e10): forward 0.335 ms on single-CTA row
+//    tiles, 0.385 swapped;
+//  * T=1024, d=4096, E=64, top-8, d_ff=1536 (5.2e10): 0.508 / 0.512 ms;
+//  * T=2048, d=4096, E=32, top-8, d_ff=1536 (1.0e11): 0.551 / 0.528 ms, backward 1.200 / 1.139;
+//  * T=1..128 with d=7168, E=256, top-8, d_ff=2048: 2-18% faster swapped; the T=16384 layer
+//    of that shape and T=8192, d=4096, E=128, top-8, d_ff=1536: 1-2%.
+bool swap_size(int64_t T, int k, int d, int dff) {
+  if (T <= kTileRows || row_pairs(T, k, d, dff)) return true;
+  const double work = static_cast<double>(T) * k * d * dff;
+  return pair_mode() == kPairsAuto && work >= 68719476736.0;
+}
+
+// Forward GEMMs with swapped operands by the size rule above; the row-tile kernels (single
+// CTAs) below it.  MOE_FWD_SWAP="0" turns the swapped kernels off, "1" uses them for every
+// size; MOE_GEMM_PAIR="0" (single CTAs only) turns them off too.  Read once per process;
+// every choice gives bitwise the same rows.
 bool forward_swap(int64_t T, int k, int d, int dff) {
   static const int mode = [] {
     const char* e = std::getenv("MOE_FWD_SWAP");
@@ -62,12 +73,13 @@ bool forward_swap(int64_t T, int k, int d, int dff) {
     return 2;
   }();
   if (mode == 0 || !use_pairs()) return false;
-  return mode == 1 || T <= kTileRows || row_pairs(T, k, d, dff);
+  return mode == 1 || swap_size(T, k, d, dff);
 }
 
 // The backward's dX GEMM with swapped operands (every expert on CTA pairs in one launch) by the
-// same rule as the forward's (measured on GB300: the fwd_bwd workload, T=8192, d=4096, E=128,
-// top-8, d_ff=1536, whose 5-tile experts otherwise run on single CTAs in a second launch).
+// same size rule as the forward's (measured on GB300: the fwd_bwd workload, T=8192, d=4096,
+// E=128, top-8, d_ff=1536, whose 5-tile experts otherwise run on single CTAs in a second
+// launch; and T=2048, d=4096, E=32, top-8, d_ff=1536, dX 0.344 -> 0.294 ms).
 // MOE_BWD_SWAP="0" keeps the row-tile kernels, "1" swaps at every size; read once per process.
 // Bitwise the same dX rows either way.
 bool backward_swap(int64_t T, int k, int d, int dff) {
@@ -78,7 +90,7 @@ bool backward_swap(int64_t T, int k, int d, int dff) {
     return 2;
   }();
   if (mode == 0 || !use_pairs()) return false;
-  return mode == 1 || T <= kTileRows || row_pairs(T, k, d, dff);
+  return mode == 1 || swap_size(T, k, d, dff);
 }
 
 // The backward's dH GEMM with swapped operands, by the same rule unless MOE_BWD_DH_SWAP ("0"

@@ -1,6 +1,7 @@
 """Host-side logic of bench.py, on the CPU: the algorithmic FLOP and byte counts behind the
 reported roofline fractions, and the launch counts that follow the library's rule for CTA
-pairs (MOE_GEMM_PAIR: "0" never, "1" whenever T > 128, unset T > 128 and T k d d_ff >= 2^37).
+pairs (MOE_GEMM_PAIR: "0" never, "1" whenever T > 128, unset T > 128 and T k d d_ff >= 2^37) and
+for the swapped-operand kinds (T <= 128, wherever row tiles pair, and from T k d d_ff >= 2^36).
 """
 import pytest
 
@@ -77,3 +78,25 @@ def test_pair_rule_and_launch_counts(bench, monkeypatch, mode, name, pairs):
     monkeypatch.delenv("MOE_BWD_DH_SWAP")
     monkeypatch.delenv("MOE_BWD_SWAP")
     assert bench.bwd_launches(w.T, w.k, w.d, w.dff) == 8
+
+
+@pytest.mark.parametrize("T,d,E,k,dff,swap", [
+    (2048, 4096, 32, 8, 1536, True),    # 1.03e11: swapped, row tiles on single CTAs
+    (1024, 4096, 64, 8, 1536, False),   # 5.2e10 < 2^36
+    (4096, 2048, 64, 6, 1024, False),   # 5.2e10 (the mid workload)
+    (128, 128, 8, 2, 128, True),        # T <= 128
+])
+def test_swap_size_rule_between_the_thresholds(bench, monkeypatch, T, d, E, k, dff, swap):
+    # the swapped kinds start at T k d d_ff = 2^36, half the row-tile pair threshold
+    for v in ("MOE_GEMM_PAIR", "MOE_FWD_SWAP", "MOE_BWD_SWAP", "MOE_BWD_DH_SWAP"):
+        monkeypatch.delenv(v, raising=False)
+    assert bench._forward_swap(T, k, d, dff) == swap
+    assert bench._backward_swap(T, k, d, dff) == swap
+    if T > 128:
+        assert not bench._row_pairs(T, k, d, dff)
+        assert bench.fwd_launches(T, k, d, dff) == 5 + 2 + 1
+    # MOE_GEMM_PAIR "1" pairs every size above T = 128 and swaps with it; "0" never swaps
+    monkeypatch.setenv("MOE_GEMM_PAIR", "1")
+    assert bench._forward_swap(T, k, d, dff)
+    monkeypatch.setenv("MOE_GEMM_PAIR", "0")
+    assert not bench._forward_swap(T, k, d, dff)
