@@ -75,6 +75,13 @@ struct KindTraits {
   static constexpr int kAmn =
       (KIND == kDw2 || KIND == kDw13 || (kSwap && KIND != kDxT && KIND != kDhT)) ? 1 : 0;
   static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8 || kSwap) ? 0 : 1;
+  // K blocks (of 64) per pipeline stage: two for the swapped GEMM2 and dX (3 stages of 64 KB:
+  // one producer / MMA-issuer handshake per 128 K), one elsewhere.  Measured on GB300 against
+  // one for every swapped kind, 3 alternations: GEMM2 of the T=16384, d=7168, E=256, top-8,
+  // d_ff=2048 layer 2.87 -> 2.77 ms, dX of T=8192, d=4096, E=128, top-8, d_ff=1536 1.171 ->
+  // 1.159 ms; GEMM1 (5.61 -> 5.57 there, but +0.6% at T=2048, +1.6% at T=128) and dH (+2.7%)
+  // keep one.  Bitwise the same results.
+  static constexpr int kKPS = (KIND == kFwd2T || KIND == kDxT) ? 2 : 1;
 };
 
 // Epilogue warps of a launch: 4, one per TMEM lane quadrant, or 8 for the row-tile dH pair
@@ -158,15 +165,18 @@ constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kL2HintA = 0;
 constexpr int kL2HintB = 1;
 
-template <int BN, bool PAIR = false, int EPI_WARPS = 4>
+template <int BN, bool PAIR = false, int EPI_WARPS = 4, int KPS = 1>
 struct GemmCfg {
   // a CTA pair holds half of the B tile in each CTA
   static constexpr int kBLocal = PAIR ? BN / 2 : BN;
-  // 32 KB stages: 6 (5 with 8 epilogue warps); 48 KB stages: 4
-  static constexpr int kStages =
-      (kABytes + kBLocal * kBK * 2 <= 32768) ? (EPI_WARPS > 4 ? 5 : 6) : 4;
   static constexpr uint32_t kBBytes = kBLocal * kBK * 2;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  // one K block's A and B tiles; a stage holds KPS of them back to back
+  static constexpr uint32_t kSubBytes = kABytes + kBBytes;
+  // 32 KB of K blocks: 6 (5 with 8 epilogue warps); 48 KB: 4; divided among KPS per stage
+  static constexpr int kStages =
+      ((kSubBytes <= 32768) ? (EPI_WARPS > 4 ? 5 : 6) : 4) / KPS;
+  static_assert(kStages >= 2, "a ring of at least two stages");
+  static constexpr uint32_t kStageBytes = KPS * kSubBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
   // full, empty, tfull x2, tempty x2, drain, gathered-rows landed
   static constexpr int kBars = 3 * kStages + 5;
@@ -894,7 +904,8 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap mapB1,
                         const __grid_constant__ GemmParams p) {
   constexpr int EW = EpiCfg<KIND, PAIR>::kWarps;
-  using Cfg = GemmCfg<BN, PAIR, EW>;
+  constexpr int KPS = KindTraits<KIND>::kKPS;
+  using Cfg = GemmCfg<BN, PAIR, EW, KPS>;
   using Tr = KindTraits<KIND>;
   constexpr int S = Cfg::kStages;
   constexpr int BL = Cfg::kBLocal;  // B columns held by this CTA
@@ -925,8 +936,9 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
   volatile uint32_t* peer_tx = reinterpret_cast<volatile uint32_t*>(misc + 16 + 4 * S);
   static_assert(16 + 8 * S <= 128, "misc region");
   float* epi_buf = reinterpret_cast<float*>(gbase + S * Cfg::kStageBytes);
-  auto stage_a = [&](int s) { return base + s * Cfg::kStageBytes; };
-  auto stage_b = [&](int s) { return base + s * Cfg::kStageBytes + kABytes; };
+  // K block j (< KPS) of stage s
+  auto stage_a = [&](int s, int j = 0) { return base + s * Cfg::kStageBytes + j * Cfg::kSubBytes; };
+  auto stage_b = [&](int s, int j = 0) { return stage_a(s, j) + kABytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
@@ -953,7 +965,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
     *abort_flag = 0;
     *consumed = 0u;
     *peer_issued = 0u;
-    for (int s = 0; s < S; ++s) tx_ring[s] = peer_tx[s] = Cfg::kStageBytes;
+    for (int s = 0; s < S; ++s) tx_ring[s] = peer_tx[s] = Cfg::kStageBytes;  // overwritten
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -1039,13 +1051,9 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
         }
       }
       const int nb0 = ti.n0 + rank * BL;  // first B column held by this CTA
-      // lane 0: arm stage (fb) and issue the tile loads of K block kb (A too unless gathered)
-      auto issue_stage = [&](int kb, uint32_t fb, uint32_t sa, uint32_t sb) {
-        // rank 0 arms its barrier for both CTAs' bytes; rank 1 only loads
-        uint32_t tx = gather ? Cfg::kBBytes : Cfg::kStageBytes;
-        if constexpr (Tr::kSwap) tx = kABytes + static_cast<uint32_t>(ti.box) * 128u;
-        tx_ring[(fb - full_bar(0)) / 8u] = tx;
-        if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * tx : tx);
+      // lane 0: the tile loads of K block kb into (sa, sb), completing on fb (A too unless
+      // gathered)
+      auto load_kblock = [&](int kb, uint32_t fb, uint32_t sa, uint32_t sb) {
         const int k0 = kb * kBK;
         if constexpr (Tr::kSwap) {
           // A: this CTA's 128 weight columns as two 64-column boxes (MN-major); B: this CTA's
@@ -1136,6 +1144,21 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
           for (int i = 0; i < BL / 64; ++i) load(sb + 8192u * i, &mapB0, fb, nb0 + 64 * i, r);
         }
       };
+      // lane 0: arm stage s for the K blocks of the tile's stage `st` (KPS of them, fewer in a
+      // last stage) and issue their loads; rank 0 arms its barrier for both CTAs' bytes, rank 1
+      // only loads
+      auto issue_stage = [&](int st, int s) {
+        const uint32_t fb = full_bar(s);
+        const int kb0 = st * KPS;
+        const int nsub = ti.nk - kb0 < KPS ? ti.nk - kb0 : KPS;
+        uint32_t tx = gather ? Cfg::kBBytes : Cfg::kSubBytes;
+        if constexpr (Tr::kSwap) tx = kABytes + static_cast<uint32_t>(ti.box) * 128u;
+        tx *= static_cast<uint32_t>(nsub);
+        tx_ring[s] = tx;
+        if (rank == 0) mbar_arrive_expect_tx(fb, PAIR ? 2 * tx : tx);
+        for (int j = 0; j < nsub; ++j) load_kblock(kb0 + j, fb, stage_a(s, j), stage_b(s, j));
+      };
+      const int nst = (ti.nk + KPS - 1) / KPS;  // pipeline stages of the tile
       const bool skip_hook = (p.debug_flags & 1) && blockIdx.x == 0;
       if (gather) {
         // Warps 0 and 2 walk the K blocks together, each copying 64 of the stage's 128 A rows
@@ -1166,7 +1189,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
                           src_row[i] + kb * kBK + 8 * c);
             }
             cp_async_arrive_noinc(gather_bar(s));
-            if (warp == 0 && lane == 0) issue_stage(kb, fb, sa, sb);
+            if (warp == 0 && lane == 0) issue_stage(kb, s);  // one K block per stage
           }
           ++fill;
         }
@@ -1183,7 +1206,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
             }
           }
         }
-        for (int kb = 0; kb < ti.nk && ok; ++kb) {
+        for (int st = 0; st < nst && ok; ++st) {
           const int s = fill % S;
           const uint32_t ph = (fill / S) & 1u;
           if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, 1)) {
@@ -1191,7 +1214,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
             break;
           }
           if (skip_hook && fill == 0) skipped = 0;  // test hook (see above)
-          else issue_stage(kb, full_bar(s), stage_a(s), stage_b(s));
+          else issue_stage(st, s);
           ++fill;
         }
       }
@@ -1214,7 +1237,8 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
       const uint32_t dtm = tmem_base + acc * BN;
       // swapped kinds: M = 256 weight columns, N = the block's rows (2 box)
       const uint32_t idesc = Tr::kSwap ? idesc_bf16_f32(2 * kBM, 2 * ti.box, Tr::kAmn, 0) : IDESC;
-      for (int kb = 0; kb < ti.nk; ++kb) {
+      const int nst = (ti.nk + KPS - 1) / KPS;
+      for (int st = 0; st < nst; ++st) {
         const int s = fill % S;
         const uint32_t ph = (fill / S) & 1u;
         if (!wait_bar(full_bar(s), ph, abort_flag, 3)) {
@@ -1222,22 +1246,26 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t sa = stage_a(s), sb = stage_b(s);
+        const int kb0 = st * KPS;
+        const int nsub = ti.nk - kb0 < KPS ? ti.nk - kb0 : KPS;
+        for (int j = 0; j < nsub; ++j) {
+          const uint32_t sa = stage_a(s, j), sb = stage_b(s, j);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t ad = Tr::kAmn ? smem_desc_sw128(sa + kk * 2048u, 8192u, 1024u)
-                                       : smem_desc_sw128(sa + kk * 32u, 16u, 1024u);
-          const uint64_t bd = Tr::kBmn ? smem_desc_sw128(sb + kk * 2048u, 8192u, 1024u)
-                                       : smem_desc_sw128(sb + kk * 32u, 16u, 1024u);
-          // bf16: K = 16 per instruction (32 bytes); E4M3: K = 32 (32 bytes), so the same
-          // 32-byte descriptor step covers both
-          const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
-          if constexpr (KIND == kFwd1F8) {
-            if constexpr (PAIR) umma_f8_pair(dtm, ad, bd, IDESC, accum);
-            else umma_f8(dtm, ad, bd, IDESC, accum);
-          } else {
-            if constexpr (PAIR) umma_f16_pair(dtm, ad, bd, idesc, accum);
-            else umma_f16(dtm, ad, bd, idesc, accum);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = Tr::kAmn ? smem_desc_sw128(sa + kk * 2048u, 8192u, 1024u)
+                                         : smem_desc_sw128(sa + kk * 32u, 16u, 1024u);
+            const uint64_t bd = Tr::kBmn ? smem_desc_sw128(sb + kk * 2048u, 8192u, 1024u)
+                                         : smem_desc_sw128(sb + kk * 32u, 16u, 1024u);
+            // bf16: K = 16 per instruction (32 bytes); E4M3: K = 32 (32 bytes), so the same
+            // 32-byte descriptor step covers both
+            const uint32_t accum = ((kb0 + j) | kk) != 0 ? 1u : 0u;
+            if constexpr (KIND == kFwd1F8) {
+              if constexpr (PAIR) umma_f8_pair(dtm, ad, bd, IDESC, accum);
+              else umma_f8(dtm, ad, bd, IDESC, accum);
+            } else {
+              if constexpr (PAIR) umma_f16_pair(dtm, ad, bd, idesc, accum);
+              else umma_f16(dtm, ad, bd, idesc, accum);
+            }
           }
         }
         if constexpr (PAIR) umma_commit_pair(empty_bar(s), 3);
@@ -1387,7 +1415,7 @@ template <int KIND, int BN, bool PAIR>
 cudaError_t run_grouped_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                              const GemmParams& p, int64_t max_tiles, int num_sms,
                              cudaStream_t s) {
-  using Cfg = GemmCfg<BN, PAIR, EpiCfg<KIND, PAIR>::kWarps>;
+  using Cfg = GemmCfg<BN, PAIR, EpiCfg<KIND, PAIR>::kWarps, KindTraits<KIND>::kKPS>;
   auto kern = grouped_gemm_kernel<KIND, BN, PAIR>;
   // the opt-in shared-memory size is a per-device function attribute: set it once per device
   // (two threads racing here both set the same value)
