@@ -523,7 +523,9 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uin
   c.out = out;
   MOE_TRY(launch_gemm_fwd1_fp8(c, stream));
   record(stage_events, 2, stream);
-  MOE_TRY(launch_gemm_fwd2(c, stream));
+  // GEMM2 takes the bf16 H rows as in moe_forward, swapped by the same rule
+  MOE_TRY(forward_swap(T, k, d, d_ff) ? launch_gemm_fwd2_swap(c, stream)
+                                      : launch_gemm_fwd2(c, stream));
   record(stage_events, 3, stream);
   MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), gate, pos, T, k, d, out,
                          stream));

@@ -104,7 +104,10 @@ def _digest(env_extra):
 
 
 def test_fp8_schedule_does_not_change_results():
-    assert _digest({"MOE_GEMM_PAIR": "0"}) == _digest({"MOE_GEMM_PAIR": "1"})
+    # single CTAs / CTA pairs with GEMM2 swapped / CTA pairs with row-tile GEMM2
+    ref = _digest({"MOE_GEMM_PAIR": "0"})
+    assert _digest({"MOE_GEMM_PAIR": "1"}) == ref
+    assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "0"}) == ref
 
 
 def test_fp8_large_workload_sampled(moe):
