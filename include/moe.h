@@ -45,6 +45,13 @@
  *     d_ff <= 65536, T*k + 128*E < 2^31.  Violations return MOE_ERR_UNSUPPORTED.
  *   - Results are bitwise reproducible run to run, and each token's outputs are bitwise
  *     independent of the other tokens in the batch and of T.
+ *   - Schedule overrides (environment variables, each read once per process; every choice
+ *     gives bitwise the same results, only the kernels that compute them change):
+ *     MOE_GEMM_PAIR "0" runs every GEMM on single CTAs, "1" uses CTA pairs whenever T > 128;
+ *     MOE_FWD_SWAP, MOE_BWD_SWAP and MOE_BWD_DH_SWAP "0" / "1" turn the swapped-operand
+ *     forward GEMMs, the backward's dX (and dH) and the backward's dH alone off / on at every
+ *     size; MOE_FWD_FUSED "0" / "1" runs the two swapped forward GEMMs as two launches / one.
+ *     Unset, a size rule on T, k, d and d_ff chooses.
  */
 #ifndef MOE_H_
 #define MOE_H_
