@@ -65,13 +65,20 @@ enum GemmKind : int {
   // and dH: the expert's W2 rows (d_ff of them, K = d contiguous) as the M operand, a block of
   // dO rows as N; the epilogue applies the saved multipliers per (row, d_ff column)
   kDhT = 11,    // dH^T = W2 dO^T -> dA, dB (bf16)                            (dff x rows)
+  // kFwd1T with 8 epilogue warps (two per TMEM lane quadrant, alternate 32-row chunks) and 5
+  // stages: its SwiGLU epilogue keeps up with short main loops of full row blocks (K = d of
+  // 2048: GEMM1 of the T=4096, d=2048, E=64, top-6, d_ff=1024 layer 0.238 -> 0.187 ms on
+  // GB300; the T=16384, d=7168, E=256 layer 5.71 -> 5.63 ms), while layers of mostly light
+  // experts, which stream weights, keep the sixth stage of kFwd1T (T=128 and T=1024 of the
+  // d=7168 layer: 2.23 vs 2.28 ms and 1.029 vs 1.059 ms)
+  kFwd1TW = 12,
 };
 
 template <int KIND>
 struct KindTraits {
   static constexpr bool kRowsM = (KIND <= kDx || KIND == kFwd1F8);  // M = permuted rows
   static constexpr bool kSwap = (KIND == kFwd1T || KIND == kFwd2T || KIND == kFwdT ||
-                                 KIND == kDxT || KIND == kDhT);  // N = rows
+                                 KIND == kDxT || KIND == kDhT || KIND == kFwd1TW);  // N = rows
   static constexpr int kAmn =
       (KIND == kDw2 || KIND == kDw13 || (kSwap && KIND != kDxT && KIND != kDhT)) ? 1 : 0;
   static constexpr int kBmn = (KIND == kDh || KIND == kDx || KIND == kFwd1F8 || kSwap) ? 0 : 1;
@@ -86,13 +93,13 @@ struct KindTraits {
 
 // Epilogue warps of a launch: 4, one per TMEM lane quadrant, or 8 for the row-tile dH pair
 // launch, whose epilogue (the saved multipliers of dA and dB read from HBM, 12 bytes of
-// traffic per accumulator element) is slower than its MMAs with 4 warps; two warps then share
-// a lane quadrant and split the accumulator columns.  (The swapped dH runs faster with 4
-// warps and the sixth stage they leave room for: measured on GB300, 0.697 -> 0.662 ms at the
-// fwd_bwd workload, T=8192, d=4096, E=128, top-8, d_ff=1536.)
+// traffic per accumulator element) is slower than its MMAs with 4 warps, and for kFwd1TW;
+// two warps then share a lane quadrant and split the accumulator.  (The swapped dH runs
+// faster with 4 warps and the sixth stage they leave room for: measured on GB300, 0.697 ->
+// 0.662 ms at the fwd_bwd workload, T=8192, d=4096, E=128, top-8, d_ff=1536.)
 template <int KIND, bool PAIR>
 struct EpiCfg {
-  static constexpr int kWarps = (KIND == kDh && PAIR) ? 8 : 4;
+  static constexpr int kWarps = ((KIND == kDh || KIND == kFwd1TW) && PAIR) ? 8 : 4;
   static constexpr int kThreads = 128 + 32 * kWarps;  // + producer, MMA, TMEM, spare warps
 };
 
@@ -799,10 +806,12 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
     if (p.gated) {
       const bool is_a = q < 2;
       const int col = ti.n0 + 64 * rank + 32 * (q & 1) + lane;  // h column of this lane
-      const int bar = 1 + (q & 1);
+      // named barrier of the warp pair: 1 and 2, or 5 and 6 for the second warp of each lane
+      // quadrant (3 and 4 are the tile-level barriers)
+      const int bar = 1 + (q & 1) + 4 * half;
       const int j0 = is_a ? 0 : 16;
 #pragma unroll 1
-      for (int ch = 0; ch < nch; ++ch) {
+      for (int ch = half; ch < nch; ch += nhalves) {
         float v[32];
         tmem_ld32(tacc + ch * 32, v);
 #pragma unroll
@@ -842,11 +851,11 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
         __syncwarp();  // stores have read `mine` before the next chunk rewrites it
       }
       if (is_a)
-        for (int r = nch * 32; r < ti.nseg; ++r) H[(row0 + r) * p.dff + col] = 0;
+        for (int r = nch * 32 + half; r < ti.nseg; r += nhalves) H[(row0 + r) * p.dff + col] = 0;
     } else {
       const int col = ti.n0 + 128 * rank + 32 * q + lane;
 #pragma unroll 1
-      for (int ch = 0; ch < nch; ++ch) {
+      for (int ch = half; ch < nch; ch += nhalves) {
         float v[32];
         tmem_ld32(tacc + ch * 32, v);
 #pragma unroll
@@ -860,7 +869,7 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
           }
         }
       }
-      for (int r = nch * 32; r < ti.nseg; ++r) H[(row0 + r) * p.dff + col] = 0;
+      for (int r = nch * 32 + half; r < ti.nseg; r += nhalves) H[(row0 + r) * p.dff + col] = 0;
     }
   } else {
     const int c0 = ti.n0 + 128 * rank + 32 * q;  // first output column of this warp

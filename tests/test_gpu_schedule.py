@@ -30,7 +30,7 @@ import torch
 import moe_synth
 import combine_fp32_router_gb300 as moe
 from moe_harness import forward, backward, to_dev
-w = moe_synth.custom(T=3000, d=512, E=64, k=4, dff=%(dff)d, seed=77, zipf_s=1.2,
+w = moe_synth.custom(T=3000, d=512, E=%(E)d, k=4, dff=%(dff)d, seed=77, zipf_s=1.2,
                      gated=%(gated)s)
 inp = moe_synth.generate(w, with_dy=True)
 g = to_dev(inp)
@@ -49,12 +49,12 @@ print(h.hexdigest())
 """
 
 
-def _digest(env_extra, gated=True):
+def _digest(env_extra, gated=True, E=64):
     env = {k: v for k, v in os.environ.items()
            if k not in ("MOE_GEMM_PAIR", "MOE_FWD_SWAP", "MOE_FWD_FUSED", "MOE_BWD_SWAP",
                         "MOE_BWD_DH_SWAP")}
     env.update(env_extra)
-    script = _SCRIPT % {"root": ROOT, "gated": gated, "dff": 384 if gated else 512}
+    script = _SCRIPT % {"root": ROOT, "gated": gated, "dff": 384 if gated else 512, "E": E}
     r = subprocess.run([sys.executable, "-c", script], env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-3000:]
@@ -76,3 +76,12 @@ def test_schedule_does_not_change_results(gated):
                    gated) == ref
     assert _digest({"MOE_GEMM_PAIR": "1", "MOE_BWD_SWAP": "1", "MOE_BWD_DH_SWAP": "0"},
                    gated) == ref
+
+
+@pytest.mark.parametrize("gated", [True, False])
+def test_wide_epilogue_gemm1_matches_row_tiles(gated):
+    # 16 experts for 12000 token-expert pairs (P >= 256 E): the swapped GEMM1 runs its 8-warp
+    # epilogue form; bitwise the row-tile kernels' rows
+    ref = _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "0"}, gated, E=16)
+    assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "1"}, gated, E=16) == ref
+    assert _digest({}, gated, E=16) == ref
