@@ -8,9 +8,9 @@
 //   warp 1      MMA issuer (one lane): tcgen05.mma 128 x BN x K into a TMEM accumulator
 //               (bf16: K = 16; E4M3: K = 32; with CTA pairs, rank 0 issues M = 256)
 //   warp 2      TMEM allocator
-//   warps 4..7  epilogue: tcgen05.ld of the accumulator, activation, global stores (the dH
-//               pair launch: warps 4..11, two per TMEM lane quadrant, each taking half of
-//               the accumulator columns)
+//   warps 4..7  epilogue: tcgen05.ld of the accumulator, activation, global stores (the
+//               row-tile dH pair launch and kFwd1TW: warps 4..11, two per TMEM lane
+//               quadrant, each taking half of the accumulator)
 // Two TMEM accumulators alternate so the epilogue of tile i overlaps the MMAs of tile i+1.
 // GEMM1 with rows gathered from x (opt-in) adds warp 2 as a second row-copying warp next to
 // warp 0 and warp 3 (one lane) as the proxy-fence thread.
