@@ -877,7 +877,7 @@ __device__ __forceinline__ void epilogue_swap(const GemmParams& p, const TileInf
     uint16_t* Y = static_cast<uint16_t*>(KIND == kFwdT ? p.out1 : p.out0);
     uint16_t* yb = reinterpret_cast<uint16_t*>(mine);
 #pragma unroll 1
-    for (int ch = 0; ch < nch; ++ch) {
+    for (int ch = half; ch < nch; ch += nhalves) {
       float v[32];
       tmem_ld32(tacc + ch * 32, v);
       if (!live) continue;
