@@ -162,7 +162,15 @@ struct GemmParams {
   int nb2, nkb2;
   CUtensorMap mapR2[4];
   int32_t* done1;
+  // swapped GEMM1 copying its own rows: warps 2 and 3 of every CTA write
+  // copy_dst[r] = gather_src[perm[r] / k] block by block, counting each block's finished
+  // units in done1; a tile's loads wait for its block
+  int copy_rows;
+  uint16_t* copy_dst;
 };
+
+// Row copy units of a 256-row block (4 rows each).
+constexpr int kCopyUnits = 64;
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -952,6 +960,7 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
   const bool gather = KIND == kFwd1 && p.gather_x != 0;
+  const bool copy = (KIND == kFwd1T || KIND == kFwd1TW) && p.copy_rows != 0;
   const int unit = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   const int nunits = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
@@ -1203,6 +1212,15 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
           ++fill;
         }
       } else if (lane == 0) {
+        if (copy) {
+          // the block's rows are copied by the grid's copy warps: wait for all its units, then
+          // order their generic-proxy stores before this thread's TMA loads of the rows
+          if (!wait_count(p.done1 + ti.st, kCopyUnits, abort_flag, p.err, 12, p.wait_ns)) {
+            ok = false;
+          } else {
+            fence_proxy_async_global();
+          }
+        }
         if constexpr (KIND == kFwdT) {
           // a GEMM2 tile reads H rows that GEMM1 tiles of its block store: wait for all of
           // them (each CTA of a pair counts once), then order those generic-proxy stores
@@ -1314,6 +1332,58 @@ __global__ void __launch_bounds__(EpiCfg<KIND, PAIR>::kThreads, 1)
         else mbar_arrive(full_bar(s));
         ++fill;
       }
+    }
+  } else if (copy && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------------ row copy
+    // The permuted rows of the block table, in table order (the order the tiles consume
+    // them): unit u is rows 4 (u % 64) .. + 3 of block u / 64, dealt round-robin over the
+    // grid's copy warps.  Each lane loads its 16-byte pieces of the unit's rows, all in
+    // flight together, then stores them; after the stores every lane fences and lane 0 adds
+    // one to the block's count (release).  Units past a block's rows only count.
+    const int n16 = p.d >> 3;
+    int64_t nblk = p.n_st[0];
+    if (nblk < 0 || nblk * p.nb > p.max_tiles) nblk = 0;  // the tile loops record the error
+    const int64_t ncw = 2ll * gridDim.x;
+    for (int64_t u = 2ll * blockIdx.x + (warp - 2); u < nblk * kCopyUnits; u += ncw) {
+      const int st = static_cast<int>(u / kCopyUnits), sub = static_cast<int>(u % kCopyUnits);
+      const int e = p.st_expert[st];
+      const int64_t row0 = p.st_row0[st];
+      int nv = 0;
+      if (e >= 0 && e < p.E && row0 >= 0) {
+        nv = p.poff[e] + p.counts[e] - static_cast<int>(row0) - 4 * sub;
+        nv = nv < 0 ? 0 : (nv > 4 ? 4 : nv);
+        if (row0 + 4 * sub + nv > p.rows_cap) nv = 0;
+      }
+      const uint4* src[4];
+      uint4* dst[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t row = row0 + 4 * sub + i;
+        int pr = i < nv ? p.perm[row] : 0;
+        if (pr < 0) {  // a valid row without its pair: recorded, and copied from token 0
+          set_error(p.err, MOE_ERR_DEVICE_BOUNDS, 13);
+          pr = 0;
+        }
+        src[i] = reinterpret_cast<const uint4*>(p.gather_src) + static_cast<int64_t>(pr / p.k) * n16;
+        dst[i] = reinterpret_cast<uint4*>(p.copy_dst) + (i < nv ? row : 0) * n16;
+      }
+      // 16 loads of 16 bytes in flight per lane: 4 rows x 4 column steps
+      for (int c = lane; c < n16; c += 128) {
+        uint4 v[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (i < nv && c + 32 * j < n16) v[i][j] = ld_nc_v4(src[i] + c + 32 * j);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (i < nv && c + 32 * j < n16) st_v4(dst[i] + c + 32 * j, v[i][j]);
+      }
+      __threadfence();  // this lane's stores are visible device-wide ...
+      __syncwarp();     // ... before lane 0 counts the unit
+      if (lane == 0) red_release_add(p.done1 + st, 1);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue

@@ -238,6 +238,15 @@ cudaError_t launch_gemm_fwd1_swap(const GemmCtx& c, cudaStream_t s) {
   p.save_ab = c.save_ab;
   p.save_a = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Asave) : nullptr;
   p.save_b = c.save_ab ? reinterpret_cast<float*>(c.ws + L.Bsave) : nullptr;
+  if (c.copy_rows) {
+    // the kernel's copy warps write the permuted rows the tiles read (see GemmParams)
+    p.copy_rows = 1;
+    p.copy_dst = reinterpret_cast<uint16_t*>(c.ws + L.xperm);
+    p.gather_src = c.x;
+    p.perm = reinterpret_cast<const int32_t*>(c.ws + L.perm);
+    p.k = L.k;
+    p.done1 = reinterpret_cast<int32_t*>(c.ws + L.done1);
+  }
   // 8 epilogue warps (kFwd1TW) where an average expert fills a 256-row block, P >= 256 E:
   // measured on GB300 at d=7168, E=256, top-8, d_ff=2048, GEMM1 of T=16384 (P = 512 E)
   // 5.71 -> 5.63 ms, of T=1024 (P = 32 E) 1.029 -> 1.059 ms with 8 warps

@@ -113,6 +113,7 @@ struct GemmCtx {
   bool swap;  // forward GEMMs with weight columns as M and row blocks as N (one pair launch)
   bool fuse_combine;     // GEMM2 also combines finished tokens into `out`
   bool gather_x;         // GEMM1 gathers its A rows from x (no x_perm)
+  bool copy_rows;        // the swapped GEMM1 writes x_perm itself, block by block
   uint16_t* out;         // layer output [T, d] (fused combine)
   bool gated;            // SwiGLU (W1, W3); false: squared ReLU on W1 alone
   // FP8 GEMM1: transposed E4M3 weights [E][dff][d] and their scales [E][dff]

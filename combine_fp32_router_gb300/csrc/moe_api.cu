@@ -106,6 +106,19 @@ bool backward_swap_dh(int64_t T, int k, int d, int dff) {
   return mode == 1 || backward_swap(T, k, d, dff);
 }
 
+// Whether the swapped GEMM1 copies the permuted rows itself (its copy warps write x_perm
+// block by block in the order its tiles read them, so the copy runs under the MMAs) instead
+// of the dispatch's scatter kernel.  MOE_FWD_ROW_COPY="0" keeps the scatter's copies, "1"
+// (or unset) the GEMM's; read once per process.  Bitwise the same rows either way.
+bool gemm_row_copy() {
+  static const int mode = [] {
+    const char* e = std::getenv("MOE_FWD_ROW_COPY");
+    if (e && e[0] == '0' && e[1] == 0) return 0;
+    return 1;
+  }();
+  return mode == 1;
+}
+
 // The swapped GEMMs as one persistent launch (GEMM2 of a row block after its GEMM1 tiles) for
 // T <= 64, where one launch's ramp and tail matter (measured on GB300: tiny 0.037 -> 0.034 ms,
 // T=1 at d=7168, E=256, top-8, d_ff=2048 0.158 -> 0.154 ms; T=8 and larger layers within
@@ -382,6 +395,15 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   // gathers its rows from x itself: the dispatch copy of the next tiles overlaps the MMAs of
   // the current ones.
   const bool gather = !save && (flags & MOE_FWD_GATHER_ROWS) != 0;
+  // the plain forward runs both GEMMs with swapped operands on CTA pairs; the row-gather and
+  // fused-combine variants keep the row-tile kernels
+  const bool swap = forward_swap(T, k, d, d_ff) && !gather &&
+                    (flags & MOE_FWD_FUSED_COMBINE) == 0;
+  // above the single-launch dispatch's batch size, the swapped GEMM1 copies the rows
+  // (gemm_row_copy); the one-launch pair of GEMMs (forward_fused) reads rows the dispatch
+  // copied
+  const bool copy_in_gemm =
+      T > kRouteTokensPerBlock && swap && !forward_fused(T) && gemm_row_copy();
   const TileTables tt = tile_tables(L, w);
   const int num_sms = num_sms_of_current_device();
   if (small) {
@@ -396,7 +418,7 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
     MOE_TRY(launch_scan_cols(hist, L.nblk, E, bbase, counts, stream));
     MOE_TRY(launch_offsets(counts, E, kTileRows, offsets, poff, &tt, err, stream));
     MOE_TRY(launch_scatter(x, T, d, E, k, topk, bbase, poff, pos, perm,
-                           gather ? nullptr : xperm, L.P_pad, err, stream));
+                           (gather || copy_in_gemm) ? nullptr : xperm, L.P_pad, err, stream));
     // padding rows: perm = -1; zero x rows when the backward will read them as a K operand
     MOE_TRY(launch_pad_rows(counts, poff, E, perm, save ? xperm : nullptr, 2ll * d, stream));
   }
@@ -418,10 +440,9 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   c.fuse_combine = (flags & MOE_FWD_FUSED_COMBINE) != 0;
   c.gated = W3 != nullptr;
   c.gather_x = gather;
+  c.copy_rows = copy_in_gemm;
   c.out = out;
-  // the plain forward runs both GEMMs with swapped operands on CTA pairs; the row-gather and
-  // fused-combine variants keep the row-tile kernels
-  c.swap = forward_swap(T, k, d, d_ff) && !gather && !c.fuse_combine;
+  c.swap = swap;
   if (c.swap && forward_fused(T)) {
     // both GEMMs in one launch: the GEMM1 and GEMM2 stage events bracket it together
     MOE_TRY(launch_gemm_fwd_fused(c, stream));

@@ -50,7 +50,8 @@
  *     MOE_GEMM_PAIR "0" runs every GEMM on single CTAs, "1" uses CTA pairs whenever T > 128;
  *     MOE_FWD_SWAP, MOE_BWD_SWAP and MOE_BWD_DH_SWAP "0" / "1" turn the swapped-operand
  *     forward GEMMs, the backward's dX (and dH) and the backward's dH alone off / on at every
- *     size; MOE_FWD_FUSED "0" / "1" runs the two swapped forward GEMMs as two launches / one.
+ *     size; MOE_FWD_FUSED "0" / "1" runs the two swapped forward GEMMs as two launches / one;
+ *     MOE_FWD_ROW_COPY "0" has the dispatch copy the permuted rows instead of the swapped GEMM1.
  *     Unset, a size rule on T, k, d and d_ff chooses.
  */
 #ifndef MOE_H_

@@ -6,7 +6,8 @@ rows, CTA pairs; MOE_FWD_SWAP=1), or as row tiles: 256-row tiles on CTA pairs fo
 the tile tables pick and the rest on single CTAs (MOE_FWD_SWAP=0, MOE_GEMM_PAIR=1), or
 128-row tiles on single CTAs only (MOE_GEMM_PAIR=0); the backward's row-grouped GEMMs follow
 MOE_GEMM_PAIR or the library's size rule (unset).  The swapped GEMMs also run as one launch
-(MOE_FWD_FUSED=1: GEMM2 of a row block after its GEMM1 tiles), and the backward's dX and dH
+(MOE_FWD_FUSED=1: GEMM2 of a row block after its GEMM1 tiles), the swapped GEMM1 copies the
+permuted rows itself or leaves them to the dispatch (MOE_FWD_ROW_COPY=0), and the backward's dX and dH
 GEMMs run swapped (MOE_BWD_SWAP=1; MOE_BWD_DH_SWAP for dH alone) or as row tiles ("0").  The forward variant that gathers GEMM1's
 rows from x and fuses the combine into GEMM2 must match the default forward bitwise.  Each
 schedule runs in its own process (the switches are read once per process).
@@ -52,7 +53,7 @@ print(h.hexdigest())
 def _digest(env_extra, gated=True, E=64):
     env = {k: v for k, v in os.environ.items()
            if k not in ("MOE_GEMM_PAIR", "MOE_FWD_SWAP", "MOE_FWD_FUSED", "MOE_BWD_SWAP",
-                        "MOE_BWD_DH_SWAP")}
+                        "MOE_BWD_DH_SWAP", "MOE_FWD_ROW_COPY")}
     env.update(env_extra)
     script = _SCRIPT % {"root": ROOT, "gated": gated, "dff": 384 if gated else 512, "E": E}
     r = subprocess.run([sys.executable, "-c", script], env=env,
@@ -66,6 +67,9 @@ def test_schedule_does_not_change_results(gated):
     ref = _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "0"}, gated)
     assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "1"}, gated) == ref
     assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "1", "MOE_FWD_FUSED": "1"}, gated) == ref
+    # the swapped GEMM1 copying the permuted rows itself, or the dispatch's scatter copying them
+    assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "1", "MOE_FWD_ROW_COPY": "0"},
+                   gated) == ref
     assert _digest({"MOE_GEMM_PAIR": "0"}, gated) == ref
     assert _digest({}, gated) == ref
     # the backward's dX and dH GEMMs with swapped operands (CTA pairs, one launch each) or as
@@ -84,4 +88,6 @@ def test_wide_epilogue_gemm1_matches_row_tiles(gated):
     # epilogue form; bitwise the row-tile kernels' rows
     ref = _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "0"}, gated, E=16)
     assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "1"}, gated, E=16) == ref
+    assert _digest({"MOE_GEMM_PAIR": "1", "MOE_FWD_SWAP": "1", "MOE_FWD_ROW_COPY": "0"},
+                   gated, E=16) == ref
     assert _digest({}, gated, E=16) == ref
