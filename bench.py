@@ -135,6 +135,9 @@ def _algorithmic(w, P):
         gemm2_flops=2 * d * dff * P,            # down projection
         # logits read; topk, gate, pos, perm written; x read; x_perm written
         dispatch_bytes=T * E * 4 + T * k * 16 + T * d * 2 + P * d * 2,
+        # the routing part alone (when GEMM1 copies the rows): logits read, topk, gate, pos,
+        # perm written
+        dispatch_route_bytes=T * E * 4 + T * k * 16,
         # combine: bf16 expert-output rows read (the pages' BF16 gather), gate + pos read,
         # out written (bf16)
         combine_bytes=P * d * 2 + T * k * 8 + T * d * 2,
@@ -175,6 +178,15 @@ def _forward_swap(T, k, d, dff):
     if mode == "0" or os.environ.get("MOE_GEMM_PAIR", "") == "0":
         return False
     return mode == "1" or _swap_size(T, k, d, dff)
+
+
+def _gemm_row_copy(T, k, d, dff):
+    # the library's rule for the swapped GEMM1 copying the permuted rows itself
+    # (MOE_FWD_ROW_COPY "0" leaves them to the dispatch's scatter): T > 128, swapped GEMMs as
+    # two launches
+    if os.environ.get("MOE_FWD_ROW_COPY", "") == "0":
+        return False
+    return T > 128 and _forward_swap(T, k, d, dff) and not _forward_fused(T, k, d, dff)
 
 
 def _forward_fused(T, k, d, dff):
@@ -547,7 +559,10 @@ def bench_native(args, w):
     g1_flops = alg["gemm_flops"] if fused else alg["gemm1_flops"]
     g1_tflops = g1_flops / (stages["gemm1_swiglu"] * 1e-3) / 1e12
     g_tflops = alg["gemm_flops"] / ((stages["gemm1_swiglu"] + stages["gemm2"]) * 1e-3) / 1e12
-    disp_gbs = alg["dispatch_bytes"] / (stages["dispatch"] * 1e-3) / 1e9
+    # with GEMM1 copying the rows, the dispatch stage moves only the routing bytes
+    row_copy = _gemm_row_copy(T, k, d, dff)
+    disp_bytes = alg["dispatch_route_bytes"] if row_copy else alg["dispatch_bytes"]
+    disp_gbs = disp_bytes / (stages["dispatch"] * 1e-3) / 1e9
     comb_gbs = alg["combine_bytes"] / (stages["combine"] * 1e-3) / 1e9
     # GEMM1 runs for milliseconds inside a sub-second timed loop: the burst peak applies
     peak = peaks["bf16"]
@@ -572,6 +587,7 @@ def bench_native(args, w):
         "gemm_frac_of_bf16_burst": g_tflops / peaks["bf16"],
         "gemm_roofline_under_load": roof,
         "dispatch_gbs": disp_gbs, "dispatch_frac_of_hbm": disp_gbs / peaks["hbm"],
+        "dispatch_rows_copied_by": "gemm1" if row_copy else "scatter",
         "combine_gbs": comb_gbs, "combine_frac_of_hbm": comb_gbs / peaks["hbm"],
         "waved_forward_ms_per_step": waved_ms,
         "graph_forward_ms_per_step": graph_ms,

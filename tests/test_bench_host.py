@@ -14,7 +14,7 @@ def bench():
     return b
 
 
-def test_algorithmic_counts_of_the_large_workload(bench):
+def test_algorithmic_counts_of_the_large_workload(bench, monkeypatch):
     w = moe_synth.by_name("large_skewed")
     P = w.T * w.k
     a = bench._algorithmic(w, P)
@@ -26,6 +26,16 @@ def test_algorithmic_counts_of_the_large_workload(bench):
     # dispatch: logits read (fp32), 16 B of routing results per pair, x read and x_perm written
     assert a["dispatch_bytes"] == w.T * w.E * 4 + P * 16 + w.T * w.d * 2 + P * w.d * 2
     assert abs(a["dispatch_bytes"] / 1e9 - 2.133) < 5e-4
+    # the routing part alone, when GEMM1 copies the rows (the default above T = 128)
+    assert a["dispatch_route_bytes"] == w.T * w.E * 4 + P * 16
+    monkeypatch.delenv("MOE_FWD_ROW_COPY", raising=False)
+    monkeypatch.delenv("MOE_FWD_SWAP", raising=False)
+    monkeypatch.delenv("MOE_GEMM_PAIR", raising=False)
+    monkeypatch.delenv("MOE_FWD_FUSED", raising=False)
+    assert bench._gemm_row_copy(w.T, w.k, w.d, w.dff)
+    assert not bench._gemm_row_copy(128, w.k, w.d, w.dff)
+    monkeypatch.setenv("MOE_FWD_ROW_COPY", "0")
+    assert not bench._gemm_row_copy(w.T, w.k, w.d, w.dff)
     # combine: bf16 expert rows read, gate + pos read, bf16 output written
     assert a["combine_bytes"] == P * w.d * 2 + P * 8 + w.T * w.d * 2
     assert abs(a["combine_bytes"] / 1e9 - 2.115) < 5e-4
