@@ -39,6 +39,7 @@ EXPORTS = ("moe_route_workspace_bytes", "moe_workspace_bytes", "moe_route_dispat
            "moe_backward",
            "moe_route_dispatch_noalloc", "moe_route_dispatch_noalloc_get_error",
            "moe_ep_first_expert", "moe_ep_plan", "moe_ep_return_plan", "moe_ep_copy_rows",
+           "moe_expert_workspace_bytes", "moe_expert_forward", "moe_combine",
            "moe_probe_dram_read", "moe_get_error", "moe_set_wait_timeout_ns",
            "moe_debug_set_flags", "moe_status_string")
 
@@ -94,6 +95,12 @@ def _load():
     lib.moe_ep_return_plan.restype = i
     lib.moe_ep_copy_rows.argtypes = [p, p, i, p, p, p, p, i, i64, p, i64, p, p]
     lib.moe_ep_copy_rows.restype = i
+    lib.moe_expert_workspace_bytes.argtypes = [i64, i, i, i]
+    lib.moe_expert_workspace_bytes.restype = sz
+    lib.moe_expert_forward.argtypes = [p, p, i64, i, i, i, p, p, p, p, p, sz, p]
+    lib.moe_expert_forward.restype = i
+    lib.moe_combine.argtypes = [p, i64, p, p, i64, i, i, p, p, p]
+    lib.moe_combine.restype = i
     lib.moe_probe_dram_read.argtypes = [p, sz, i, i, p, p]
     lib.moe_probe_dram_read.restype = i
     lib.moe_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -348,6 +355,29 @@ def moe_ep_copy_rows(peers, peer_rows, seg_src_rank, seg_src_row, seg_dst_row, s
                                  _ptr(seg_src_row), _ptr(seg_dst_row), _ptr(seg_rows), n_seg,
                                  row_bytes, _ptr(dst), dst.shape[0], _ptr(err_word),
                                  _stream(stream)), "moe_ep_copy_rows")
+
+
+def moe_expert_workspace_bytes(n_rows, d, E, d_ff):
+    return int(_lib.moe_expert_workspace_bytes(int(n_rows), int(d), int(E), int(d_ff)))
+
+
+def moe_expert_forward(rows, counts, W1, W3, W2, y_rows, ws, stream=None):
+    """The expert stage on ``rows`` [n_rows, d] bf16 laid out with each local expert's
+    ``counts`` (int32 device tensor [E]) rows starting on a 128-row boundary; writes
+    ``y_rows`` [n_rows, d] bf16 (see include/moe.h)."""
+    n_rows, d = rows.shape
+    E, _, d_ff = W1.shape
+    _check(_lib.moe_expert_forward(_ptr(rows), _ptr(counts), n_rows, d, E, d_ff, _ptr(W1),
+                                   _ptr(W3), _ptr(W2), _ptr(y_rows), _ptr(ws), _nbytes(ws),
+                                   _stream(stream)), "moe_expert_forward")
+
+
+def moe_combine(y_rows, gate, pos, out, err_word, stream=None):
+    """out [T, d] = bf16(sum_j gate[t, j] y_rows[pos[t, j]]), fp32 in slot order."""
+    T, k = gate.shape
+    d = out.shape[1]
+    _check(_lib.moe_combine(_ptr(y_rows), y_rows.shape[0], _ptr(gate), _ptr(pos), T, k, d,
+                            _ptr(out), _ptr(err_word), _stream(stream)), "moe_combine")
 
 
 def moe_probe_dram_read(buf, ctas, mode, out, stream=None):

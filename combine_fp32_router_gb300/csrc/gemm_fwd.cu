@@ -114,7 +114,7 @@ GemmParams base_params(const GemmCtx& c) {
   p.err = c.err;
   p.wait_ns = c.wait_ns;
   p.debug_flags = c.debug_flags;
-  p.rows_cap = L.P_pad;
+  p.rows_cap = c.rows ? c.rows_cap : L.P_pad;
   p.gated = c.gated ? 1 : 0;
   return p;
 }
@@ -230,7 +230,10 @@ cudaError_t launch_gemm_fwd1_swap(const GemmCtx& c, cudaStream_t s) {
                                      2ull * L.dff, 64, 64, &st);
   if (st != cudaSuccess) return st;
   GemmParams p = swap_params(c);
-  st = row_maps(p, c.ws + L.xperm, L.d, L.P_pad, 2ull * L.d);
+  // the rows: the workspace's x_perm, or the caller's (moe_expert_forward; the map ends at
+  // their last row, so nothing past it is read)
+  if (c.rows) st = row_maps(p, c.rows, L.d, static_cast<uint64_t>(c.rows_cap), 2ull * L.d);
+  else st = row_maps(p, c.ws + L.xperm, L.d, L.P_pad, 2ull * L.d);
   if (st != cudaSuccess) return st;
   p.nb = c.gated ? L.dff / 128 : L.dff / 256;
   p.nkb = L.d / kBK;
@@ -266,7 +269,7 @@ cudaError_t launch_gemm_fwd2_swap(const GemmCtx& c, cudaStream_t s) {
   if (st != cudaSuccess) return st;
   p.nb = (L.d + 255) / 256;  // d % 256 == 128: the last block's second CTA has no columns
   p.nkb = L.dff / kBK;
-  p.out0 = c.ws + L.Y;
+  p.out0 = c.y ? static_cast<void*>(c.y) : static_cast<void*>(c.ws + L.Y);
   return run_grouped_gemm<kFwd2T, 256, true>(w2, w2, w2, p, L.max_mt * p.nb, c.num_sms, s);
 }
 

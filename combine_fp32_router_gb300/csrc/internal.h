@@ -88,8 +88,10 @@ cudaError_t launch_quantize_weights_fp8(const uint16_t* W, int E, int K, int N, 
 // Padding rows of every expert segment: perm = -1 and (if rows != null) zero bytes.
 cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, int32_t* perm,
                             void* rows, int64_t row_bytes, cudaStream_t s);
-cudaError_t launch_combine(const uint16_t* y_rows, const float* gate, const int32_t* pos,
-                           int64_t T, int k, int d, uint16_t* out, cudaStream_t s);
+// y_rows holds rows_cap rows; a pos outside them records MOE_ERR_DEVICE_BOUNDS in err
+cudaError_t launch_combine(const uint16_t* y_rows, int64_t rows_cap, const float* gate,
+                           const int32_t* pos, int64_t T, int k, int d, uint16_t* out,
+                           DevErr* err, cudaStream_t s);
 // `part`: scratch of T * ceil(d / 1024) * k floats (per-block partial dot products).
 cudaError_t launch_bwd_gate(const uint16_t* dy, const uint16_t* y_rows, const float* gate,
                             const int32_t* pos, const int32_t* topk, int64_t T, int k, int d,
@@ -114,6 +116,11 @@ struct GemmCtx {
   bool fuse_combine;     // GEMM2 also combines finished tokens into `out`
   bool gather_x;         // GEMM1 gathers its A rows from x (no x_perm)
   bool copy_rows;        // the swapped GEMM1 writes x_perm itself, block by block
+  // the rows the swapped forward GEMMs read and GEMM2's output rows: the workspace's x_perm
+  // and Y unless set (moe_expert_forward: the caller's buffers of rows_cap rows)
+  const uint16_t* rows;
+  uint16_t* y;
+  int64_t rows_cap;
   uint16_t* out;         // layer output [T, d] (fused combine)
   bool gated;            // SwiGLU (W1, W3); false: squared ReLU on W1 alone
   // FP8 GEMM1: transposed E4M3 weights [E][dff][d] and their scales [E][dff]

@@ -448,8 +448,8 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
     MOE_TRY(launch_gemm_fwd_fused(c, stream));
     record(stage_events, 2, stream);
     record(stage_events, 3, stream);
-    MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), gate, pos, T, k, d, out,
-                           stream));
+    MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), L.P_pad, gate, pos, T, k,
+                           d, out, err, stream));
     record(stage_events, 4, stream);
     return MOE_OK;
   }
@@ -466,8 +466,8 @@ moe_status_t moe_forward(const moe_bf16_t* x, const float* logits, const moe_bf1
   }
   MOE_TRY(c.swap ? launch_gemm_fwd2_swap(c, stream) : launch_gemm_fwd2(c, stream));
   record(stage_events, 3, stream);
-  MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), gate, pos, T, k, d, out,
-                         stream));
+  MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), L.P_pad, gate, pos, T, k, d,
+                         out, err, stream));
   record(stage_events, 4, stream);
   return MOE_OK;
 }
@@ -548,9 +548,79 @@ moe_status_t moe_forward_fp8(const moe_bf16_t* x, const float* logits, const uin
   MOE_TRY(forward_swap(T, k, d, d_ff) ? launch_gemm_fwd2_swap(c, stream)
                                       : launch_gemm_fwd2(c, stream));
   record(stage_events, 3, stream);
-  MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), gate, pos, T, k, d, out,
-                         stream));
+  MOE_TRY(launch_combine(reinterpret_cast<const uint16_t*>(w + L.Y), L.P_pad, gate, pos, T, k, d,
+                         out, err, stream));
   record(stage_events, 4, stream);
+  return MOE_OK;
+}
+
+size_t moe_expert_workspace_bytes(int64_t n_rows, int d, int E, int d_ff) {
+  if (check_dims(n_rows, d, E, 1, d_ff, true) != MOE_OK) return 0;
+  return make_layout(n_rows, d, E, 1, d_ff).fwd_total;
+}
+
+// The expert stage on the caller's rows: the tile tables from the caller's counts, then the
+// swapped GEMM1 and GEMM2 with the caller's rows as the row operand and y_rows as GEMM2's
+// output (the workspace holds the tables and H).  The same kernels as moe_forward's, so each
+// row's results are bitwise moe_forward's.
+moe_status_t moe_expert_forward(const moe_bf16_t* rows, const int32_t* counts, int64_t n_rows,
+                                int d, int E, int d_ff, const moe_bf16_t* W1,
+                                const moe_bf16_t* W3, const moe_bf16_t* W2, moe_bf16_t* y_rows,
+                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status_t st = check_dims(n_rows, d, E, 1, d_ff, true);
+  if (st != MOE_OK) return st;
+  if (!counts || !W1 || !W2 || !ws) return MOE_ERR_INVALID_ARG;
+  if (!W3 && d_ff % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  if (n_rows > 0 && (!rows || !y_rows)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {rows, W1, W3, W2, y_rows};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(counts) & 3u) != 0) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_layout(n_rows, d, E, 1, d_ff);
+  if (ws_bytes < L.fwd_total) return MOE_ERR_WORKSPACE;
+  char* w = static_cast<char*>(ws);
+  DevErr* err = reinterpret_cast<DevErr*>(w + L.err);
+  MOE_TRY(cudaMemsetAsync(err, 0, sizeof(DevErr), stream));
+  if (n_rows == 0) return MOE_OK;
+  int32_t* cnt = reinterpret_cast<int32_t*>(w + L.counts);
+  MOE_TRY(cudaMemcpyAsync(cnt, counts, static_cast<size_t>(E) * 4, cudaMemcpyDeviceToDevice,
+                          stream));
+  const TileTables tt = tile_tables(L, w);
+  MOE_TRY(launch_offsets(cnt, E, kTileRows, reinterpret_cast<int32_t*>(w + L.offsets),
+                         reinterpret_cast<int32_t*>(w + L.poff), &tt, err, stream));
+  GemmCtx c{};
+  c.L = &L;
+  c.ws = w;
+  c.W1 = W1;
+  c.W3 = W3;
+  c.W2 = W2;
+  c.err = err;
+  c.wait_ns = g_wait_ns.load();
+  c.debug_flags = g_debug_flags.load();
+  c.num_sms = num_sms_of_current_device();
+  c.gated = W3 != nullptr;
+  c.rows = rows;
+  c.y = y_rows;
+  c.rows_cap = n_rows;
+  MOE_TRY(launch_gemm_fwd1_swap(c, stream));
+  MOE_TRY(launch_gemm_fwd2_swap(c, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_bf16_t* y_rows, int64_t n_rows, const float* gate,
+                         const int32_t* pos, int64_t T, int k, int d, moe_bf16_t* out,
+                         void* err_word, cudaStream_t stream) {
+  if (T < 0 || k < 1 || d <= 0 || n_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (k > kMaxK || d % 8 != 0 || d > 65536 || T > (int64_t{1} << 31) / k)
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_rows || n_rows < 1 || !gate || !pos || !out || !err_word) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_rows) || !aligned16(out) || !aligned16(err_word)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(gate) & 3u) != 0 || (reinterpret_cast<uintptr_t>(pos) & 3u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(launch_combine(y_rows, n_rows, gate, pos, T, k, d, out,
+                         static_cast<DevErr*>(err_word), stream));
   return MOE_OK;
 }
 

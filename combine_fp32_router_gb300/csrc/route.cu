@@ -712,7 +712,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
                                                       const float* __restrict__ gate,
                                                       const int32_t* __restrict__ pos,
                                                       int64_t T, int k, int d, int cpu,
-                                                      uint4* __restrict__ out) {
+                                                      int64_t rows_cap,
+                                                      uint4* __restrict__ out, DevErr* err) {
   griddep_wait();  // the previous kernel in the stream has finished (PDL)
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -727,6 +728,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     if (lane < k) {
       row = pos[t * k + lane];
       g = gate[t * k + lane];
+      if (row < 0 || row >= rows_cap) {  // recorded; row 0 is read instead
+        set_error(err, MOE_ERR_DEVICE_BOUNDS, 220);
+        row = 0;
+      }
     }
     int rows[KC];
     float gs[KC];
@@ -974,16 +979,17 @@ int unit_grid(K kern, int64_t units) {
               : KERNEL<16>(__VA_ARGS__))
 
 template <int KC>
-cudaError_t launch_combine_kc(const uint16_t* y_rows, const float* gate, const int32_t* pos,
-                              int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
+cudaError_t launch_combine_kc(const uint16_t* y_rows, int64_t rows_cap, const float* gate,
+                              const int32_t* pos, int64_t T, int k, int d, uint16_t* out,
+                              DevErr* err, cudaStream_t s) {
   // one iteration per lane (two column steps) while the units do not fill the GPU's warps a
   // few times over
   const int64_t small_units = T * ((d / 8 + 63) / 64);
   const int cpu = small_units <= 8192 ? 64 : kCombChunks;
   const int64_t units = T * ((d / 8 + cpu - 1) / cpu);
   return launch_pdl(combine_kernel<KC>, dim3(unit_grid(combine_kernel<KC>, units)), dim3(256), 0,
-                    s, reinterpret_cast<const uint4*>(y_rows), gate, pos, T, k, d, cpu,
-                    reinterpret_cast<uint4*>(out));
+                    s, reinterpret_cast<const uint4*>(y_rows), gate, pos, T, k, d, cpu, rows_cap,
+                    reinterpret_cast<uint4*>(out), err);
 }
 template <int KC>
 cudaError_t launch_combine_f32_kc(const float* rows, const int32_t* pos, int64_t T, int k, int d,
@@ -1113,10 +1119,12 @@ cudaError_t launch_pad_rows(const int32_t* counts, const int32_t* poff, int E, i
                     reinterpret_cast<uint4*>(rows), row_bytes / 16);
 }
 
-cudaError_t launch_combine(const uint16_t* y_rows, const float* gate, const int32_t* pos,
-                           int64_t T, int k, int d, uint16_t* out, cudaStream_t s) {
+cudaError_t launch_combine(const uint16_t* y_rows, int64_t rows_cap, const float* gate,
+                           const int32_t* pos, int64_t T, int k, int d, uint16_t* out,
+                           DevErr* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  return MOE_DISPATCH_KC(k, launch_combine_kc, y_rows, gate, pos, T, k, d, out, s);
+  return MOE_DISPATCH_KC(k, launch_combine_kc, y_rows, rows_cap, gate, pos, T, k, d, out, err,
+                         s);
 }
 
 cudaError_t launch_bwd_gate(const uint16_t* dy, const uint16_t* y_rows, const float* gate,

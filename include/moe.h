@@ -351,6 +351,39 @@ moe_status_t moe_ep_copy_rows(const void* const* peers, const int64_t* peer_rows
                               int64_t row_bytes, void* dst, int64_t dst_rows, void* err_word,
                               cudaStream_t stream);
 
+/* The expert stage alone (GEMM1 + SwiGLU, GEMM2) on rows the caller holds: an expert-
+ * parallel owner's receive buffer, laid out by moe_ep_plan with row_align = 128.
+ *   rows [n_rows, d] bf16 (device): local expert i's counts[i] rows start at row
+ *        sum_{j<i} round_up(counts[j], 128); rows between the segments are not read into
+ *        any result (any content),
+ *   counts [E] int32 (DEVICE array), W1 / W3 [E, d, d_ff], W2 [E, d_ff, d] bf16: the E local
+ *        experts (W3 = NULL: squared ReLU, d_ff a multiple of 256),
+ *   y_rows [n_rows, d] bf16 (device): y = bf16(bf16(h) W2) of each row, in the same layout;
+ *        rows between the segments are left as they were.
+ * Each row's h and y are bitwise the ones moe_forward computes for the same token-expert
+ * pair: every tile's arithmetic depends only on the model sizes.  ws: device memory of
+ * moe_expert_workspace_bytes(n_rows, d, E, d_ff) bytes, 256-byte aligned, caller-owned; its
+ * error record is read with moe_get_error.  Errors as moe_forward; a segment layout that does
+ * not fit n_rows records MOE_ERR_DEVICE_BOUNDS (nothing past n_rows is written).
+ * Asynchronous on `stream`. */
+size_t moe_expert_workspace_bytes(int64_t n_rows, int d, int E, int d_ff);
+moe_status_t moe_expert_forward(const moe_bf16_t* rows, const int32_t* counts, int64_t n_rows,
+                                int d, int E, int d_ff, const moe_bf16_t* W1,
+                                const moe_bf16_t* W3, const moe_bf16_t* W2, moe_bf16_t* y_rows,
+                                void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The combine alone: out[t] = bf16(sum_j gate[t, j] * y_rows[pos[t, j]]), an fp32
+ * accumulation in slot order j = 0..k-1, exactly as moe_forward's last stage (an expert-
+ * parallel source rank combines the output rows it pulled back).  y_rows [n_rows, d] bf16,
+ * gate [T, k] fp32, pos [T, k] int32, out [T, d] bf16: device memory.  A pos outside
+ * [0, n_rows) records MOE_ERR_DEVICE_BOUNDS in the 16-byte error word err_word (device memory,
+ * read with moe_get_error) and row 0 is read in its place.  Errors: MOE_ERR_INVALID_ARG (null
+ * or misaligned pointers), MOE_ERR_UNSUPPORTED (k or d outside the layer's limits).
+ * Asynchronous on `stream`. */
+moe_status_t moe_combine(const moe_bf16_t* y_rows, int64_t n_rows, const float* gate,
+                         const int32_t* pos, int64_t T, int k, int d, moe_bf16_t* out,
+                         void* err_word, cudaStream_t stream);
+
 /* Measurement probe (not part of the layer; the pages have no counterpart): the DRAM read
  * rate one SM sustains by load path.  Launches `ctas` CTAs (one per SM when ctas <= the SM
  * count), each streaming its own slice of floor(bytes / 152) bytes (rounded down to 16 KB)

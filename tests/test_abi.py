@@ -169,3 +169,34 @@ def test_relu2_validation(lib):
     st = raw.moe_backward(*p, fake, None, fake, 64, 128, 8, 2, 256, fake, fake, fake, fake, fake,
                           fake, fake, need, None, None)
     assert st == lib.MOE_ERR_INVALID_ARG
+
+
+def test_expert_forward_and_combine_validation(lib):
+    raw = lib.library()
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    need = lib.moe_expert_workspace_bytes(1000, 256, 4, 256)
+    assert need > 0 and need % 256 == 0
+    assert lib.moe_expert_workspace_bytes(1000, 100, 4, 256) == 0     # d % 128 != 0
+    assert lib.moe_expert_workspace_bytes(1000, 256, 2048, 256) == 0  # E > 1024
+    args = lambda: [fake, fake, 1000, 256, 4, 256, fake, fake, fake, fake, fake, need, None]
+    a = args()
+    a[1] = None                                                        # null counts
+    assert raw.moe_expert_forward(*a) == lib.MOE_ERR_INVALID_ARG
+    a = args()
+    a[11] = need - 256                                                 # workspace too small
+    assert raw.moe_expert_forward(*a) == lib.MOE_ERR_WORKSPACE
+    a = args()
+    a[7] = None                                                        # no W3: d_ff % 256
+    a[5] = 384
+    assert raw.moe_expert_forward(*a) == lib.MOE_ERR_UNSUPPORTED
+    a = args()
+    a[0] = ctypes.c_void_p((1 << 20) + 8)                              # rows misaligned
+    assert raw.moe_expert_forward(*a) == lib.MOE_ERR_INVALID_ARG
+    # combine: k beyond 16, misaligned rows, no rows for T > 0; T = 0 launches nothing
+    assert raw.moe_combine(fake, 10, fake, fake, 5, 17, 128, fake, fake, None) == \
+        lib.MOE_ERR_UNSUPPORTED
+    assert raw.moe_combine(ctypes.c_void_p((1 << 20) + 8), 10, fake, fake, 5, 2, 128, fake,
+                           fake, None) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_combine(fake, 0, fake, fake, 5, 2, 128, fake, fake, None) == \
+        lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_combine(None, 0, None, None, 0, 2, 128, None, None, None) == lib.MOE_OK

@@ -101,3 +101,72 @@ def test_ep_copy_rows_rejects_segments_outside_the_buffers(moe):
     assert moe.moe_get_error(err) == moe.MOE_ERR_DEVICE_BOUNDS
     assert torch.equal(dst[:4], src[2:6])
     assert (dst[4:] == 0).all()
+
+
+@pytest.mark.parametrize("gated", [True, False])
+def test_ep_layer_end_to_end_matches_the_single_gpu_forward(moe, gated):
+    # Three emulated ranks run the whole expert-parallel layer: dispatch their own tokens,
+    # owners pull their experts' rows, run the expert stage on the receive buffer
+    # (moe_expert_forward), every rank pulls its rows' outputs back and combines them
+    # (moe_combine).  Each rank's output is bitwise the single-GPU forward's rows for its
+    # tokens.
+    from moe_harness import forward
+    R, Tl, d, E, k = 3, 300, 256, 10, 3
+    dff = 384 if gated else 256
+    w = moe_synth.custom(R * Tl, d, E, k, dff, seed=72, zipf_s=1.2, gated=gated)
+    g = to_dev(moe_synth.generate(w))
+    dev = g["x"].device
+    ref, ws_ref = forward(moe, g, k)
+    assert moe.moe_get_error(ws_ref) == moe.MOE_OK
+    ranks = [route_dispatch(moe, {"x": g["x"][r * Tl:(r + 1) * Tl].contiguous(),
+                                  "logits": g["logits"][r * Tl:(r + 1) * Tl].contiguous()}, k)
+             for r in range(R)]
+    counts_all = np.stack([rk["counts"].cpu().numpy() for rk in ranks]).astype(np.int32)
+    peers = torch.tensor([rk["x_perm"].data_ptr() for rk in ranks], dtype=torch.int64,
+                         device=dev)
+    peer_rows = torch.tensor([rk["x_perm"].shape[0] for rk in ranks], dtype=torch.int64,
+                             device=dev)
+    err = torch.zeros(64, dtype=torch.uint8, device=dev)
+    y_out = []
+    for r in range(R):
+        pl = moe.moe_ep_plan(counts_all, r, row_align=128, wave_experts=2)
+        e0 = moe.moe_ep_first_expert(E, R, r)
+        nloc = pl["recv_counts"].shape[0]
+        rows = max(pl["rows"], 1)
+        recv = torch.full((rows, d), 7.0, dtype=torch.bfloat16, device=dev)
+        seg = [(s, pl["src_off"][i, s], pl["recv_off"][i, s], counts_all[s, e0 + i])
+               for i in range(nloc) for s in range(R)]
+        moe.moe_ep_copy_rows(peers, peer_rows, *_segments(dev, *zip(*seg)), recv, err)
+        assert moe.moe_get_error(err) == moe.MOE_OK
+        cnt = torch.tensor(np.asarray(pl["recv_counts"], np.int32), device=dev)
+        y = torch.full((rows, d), -5.0, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(moe.moe_expert_workspace_bytes(rows, d, nloc, dff), dtype=torch.uint8,
+                         device=dev)
+        W3 = g["W3"][e0:e0 + nloc].contiguous() if gated else None
+        moe.moe_expert_forward(recv, cnt, g["W1"][e0:e0 + nloc].contiguous(), W3,
+                               g["W2"][e0:e0 + nloc].contiguous(), y, ws)
+        assert moe.moe_get_error(ws) == moe.MOE_OK
+        y_out.append(y)
+    ypeers = torch.tensor([y.data_ptr() for y in y_out], dtype=torch.int64, device=dev)
+    yrows = torch.tensor([y.shape[0] for y in y_out], dtype=torch.int64, device=dev)
+    for s in range(R):
+        owner, orow, own = moe.moe_ep_return_plan(counts_all, s, row_align=128)
+        seg = [(owner[e], orow[e], own[e], counts_all[s, e]) for e in range(E)]
+        y_perm = torch.empty(Tl * k, d, dtype=torch.bfloat16, device=dev)
+        moe.moe_ep_copy_rows(ypeers, yrows, *_segments(dev, *zip(*seg)), y_perm, err)
+        out = torch.empty(Tl, d, dtype=torch.bfloat16, device=dev)
+        moe.moe_combine(y_perm, ranks[s]["gate"], ranks[s]["pos"], out, err)
+        assert moe.moe_get_error(err) == moe.MOE_OK
+        assert torch.equal(out.view(torch.int16), ref[s * Tl:(s + 1) * Tl].view(torch.int16)), s
+
+
+def test_combine_rejects_rows_outside_its_buffer(moe):
+    dev = torch.device("cuda")
+    y = torch.ones(8, 128, dtype=torch.bfloat16, device=dev)
+    gate = torch.full((2, 2), 0.5, dtype=torch.float32, device=dev)
+    pos = torch.tensor([[0, 1], [2, 8]], dtype=torch.int32, device=dev)   # row 8 is past y
+    out = torch.empty(2, 128, dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(64, dtype=torch.uint8, device=dev)
+    moe.moe_combine(y, gate, pos, out, err)
+    assert moe.moe_get_error(err) == moe.MOE_ERR_DEVICE_BOUNDS
+    assert (out[0] == 1.0).all()
