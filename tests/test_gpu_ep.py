@@ -103,13 +103,14 @@ def test_ep_copy_rows_rejects_segments_outside_the_buffers(moe):
     assert (dst[4:] == 0).all()
 
 
-@pytest.mark.parametrize("gated", [True, False])
-def test_ep_layer_end_to_end_matches_the_single_gpu_forward(moe, gated):
+@pytest.mark.parametrize("gated,waves", [(True, False), (False, False), (True, True)])
+def test_ep_layer_end_to_end_matches_the_single_gpu_forward(moe, gated, waves):
     # Three emulated ranks run the whole expert-parallel layer: dispatch their own tokens,
     # owners pull their experts' rows, run the expert stage on the receive buffer
     # (moe_expert_forward), every rank pulls its rows' outputs back and combines them
     # (moe_combine).  Each rank's output is bitwise the single-GPU forward's rows for its
-    # tokens.
+    # tokens.  With waves, an owner pulls wave i+1's rows on a copy stream while the expert
+    # stage of wave i runs on its own slice of the receive buffer.
     from moe_harness import forward
     R, Tl, d, E, k = 3, 300, 256, 10, 3
     dff = 384 if gated else 256
@@ -134,18 +135,38 @@ def test_ep_layer_end_to_end_matches_the_single_gpu_forward(moe, gated):
         nloc = pl["recv_counts"].shape[0]
         rows = max(pl["rows"], 1)
         recv = torch.full((rows, d), 7.0, dtype=torch.bfloat16, device=dev)
-        seg = [(s, pl["src_off"][i, s], pl["recv_off"][i, s], counts_all[s, e0 + i])
-               for i in range(nloc) for s in range(R)]
-        moe.moe_ep_copy_rows(peers, peer_rows, *_segments(dev, *zip(*seg)), recv, err)
-        assert moe.moe_get_error(err) == moe.MOE_OK
         cnt = torch.tensor(np.asarray(pl["recv_counts"], np.int32), device=dev)
         y = torch.full((rows, d), -5.0, dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(moe.moe_expert_workspace_bytes(rows, d, nloc, dff), dtype=torch.uint8,
-                         device=dev)
-        W3 = g["W3"][e0:e0 + nloc].contiguous() if gated else None
-        moe.moe_expert_forward(recv, cnt, g["W1"][e0:e0 + nloc].contiguous(), W3,
-                               g["W2"][e0:e0 + nloc].contiguous(), y, ws)
-        assert moe.moe_get_error(ws) == moe.MOE_OK
+        W3 = g["W3"] if gated else None
+        # waves of experts [a, b): their rows are [recv_off[a, 0], recv_off[b, 0]) of the
+        # receive buffer, each expert's from a 128-row boundary
+        bounds = list(pl["waves"]) if waves else [0, nloc]
+        copy, comp = torch.cuda.Stream(dev), torch.cuda.current_stream(dev)
+        pulled = []
+        for wv in range(len(bounds) - 1):
+            a, b = bounds[wv], bounds[wv + 1]
+            seg = [(s, pl["src_off"][i, s], pl["recv_off"][i, s], counts_all[s, e0 + i])
+                   for i in range(a, b) for s in range(R)]
+            with torch.cuda.stream(copy):
+                moe.moe_ep_copy_rows(peers, peer_rows, *_segments(dev, *zip(*seg)), recv, err,
+                                     stream=copy)
+                ev = torch.cuda.Event()
+                ev.record(copy)
+            pulled.append(ev)
+        for wv in range(len(bounds) - 1):
+            a, b = bounds[wv], bounds[wv + 1]
+            r0 = int(pl["recv_off"][a, 0])
+            r1 = int(pl["recv_off"][b, 0]) if b < nloc else pl["rows"]
+            if r1 == r0:
+                continue
+            comp.wait_event(pulled[wv])
+            ws = torch.empty(moe.moe_expert_workspace_bytes(r1 - r0, d, b - a, dff),
+                             dtype=torch.uint8, device=dev)
+            moe.moe_expert_forward(recv[r0:r1], cnt[a:b], g["W1"][e0 + a:e0 + b],
+                                   W3[e0 + a:e0 + b] if gated else None,
+                                   g["W2"][e0 + a:e0 + b], y[r0:r1], ws)
+            assert moe.moe_get_error(ws) == moe.MOE_OK
+        assert moe.moe_get_error(err) == moe.MOE_OK
         y_out.append(y)
     ypeers = torch.tensor([y.data_ptr() for y in y_out], dtype=torch.int64, device=dev)
     yrows = torch.tensor([y.shape[0] for y in y_out], dtype=torch.int64, device=dev)
