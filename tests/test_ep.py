@@ -177,6 +177,11 @@ def test_ep_plan_invariants():
                 assert np.array_equal(np.diff(pl["recv_off"][i]), counts[:-1, e0 + i])
             ends = starts + pl["recv_counts"]
             assert (ends <= np.append(starts[1:], pl["rows"])).all()
+            # the layout moe_expert_forward reads: expert i from the exclusive prefix of the
+            # counts rounded up to 128, the buffer exactly their sum
+            padded = -(-pl["recv_counts"].astype(np.int64) // 128) * 128
+            assert np.array_equal(starts, np.concatenate([[0], np.cumsum(padded)[:-1]]))
+            assert pl["rows"] == int(padded.sum())
             # sources: the exclusive prefix of each rank's counts (its dispatch offsets)
             excl = np.concatenate([np.zeros((R, 1), np.int64), np.cumsum(counts, 1)], 1)
             assert np.array_equal(pl["src_off"], excl[:, e0:e1].T)
